@@ -1,0 +1,231 @@
+// K3: BN apply + ReLU + bit-packed mask (Tech-Renaissance CBR page, section 4.3:
+//     relu(conv_out*eq_scale + eq_bias) with a CMP_GT mask stored as one bit per element).
+// B1: BN + ReLU backward reduction (CBR page, section 5.1: dY*mask before batchnorm_backward;
+//     BatchNorm CUDA page, section 3.1: dbeta = sum g, dgamma = sum g*xhat).  It also emits the
+//     per-channel coefficients of dz = gamma*inv_std*(g - dbeta/M - xhat*dgamma/M), written as
+//     dz = a*g - d*z + e, which the dgrad and wgrad kernels apply while loading their operands.
+//
+// Both passes are HBM-bound streams over NHWC tensors: 128-bit loads of 8 channels, several
+// independent vectors in flight per thread, grid sized to the SM count.
+#include <algorithm>
+
+#include "cbr_internal.h"
+#include "common.cuh"
+
+namespace cbr {
+namespace {
+
+constexpr int kApplyThreads = 256;
+constexpr int kApplyUnroll = 4;
+constexpr int kRedThreads = 512;
+constexpr int kRedUnroll = 4;
+
+template <bool BF16, bool MASK>
+__global__ void __launch_bounds__(kApplyThreads)
+    bn_apply_relu_kernel(const ApplyArgs a) {
+  __shared__ float s_eq[512];
+  for (int i = threadIdx.x; i < 2 * a.c; i += kApplyThreads) s_eq[i] = a.eq[i];
+  __syncthreads();
+  const long long nvec = a.total / 8;
+  const int cvec = a.c / 8;
+  const long long stride = (long long)gridDim.x * kApplyThreads;
+  const uint8_t* zb = static_cast<const uint8_t*>(a.z);
+  uint8_t* yb = static_cast<uint8_t*>(a.y);
+  for (long long v0 = (long long)blockIdx.x * kApplyThreads + threadIdx.x; v0 < nvec;
+       v0 += stride * kApplyUnroll) {
+    uint4 in[kApplyUnroll];
+#pragma unroll
+    for (int k = 0; k < kApplyUnroll; ++k) {
+      const long long v = v0 + k * stride;
+      if (v < nvec) in[k] = ld_global_nc_v4(zb + v * 16);
+    }
+#pragma unroll
+    for (int k = 0; k < kApplyUnroll; ++k) {
+      const long long v = v0 + k * stride;
+      if (v < nvec) {
+        const int c0 = (int)(v % cvec) * 8;
+        const uint32_t w[4] = {in[k].x, in[k].y, in[k].z, in[k].w};
+        uint32_t o[4];
+        uint32_t bits = 0;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const float2 zz = unpack2<BF16>(w[j]);
+          const float p0 = fmaf(zz.x, s_eq[c0 + 2 * j], s_eq[a.c + c0 + 2 * j]);
+          const float p1 = fmaf(zz.y, s_eq[c0 + 2 * j + 1], s_eq[a.c + c0 + 2 * j + 1]);
+          bits |= (p0 > 0.f ? 1u : 0u) << (2 * j);
+          bits |= (p1 > 0.f ? 1u : 0u) << (2 * j + 1);
+          o[j] = pack2<BF16>(fmaxf(p0, 0.f), fmaxf(p1, 0.f));
+        }
+        st_global_v4(yb + v * 16, make_uint4(o[0], o[1], o[2], o[3]));
+        if (MASK) a.mask[v] = (uint8_t)bits;
+      }
+    }
+  }
+}
+
+template <bool BF16, bool MASKBITS>
+__global__ void __launch_bounds__(kRedThreads)
+    bn_bwd_reduce_kernel(const BwdReduceArgs a) {
+  __shared__ __align__(16) float red[kRedThreads * 16];  // reused as fp64 [8][2*c] at the end
+  __shared__ uint32_t ticket;
+  const int c = a.c;
+  const int cvec = c / 8;
+  const long long nvec = a.m_count * cvec;
+  const long long stride = (long long)gridDim.x * kRedThreads;  // multiple of cvec
+  const long long gtid = (long long)blockIdx.x * kRedThreads + threadIdx.x;
+  const int c0 = (int)(gtid % cvec) * 8;
+  float mean[8];
+#pragma unroll
+  for (int e = 0; e < 8; ++e) mean[e] = a.mean[c0 + e];
+  float sg[8], sgx[8];
+#pragma unroll
+  for (int e = 0; e < 8; ++e) sg[e] = sgx[e] = 0.f;
+  const uint8_t* dyb = static_cast<const uint8_t*>(a.dy);
+  const uint8_t* zb = static_cast<const uint8_t*>(a.z);
+  const uint8_t* yb = static_cast<const uint8_t*>(a.y);
+  for (long long v0 = gtid; v0 < nvec; v0 += stride * kRedUnroll) {
+    uint4 dyv[kRedUnroll], zv[kRedUnroll], yv[kRedUnroll];
+    uint32_t mb[kRedUnroll];
+#pragma unroll
+    for (int k = 0; k < kRedUnroll; ++k) {
+      const long long v = v0 + k * stride;
+      if (v < nvec) {
+        dyv[k] = ld_global_nc_v4(dyb + v * 16);
+        zv[k] = ld_global_nc_v4(zb + v * 16);
+        if (MASKBITS) mb[k] = a.mask[v];
+        else yv[k] = ld_global_nc_v4(yb + v * 16);
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < kRedUnroll; ++k) {
+      const long long v = v0 + k * stride;
+      if (v < nvec) {
+        const uint32_t dw[4] = {dyv[k].x, dyv[k].y, dyv[k].z, dyv[k].w};
+        const uint32_t zw[4] = {zv[k].x, zv[k].y, zv[k].z, zv[k].w};
+        uint32_t bits;
+        if (MASKBITS) {
+          bits = mb[k];
+        } else {
+          const uint32_t yw[4] = {yv[k].x, yv[k].y, yv[k].z, yv[k].w};
+          bits = 0;
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const float2 yy = unpack2<BF16>(yw[j]);
+            bits |= (yy.x > 0.f ? 1u : 0u) << (2 * j);
+            bits |= (yy.y > 0.f ? 1u : 0u) << (2 * j + 1);
+          }
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const float2 d = unpack2<BF16>(dw[j]);
+          const float2 z = unpack2<BF16>(zw[j]);
+          const float g0 = (bits >> (2 * j)) & 1u ? d.x : 0.f;
+          const float g1 = (bits >> (2 * j + 1)) & 1u ? d.y : 0.f;
+          sg[2 * j] += g0;
+          sg[2 * j + 1] += g1;
+          sgx[2 * j] = fmaf(g0, z.x - mean[2 * j], sgx[2 * j]);
+          sgx[2 * j + 1] = fmaf(g1, z.y - mean[2 * j + 1], sgx[2 * j + 1]);
+        }
+      }
+    }
+  }
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    red[threadIdx.x * 16 + e] = sg[e];
+    red[threadIdx.x * 16 + 8 + e] = sgx[e];
+  }
+  __syncthreads();
+  // block partial: threads t = grp + k*cvec share channel group grp (fixed summation order)
+  for (int i = threadIdx.x; i < 2 * c; i += kRedThreads) {
+    const int st = i / c, ch = i - st * c;
+    const int grp = ch >> 3, e = ch & 7;
+    float acc = 0.f;
+    for (int t = grp; t < kRedThreads; t += cvec) acc += red[t * 16 + st * 8 + e];
+    a.part[(size_t)blockIdx.x * 2 * c + i] = acc;
+  }
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) ticket = atomicInc(a.ticket, gridDim.x - 1);
+  __syncthreads();
+  if (ticket != gridDim.x - 1) return;
+  // ------------------------------------------------------------ last block: finalize
+  __threadfence();
+  constexpr int kFinWarps = 8;
+  double* dred = reinterpret_cast<double*>(red);  // [kFinWarps][2*c], c <= 256
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nv4 = (2 * c) / 4;
+  if (warp < kFinWarps) {
+    for (int c4 = lane; c4 < nv4; c4 += 32) {
+      double s0 = 0, s1 = 0, s2 = 0, s3 = 0;
+      for (int b = warp; b < (int)gridDim.x; b += kFinWarps) {
+        const float4 v = __ldcg(reinterpret_cast<const float4*>(a.part + (size_t)b * 2 * c) + c4);
+        s0 += v.x;
+        s1 += v.y;
+        s2 += v.z;
+        s3 += v.w;
+      }
+      dred[warp * 2 * c + 4 * c4 + 0] = s0;
+      dred[warp * 2 * c + 4 * c4 + 1] = s1;
+      dred[warp * 2 * c + 4 * c4 + 2] = s2;
+      dred[warp * 2 * c + 4 * c4 + 3] = s3;
+    }
+  }
+  __syncthreads();
+  for (int ch = threadIdx.x; ch < c; ch += kRedThreads) {
+    double g = 0, gx = 0;
+    for (int w = 0; w < kFinWarps; ++w) {
+      g += dred[w * 2 * c + ch];
+      gx += dred[w * 2 * c + c + ch];
+    }
+    const double M = (double)a.m_count;
+    const double inv = a.inv_std[ch];
+    const double dgamma = gx * inv;  // sum g * xhat
+    const double dbeta = g;
+    const double ac = (double)a.gamma[ch] * inv;
+    const double dc = ac * dgamma * inv / M;
+    const double ec = -ac * dbeta / M + dc * (double)a.mean[ch];
+    a.dgamma[ch] = (float)dgamma;
+    a.dbeta[ch] = (float)dbeta;
+    a.coef[ch] = (float)ac;
+    a.coef[c + ch] = (float)dc;
+    a.coef[2 * c + ch] = (float)ec;
+  }
+}
+
+}  // namespace
+
+int launch_apply(const ApplyArgs& a, bool bf16, int num_sms, cudaStream_t st) {
+  if (a.c % 8 != 0 || a.c > 256) return 3;
+  const long long nvec = a.total / 8;
+  const long long want = (nvec + kApplyThreads * kApplyUnroll - 1) / (kApplyThreads * kApplyUnroll);
+  const int grid = (int)std::max<long long>(1, std::min<long long>(want, (long long)num_sms * 8));
+  const bool mask = a.mask != nullptr;
+  if (bf16) {
+    if (mask) bn_apply_relu_kernel<true, true><<<grid, kApplyThreads, 0, st>>>(a);
+    else bn_apply_relu_kernel<true, false><<<grid, kApplyThreads, 0, st>>>(a);
+  } else {
+    if (mask) bn_apply_relu_kernel<false, true><<<grid, kApplyThreads, 0, st>>>(a);
+    else bn_apply_relu_kernel<false, false><<<grid, kApplyThreads, 0, st>>>(a);
+  }
+  return cudaGetLastError() == cudaSuccess ? 0 : 6;
+}
+
+size_t bwd_reduce_partial_floats(int num_sms, int c) { return (size_t)num_sms * 2 * 2 * c; }
+
+int launch_bwd_reduce(const BwdReduceArgs& a, bool bf16, int num_sms, cudaStream_t st) {
+  if (a.c % 8 != 0 || a.c > 256 || (kRedThreads % (a.c / 8)) != 0) return 3;
+  const long long nvec = a.m_count * (a.c / 8);
+  const long long want = (nvec + kRedThreads * kRedUnroll - 1) / (kRedThreads * kRedUnroll);
+  const int grid = (int)std::max<long long>(1, std::min<long long>(want, (long long)num_sms * 2));
+  const bool bits = a.mask != nullptr;
+  if (bf16) {
+    if (bits) bn_bwd_reduce_kernel<true, true><<<grid, kRedThreads, 0, st>>>(a);
+    else bn_bwd_reduce_kernel<true, false><<<grid, kRedThreads, 0, st>>>(a);
+  } else {
+    if (bits) bn_bwd_reduce_kernel<false, true><<<grid, kRedThreads, 0, st>>>(a);
+    else bn_bwd_reduce_kernel<false, false><<<grid, kRedThreads, 0, st>>>(a);
+  }
+  return cudaGetLastError() == cudaSuccess ? 0 : 6;
+}
+
+}  // namespace cbr

@@ -1,0 +1,484 @@
+// C ABI of libcbr.so: argument validation, workspace layout, tensor-map encoding and the
+// ordering of the kernel launches for each public call (declared in include/cbr.h).
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/cbr.h"
+#include "cbr_internal.h"
+
+namespace cbr {
+
+// Device error word: kernels OR failure bits into it instead of trapping.
+__device__ uint32_t g_error_word;
+
+namespace {
+
+constexpr size_t kHdrBytes = 256;    // arrival counters live here
+constexpr int kMaxCtas = 256;        // partial-statistics buffers are sized for this many CTAs
+constexpr int kMaxDevices = 64;
+
+size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+struct DeviceInfo {
+  bool probed = false;
+  bool ok = false;
+  int num_sms = 0;
+  uint32_t* err = nullptr;
+};
+std::mutex g_mu;
+DeviceInfo g_dev[kMaxDevices];
+
+// Returns CBR status; fills *info for the current device.
+int current_device(DeviceInfo** info) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    cudaGetLastError();
+    return CBR_ERR_DEVICE;
+  }
+  std::lock_guard<std::mutex> lk(g_mu);
+  DeviceInfo& d = g_dev[dev];
+  if (!d.probed) {
+    d.probed = true;
+    int major = 0, minor = 0, sms = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+      cudaGetLastError();
+      return CBR_ERR_DEVICE;
+    }
+    void* p = nullptr;
+    if (major == 10 && minor == 3 && cudaGetSymbolAddress(&p, g_error_word) == cudaSuccess) {
+      d.ok = true;
+      d.num_sms = sms < kMaxCtas ? sms : kMaxCtas;
+      d.err = static_cast<uint32_t*>(p);
+    }
+    cudaGetLastError();
+  }
+  if (!d.ok) return CBR_ERR_DEVICE;
+  *info = &d;
+  return CBR_OK;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+// ----------------------------------------------------------------------- profiling hook
+thread_local void* const* t_prof_events = nullptr;
+thread_local int t_prof_count = 0;
+thread_local int t_prof_used = 0;
+
+struct Prof {
+  void* const* ev;
+  int count;
+  int used = 0;
+  cudaStream_t st;
+  Prof(cudaStream_t s) : ev(t_prof_events), count(t_prof_count), st(s) {
+    t_prof_events = nullptr;
+    t_prof_count = 0;
+    mark();
+  }
+  void mark() {
+    if (ev && used < count) cudaEventRecord(static_cast<cudaEvent_t>(ev[used++]), st);
+  }
+  ~Prof() { t_prof_used = used; }
+};
+
+// ----------------------------------------------------------------------- validation helpers
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+struct Shape {
+  long long n, h, w, cin, cout, r, s, stride, pad, p, q, m;
+  bool bf16;
+  size_t elt;
+};
+
+int check_desc(const cbr_desc_t* d, Shape* sh) {
+  if (!d) return CBR_ERR_INVALID_ARG;
+  if (d->n < 1 || d->h < 1 || d->w < 1 || d->c_in < 1 || d->c_out < 1 || d->r < 1 || d->s < 1 ||
+      d->stride < 1 || d->pad < 0)
+    return CBR_ERR_INVALID_ARG;
+  if (d->dtype != CBR_F16 && d->dtype != CBR_BF16) return CBR_ERR_UNSUPPORTED;
+  if (d->c_out % 8 != 0) return CBR_ERR_INVALID_ARG;
+  Shape s;
+  s.n = d->n; s.h = d->h; s.w = d->w; s.cin = d->c_in; s.cout = d->c_out;
+  s.r = d->r; s.s = d->s; s.stride = d->stride; s.pad = d->pad;
+  if (s.h + 2 * s.pad < s.r || s.w + 2 * s.pad < s.s) return CBR_ERR_INVALID_ARG;
+  s.p = (s.h + 2 * s.pad - s.r) / s.stride + 1;
+  s.q = (s.w + 2 * s.pad - s.s) / s.stride + 1;
+  s.m = s.n * s.p * s.q;
+  if (s.m < 2) return CBR_ERR_INVALID_ARG;
+  s.bf16 = d->dtype == CBR_BF16;
+  s.elt = 2;
+  *sh = s;
+  return CBR_OK;
+}
+
+bool is_first_layer(const Shape& s) { return s.cin == 3; }
+
+// Shapes this build runs on the device.
+int check_supported(const Shape& s) {
+  if (!(s.cout == 16 || s.cout == 32 || s.cout == 64 || s.cout == 128)) return CBR_ERR_UNSUPPORTED;
+  if (is_first_layer(s)) return CBR_ERR_UNSUPPORTED;  // first-layer kernels not built yet
+  if (s.stride != 1) return CBR_ERR_UNSUPPORTED;
+  if (s.cin % 8 != 0 || s.cin > 128) return CBR_ERR_UNSUPPORTED;
+  if (s.w + 2 * s.pad > 256) return CBR_ERR_UNSUPPORTED;
+  return CBR_OK;
+}
+
+size_t act_bytes(long long n, long long h, long long w, long long c, size_t elt) {
+  return (size_t)n * h * w * c * elt;
+}
+
+// Workspace layouts (offsets from ws).
+struct FwdWs {
+  size_t eq, part, z, total;
+};
+FwdWs fwd_ws(const Shape& s, bool need_z) {
+  FwdWs L;
+  L.eq = kHdrBytes;
+  L.part = align_up(L.eq + 2 * s.cout * sizeof(float), 256);
+  L.z = align_up(L.part + fprop_partial_floats(kMaxCtas, (int)s.cout) * sizeof(float), 256);
+  L.total = need_z ? align_up(L.z + act_bytes(s.n, s.p, s.q, s.cout, s.elt), 256) : L.z;
+  return L;
+}
+struct BwdWs {
+  size_t coef, part, wpart, z, total;
+};
+BwdWs bwd_ws(const Shape& s, bool need_z) {
+  BwdWs L;
+  L.coef = kHdrBytes;
+  L.part = align_up(L.coef + 3 * s.cout * sizeof(float), 256);
+  L.wpart = align_up(L.part + bwd_reduce_partial_floats(kMaxCtas, (int)s.cout) * sizeof(float), 256);
+  L.z = align_up(L.wpart + wgrad_partial_floats(kMaxCtas, (int)s.cin, (int)s.cout, (int)(s.r * s.s)) * sizeof(float), 256);
+  L.total = need_z ? align_up(L.z + act_bytes(s.n, s.p, s.q, s.cout, s.elt), 256) : L.z;
+  return L;
+}
+
+bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
+  const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+  return x < y + nb && y < x + na;
+}
+
+HaloGeom make_geom(const Shape& s) {
+  HaloGeom g{};
+  g.n_img = (int)s.n;
+  g.h = (int)s.h;
+  g.w = (int)s.w;
+  g.r = (int)s.r;
+  g.s = (int)s.s;
+  g.pad = (int)s.pad;
+  return g;
+}
+
+}  // namespace
+
+bool encode_tiled(CUtensorMap* map, CUtensorMapDataType dt, int rank, const void* base,
+                  const uint64_t* dims, const uint64_t* strides_bytes, const uint32_t* box) {
+  std::call_once(g_encode_once, [] {
+    cudaDriverEntryPointQueryResult q;
+    void* fn = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    cudaGetLastError();
+  });
+  if (!g_encode) return false;
+  cuuint64_t d[5], st[4];
+  cuuint32_t b[5], es[5];
+  for (int i = 0; i < rank; ++i) {
+    d[i] = dims[i];
+    b[i] = box[i];
+    es[i] = 1;
+    if (i + 1 < rank) st[i] = strides_bytes[i];
+  }
+  return g_encode(map, dt, (cuuint32_t)rank, const_cast<void*>(base), d, st, b, es,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int launch_fold(const void* w, const float* conv_bias, const float* gamma, const float* beta,
+                const float* rm, const float* rv, float eps, void* w_fold, float* b_fold, int cout,
+                int rsc, bool bf16, cudaStream_t st);
+
+}  // namespace cbr
+
+using namespace cbr;
+
+extern "C" {
+
+int32_t cbr_version(void) { return 100; }
+
+const char* cbr_status_string(cbr_status_t s) {
+  switch (s) {
+    case CBR_OK: return "CBR_OK";
+    case CBR_ERR_INVALID_ARG: return "CBR_ERR_INVALID_ARG";
+    case CBR_ERR_MISALIGNED: return "CBR_ERR_MISALIGNED";
+    case CBR_ERR_UNSUPPORTED: return "CBR_ERR_UNSUPPORTED";
+    case CBR_ERR_WORKSPACE: return "CBR_ERR_WORKSPACE";
+    case CBR_ERR_DEVICE: return "CBR_ERR_DEVICE";
+    case CBR_ERR_CUDA: return "CBR_ERR_CUDA";
+    case CBR_ERR_TIMEOUT: return "CBR_ERR_TIMEOUT";
+  }
+  return "CBR_ERR_UNKNOWN";
+}
+
+cbr_status_t cbr_workspace_size(const cbr_desc_t* desc, size_t* fwd_bytes, size_t* bwd_bytes) {
+  Shape s;
+  int st = check_desc(desc, &s);
+  if (st) return (cbr_status_t)st;
+  if (fwd_bytes) *fwd_bytes = fwd_ws(s, true).total;
+  if (bwd_bytes) *bwd_bytes = bwd_ws(s, true).total;
+  return CBR_OK;
+}
+
+cbr_status_t cbr_forward_train(const cbr_desc_t* desc, const void* x, const void* w,
+                               const float* gamma, const float* beta, float* running_mean,
+                               float* running_var, float momentum, float eps, void* y,
+                               uint32_t* relu_mask, void* z_saved, float* saved_mean,
+                               float* saved_inv_var, void* ws, size_t ws_bytes,
+                               cbr_stream_t stream) {
+  Shape s;
+  int st = check_desc(desc, &s);
+  if (st) return (cbr_status_t)st;
+  if (!x || !w || !gamma || !beta || !running_mean || !running_var || !y || !saved_mean ||
+      !saved_inv_var || !ws)
+    return CBR_ERR_INVALID_ARG;
+  if (!(momentum >= 0.f && momentum <= 1.f) || !(eps > 0.f) || !std::isfinite(eps))
+    return CBR_ERR_INVALID_ARG;
+  if (!aligned(x, 16) || !aligned(w, 16) || !aligned(y, 16) || !aligned(ws, 16) ||
+      (z_saved && !aligned(z_saved, 16)) || (relu_mask && !aligned(relu_mask, 4)) ||
+      !aligned(gamma, 4) || !aligned(beta, 4) || !aligned(running_mean, 4) ||
+      !aligned(running_var, 4) || !aligned(saved_mean, 4) || !aligned(saved_inv_var, 4))
+    return CBR_ERR_MISALIGNED;
+  if ((st = check_supported(s))) return (cbr_status_t)st;
+  const FwdWs L = fwd_ws(s, z_saved == nullptr);
+  if (ws_bytes < L.total) return CBR_ERR_WORKSPACE;
+  DeviceInfo* dev = nullptr;
+  if ((st = current_device(&dev))) return (cbr_status_t)st;
+
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  uint8_t* wsb = static_cast<uint8_t*>(ws);
+  void* z = z_saved ? z_saved : wsb + L.z;
+  Prof prof(cs);
+
+  FpropArgs a{};
+  a.g = make_geom(s);
+  a.z = z;
+  a.part = reinterpret_cast<float*>(wsb + L.part);
+  a.ticket = reinterpret_cast<uint32_t*>(wsb);
+  a.gamma = gamma;
+  a.beta = beta;
+  a.running_mean = running_mean;
+  a.running_var = running_var;
+  a.saved_mean = saved_mean;
+  a.saved_inv_var = saved_inv_var;
+  a.eq = reinterpret_cast<float*>(wsb + L.eq);
+  a.momentum = momentum;
+  a.eps = eps;
+  a.m_count = s.m;
+  a.err = dev->err;
+  a.mode = kFpropStats;
+  st = launch_fprop(a, (int)s.cin, (int)s.cout, s.bf16, x, w, dev->num_sms, cs);
+  if (st) return (cbr_status_t)st;
+  prof.mark();
+
+  ApplyArgs ap{};
+  ap.z = z;
+  ap.y = y;
+  ap.mask = reinterpret_cast<uint8_t*>(relu_mask);
+  ap.eq = a.eq;
+  ap.total = s.m * s.cout;
+  ap.c = (int)s.cout;
+  st = launch_apply(ap, s.bf16, dev->num_sms, cs);
+  if (st) return (cbr_status_t)st;
+  prof.mark();
+  return CBR_OK;
+}
+
+cbr_status_t cbr_backward(const cbr_desc_t* desc, const void* dy, const void* x, const void* w,
+                          const void* y_or_relu_mask, int32_t mask_kind, const void* z_saved,
+                          const float* gamma, const float* saved_mean,
+                          const float* saved_inv_var, void* dx, float* dw, float* dgamma,
+                          float* dbeta, void* ws, size_t ws_bytes, cbr_stream_t stream) {
+  Shape s;
+  int st = check_desc(desc, &s);
+  if (st) return (cbr_status_t)st;
+  if (!dy || !x || !w || !y_or_relu_mask || !gamma || !saved_mean || !saved_inv_var || !dw ||
+      !dgamma || !dbeta || !ws)
+    return CBR_ERR_INVALID_ARG;
+  if (mask_kind != CBR_MASK_BITS && mask_kind != CBR_MASK_FROM_Y) return CBR_ERR_INVALID_ARG;
+  if (dx && overlaps(dx, act_bytes(s.n, s.h, s.w, s.cin, s.elt), x,
+                     act_bytes(s.n, s.h, s.w, s.cin, s.elt)))
+    return CBR_ERR_INVALID_ARG;
+  if (!aligned(dy, 16) || !aligned(x, 16) || !aligned(w, 16) || !aligned(ws, 16) ||
+      (dx && !aligned(dx, 16)) || (z_saved && !aligned(z_saved, 16)) ||
+      !aligned(y_or_relu_mask, mask_kind == CBR_MASK_FROM_Y ? 16 : 4) || !aligned(dw, 16) ||
+      !aligned(gamma, 4) || !aligned(saved_mean, 4) || !aligned(saved_inv_var, 4) ||
+      !aligned(dgamma, 4) || !aligned(dbeta, 4))
+    return CBR_ERR_MISALIGNED;
+  if ((st = check_supported(s))) return (cbr_status_t)st;
+  const BwdWs L = bwd_ws(s, z_saved == nullptr);
+  if (ws_bytes < L.total) return CBR_ERR_WORKSPACE;
+  DeviceInfo* dev = nullptr;
+  if ((st = current_device(&dev))) return (cbr_status_t)st;
+
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  uint8_t* wsb = static_cast<uint8_t*>(ws);
+  Prof prof(cs);
+  const void* z = z_saved;
+  if (!z) {
+    // recompute z = conv(x, W) (no statistics)
+    FpropArgs a{};
+    a.g = make_geom(s);
+    a.z = wsb + L.z;
+    a.m_count = s.m;
+    a.err = dev->err;
+    a.mode = kFpropPlain;
+    st = launch_fprop(a, (int)s.cin, (int)s.cout, s.bf16, x, w, dev->num_sms, cs);
+    if (st) return (cbr_status_t)st;
+    prof.mark();
+    z = wsb + L.z;
+  }
+  const uint8_t* mask = mask_kind == CBR_MASK_BITS ? static_cast<const uint8_t*>(y_or_relu_mask) : nullptr;
+  const void* yv = mask_kind == CBR_MASK_FROM_Y ? y_or_relu_mask : nullptr;
+  float* coef = reinterpret_cast<float*>(wsb + L.coef);
+
+  BwdReduceArgs b{};
+  b.dy = dy;
+  b.z = z;
+  b.y = yv;
+  b.mask = mask;
+  b.gamma = gamma;
+  b.mean = saved_mean;
+  b.inv_std = saved_inv_var;
+  b.dgamma = dgamma;
+  b.dbeta = dbeta;
+  b.coef = coef;
+  b.part = reinterpret_cast<float*>(wsb + L.part);
+  b.ticket = reinterpret_cast<uint32_t*>(wsb) + 1;
+  b.m_count = s.m;
+  b.c = (int)s.cout;
+  b.err = dev->err;
+  st = launch_bwd_reduce(b, s.bf16, dev->num_sms, cs);
+  if (st) return (cbr_status_t)st;
+  prof.mark();
+
+  // WGrad first, then DGrad (CBR page, section 5.2 orders DGrad after WGrad because its dX
+  // overwrote X there; here dx may not alias x, so the order is only kept for familiarity).
+  WgradArgs wa{};
+  wa.g = make_geom(s);
+  wa.dy = dy;
+  wa.z = z;
+  wa.y = yv;
+  wa.mask = mask;
+  wa.coef = coef;
+  wa.part = reinterpret_cast<float*>(wsb + L.wpart);
+  wa.dw = dw;
+  wa.err = dev->err;
+  st = launch_wgrad(wa, (int)s.cin, (int)s.cout, s.bf16, x, dev->num_sms, cs);
+  if (st) return (cbr_status_t)st;
+  prof.mark();
+
+  if (dx) {
+    DgradArgs da{};
+    // dgrad = stride-1 conv of dz (P x Q, cout channels) with the flipped filter, pad R-1-pad
+    da.g.n_img = (int)s.n;
+    da.g.h = (int)s.p;
+    da.g.w = (int)s.q;
+    da.g.r = (int)s.r;
+    da.g.s = (int)s.s;
+    da.g.pad = (int)(s.r - 1 - s.pad);
+    da.dy = dy;
+    da.z = z;
+    da.y = yv;
+    da.mask = mask;
+    da.coef = coef;
+    da.dx = dx;
+    da.err = dev->err;
+    if (s.r - 1 - s.pad < 0 || s.s - 1 - s.pad < 0 || s.r != s.s) return CBR_ERR_UNSUPPORTED;
+    st = launch_dgrad(da, (int)s.cin, (int)s.cout, s.bf16, w, dev->num_sms, cs);
+    if (st) return (cbr_status_t)st;
+    prof.mark();
+  }
+  return CBR_OK;
+}
+
+cbr_status_t cbr_fold_bn(const cbr_desc_t* desc, const void* w, const float* conv_bias,
+                         const float* gamma, const float* beta, const float* running_mean,
+                         const float* running_var, float eps, void* w_fold, float* b_fold,
+                         cbr_stream_t stream) {
+  Shape s;
+  int st = check_desc(desc, &s);
+  if (st) return (cbr_status_t)st;
+  if (!w || !gamma || !beta || !running_mean || !running_var || !w_fold || !b_fold)
+    return CBR_ERR_INVALID_ARG;
+  if (!(eps > 0.f) || !std::isfinite(eps)) return CBR_ERR_INVALID_ARG;
+  if (!aligned(w, 16) || !aligned(w_fold, 16) || !aligned(gamma, 4) || !aligned(beta, 4) ||
+      !aligned(running_mean, 4) || !aligned(running_var, 4) || !aligned(b_fold, 4) ||
+      (conv_bias && !aligned(conv_bias, 4)))
+    return CBR_ERR_MISALIGNED;
+  DeviceInfo* dev = nullptr;
+  if ((st = current_device(&dev))) return (cbr_status_t)st;
+  return (cbr_status_t)launch_fold(w, conv_bias, gamma, beta, running_mean, running_var, eps,
+                                   w_fold, b_fold, (int)s.cout, (int)(s.r * s.s * s.cin), s.bf16,
+                                   reinterpret_cast<cudaStream_t>(stream));
+}
+
+cbr_status_t cbr_forward_infer(const cbr_desc_t* desc, const void* x, const void* w_fold,
+                               const float* b_fold, void* y, cbr_stream_t stream) {
+  Shape s;
+  int st = check_desc(desc, &s);
+  if (st) return (cbr_status_t)st;
+  if (!x || !w_fold || !b_fold || !y) return CBR_ERR_INVALID_ARG;
+  if (!aligned(x, 16) || !aligned(w_fold, 16) || !aligned(y, 16) || !aligned(b_fold, 4))
+    return CBR_ERR_MISALIGNED;
+  if ((st = check_supported(s))) return (cbr_status_t)st;
+  DeviceInfo* dev = nullptr;
+  if ((st = current_device(&dev))) return (cbr_status_t)st;
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  Prof prof(cs);
+  FpropArgs a{};
+  a.g = make_geom(s);
+  a.z = y;
+  a.bias = b_fold;
+  a.m_count = s.m;
+  a.err = dev->err;
+  a.mode = kFpropBiasRelu;
+  st = launch_fprop(a, (int)s.cin, (int)s.cout, s.bf16, x, w_fold, dev->num_sms, cs);
+  if (st) return (cbr_status_t)st;
+  prof.mark();
+  return CBR_OK;
+}
+
+cbr_status_t cbr_stream_status(cbr_stream_t stream) {
+  DeviceInfo* dev = nullptr;
+  int st = current_device(&dev);
+  if (st) return (cbr_status_t)st;
+  if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) {
+    cudaGetLastError();
+    return CBR_ERR_CUDA;
+  }
+  uint32_t word = 0;
+  if (cudaMemcpyFromSymbol(&word, g_error_word, sizeof(word)) != cudaSuccess) return CBR_ERR_CUDA;
+  if (word) {
+    const uint32_t zero = 0;
+    cudaMemcpyToSymbol(g_error_word, &zero, sizeof(zero));
+    return CBR_ERR_TIMEOUT;
+  }
+  return CBR_OK;
+}
+
+cbr_status_t cbr_profile_next_call(void* const* events, int32_t count) {
+  if (events && count <= 0) return CBR_ERR_INVALID_ARG;
+  t_prof_events = events;
+  t_prof_count = events ? count : 0;
+  return CBR_OK;
+}
+
+int32_t cbr_profile_last_count(void) { return t_prof_used; }
+
+}  // extern "C"

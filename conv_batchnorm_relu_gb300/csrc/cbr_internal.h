@@ -1,0 +1,130 @@
+// Host-side interface between the C ABI (cbr_api.cu) and the kernel launchers.
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstddef>
+#include <cstdint>
+
+namespace cbr {
+
+// Geometry of a stride-1 convolution computed over "padded-linear" rows.
+//
+// Output pixel (p, q) of image n is row m = p*wp + q of a per-image row space whose width is
+// the padded input width wp = w + 2*pad; the wp - q_out columns past the last output column
+// are computed and discarded.  In that space, filter tap (r, s) of output row m reads row
+// m + r*wp + s of the zero-padded input, so each tap is the same contiguous slab of a halo
+// tile shifted by r*wp + s rows.  A work unit is `um` consecutive rows of one image; its halo
+// is `hr` input rows (wp wide) starting at input row floor(m0/wp) - pad.
+struct HaloGeom {
+  int n_img, h, w;   // conv input (NHWC)
+  int p, q;          // conv output rows / cols
+  int r, s, pad;     // filter taps; stride 1
+  int wp;            // padded width
+  int hr;            // halo rows per unit
+  int um;            // output rows per unit (U * 128)
+  int upi;           // units per image
+  int total_units;
+};
+
+struct FpropArgs {
+  HaloGeom g;
+  void* z;                  // [n][p][q][cout] conv output (storage dtype)
+  float* part;              // [grid][2][cout] per-CTA sum / sum of squares
+  uint32_t* ticket;         // wrap-around arrival counter (must start at 0)
+  const float* gamma;
+  const float* beta;
+  float* running_mean;
+  float* running_var;
+  float* saved_mean;
+  float* saved_inv_var;
+  float* eq;                // [2][cout] eq_scale, eq_bias for the apply pass
+  const float* bias;        // inference: per-channel bias added before ReLU
+  float momentum;
+  float eps;
+  long long m_count;        // n*p*q
+  uint32_t* err;            // device error word
+  int mode;                 // FpropMode
+};
+
+enum FpropMode : int {
+  kFpropStats = 0,   // z + per-channel statistics + finalize (training forward)
+  kFpropPlain = 1,   // z only (recompute for backward)
+  kFpropBiasRelu = 2 // y = relu(conv + bias) (folded inference)
+};
+
+// Returns cudaSuccess or an error; `status` receives a CBR status code on validation issues.
+struct LaunchResult {
+  int status;        // cbr_status_t
+  cudaError_t cuda;
+};
+
+// Tensor-map helpers (cbr_api.cu).
+bool encode_tiled(CUtensorMap* map, CUtensorMapDataType dt, int rank, const void* base,
+                  const uint64_t* dims, const uint64_t* strides_bytes, const uint32_t* box);
+
+// Launchers (one per kernel family).  Each validates only what its kernel needs beyond the
+// C-ABI checks and returns a CBR status.
+int launch_fprop(const FpropArgs& a, int c_in, int c_out, bool bf16, const void* x,
+                 const void* w, int num_sms, cudaStream_t st);
+size_t fprop_partial_floats(int num_sms, int c_out);
+
+struct ApplyArgs {
+  const void* z;
+  void* y;
+  uint8_t* mask;            // bit-packed, bit i of byte j <-> element 8j+i; may be null
+  const float* eq;          // [2][c]
+  long long total;          // elements
+  int c;
+};
+int launch_apply(const ApplyArgs& a, bool bf16, int num_sms, cudaStream_t st);
+
+struct BwdReduceArgs {
+  const void* dy;
+  const void* z;
+  const void* y;            // mask source when mask == null (y > 0)
+  const uint8_t* mask;      // bit-packed mask or null
+  const float* gamma;
+  const float* mean;
+  const float* inv_std;
+  float* dgamma;
+  float* dbeta;
+  float* coef;              // [3][c]: a, d, e with dz = a*g - d*z + e
+  float* part;              // [grid][2][c]
+  uint32_t* ticket;
+  long long m_count;
+  int c;
+  uint32_t* err;
+};
+int launch_bwd_reduce(const BwdReduceArgs& a, bool bf16, int num_sms, cudaStream_t st);
+size_t bwd_reduce_partial_floats(int num_sms, int c);
+
+struct DgradArgs {
+  HaloGeom g;               // geometry of the dgrad conv: input = dz (P x Q), output = dx
+  const void* dy;
+  const void* z;
+  const void* y;
+  const uint8_t* mask;
+  const float* coef;
+  void* dx;
+  uint32_t* err;
+};
+int launch_dgrad(const DgradArgs& a, int c_in, int c_out, bool bf16, const void* w, int num_sms,
+                 cudaStream_t st);
+
+struct WgradArgs {
+  HaloGeom g;               // geometry of the forward conv
+  const void* dy;
+  const void* z;
+  const void* y;
+  const uint8_t* mask;
+  const float* coef;
+  float* part;              // [grid][taps*cin][cout] per-CTA partial dW
+  float* dw;                // [cout][r][s][cin]
+  uint32_t* err;
+};
+int launch_wgrad(const WgradArgs& a, int c_in, int c_out, bool bf16, const void* x, int num_sms,
+                 cudaStream_t st);
+size_t wgrad_partial_floats(int num_sms, int c_in, int c_out, int taps);
+
+}  // namespace cbr

@@ -1,0 +1,179 @@
+/*
+ * cbr.h -- C ABI of libcbr.so: the training-mode Conv2d -> BatchNorm -> ReLU (CBR) operator
+ * on NVIDIA GB300 (sm_103a), forward, backward and folded inference.
+ *
+ * What is computed (all citations are to the source pages, by title and section):
+ *   z      = conv(x, W)          cross-correlation, no bias, dilation 1
+ *                                ("CBR fused operator" (Tech-Renaissance), section 4.1;
+ *                                 "TileLang Conv2D+ReLU fusion", basic convolution section)
+ *   mean, var over the M = N*P*Q rows of each output channel (biased var for normalising)
+ *   inv_std = 1/sqrt(var + eps)
+ *   y      = max(0, gamma*(z - mean)*inv_std + beta)        (CBR page, sections 4.2-4.3)
+ *   mask   = (gamma*(z - mean)*inv_std + beta > 0), one bit per element (section 4.3, CMP_GT)
+ *   running_mean <- (1-momentum)*running_mean + momentum*mean
+ *   running_var  <- (1-momentum)*running_var  + momentum*var*M/(M-1)   (unbiased)
+ *                                (CBR page section 4.2; "BatchNorm CUDA implementation",
+ *                                 section 2.4)
+ *   backward: g = dy*mask; dbeta = sum g; dgamma = sum g*xhat;
+ *             dz = gamma*inv_std*(g - dbeta/M - xhat*dgamma/M);  dW = wgrad(dz, x);
+ *             dx = dgrad(dz, W)   (CBR page sections 5.1-5.3; BatchNorm page section 3.1)
+ *   inference: W_fold = W*gamma/sqrt(rv+eps), b_fold = (b - rm)*gamma/sqrt(rv+eps) + beta,
+ *             y = relu(conv(x, W_fold) + b_fold)   (CBR page sections 2 and 6;
+ *                                                    BatchNorm page section 4.4)
+ *
+ * Layouts (CBR page, section 8): activations NHWC, filters KRSC ([Cout][R][S][Cin]), both in
+ * the storage dtype (fp16 or bf16).  gamma, beta, statistics and dW are fp32.  Output size
+ * P = (H + 2*pad - R)/stride + 1, Q likewise.
+ *
+ * Conventions for every call:
+ *   - The caller owns every buffer; pointers are device pointers unless stated otherwise.
+ *     The library allocates no device memory on any call.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy default stream).
+ *     A returned CBR_OK means the work was validated and enqueued.  Device-side failures
+ *     (a bounded wait that ran out) are reported by cbr_stream_status().
+ *   - Arguments are validated on the host before anything is enqueued; on any error nothing
+ *     is launched and no output is touched.
+ *   - Activation / filter / workspace pointers must be 16-byte aligned, fp32 vectors 4-byte.
+ *   - No call throws; the library holds no per-call state.
+ *   - Supported shapes (else CBR_ERR_UNSUPPORTED): Cout in {16, 32, 64, 128}; and either
+ *     stride 1 with Cin a multiple of 8, Cin <= 128, W + 2*pad <= 256; or the first-layer
+ *     form Cin = 3 (any stride, R*S*3 <= 160).  Cout % 8 != 0 is CBR_ERR_INVALID_ARG
+ *     (CBR page, section 8: output channels must be a multiple of 8).
+ */
+#ifndef CBR_H_
+#define CBR_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+struct CUstream_st;
+typedef struct CUstream_st* cbr_stream_t; /* identical to cudaStream_t */
+
+typedef enum {
+  CBR_OK = 0,
+  CBR_ERR_INVALID_ARG = 1, /* null pointer, bad shape, bad scalar, dx aliases x, M < 2 */
+  CBR_ERR_MISALIGNED = 2,  /* pointer alignment rule violated */
+  CBR_ERR_UNSUPPORTED = 3, /* valid arguments outside the shapes/dtypes this build runs */
+  CBR_ERR_WORKSPACE = 4,   /* ws_bytes smaller than cbr_workspace_size() requires */
+  CBR_ERR_DEVICE = 5,      /* no CUDA device, or the current device is not compute 10.3 */
+  CBR_ERR_CUDA = 6,        /* a CUDA runtime / driver call failed */
+  CBR_ERR_TIMEOUT = 7      /* (cbr_stream_status) a kernel gave up on a bounded wait */
+} cbr_status_t;
+
+typedef enum { CBR_F16 = 0, CBR_BF16 = 1 } cbr_dtype_t;
+
+/* Source of the ReLU mask for cbr_backward. */
+typedef enum {
+  CBR_MASK_BITS = 0,  /* bit-packed mask written by cbr_forward_train */
+  CBR_MASK_FROM_Y = 1 /* recompute the mask as y > 0 from the forward output y */
+} cbr_mask_kind_t;
+
+/* One CBR layer.  dtype is a cbr_dtype_t. */
+typedef struct {
+  int32_t n, h, w, c_in, c_out, r, s, stride, pad;
+  int32_t dtype;
+} cbr_desc_t;
+
+/* Version of this ABI (major*100 + minor). */
+int32_t cbr_version(void);
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char* cbr_status_string(cbr_status_t status);
+
+/*
+ * Workspace bytes needed by cbr_forward_train (fwd_bytes) and cbr_backward (bwd_bytes) for
+ * `desc`, assuming the caller passes z_saved = NULL (the largest case; with z_saved the calls
+ * need less, and check the actual need).  Pure host computation; either output may be NULL.
+ * The first 256 bytes of a workspace hold arrival counters: they must be zero the first
+ * time a workspace is used (e.g. allocate it zero-filled); every call leaves them at zero.
+ */
+cbr_status_t cbr_workspace_size(const cbr_desc_t* desc, size_t* fwd_bytes, size_t* bwd_bytes);
+
+/*
+ * Training forward (CBR page, sections 4.1-4.3).
+ *   x [n][h][w][c_in], w [c_out][r][s][c_in]          storage dtype, read only
+ *   gamma, beta [c_out]                                fp32, read only
+ *   running_mean, running_var [c_out]                  fp32, updated in place
+ *   momentum in [0,1] (weight of the new batch), eps > 0
+ *   y [n][p][q][c_out]                                 storage dtype, written
+ *   relu_mask: ceil(n*p*q*c_out/32) uint32 words or NULL; bit i of word j is the mask of
+ *              NHWC element 32*j + i (bits past the last element are unspecified)
+ *   z_saved [n][p][q][c_out] or NULL: receives the conv output; pass it to cbr_backward to
+ *              avoid recomputing the convolution there
+ *   saved_mean, saved_inv_var [c_out]                  fp32 batch mean and 1/sqrt(var+eps)
+ *   ws, ws_bytes                                       workspace (see cbr_workspace_size)
+ * Errors: INVALID_ARG (null required pointer, bad desc, momentum/eps out of range,
+ * n*p*q < 2), MISALIGNED, UNSUPPORTED, WORKSPACE, DEVICE, CUDA.
+ */
+cbr_status_t cbr_forward_train(const cbr_desc_t* desc, const void* x, const void* w,
+                               const float* gamma, const float* beta, float* running_mean,
+                               float* running_var, float momentum, float eps, void* y,
+                               uint32_t* relu_mask, void* z_saved, float* saved_mean,
+                               float* saved_inv_var, void* ws, size_t ws_bytes,
+                               cbr_stream_t stream);
+
+/*
+ * Training backward (CBR page, sections 5.1-5.3; BatchNorm page, section 3.1).
+ *   dy [n][p][q][c_out]            upstream gradient, storage dtype
+ *   x, w                           the forward's inputs
+ *   y_or_relu_mask, mask_kind      the forward's relu_mask words (CBR_MASK_BITS) or its y
+ *                                  (CBR_MASK_FROM_Y)
+ *   z_saved                        the forward's z_saved, or NULL to recompute conv(x, W)
+ *   gamma, saved_mean, saved_inv_var   fp32 [c_out] (saved_* from cbr_forward_train)
+ *   dx [n][h][w][c_in] or NULL     NULL = first layer: the data gradient is skipped
+ *                                  (CBR page, section 5.3).  dx must not overlap x
+ *                                  (section 5.2's write-after-read hazard): INVALID_ARG.
+ *   dw [c_out][r][s][c_in]         fp32, written
+ *   dgamma, dbeta [c_out]          fp32, written
+ */
+cbr_status_t cbr_backward(const cbr_desc_t* desc, const void* dy, const void* x, const void* w,
+                          const void* y_or_relu_mask, int32_t mask_kind, const void* z_saved,
+                          const float* gamma, const float* saved_mean,
+                          const float* saved_inv_var, void* dx, float* dw, float* dgamma,
+                          float* dbeta, void* ws, size_t ws_bytes, cbr_stream_t stream);
+
+/*
+ * BN folding for inference (CBR page, section 2; BatchNorm page, section 4.4):
+ *   w_fold[k,...] = w[k,...]*gamma[k]/sqrt(running_var[k]+eps)   (computed in fp32, stored
+ *                   rounded to the storage dtype, same layout as w)
+ *   b_fold[k]     = (conv_bias[k] - running_mean[k])*gamma[k]/sqrt(running_var[k]+eps)
+ *                   + beta[k]                                    (fp32; conv_bias may be NULL)
+ */
+cbr_status_t cbr_fold_bn(const cbr_desc_t* desc, const void* w, const float* conv_bias,
+                         const float* gamma, const float* beta, const float* running_mean,
+                         const float* running_var, float eps, void* w_fold, float* b_fold,
+                         cbr_stream_t stream);
+
+/*
+ * Folded inference forward (CBR page, section 6): y = relu(conv(x, w_fold) + b_fold), with
+ * the bias and ReLU applied to the fp32 accumulator before rounding.
+ */
+cbr_status_t cbr_forward_infer(const cbr_desc_t* desc, const void* x, const void* w_fold,
+                               const float* b_fold, void* y, cbr_stream_t stream);
+
+/*
+ * Synchronise `stream`, then read and clear the device error word of the current device.
+ * Returns CBR_OK, CBR_ERR_TIMEOUT if a kernel abandoned a bounded wait (its outputs are then
+ * undefined), or CBR_ERR_CUDA if the stream reports a CUDA error.
+ */
+cbr_status_t cbr_stream_status(cbr_stream_t stream);
+
+/*
+ * Profiling hook for the calling host thread.  When `events` is non-NULL, the next
+ * cbr_forward_train / cbr_backward / cbr_forward_infer call records events[0] before its
+ * first kernel and events[i] after its i-th kernel (cudaEvent_t handles owned by the caller,
+ * at most `count`), then clears the hook.  cbr_profile_last_count() returns how many events
+ * that call recorded.  Used to time each kernel inside the real calls.
+ */
+cbr_status_t cbr_profile_next_call(void* const* events, int32_t count);
+int32_t cbr_profile_last_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* CBR_H_ */

@@ -1,0 +1,89 @@
+"""GPU parity of the training forward (conv + genstats + finalize + apply/ReLU/mask) and of the
+folded inference path against the fp64 CPU oracle, through the C ABI."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from conv_batchnorm_relu_gb300 import cbr
+from conv_batchnorm_relu_gb300.inputs import CONFIGS, CBRSpec, make_inputs
+from parity import mask_ok, max_err_ok, oracle_inputs, rel_close, stat_close, to_np, unpack_mask
+
+pytestmark = pytest.mark.gpu
+
+CASES = {
+    "cfg1": (CONFIGS[1], 1235),
+    "n3_56_64": (CONFIGS[3].with_(n=3), 2001),
+    "ragged_13x29": (CBRSpec("ragged", n=2, h=13, w=29, c_in=64, c_out=64), 2002),
+    "cin16_cout32_bf16": (CBRSpec("small bf16", n=5, h=9, w=9, c_in=16, c_out=32, dtype="bf16"), 2003),
+    "c128_bf16": (CBRSpec("c128", n=2, h=24, w=24, c_in=128, c_out=128, dtype="bf16"), 2004),
+    "c128_f16_odd": (CBRSpec("c128 odd", n=1, h=17, w=30, c_in=128, c_out=128), 2005),
+    "k1x1": (CBRSpec("1x1", n=2, h=20, w=20, c_in=64, c_out=64, r=1, s=1, pad=0), 2006),
+    "k5x5": (CBRSpec("5x5", n=2, h=16, w=16, c_in=32, c_out=64, r=5, s=5, pad=2), 2007),
+    "cfg2": (CONFIGS[2], 1236),
+}
+
+
+def run_forward(spec, seed, save_z=True):
+    inp = make_inputs(spec, seed, with_dy=False)
+    layer = cbr.Layer.from_spec(spec)
+    g = {k: v.cuda() for k, v in inp.items()}
+    fwd_ws, _ = cbr.workspace_size(layer)
+    ws = cbr.new_workspace(fwd_ws)
+    out = cbr.forward_train(layer, g["x"], g["w"], g["gamma"], g["beta"], g["running_mean"],
+                            g["running_var"], spec.momentum, spec.eps, ws=ws, save_z=save_z)
+    cbr.stream_status()
+    return inp, g, out
+
+
+@pytest.mark.parametrize("case", list(CASES))
+def test_forward_train_parity(case):
+    spec, seed = CASES[case]
+    inp, g, out = run_forward(spec, seed)
+    o = oracle_inputs(inp)
+    ref = oracle.forward_train(o["x"], o["w"], o["gamma"], o["beta"], o["running_mean"],
+                               o["running_var"], spec.momentum, spec.eps, spec.stride, spec.pad)
+    max_err_ok(to_np(out["z"]), ref["z"], "z")
+    max_err_ok(to_np(out["y"]), ref["y"], "y")
+    sd = np.sqrt(ref["var"])
+    stat_close(to_np(out["saved_mean"]), ref["mean"], sd, "saved_mean")
+    rel_close(to_np(out["saved_inv_var"]), ref["inv_std"], "saved_inv_var")
+    stat_close(to_np(g["running_mean"]), ref["running_mean"], spec.momentum * sd, "running_mean")
+    rel_close(to_np(g["running_var"]), ref["running_var"], "running_var")
+    mask_ok(unpack_mask(out["mask"], spec.m * spec.c_out), ref["pre"])
+
+
+def test_forward_without_z_saved_matches():
+    spec, seed = CASES["ragged_13x29"]
+    _, _, a = run_forward(spec, seed, save_z=True)
+    _, _, b = run_forward(spec, seed, save_z=False)
+    assert torch.equal(a["y"], b["y"])
+    assert torch.equal(a["saved_mean"], b["saved_mean"])
+
+
+def test_forward_deterministic():
+    spec, seed = CASES["n3_56_64"]
+    _, _, a = run_forward(spec, seed)
+    _, _, b = run_forward(spec, seed)
+    for k in ("y", "z", "mask", "saved_mean", "saved_inv_var"):
+        assert torch.equal(a[k], b[k]), k
+
+
+@pytest.mark.parametrize("case", ["ragged_13x29", "c128_bf16"])
+def test_fold_and_infer_parity(case):
+    spec, seed = CASES[case]
+    inp = make_inputs(spec, seed, with_dy=False)
+    gen = torch.Generator().manual_seed(seed + 7)
+    rm = torch.randn(spec.c_out, generator=gen) * 0.2
+    rv = torch.rand(spec.c_out, generator=gen) + 0.5
+    layer = cbr.Layer.from_spec(spec)
+    g = {k: v.cuda() for k, v in inp.items()}
+    w_fold, b_fold = cbr.fold_bn(layer, g["w"], g["gamma"], g["beta"], rm.cuda(), rv.cuda(), spec.eps)
+    y = cbr.forward_infer(layer, g["x"], w_fold, b_fold)
+    cbr.stream_status()
+    o = oracle_inputs(inp)
+    ref = oracle.forward_infer(o["x"], o["w"], o["gamma"], o["beta"], rm.double().numpy(),
+                               rv.double().numpy(), spec.eps, spec.stride, spec.pad)
+    max_err_ok(to_np(b_fold), ref["b_fold"], "b_fold")
+    max_err_ok(to_np(w_fold), ref["w_fold"], "w_fold")
+    max_err_ok(to_np(y), ref["y"], "y_infer")
