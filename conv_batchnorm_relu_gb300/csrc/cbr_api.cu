@@ -5,6 +5,8 @@
 #include <cmath>
 #include <cstring>
 #include <mutex>
+#include <set>
+#include <utility>
 
 #include "../../include/cbr.h"
 #include "cbr_internal.h"
@@ -200,6 +202,19 @@ bool encode_tiled(CUtensorMap* map, CUtensorMapDataType dt, int rank, const void
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+bool ensure_smem_attr(const void* func, int bytes) {
+  static std::mutex mu;
+  static std::set<std::pair<int, const void*>> done;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return false;
+  std::lock_guard<std::mutex> lk(mu);
+  if (done.count({dev, func})) return true;
+  if (cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess)
+    return false;
+  done.insert({dev, func});
+  return true;
+}
+
 int launch_fold(const void* w, const float* conv_bias, const float* gamma, const float* beta,
                 const float* rm, const float* rv, float eps, void* w_fold, float* b_fold, int cout,
                 int rsc, bool bf16, cudaStream_t st);
@@ -321,6 +336,8 @@ cbr_status_t cbr_backward(const cbr_desc_t* desc, const void* dy, const void* x,
       !aligned(dgamma, 4) || !aligned(dbeta, 4))
     return CBR_ERR_MISALIGNED;
   if ((st = check_supported(s))) return (cbr_status_t)st;
+  // dgrad runs as a stride-1 conv with padding R-1-pad on both axes
+  if (dx && (s.r != s.s || s.pad > s.r - 1)) return CBR_ERR_UNSUPPORTED;
   const BwdWs L = bwd_ws(s, z_saved == nullptr);
   if (ws_bytes < L.total) return CBR_ERR_WORKSPACE;
   DeviceInfo* dev = nullptr;
@@ -399,7 +416,6 @@ cbr_status_t cbr_backward(const cbr_desc_t* desc, const void* dy, const void* x,
     da.coef = coef;
     da.dx = dx;
     da.err = dev->err;
-    if (s.r - 1 - s.pad < 0 || s.s - 1 - s.pad < 0 || s.r != s.s) return CBR_ERR_UNSUPPORTED;
     st = launch_dgrad(da, (int)s.cin, (int)s.cout, s.bf16, w, dev->num_sms, cs);
     if (st) return (cbr_status_t)st;
     prof.mark();

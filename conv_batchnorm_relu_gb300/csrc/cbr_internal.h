@@ -53,11 +53,9 @@ enum FpropMode : int {
   kFpropBiasRelu = 2 // y = relu(conv + bias) (folded inference)
 };
 
-// Returns cudaSuccess or an error; `status` receives a CBR status code on validation issues.
-struct LaunchResult {
-  int status;        // cbr_status_t
-  cudaError_t cuda;
-};
+// Opt `func` into `bytes` of dynamic shared memory on the current device (once per
+// device and kernel; thread-safe).  Returns false if the runtime refuses.
+bool ensure_smem_attr(const void* func, int bytes);
 
 // Tensor-map helpers (cbr_api.cu).
 bool encode_tiled(CUtensorMap* map, CUtensorMapDataType dt, int rank, const void* base,

@@ -1,16 +1,375 @@
-// B2 (dgrad) and B3 (wgrad) -- placeholders until the tensor-core kernels land.
-#include "cbr_internal.h"
-#include "common.cuh"
+// B2: data gradient (DGrad) and B3: weight gradient (WGrad) of the convolution
+// (Tech-Renaissance CBR page, section 5.2), both with the BN + ReLU backward expression
+// dz = gamma*inv_std*(g - dbeta/M - xhat*dgamma/M), g = dy*mask (section 5.1; BatchNorm CUDA
+// page, section 3.1) evaluated while building the tensor-core operand tiles, so dz never
+// touches HBM.
+//
+// DGrad is the stride-1 convolution of dz with the tap-flipped filter and padding R-1-pad; it
+// runs on the shared halo-conv template with 4 dz-producer warps and the filter read MN-major.
+//
+// WGrad: dW[k][r][s][c] = sum over pixels of dz[pixel][k] * x[pixel shifted by (r,s)][c].  The
+// reduction dimension is the pixel, so both operands are MN-major pixel-row tiles: A is the
+// TMA-loaded input halo, in which each tap is a row-shifted view; B is the dz tile of the unit.
+// Two taps share one M = 128 MMA (two 64-channel atoms at different row shifts, addressed by
+// the descriptor's leading-dimension offset).  Each CTA accumulates its pixels in TMEM for
+// the whole kernel, writes one fp32 partial, and a second kernel sums the partials in a fixed
+// order (deterministic).
+#include <algorithm>
+
+#include "halo_conv.cuh"
 
 namespace cbr {
+namespace {
 
-size_t wgrad_partial_floats(int num_sms, int c_in, int c_out, int taps) {
-  const int cin_pad = ((c_in + 63) / 64) * 64;
-  const int groups = (taps + 1) / 2;
-  return (size_t)num_sms * groups * 2 * cin_pad * c_out;
+constexpr int kWgThreads = 192;  // warp 0: x TMA; warp 1: MMA; warps 2-5: dz producers + epilogue
+constexpr int kMaxGroups = 64;
+constexpr int kMaxSplits = 8;
+
+struct WgPlan {
+  int nsplit, gmax, ngroups;
+  int split_chunk[kMaxSplits], split_g0[kMaxSplits], split_ng[kMaxSplits];
+  int ta[kMaxGroups], tb[kMaxGroups];
+};
+
+struct WgKArgs {
+  HaloGeom g;
+  DzSrc dz;
+  WgPlan plan;
+  float* part;
+  uint32_t* err;
+};
+
+// Tap pairs (0,1), (2,3), ...; an odd last tap is paired with itself (its second half is
+// discarded).  Groups are split into contiguous subsets so that one CTA's accumulators
+// (groups x NOUT fp32 columns) fit the 512 TMEM columns; every 64-channel input chunk is a
+// separate split as well.
+bool make_plan(WgPlan& P, int taps, int c_in, int nout) {
+  P = WgPlan{};
+  const int ngroups = (taps + 1) / 2;
+  if (ngroups > kMaxGroups) return false;
+  for (int gi = 0; gi < ngroups; ++gi) {
+    P.ta[gi] = 2 * gi;
+    P.tb[gi] = std::min(2 * gi + 1, taps - 1);
+  }
+  const int gcap = 512 / nout;
+  const int nsub = (ngroups + gcap - 1) / gcap;
+  const int nchunk = (c_in + 63) / 64;
+  if (nsub * nchunk > kMaxSplits) return false;
+  P.ngroups = ngroups;
+  P.nsplit = nsub * nchunk;
+  P.gmax = 0;
+  for (int ch = 0; ch < nchunk; ++ch)
+    for (int sb = 0; sb < nsub; ++sb) {
+      const int s = ch * nsub + sb;
+      const int g0 = ngroups * sb / nsub, g1 = ngroups * (sb + 1) / nsub;
+      P.split_chunk[s] = ch;
+      P.split_g0[s] = g0;
+      P.split_ng[s] = g1 - g0;
+      P.gmax = std::max(P.gmax, g1 - g0);
+    }
+  return true;
 }
 
-int launch_dgrad(const DgradArgs&, int, int, bool, const void*, int, cudaStream_t) { return 3; }
-int launch_wgrad(const WgradArgs&, int, int, bool, const void*, int, cudaStream_t) { return 3; }
+struct WgLayout {
+  uint32_t halo_stride, dz_stride, off_dz, off_bar, total;
+};
+
+__host__ __device__ inline WgLayout wg_layout(const HaloGeom& g, int nout) {
+  WgLayout L;
+  L.halo_stride = (((uint32_t)g.hr * g.wp * 128) + 1023u) & ~1023u;
+  const int nkc = nout > 64 ? nout / 64 : 1;
+  L.dz_stride = (uint32_t)nkc * g.um * 128;
+  L.off_dz = 2 * L.halo_stride;
+  L.off_bar = L.off_dz + 2 * L.dz_stride;
+  L.total = L.off_bar + 12 * 8 + 16;
+  return L;
+}
+
+template <int NOUT, bool BF16>
+__global__ void __launch_bounds__(kWgThreads, 1)
+    wgrad_kernel(const __grid_constant__ CUtensorMap map_x, const WgKArgs a) {
+  constexpr int kNkc = NOUT > 64 ? NOUT / 64 : 1;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  const HaloGeom& g = a.g;
+  const WgPlan& P = a.plan;
+  const WgLayout L = wg_layout(g, NOUT);
+  const uint32_t sbase = smem_u32(smem);
+  const uint32_t x_addr = sbase, dz_addr = sbase + L.off_dz;
+  const uint32_t bar0 = sbase + L.off_bar;
+  const uint32_t bar_x_full = bar0, bar_x_empty = bar0 + 16;
+  const uint32_t bar_dz_full = bar0 + 32, bar_dz_empty = bar0 + 48;
+  const uint32_t bar_acc_full = bar0 + 64, bar_drain = bar0 + 72;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L.off_bar + 12 * 8);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int split = blockIdx.x % P.nsplit;
+  const int ustart = blockIdx.x / P.nsplit;
+  const int ustride = gridDim.x / P.nsplit;
+  const int chunk = P.split_chunk[split];
+  const int g0 = P.split_g0[split], ng = P.split_ng[split];
+  const int tmem_cols = hc::pow2_at_least(P.gmax * NOUT);
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(bar_x_full + 8 * i, 1);
+      mbar_init(bar_x_empty + 8 * i, 1);
+      mbar_init(bar_dz_full + 8 * i, 128);
+      mbar_init(bar_dz_empty + 8 * i, 1);
+    }
+    mbar_init(bar_acc_full, 1);
+    mbar_init(bar_drain, 1);
+    *abort_flag = 0;
+    fence_mbarrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), tmem_cols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      prefetch_tensormap(&map_x);
+      const uint32_t tx = (uint32_t)g.hr * g.wp * 128;
+      uint32_t it = 0;
+      for (int u = ustart; u < g.total_units && !hc::is_aborted(abort_flag); u += ustride, ++it) {
+        const int n = u / g.upi;
+        const int m0 = (u - n * g.upi) * g.um;
+        const uint32_t s = it & 1, ph = (it >> 1) & 1;
+        if (!mbar_wait(bar_x_empty + 8 * s, ph ^ 1)) {
+          hc::set_abort(abort_flag, a.err, kErrWaitHalo);
+          break;
+        }
+        mbar_arrive_expect_tx(bar_x_full + 8 * s, tx);
+        tma_load_4d(x_addr + s * L.halo_stride, &map_x, chunk * 64, -g.pad, m0 / g.wp - g.pad, n,
+                    bar_x_full + 8 * s);
+      }
+      for (uint32_t k = (it > 2 ? it - 2 : 0); k < it; ++k)
+        mbar_wait(bar_x_full + 8 * (k & 1), (k >> 1) & 1);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      const uint32_t idesc = make_idesc_f16(128, NOUT, BF16, true, true);
+      uint32_t it = 0;
+      bool first = true;
+      for (int u = ustart; u < g.total_units && !hc::is_aborted(abort_flag); u += ustride, ++it) {
+        const int n = u / g.upi;
+        const int m0 = (u - n * g.upi) * g.um;
+        const int off = m0 - (m0 / g.wp) * g.wp;
+        const uint32_t s = it & 1, ph = (it >> 1) & 1;
+        if (!mbar_wait(bar_x_full + 8 * s, ph) || !mbar_wait(bar_dz_full + 8 * s, ph)) {
+          hc::set_abort(abort_flag, a.err, kErrWaitOperand);
+          break;
+        }
+        tc_fence_after();
+        const uint32_t xh = x_addr + s * L.halo_stride;
+        const uint32_t dzs = dz_addr + s * L.dz_stride;
+        for (int kk = 0; kk < g.um / 16; ++kk) {
+          const uint64_t bd = make_sw128_desc(dzs + kk * 2048, g.um * 128, 1024, 0);
+          for (int gl = 0; gl < ng; ++gl) {
+            const int ta = P.ta[g0 + gl], tb = P.tb[g0 + gl];
+            const int sha = (ta / g.s) * g.wp + ta % g.s;
+            const int shb = (tb / g.s) * g.wp + tb % g.s;
+            const uint64_t ad = make_sw128_desc(xh + (uint32_t)(off + kk * 16 + sha) * 128u,
+                                                (uint32_t)(shb - sha) * 128u, 1024, 0);
+            mma_f16_ss(tmem_base + gl * NOUT, ad, bd, idesc, (first && kk == 0) ? 0u : 1u);
+          }
+        }
+        mma_commit(bar_x_empty + 8 * s);
+        mma_commit(bar_dz_empty + 8 * s);
+        first = false;
+      }
+      mma_commit(bar_acc_full);
+      mma_commit(bar_drain);
+      mbar_wait(bar_drain, 0);
+    }
+  } else {
+    // warps 2..5: dz producers, then the epilogue
+    const int tid = threadIdx.x - 64;  // 0..127
+    uint32_t it = 0;
+    for (int u = ustart; u < g.total_units && !hc::is_aborted(abort_flag); u += ustride, ++it) {
+      const int n = u / g.upi;
+      const int m0 = (u - n * g.upi) * g.um;
+      const uint32_t s = it & 1, ph = (it >> 1) & 1;
+      if (!mbar_wait(bar_dz_empty + 8 * s, ph ^ 1)) {
+        hc::set_abort(abort_flag, a.err, kErrWaitOperand);
+        break;
+      }
+#pragma unroll
+      for (int kc = 0; kc < kNkc; ++kc)
+        fill_dz_rows<BF16>(dz_addr + s * L.dz_stride + kc * g.um * 128, g.um, m0, g.wp, 0, 0, n, a.dz,
+                           kc, tid, 128);
+      fence_proxy_async_smem();
+      mbar_arrive(bar_dz_full + 8 * s);
+    }
+    const bool ok = mbar_wait(bar_acc_full, 0);
+    if (!ok) hc::set_abort(abort_flag, a.err, kErrWaitMma);
+    tc_fence_after();
+    if (ok) {
+      const int quad = warp & 3;
+      const int e = quad * 32 + lane;  // accumulator row = (tap half, channel)
+      for (int gl = 0; gl < ng; ++gl) {
+#pragma unroll
+        for (int c16 = 0; c16 < NOUT / 16; ++c16) {
+          uint32_t r[16];
+          tmem_ld16(tmem_base + ((uint32_t)(quad * 32) << 16) + gl * NOUT + c16 * 16, r);
+          tmem_ld_wait();
+          float4* dst = reinterpret_cast<float4*>(
+              a.part + (((size_t)blockIdx.x * P.gmax + gl) * 128 + e) * NOUT + c16 * 16);
+#pragma unroll
+          for (int v = 0; v < 4; ++v)
+            dst[v] = make_float4(__uint_as_float(r[4 * v]), __uint_as_float(r[4 * v + 1]),
+                                 __uint_as_float(r[4 * v + 2]), __uint_as_float(r[4 * v + 3]));
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, tmem_cols);
+  }
+}
+
+// dW[k][tap][c] = sum over the CTAs of its split (fixed order, fp64 accumulation).
+__global__ void wgrad_reduce_kernel(const float* __restrict__ part, float* __restrict__ dw,
+                                    const WgPlan P, int grid, int cout, int cin, int taps, int nout) {
+  const long long total = (long long)taps * cin * cout;
+  for (long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
+       idx += (long long)gridDim.x * blockDim.x) {
+    const int k = (int)(idx % cout);
+    const int c = (int)((idx / cout) % cin);
+    const int tap = (int)(idx / ((long long)cout * cin));
+    const int chunk = c >> 6, cl = c & 63;
+    int grp = 0, row = 0;
+    for (int gi = 0; gi < P.ngroups; ++gi) {
+      if (P.ta[gi] == tap) { grp = gi; row = cl; break; }
+      if (P.tb[gi] == tap) { grp = gi; row = 64 + cl; break; }
+    }
+    int split = 0;
+    for (int s = 0; s < P.nsplit; ++s)
+      if (P.split_chunk[s] == chunk && grp >= P.split_g0[s] && grp < P.split_g0[s] + P.split_ng[s]) split = s;
+    const int gl = grp - P.split_g0[split];
+    double acc = 0.0;
+    for (int b = split; b < grid; b += P.nsplit)
+      acc += (double)__ldg(part + (((size_t)b * P.gmax + gl) * 128 + row) * nout + k);
+    dw[((size_t)k * taps + tap) * cin + c] = (float)acc;
+  }
+}
+
+int nout_for(int c) { return c <= 16 ? 16 : (c <= 32 ? 32 : (c <= 64 ? 64 : 128)); }
+
+}  // namespace
+
+size_t wgrad_partial_floats(int num_sms, int c_in, int c_out, int taps) {
+  WgPlan P;
+  const int nout = nout_for(c_out);
+  if (!make_plan(P, taps, c_in, nout)) return 0;
+  return (size_t)num_sms * P.gmax * 128 * nout;
+}
+
+int launch_wgrad(const WgradArgs& w, int c_in, int c_out, bool bf16, const void* x, int num_sms,
+                 cudaStream_t st) {
+  WgKArgs a{};
+  a.g = w.g;
+  a.dz = DzSrc{w.dy, w.z, w.y, w.mask, w.coef, 0, 0, c_out};
+  a.part = w.part;
+  a.err = w.err;
+  const int nout = nout_for(c_out);
+  if (c_in > 128 || nout != c_out) return 3;
+  const int U = nout <= 64 ? 2 : 1;
+  if (!hc::finish_geom(a.g, U)) return 3;
+  a.dz.p = a.g.p;
+  a.dz.q = a.g.q;
+  const int taps = a.g.r * a.g.s;
+  if (!make_plan(a.plan, taps, c_in, nout)) return 3;
+  const WgLayout L = wg_layout(a.g, nout);
+  const uint32_t smem = L.total + 1024;
+  if (smem > 227 * 1024) return 3;
+  const CUtensorMapDataType dt = bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  CUtensorMap mx;
+  const HaloGeom& g = a.g;
+  {
+    const uint64_t dims[4] = {(uint64_t)c_in, (uint64_t)g.w, (uint64_t)g.h, (uint64_t)g.n_img};
+    const uint64_t strides[3] = {(uint64_t)c_in * 2, (uint64_t)g.w * c_in * 2, (uint64_t)g.h * g.w * c_in * 2};
+    const uint32_t box[4] = {64, (uint32_t)g.wp, (uint32_t)g.hr, 1};
+    if (!encode_tiled(&mx, dt, 4, x, dims, strides, box)) return 6;
+  }
+  // every CTA gets at least one unit, so every partial it writes is initialised
+  const int per_split = std::max(1, std::min(num_sms / a.plan.nsplit, g.total_units));
+  const int grid = per_split * a.plan.nsplit;
+  auto launch = [&](auto kern) -> int {
+    if (!ensure_smem_attr(reinterpret_cast<const void*>(kern), 227 * 1024)) return 6;
+    kern<<<grid, kWgThreads, smem, st>>>(mx, a);
+    return cudaGetLastError() == cudaSuccess ? 0 : 6;
+  };
+  int rc;
+  switch (nout * 2 + (bf16 ? 1 : 0)) {
+    case 32: rc = launch(wgrad_kernel<16, false>); break;
+    case 33: rc = launch(wgrad_kernel<16, true>); break;
+    case 64: rc = launch(wgrad_kernel<32, false>); break;
+    case 65: rc = launch(wgrad_kernel<32, true>); break;
+    case 128: rc = launch(wgrad_kernel<64, false>); break;
+    case 129: rc = launch(wgrad_kernel<64, true>); break;
+    case 256: rc = launch(wgrad_kernel<128, false>); break;
+    case 257: rc = launch(wgrad_kernel<128, true>); break;
+    default: return 3;
+  }
+  if (rc) return rc;
+  const long long total = (long long)taps * c_in * c_out;
+  const int rgrid = (int)std::min<long long>((total + 255) / 256, 4LL * num_sms);
+  wgrad_reduce_kernel<<<rgrid, 256, 0, st>>>(a.part, w.dw, a.plan, grid, c_out, c_in, taps, nout);
+  return cudaGetLastError() == cudaSuccess ? 0 : 6;
+}
+
+int launch_dgrad(const DgradArgs& d, int c_in, int c_out, bool bf16, const void* w, int num_sms,
+                 cudaStream_t st) {
+  ConvArgs a{};
+  a.g = d.g;
+  a.out = d.dx;
+  a.out_c = c_in;
+  a.mode = kFpropPlain;
+  a.err = d.err;
+  a.dz = DzSrc{d.dy, d.z, d.y, d.mask, d.coef, d.g.h, d.g.w, c_out};
+  const int nch = (c_out + 63) / 64;
+  const int nout = nout_for(c_in);
+  if (nch > 2 || c_in > 128) return 3;
+  const int U = nout <= 64 ? 2 : 1;
+  HaloGeom& g = a.g;
+  if (!hc::finish_geom(g, U)) return 3;
+  const bool wres = hc::layout(g, kKindDgrad, nch, nout, true).total + 1024 <= 227 * 1024;
+  const CUtensorMapDataType dt = bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  CUtensorMap mx{}, mw;  // dgrad builds its A operand in-kernel; mx is unused
+  {
+    const uint64_t dims[3] = {(uint64_t)c_in, (uint64_t)(g.r * g.s), (uint64_t)c_out};
+    const uint64_t strides[2] = {(uint64_t)c_in * 2, (uint64_t)g.r * g.s * c_in * 2};
+    const uint32_t box[3] = {64, 1, 64};
+    if (!encode_tiled(&mw, dt, 3, w, dims, strides, box)) return 6;
+  }
+  const int grid = std::min(g.total_units, num_sms);
+#define CBR_DGRAD_CASE(NCH_, NOUT_, U_, WRES_)                                                        \
+  if (nch == NCH_ && nout == NOUT_ && U == U_ && (WRES_ == wres)) {                                  \
+    return bf16 ? hc::launch_halo_conv<kKindDgrad, NCH_, NOUT_, U_, WRES_, true>(a, mx, mw, grid, st) \
+                : hc::launch_halo_conv<kKindDgrad, NCH_, NOUT_, U_, WRES_, false>(a, mx, mw, grid, st); \
+  }
+  CBR_DGRAD_CASE(1, 16, 2, true)
+  CBR_DGRAD_CASE(1, 32, 2, true)
+  CBR_DGRAD_CASE(1, 64, 2, true)
+  CBR_DGRAD_CASE(1, 16, 2, false)
+  CBR_DGRAD_CASE(1, 32, 2, false)
+  CBR_DGRAD_CASE(1, 64, 2, false)
+  CBR_DGRAD_CASE(2, 64, 2, false)
+  CBR_DGRAD_CASE(1, 128, 1, false)
+  CBR_DGRAD_CASE(2, 128, 1, false)
+#undef CBR_DGRAD_CASE
+  return 3;
+}
 
 }  // namespace cbr

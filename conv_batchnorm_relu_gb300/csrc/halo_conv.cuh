@@ -1,0 +1,532 @@
+// Generic stride-1 implicit-GEMM convolution over a halo tile, on tcgen05 tensor cores.
+//
+// Used for the forward convolution (A = input activations, loaded by TMA) and for the data
+// gradient (A = dz, computed in-kernel from dy, z and the ReLU mask by producer warps; the
+// filter is the forward filter read MN-major with flipped taps).  See HaloGeom for the
+// padded-linear row space in which every filter tap is a row-shifted view of one halo tile.
+//
+// Warp roles (A = number of A-producer warps: 1 for TMA, 4 for the dz producer):
+//   warps [0, A)       A producers (one halo stage per (unit, 64-channel chunk))
+//   warp  A            TMEM owner and single-thread tcgen05.mma issuer
+//   warp  A+1          TMA producer for the filter slabs (resident when they fit in smem)
+//   warps A+2 .. A+5   epilogue: TMEM -> registers -> staged tile -> stats / store
+// Pipelines: 2 halo stages, 2 TMEM accumulator stages (U*NOUT fp32 columns each), and a
+// 2-deep filter ring when the filter is streamed.  All waits are bounded (ptx.cuh).
+#pragma once
+#include "cbr_internal.h"
+#include "common.cuh"
+#include "dz_producer.cuh"
+
+namespace cbr {
+
+enum ConvKind : int { kKindFprop = 0, kKindDgrad = 1 };
+
+struct ConvArgs {
+  HaloGeom g;
+  void* out;                // [n][p][q][out_c] storage dtype: z, y (inference) or dx
+  int out_c;                // channels stored per output pixel (<= NOUT)
+  int mode;                 // FpropMode (fprop only)
+  // forward statistics / finalize
+  float* part;
+  uint32_t* ticket;
+  const float* gamma;
+  const float* beta;
+  float* running_mean;
+  float* running_var;
+  float* saved_mean;
+  float* saved_inv_var;
+  float* eq;
+  const float* bias;
+  float momentum;
+  float eps;
+  long long m_count;
+  // dgrad A operand
+  DzSrc dz;
+  uint32_t* err;
+};
+
+namespace hc {
+
+constexpr int kEpiThreads = 128;
+constexpr int kStreamStages = 2;
+
+constexpr int pow2_at_least(int v) {
+  int p = 32;
+  while (p < v) p <<= 1;
+  return p;
+}
+
+template <int KIND>
+struct Roles {
+  static constexpr int kAWarps = KIND == kKindFprop ? 1 : 4;
+  static constexpr int kMmaWarp = kAWarps;
+  static constexpr int kWWarp = kAWarps + 1;
+  static constexpr int kEpiWarp0 = kAWarps + 2;
+  static constexpr int kThreads = (kAWarps + 6) * 32;
+};
+
+// Bytes of one filter slab (one 64-channel K chunk x one tap).
+__host__ __device__ constexpr int wslab_bytes(int kind, int nout) {
+  return kind == kKindFprop ? nout * 128 : (nout > 64 ? nout : 64) * 128;
+}
+
+struct Layout {
+  uint32_t halo_stride, off_w, off_stage, off_bar, total, wslab;
+  int nsw;
+};
+
+__host__ __device__ inline Layout layout(const HaloGeom& g, int kind, int nch, int nout, bool wres) {
+  Layout L;
+  const uint32_t halo = (uint32_t)g.hr * g.wp * 128;
+  L.halo_stride = (halo + 1023u) & ~1023u;
+  L.wslab = (uint32_t)wslab_bytes(kind, nout);
+  L.nsw = wres ? nch * g.r * g.s : kStreamStages;
+  L.off_w = 2 * L.halo_stride;
+  L.off_stage = L.off_w + (uint32_t)L.nsw * L.wslab;
+  const uint32_t stage = 128u * nout * 2;
+  L.off_bar = (L.off_stage + stage + 15u) & ~15u;
+  const uint32_t nbar = 8 + 2 * L.nsw + 1;
+  L.total = L.off_bar + nbar * 8 + 16;
+  return L;
+}
+
+__device__ __forceinline__ bool is_aborted(volatile int* flag) { return *flag != 0; }
+
+__device__ __forceinline__ void set_abort(volatile int* flag, uint32_t* err, uint32_t bits) {
+  *flag = 1;
+  report_error(err, bits);
+}
+
+// Offset of chunk c of staged row `row` (pitch = NOUT*2 bytes).
+template <int PITCH>
+__device__ __forceinline__ uint32_t stage_off(uint32_t row, uint32_t c) {
+  if constexpr (PITCH >= 128) return swz_off(row, c, PITCH);
+  else return row * PITCH + c * 16;
+}
+
+template <int KIND, int NCH, int NOUT, int U, bool WRES, bool BF16>
+__global__ void __launch_bounds__(Roles<KIND>::kThreads, 1)
+    halo_conv_kernel(const __grid_constant__ CUtensorMap map_x,
+                     const __grid_constant__ CUtensorMap map_w, const ConvArgs a) {
+  using R = Roles<KIND>;
+  constexpr int kThreads = R::kThreads;
+  constexpr int kPitch = NOUT * 2;
+  constexpr int kChunks = kPitch / 16;
+  constexpr int kTmemCols = pow2_at_least(2 * U * NOUT);
+  constexpr int kPairs = NOUT / 2;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  const HaloGeom& g = a.g;
+  const Layout L = layout(g, KIND, NCH, NOUT, WRES);
+  const uint32_t sbase = smem_u32(smem);
+  const uint32_t halo_addr = sbase;
+  const uint32_t w_addr = sbase + L.off_w;
+  const uint32_t stage_addr = sbase + L.off_stage;
+  const uint32_t bar0 = sbase + L.off_bar;
+  const uint32_t bar_halo_full = bar0;
+  const uint32_t bar_halo_empty = bar0 + 16;
+  const uint32_t bar_acc_full = bar0 + 32;
+  const uint32_t bar_acc_empty = bar0 + 48;
+  const uint32_t bar_w_full = bar0 + 64;
+  const uint32_t bar_w_empty = bar_w_full + 8 * L.nsw;
+  const uint32_t bar_drain = bar_w_empty + 8 * L.nsw;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L.off_bar + (8 + 2 * L.nsw + 1) * 8);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  volatile uint32_t* ticket_slot = reinterpret_cast<volatile uint32_t*>(tmem_slot + 2);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int rs = g.r * g.s;
+  const int rows_img = g.p * g.wp;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(bar_halo_full + 8 * i, KIND == kKindFprop ? 1 : 32 * R::kAWarps);
+      mbar_init(bar_halo_empty + 8 * i, 1);
+      mbar_init(bar_acc_full + 8 * i, 1);
+      mbar_init(bar_acc_empty + 8 * i, kEpiThreads);
+    }
+    for (int i = 0; i < L.nsw; ++i) {
+      mbar_init(bar_w_full + 8 * i, 1);
+      mbar_init(bar_w_empty + 8 * i, 1);
+    }
+    mbar_init(bar_drain, 1);
+    *abort_flag = 0;
+    fence_mbarrier_init();
+  }
+  if (warp == R::kMmaWarp) {
+    tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp < R::kAWarps) {
+    // ------------------------------------------------------------ A producers
+    if constexpr (KIND == kKindFprop) {
+      if (lane == 0) {
+        prefetch_tensormap(&map_x);
+        const uint32_t tx = (uint32_t)g.hr * g.wp * 128;
+        uint32_t it = 0;
+        for (int u = blockIdx.x; u < g.total_units && !is_aborted(abort_flag); u += gridDim.x) {
+          const int n = u / g.upi;
+          const int m0 = (u - n * g.upi) * g.um;
+          const int h_lo = m0 / g.wp - g.pad;
+          for (int ch = 0; ch < NCH; ++ch, ++it) {
+            const uint32_t s = it & 1, ph = (it >> 1) & 1;
+            if (!mbar_wait(bar_halo_empty + 8 * s, ph ^ 1)) {
+              set_abort(abort_flag, a.err, kErrWaitHalo);
+              break;
+            }
+            mbar_arrive_expect_tx(bar_halo_full + 8 * s, tx);
+            tma_load_4d(halo_addr + s * L.halo_stride, &map_x, ch * 64, -g.pad, h_lo, n,
+                        bar_halo_full + 8 * s);
+          }
+        }
+        // never leave the CTA with a copy in flight
+        for (uint32_t k = (it > 2 ? it - 2 : 0); k < it; ++k)
+          mbar_wait(bar_halo_full + 8 * (k & 1), (k >> 1) & 1);
+      }
+    } else {
+      // dz producer: 4 warps build the zero-padded dz halo of each unit in smem
+      const int tid = threadIdx.x;  // 0..127
+      uint32_t it = 0;
+      for (int u = blockIdx.x; u < g.total_units && !is_aborted(abort_flag); u += gridDim.x) {
+        const int n = u / g.upi;
+        const int m0 = (u - n * g.upi) * g.um;
+        const int h_lo = m0 / g.wp - g.pad;
+        bool bad = false;
+        for (int ch = 0; ch < NCH; ++ch, ++it) {
+          const uint32_t s = it & 1, ph = (it >> 1) & 1;
+          if (!mbar_wait(bar_halo_empty + 8 * s, ph ^ 1)) {
+            set_abort(abort_flag, a.err, kErrWaitOperand);
+            bad = true;
+            break;
+          }
+          fill_dz_rows<BF16>(halo_addr + s * L.halo_stride, g.hr * g.wp, 0, g.wp, h_lo, g.pad, n,
+                             a.dz, ch, tid, 32 * R::kAWarps);
+          fence_proxy_async_smem();
+          mbar_arrive(bar_halo_full + 8 * s);
+        }
+        if (bad) break;
+      }
+    }
+  } else if (warp == R::kWWarp) {
+    // ------------------------------------------------------------ filter producer
+    if (lane == 0) {
+      prefetch_tensormap(&map_w);
+      auto load_slab = [&](uint32_t dst, int ch, int tap, uint32_t bar) {
+        mbar_arrive_expect_tx(bar, L.wslab);
+        if constexpr (KIND == kKindFprop) {
+          tma_load_3d(dst, &map_w, ch * 64, tap, 0, bar);
+        } else {
+          const int ftap = rs - 1 - tap;  // (R-1-r, S-1-s)
+#pragma unroll
+          for (int at = 0; at < (NOUT > 64 ? NOUT / 64 : 1); ++at)
+            tma_load_3d(dst + at * 8192, &map_w, at * 64, ftap, ch * 64, bar);
+        }
+      };
+      if (WRES) {
+        for (int i = 0; i < NCH * rs; ++i) load_slab(w_addr + i * L.wslab, i / rs, i % rs, bar_w_full + 8 * i);
+        for (int i = 0; i < NCH * rs; ++i) mbar_wait(bar_w_full + 8 * i, 0);
+      } else {
+        uint32_t it = 0;
+        bool bad = false;
+        for (int u = blockIdx.x; u < g.total_units && !is_aborted(abort_flag) && !bad; u += gridDim.x) {
+          for (int ch = 0; ch < NCH && !bad; ++ch)
+            for (int tap = 0; tap < rs; ++tap, ++it) {
+              const uint32_t s = it % kStreamStages, ph = (it / kStreamStages) & 1;
+              if (!mbar_wait(bar_w_empty + 8 * s, ph ^ 1)) {
+                set_abort(abort_flag, a.err, kErrWaitWeights);
+                bad = true;
+                break;
+              }
+              load_slab(w_addr + s * L.wslab, ch, tap, bar_w_full + 8 * s);
+            }
+        }
+        for (uint32_t k = (it > kStreamStages ? it - kStreamStages : 0); k < it; ++k)
+          mbar_wait(bar_w_full + 8 * (k % kStreamStages), (k / kStreamStages) & 1);
+      }
+    }
+  } else if (warp == R::kMmaWarp) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr bool kBMn = KIND == kKindDgrad;
+      const uint32_t idesc = make_idesc_f16(128, NOUT, BF16, false, kBMn);
+      uint32_t hit = 0, wit = 0, ait = 0;
+      bool first = true;
+      for (int u = blockIdx.x; u < g.total_units && !is_aborted(abort_flag); u += gridDim.x) {
+        const int n = u / g.upi;
+        const int m0 = (u - n * g.upi) * g.um;
+        const int off = m0 - (m0 / g.wp) * g.wp;
+        const int ntiles = min(U, (rows_img - m0 + 127) / 128);
+        const uint32_t as = ait & 1, aph = (ait >> 1) & 1;
+        if (!mbar_wait(bar_acc_empty + 8 * as, aph ^ 1)) {
+          set_abort(abort_flag, a.err, kErrWaitAccum);
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d0 = tmem_base + as * (U * NOUT);
+        bool bad = false;
+        for (int ch = 0; ch < NCH && !bad; ++ch, ++hit) {
+          const uint32_t hs = hit & 1, hph = (hit >> 1) & 1;
+          if (!mbar_wait(bar_halo_full + 8 * hs, hph)) {
+            set_abort(abort_flag, a.err, kErrWaitHalo);
+            bad = true;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t hbase = halo_addr + hs * L.halo_stride;
+          for (int tap = 0; tap < rs; ++tap) {
+            const int r = tap / g.s, sx = tap - r * g.s;
+            uint32_t wslab, ws = 0;
+            if (WRES) {
+              const int i = ch * rs + tap;
+              if (first && !mbar_wait(bar_w_full + 8 * i, 0)) {
+                set_abort(abort_flag, a.err, kErrWaitWeights);
+                bad = true;
+                break;
+              }
+              wslab = w_addr + i * L.wslab;
+            } else {
+              ws = wit % kStreamStages;
+              if (!mbar_wait(bar_w_full + 8 * ws, (wit / kStreamStages) & 1)) {
+                set_abort(abort_flag, a.err, kErrWaitWeights);
+                bad = true;
+                break;
+              }
+              wslab = w_addr + ws * L.wslab;
+            }
+            tc_fence_after();
+            const uint32_t a_row0 = hbase + (uint32_t)(off + r * g.wp + sx) * 128u;
+            for (int t = 0; t < ntiles; ++t) {
+#pragma unroll
+              for (int kk = 0; kk < 4; ++kk) {
+                const uint64_t ad = make_sw128_desc(a_row0 + t * 128 * 128 + kk * 32, 16, 1024, 0);
+                const uint64_t bd = kBMn ? make_sw128_desc(wslab + kk * 2048, 8192, 1024, 0)
+                                         : make_sw128_desc(wslab + kk * 32, 16, 1024, 0);
+                mma_f16_ss(d0 + t * NOUT, ad, bd, idesc, (ch | tap | kk) != 0);
+              }
+            }
+            if (!WRES) {
+              mma_commit(bar_w_empty + 8 * ws);
+              ++wit;
+            }
+          }
+          mma_commit(bar_halo_empty + 8 * hs);
+        }
+        if (bad) break;
+        mma_commit(bar_acc_full + 8 * as);
+        ++ait;
+        first = false;
+      }
+      mma_commit(bar_drain);
+      mbar_wait(bar_drain, 0);
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int quad = warp & 3;                       // TMEM lanes 32*quad .. +31
+    const int e = quad * 32 + lane;                  // M-tile row owned by this thread
+    const int et = threadIdx.x - 32 * R::kEpiWarp0;  // rank among epilogue threads
+    constexpr int kPL = (kPairs + 31) / 32;
+    float s1[2 * kPL], s2[2 * kPL];
+#pragma unroll
+    for (int i = 0; i < 2 * kPL; ++i) s1[i] = s2[i] = 0.f;
+    const bool stats = KIND == kKindFprop && a.mode == kFpropStats;
+    const bool bias_relu = KIND == kKindFprop && a.mode == kFpropBiasRelu;
+    const int out_chunks = a.out_c * 2 / 16;
+    uint8_t* obase = static_cast<uint8_t*>(a.out);
+    uint32_t ait = 0;
+    for (int u = blockIdx.x; u < g.total_units && !is_aborted(abort_flag); u += gridDim.x) {
+      const int n = u / g.upi;
+      const int m0 = (u - n * g.upi) * g.um;
+      const int ntiles = min(U, (rows_img - m0 + 127) / 128);
+      const uint32_t as = ait & 1, aph = (ait >> 1) & 1;
+      bool ok = mbar_wait(bar_acc_full + 8 * as, aph);
+      if (!ok) set_abort(abort_flag, a.err, kErrWaitMma);
+      // uniform decision across the 128 epilogue threads (they share named barriers below)
+      if (!named_bar_and(2, kEpiThreads, ok && !is_aborted(abort_flag))) break;
+      tc_fence_after();
+      for (int t = 0; t < ntiles; ++t) {
+        uint32_t pk[NOUT / 2];
+#pragma unroll
+        for (int c16 = 0; c16 < NOUT / 16; ++c16) {
+          uint32_t r[16];
+          tmem_ld16(tmem_base + ((uint32_t)(quad * 32) << 16) + as * (U * NOUT) + t * NOUT + c16 * 16, r);
+          tmem_ld_wait();
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            float lo = __uint_as_float(r[2 * i]), hi = __uint_as_float(r[2 * i + 1]);
+            if (bias_relu) {
+              lo = fmaxf(lo + __ldg(a.bias + c16 * 16 + 2 * i), 0.f);
+              hi = fmaxf(hi + __ldg(a.bias + c16 * 16 + 2 * i + 1), 0.f);
+            }
+            pk[c16 * 8 + i] = pack2<BF16>(lo, hi);
+          }
+        }
+        if (t == ntiles - 1) {
+          tc_fence_before();
+          mbar_arrive(bar_acc_empty + 8 * as);
+        }
+        const int mt = m0 + t * 128;
+        {
+          const int m = mt + e;
+          const int p = m / g.wp, q = m - p * g.wp;
+          const bool valid = (p < g.p) && (q < g.q);
+#pragma unroll
+          for (int c = 0; c < kChunks; ++c) {
+            const uint4 v = valid ? make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3])
+                                  : make_uint4(0, 0, 0, 0);
+            st_shared_v4(stage_addr + stage_off<kPitch>(e, c), v);
+          }
+        }
+        named_bar_sync(1, kEpiThreads);
+        if (stats) {
+          for (int row = quad * 32; row < quad * 32 + 32; ++row) {
+#pragma unroll
+            for (int k = 0; k < kPL; ++k) {
+              const int j = lane + 32 * k;
+              if (j < kPairs) {
+                const int c = 2 * j;
+                const uint32_t o = stage_off<kPitch>(row, c >> 3) + (c & 7) * 2;
+                const float2 v = unpack2<BF16>(ld_shared_b32(stage_addr + o));
+                s1[2 * k] += v.x;
+                s1[2 * k + 1] += v.y;
+                s2[2 * k] = fmaf(v.x, v.x, s2[2 * k]);
+                s2[2 * k + 1] = fmaf(v.y, v.y, s2[2 * k + 1]);
+              }
+            }
+          }
+        }
+        // coalesced copy-out of the valid rows
+        for (int i = et; i < 128 * out_chunks; i += kEpiThreads) {
+          const int row = i / out_chunks, c = i - row * out_chunks;
+          const int m = mt + row;
+          const int p = m / g.wp, q = m - p * g.wp;
+          if (p < g.p && q < g.q) {
+            const size_t gi = ((size_t)n * g.p + p) * g.q + q;
+            st_global_v4(obase + gi * (size_t)a.out_c * 2 + c * 16,
+                         ld_shared_v4(stage_addr + stage_off<kPitch>(row, c)));
+          }
+        }
+        named_bar_sync(1, kEpiThreads);
+      }
+      ++ait;
+    }
+    if (stats) {
+      // per-warp partials -> smem; the staging buffer is free behind the last named barrier
+      float* red = reinterpret_cast<float*>(smem + L.off_stage);
+#pragma unroll
+      for (int k = 0; k < kPL; ++k) {
+        const int j = lane + 32 * k;
+        if (j < kPairs) {
+          red[(quad * 2 + 0) * NOUT + 2 * j] = s1[2 * k];
+          red[(quad * 2 + 0) * NOUT + 2 * j + 1] = s1[2 * k + 1];
+          red[(quad * 2 + 1) * NOUT + 2 * j] = s2[2 * k];
+          red[(quad * 2 + 1) * NOUT + 2 * j + 1] = s2[2 * k + 1];
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+
+  if (KIND == kKindFprop && a.mode == kFpropStats) {
+    constexpr int COUT = NOUT;
+    const float* red = reinterpret_cast<const float*>(smem + L.off_stage);
+    for (int i = threadIdx.x; i < 2 * COUT; i += kThreads) {
+      const int st = i / COUT, c = i - st * COUT;
+      float v = red[(0 * 2 + st) * COUT + c];
+      v += red[(1 * 2 + st) * COUT + c];
+      v += red[(2 * 2 + st) * COUT + c];
+      v += red[(3 * 2 + st) * COUT + c];
+      a.part[(size_t)blockIdx.x * 2 * COUT + i] = v;
+    }
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) *ticket_slot = atomicInc(a.ticket, gridDim.x - 1);
+    __syncthreads();
+    if (*ticket_slot == gridDim.x - 1 && !is_aborted(abort_flag)) {
+      // ---------------------------------------------------- bn_finalize (last CTA)
+      __threadfence();
+      constexpr int kW = kThreads / 32;
+      double* dred = reinterpret_cast<double*>(smem + L.off_stage);  // [kW][2*COUT]
+      double* fin = dred + kW * 2 * COUT;                             // [2*COUT]
+      constexpr int kV4 = (2 * COUT) / 4;
+      for (int c4 = lane; c4 < kV4; c4 += 32) {
+        double acc0 = 0, acc1 = 0, acc2 = 0, acc3 = 0;
+        for (int b = warp; b < (int)gridDim.x; b += kW) {
+          const float4 v = __ldcg(reinterpret_cast<const float4*>(a.part + (size_t)b * 2 * COUT) + c4);
+          acc0 += v.x;
+          acc1 += v.y;
+          acc2 += v.z;
+          acc3 += v.w;
+        }
+        dred[warp * 2 * COUT + 4 * c4 + 0] = acc0;
+        dred[warp * 2 * COUT + 4 * c4 + 1] = acc1;
+        dred[warp * 2 * COUT + 4 * c4 + 2] = acc2;
+        dred[warp * 2 * COUT + 4 * c4 + 3] = acc3;
+      }
+      __syncthreads();
+      for (int i = threadIdx.x; i < 2 * COUT; i += kThreads) {
+        double t = 0;
+        for (int w = 0; w < kW; ++w) t += dred[w * 2 * COUT + i];
+        fin[i] = t;
+      }
+      __syncthreads();
+      for (int c = threadIdx.x; c < COUT; c += kThreads) {
+        const double M = (double)a.m_count;
+        const double mean = fin[c] / M;
+        double var = fin[COUT + c] / M - mean * mean;
+        var = var > 0.0 ? var : 0.0;
+        const double inv = 1.0 / sqrt(var + (double)a.eps);
+        const double gm = a.gamma[c];
+        a.saved_mean[c] = (float)mean;
+        a.saved_inv_var[c] = (float)inv;
+        a.eq[c] = (float)(gm * inv);
+        a.eq[COUT + c] = (float)((double)a.beta[c] - gm * mean * inv);
+        const double mom = a.momentum;
+        a.running_mean[c] = (float)((1.0 - mom) * a.running_mean[c] + mom * mean);
+        a.running_var[c] = (float)((1.0 - mom) * a.running_var[c] + mom * var * M / (M - 1.0));
+      }
+    }
+  }
+
+  if (warp == R::kMmaWarp) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, kTmemCols);
+  }
+}
+
+// Host: geometry of a stride-1 halo conv (fills wp, p, q, hr, upi, total_units, um).
+inline bool finish_geom(HaloGeom& g, int U) {
+  g.um = U * 128;
+  g.wp = g.w + 2 * g.pad;
+  g.p = g.h + 2 * g.pad - g.r + 1;
+  g.q = g.w + 2 * g.pad - g.s + 1;
+  if (g.p <= 0 || g.q <= 0 || g.wp > 256) return false;
+  g.hr = (g.wp - 1 + g.um - 1 + (g.r - 1) * g.wp + g.s - 1) / g.wp + 1;
+  if (g.hr > 256) return false;
+  g.upi = (g.p * g.wp + g.um - 1) / g.um;
+  g.total_units = g.n_img * g.upi;
+  return true;
+}
+
+template <int KIND, int NCH, int NOUT, int U, bool WRES, bool BF16>
+int launch_halo_conv(const ConvArgs& a, const CUtensorMap& mx, const CUtensorMap& mw, int grid,
+                     cudaStream_t st) {
+  auto kern = halo_conv_kernel<KIND, NCH, NOUT, U, WRES, BF16>;
+  const Layout L = layout(a.g, KIND, NCH, NOUT, WRES);
+  const uint32_t smem = L.total + 1024;
+  if (smem > 227 * 1024) return 3;
+  if (!ensure_smem_attr(reinterpret_cast<const void*>(kern), 227 * 1024)) return 6;
+  kern<<<grid, Roles<KIND>::kThreads, smem, st>>>(mx, mw, a);
+  return cudaGetLastError() == cudaSuccess ? 0 : 6;
+}
+
+}  // namespace hc
+}  // namespace cbr
