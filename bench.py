@@ -1,0 +1,374 @@
+"""Benchmark of the CBR training step (forward train + backward) on GB300.
+
+Default workload: N=256, 56x56, 64->64, 3x3, fp16 (the large-batch feature-map case of the
+Tech-Renaissance CBR page, section 1).  One step = cbr_forward_train + cbr_backward (the whole
+hot path: conv+genstats+finalize, apply+ReLU+mask, masked BN reduction, wgrad, dgrad).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl cbr|reference] [--config ID]
+
+Prints ONE JSON line on rank 0.  Timing: CUDA events on the launching stream around each step
+(and, through the library's profiling hook, around each kernel), L2 flushed between steps
+outside the step events, clocks sampled with nvidia-smi during the timed region.
+`--impl reference` times the CPU oracle on the host cores instead (the reference arm).
+Multi-GPU runs are independent replicas (weak scaling; no collective on the data path).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+from conv_batchnorm_relu_gb300 import roofline  # noqa: E402
+from conv_batchnorm_relu_gb300.inputs import CONFIGS, make_inputs, seed_for  # noqa: E402
+
+METRIC = "CBR fwd+bwd images/s and TFLOP/s at N=256 56x56 64->64 3x3; % of roofline"
+FWD_KERNELS = ["conv_fprop_genstats", "bn_apply_relu"]
+BWD_KERNELS = ["bn_bwd_reduce", "conv_wgrad", "conv_wgrad_reduce", "conv_dgrad"]
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="cbr", choices=["cbr", "reference"])
+    ap.add_argument("--config", type=int, default=3)
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def workload_config(spec, l2_note: str) -> dict:
+    return {"workload": spec.name + (" fwd-train + bwd" + (" (no dx)" if spec.first_layer else "")),
+            "n": spec.n, "h": spec.h, "w": spec.w, "c_in": spec.c_in, "c_out": spec.c_out,
+            "r": spec.r, "s": spec.s, "stride": spec.stride, "pad": spec.pad, "dtype": spec.dtype,
+            "global_batch": spec.n, "parallelism": "replicas", "l2": l2_note}
+
+
+# ----------------------------------------------------------------------------- distributed
+def dist_setup(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if args.impl == "cbr" else "gloo"
+        dist.init_process_group(backend=backend)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(v: float, world: int, device) -> float:
+    if world == 1:
+        return v
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ----------------------------------------------------------------------------- clocks
+CLOCK_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+                "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+                "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+
+def start_clock_sampler(dev_index: int):
+    try:
+        return subprocess.Popen(["nvidia-smi", f"--query-gpu={CLOCK_FIELDS}", "--format=csv,noheader,nounits",
+                                 "-i", str(dev_index), "-lms", "100"],
+                                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+    except OSError:
+        return None
+
+
+def stop_clock_sampler(proc) -> dict:
+    if proc is None:
+        return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+    proc.terminate()
+    try:
+        out, _ = proc.communicate(timeout=5)
+    except subprocess.TimeoutExpired:
+        proc.kill()
+        out, _ = proc.communicate()
+    sm, smax, power, reasons = [], [], [], set()
+    names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+    for line in out.strip().splitlines():
+        f = [x.strip() for x in line.split(",")]
+        if len(f) < 9:
+            continue
+        try:
+            sm.append(float(f[1]))
+            smax.append(float(f[2]))
+            power.append(float(f[3]))
+        except ValueError:
+            continue
+        for nm, v in zip(names, f[5:9]):
+            if v.lower() == "active":
+                reasons.add(nm)
+    return {"sm_mhz": statistics.median(sm) if sm else None,
+            "sm_max_mhz": max(smax) if smax else None,
+            "power_w_max": max(power) if power else None,
+            "samples": len(sm), "reasons": sorted(reasons)}
+
+
+# ----------------------------------------------------------------------------- CPU oracle arm
+def oracle_images_per_s(spec, budget_s: float, max_images: int) -> dict:
+    """Time the fp64 CPU oracle (forward train + backward, as it stands) on a bounded sample of
+    the workload: the first k images of the batch, k sized to about `budget_s` of CPU work."""
+    import numpy as np
+
+    import oracle
+    oracle.build_lib()
+
+    def run(k):
+        sp = spec.with_(n=k)
+        inp = make_inputs(sp, seed_for(3))
+        o = {kk: v.double().numpy() for kk, v in inp.items()}
+        t0 = time.perf_counter()
+        f = oracle.forward_train(o["x"], o["w"], o["gamma"], o["beta"], o["running_mean"],
+                                 o["running_var"], sp.momentum, sp.eps, sp.stride, sp.pad)
+        oracle.backward(o["dy"], o["x"], o["w"], f, o["gamma"], sp.eps, sp.stride, sp.pad,
+                        need_dx=not sp.first_layer)
+        return time.perf_counter() - t0
+
+    t1 = run(1)
+    k = int(max(1, min(max_images, budget_s / max(t1, 1e-3))))
+    tk = run(k) if k > 1 else t1
+    return {"value": k / tk, "unit": "images/s", "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": f"{k} of {spec.n} images of the workload, fp64 forward train + backward "
+                      f"({tk:.1f} s; calibrated on 1 image in {t1:.2f} s)"}
+
+
+def run_reference(args, world, rank):
+    spec = CONFIGS[args.config]
+    if rank != 0:
+        return
+    import oracle
+    oracle.build_lib()
+    sp = spec.with_(n=1)
+    inp = make_inputs(sp, seed_for(args.config))
+    o = {k: v.double().numpy() for k, v in inp.items()}
+
+    def step():
+        f = oracle.forward_train(o["x"], o["w"], o["gamma"], o["beta"], o["running_mean"],
+                                 o["running_var"], sp.momentum, sp.eps, sp.stride, sp.pad)
+        oracle.backward(o["dy"], o["x"], o["w"], f, o["gamma"], sp.eps, sp.stride, sp.pad,
+                        need_dx=not sp.first_layer)
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    dt = time.perf_counter() - t0
+    value = args.steps / dt
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "images/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": workload_config(spec, "n/a (host CPU)"),
+            "cpu_baseline": {"value": value, "unit": "images/s", "cores": oracle.num_threads(),
+                             "kind": "oracle",
+                             "sample": "each step: 1 image of the workload, fp64 forward train + backward"},
+            "e2e": {"value": value, "unit": "images/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ----------------------------------------------------------------------------- GPU arm
+def traffic_for(kernel: str):
+    """Per-launch DRAM bytes from a committed ncu summary, if it matches the current source."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    import hashlib
+    with open(p) as f:
+        t = json.load(f)
+    ent = t.get(kernel)
+    if not ent:
+        return None
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "conv_batchnorm_relu_gb300", "csrc")
+    for fn in sorted(os.listdir(csrc)):
+        if fn.endswith((".cu", ".cuh", ".h")):
+            with open(os.path.join(csrc, fn), "rb") as f:
+                h.update(f.read())
+    if ent.get("csrc_sha256") != h.hexdigest():
+        return None
+    return ent.get("bytes_per_launch")
+
+
+def run_cbr(args, world, rank, local):
+    from conv_batchnorm_relu_gb300 import build, cbr
+    build.build()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    spec = CONFIGS[args.config]
+    need_dx = not spec.first_layer
+    layer = cbr.Layer.from_spec(spec)
+    inp = make_inputs(spec, seed_for(args.config) + rank)
+    g = {k: v.to(dev) for k, v in inp.items()}
+    fwd_b, bwd_b = cbr.workspace_size(layer)
+    ws_f, ws_b = cbr.new_workspace(fwd_b, dev), cbr.new_workspace(bwd_b, dev)
+    y = torch.empty((spec.n, spec.p, spec.q, spec.c_out), dtype=spec.torch_dtype, device=dev)
+    fo = {"y": y, "z": torch.empty_like(y), "mask": torch.empty(cbr.mask_words(layer), dtype=torch.int32, device=dev),
+          "saved_mean": torch.empty(spec.c_out, device=dev), "saved_inv_var": torch.empty(spec.c_out, device=dev)}
+    bo = {"dw": torch.empty((spec.c_out, spec.r, spec.s, spec.c_in), dtype=torch.float32, device=dev),
+          "dgamma": torch.empty(spec.c_out, device=dev), "dbeta": torch.empty(spec.c_out, device=dev)}
+    if need_dx:
+        bo["dx"] = torch.empty_like(g["x"])
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step(x, dy, fev=None, bev=None):
+        if fev:
+            cbr.profile_next_call(fev)
+        cbr.forward_train(layer, x, g["w"], g["gamma"], g["beta"], g["running_mean"],
+                          g["running_var"], spec.momentum, spec.eps, ws=ws_f, out=fo)
+        if bev:
+            cbr.profile_next_call(bev)
+        cbr.backward(layer, dy, x, g["w"], fo["mask"], cbr.CBR_MASK_BITS, fo["z"], g["gamma"],
+                     fo["saved_mean"], fo["saved_inv_var"], ws=ws_b, need_dx=need_dx, out=bo)
+
+    nf, nb = len(FWD_KERNELS) + 1, (len(BWD_KERNELS) if need_dx else len(BWD_KERNELS) - 1) + 1
+    K = args.steps
+    mk = lambda: torch.cuda.Event(enable_timing=True)
+    fevs = [[mk() for _ in range(nf)] for _ in range(K)]
+    bevs = [[mk() for _ in range(nb)] for _ in range(K)]
+    s_ev, e_ev = [mk() for _ in range(K)], [mk() for _ in range(K)]
+    for lst in fevs + bevs + [s_ev, e_ev]:
+        for e in lst:
+            e.record(stream)  # materialise the CUDA event handles
+    for _ in range(args.warmup):
+        flush.zero_()
+        step(g["x"], g["dy"])
+    cbr.stream_status()
+    barrier(world)
+    torch.cuda.synchronize()
+    clocks_proc = start_clock_sampler(local)
+    time.sleep(0.25)
+    t_wall0 = time.perf_counter()
+    for i in range(K):
+        flush.zero_()
+        s_ev[i].record(stream)
+        step(g["x"], g["dy"], fevs[i], bevs[i])
+        e_ev[i].record(stream)
+    torch.cuda.synchronize()
+    t_wall = time.perf_counter() - t_wall0
+    clocks = stop_clock_sampler(clocks_proc)
+    cbr.stream_status()
+    barrier(world)
+    step_ms = [s_ev[i].elapsed_time(e_ev[i]) for i in range(K)]
+    ms_local = sum(step_ms) / K
+    ms = max_over_ranks(ms_local, world, dev)
+    kern_names = FWD_KERNELS + (BWD_KERNELS if need_dx else BWD_KERNELS[:-1])
+    kern_ms = {}
+    for j, nm in enumerate(FWD_KERNELS):
+        kern_ms[nm] = sum(fevs[i][j].elapsed_time(fevs[i][j + 1]) for i in range(K)) / K
+    for j, nm in enumerate(kern_names[len(FWD_KERNELS):]):
+        kern_ms[nm] = sum(bevs[i][j].elapsed_time(bevs[i][j + 1]) for i in range(K)) / K
+
+    # ---------------------------------------------------------------- e2e (public API, host buffers)
+    E = args.e2e_steps
+    hx = inp["x"].pin_memory()
+    hdy = inp["dy"].pin_memory()
+    hdw = torch.empty(bo["dw"].shape, dtype=torch.float32).pin_memory()
+    hdg = torch.empty(spec.c_out, dtype=torch.float32).pin_memory()
+    hdb = torch.empty(spec.c_out, dtype=torch.float32).pin_memory()
+    xd, dyd = torch.empty_like(g["x"]), torch.empty_like(g["dy"])
+    h2d = hx.numel() * hx.element_size() + hdy.numel() * hdy.element_size()
+    d2h = (hdw.numel() + hdg.numel() + hdb.numel()) * 4
+    for _ in range(2):
+        xd.copy_(hx, non_blocking=True)
+        dyd.copy_(hdy, non_blocking=True)
+        step(xd, dyd)
+    torch.cuda.synchronize()
+    barrier(world)
+    t0 = time.perf_counter()
+    for _ in range(E):
+        xd.copy_(hx, non_blocking=True)
+        dyd.copy_(hdy, non_blocking=True)
+        step(xd, dyd)
+        hdw.copy_(bo["dw"], non_blocking=True)
+        hdg.copy_(bo["dgamma"], non_blocking=True)
+        hdb.copy_(bo["dbeta"], non_blocking=True)
+        torch.cuda.synchronize()
+    e2e_s = max_over_ranks((time.perf_counter() - t0) / E, world, dev)
+    cbr.stream_status()
+
+    if rank != 0:
+        return
+    peaks, peak_src = roofline.load_peaks()
+    ledger = {p.name: p for p in roofline.ledger(spec, need_dx)}
+    passes = {}
+    for nm, p in ledger.items():
+        roof_us, bound = p.roof_us(peaks, sustained=True)
+        t_us = kern_ms[nm] * 1e3
+        passes[nm] = {"us": round(t_us, 2), "roof_us": round(roof_us, 2), "bound": bound,
+                      "frac": round(roof_us / t_us, 4),
+                      "gbs": round(p.bytes / (t_us * 1e-6) / 1e9, 1),
+                      "tflops": round(p.flops / (t_us * 1e-6) / 1e12, 1)}
+    passes["conv_wgrad_reduce"] = {"us": round(kern_ms["conv_wgrad_reduce"] * 1e3, 2)}
+    dom = max(ledger, key=lambda nm: kern_ms[nm])
+    dp = ledger[dom]
+    _, dbound = dp.roof_us(peaks, sustained=True)
+    dt_s = kern_ms[dom] * 1e-3
+    if dbound == "tensor":
+        ach, pk, unit = dp.flops / dt_s / 1e12, peaks["bf16_tflops_sustained"], "TFLOP/s"
+    else:
+        ach, pk, unit = dp.bytes / dt_s / 1e9, peaks["hbm_gbs"], "GB/s"
+    conv_flops = spec.conv_flops() * (3 if need_dx else 2)
+    step_roof = roofline.step_roof_us(spec, peaks, need_dx)
+    images = spec.n * world
+    line = {
+        "metric": METRIC, "value": images / (ms * 1e-3), "unit": "images/s", "n_gpus": world,
+        "steps": K, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": spec.dtype, "data": "synthetic",
+        "config": workload_config(spec, "flushed (256 MB write) between timed steps, outside the step events"),
+        "tflops": conv_flops * world / (ms * 1e-3) / 1e12,
+        "roofline": {"kernel": dom, "bound": dbound, "achieved": ach, "peak": pk, "unit": unit,
+                     "frac": ach / pk, "traffic": traffic_for(dom),
+                     "peak_source": f"{peak_src} ({'sustained bf16 GEMM' if dbound == 'tensor' else 'STREAM copy'})"},
+        "roofline_step": {"ledger_us": round(step_roof, 2), "measured_us": round(ms * 1e3, 2),
+                          "frac": round(step_roof / (ms * 1e3), 4),
+                          "note": "sum of per-pass max(FLOPs/peak, min bytes/HBM) over the measured step"},
+        "passes": passes,
+        "e2e": {"value": images / e2e_s, "unit": "images/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": K * (len(kern_names)),
+        "clocks": clocks,
+        "wall_s_timed": round(t_wall, 3),
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = oracle_images_per_s(spec, budget_s=15.0, max_images=spec.n)
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    world, rank, local = dist_setup(args)
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+    else:
+        run_cbr(args, world, rank, local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

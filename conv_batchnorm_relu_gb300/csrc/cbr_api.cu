@@ -396,7 +396,8 @@ cbr_status_t cbr_backward(const cbr_desc_t* desc, const void* dy, const void* x,
   wa.part = reinterpret_cast<float*>(wsb + L.wpart);
   wa.dw = dw;
   wa.err = dev->err;
-  st = launch_wgrad(wa, (int)s.cin, (int)s.cout, s.bf16, x, dev->num_sms, cs);
+  st = launch_wgrad(wa, (int)s.cin, (int)s.cout, s.bf16, x, dev->num_sms, cs,
+                    [](void* p) { static_cast<Prof*>(p)->mark(); }, &prof);
   if (st) return (cbr_status_t)st;
   prof.mark();
 

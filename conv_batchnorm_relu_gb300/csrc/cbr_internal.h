@@ -121,8 +121,9 @@ struct WgradArgs {
   float* dw;                // [cout][r][s][cin]
   uint32_t* err;
 };
+// Launches the wgrad kernel, calls `between(ctx)` (if set), then the fixed-order reduction.
 int launch_wgrad(const WgradArgs& a, int c_in, int c_out, bool bf16, const void* x, int num_sms,
-                 cudaStream_t st);
+                 cudaStream_t st, void (*between)(void*) = nullptr, void* ctx = nullptr);
 size_t wgrad_partial_floats(int num_sms, int c_in, int c_out, int taps);
 
 }  // namespace cbr

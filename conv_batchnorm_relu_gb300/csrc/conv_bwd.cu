@@ -276,7 +276,7 @@ size_t wgrad_partial_floats(int num_sms, int c_in, int c_out, int taps) {
 }
 
 int launch_wgrad(const WgradArgs& w, int c_in, int c_out, bool bf16, const void* x, int num_sms,
-                 cudaStream_t st) {
+                 cudaStream_t st, void (*between)(void*), void* ctx) {
   WgKArgs a{};
   a.g = w.g;
   a.dz = DzSrc{w.dy, w.z, w.y, w.mask, w.coef, 0, 0, c_out};
@@ -323,6 +323,7 @@ int launch_wgrad(const WgradArgs& w, int c_in, int c_out, bool bf16, const void*
     default: return 3;
   }
   if (rc) return rc;
+  if (between) between(ctx);
   const long long total = (long long)taps * c_in * c_out;
   const int rgrid = (int)std::min<long long>((total + 255) / 256, 4LL * num_sms);
   wgrad_reduce_kernel<<<rgrid, 256, 0, st>>>(a.part, w.dw, a.plan, grid, c_out, c_in, taps, nout);
