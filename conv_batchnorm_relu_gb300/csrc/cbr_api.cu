@@ -202,6 +202,14 @@ bool encode_tiled(CUtensorMap* map, CUtensorMapDataType dt, int rank, const void
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+int forward_workspace_bytes(const void* desc, bool need_z, size_t* bytes) {
+  Shape s;
+  const int st = check_desc(static_cast<const cbr_desc_t*>(desc), &s);
+  if (st) return st;
+  *bytes = fwd_ws(s, need_z).total;
+  return CBR_OK;
+}
+
 bool ensure_smem_attr(const void* func, int bytes) {
   static std::mutex mu;
   static std::set<std::pair<int, const void*>> done;

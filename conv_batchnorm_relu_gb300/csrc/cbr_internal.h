@@ -57,6 +57,10 @@ enum FpropMode : int {
 // device and kernel; thread-safe).  Returns false if the runtime refuses.
 bool ensure_smem_attr(const void* func, int bytes);
 
+// Forward workspace bytes for a descriptor (z kept by the caller when !need_z); returns a
+// CBR status (cbr_api.cu).
+int forward_workspace_bytes(const void* desc, bool need_z, size_t* bytes);
+
 // Tensor-map helpers (cbr_api.cu).
 bool encode_tiled(CUtensorMap* map, CUtensorMapDataType dt, int rank, const void* base,
                   const uint64_t* dims, const uint64_t* strides_bytes, const uint32_t* box);

@@ -156,6 +156,32 @@ cbr_status_t cbr_forward_infer(const cbr_desc_t* desc, const void* x, const void
                                const float* b_fold, void* y, cbr_stream_t stream);
 
 /*
+ * Training forward that allocates nothing and takes no workspace.  The pages have no
+ * counterpart; this exists for callers that must not allocate device memory on their
+ * execution path, such as plug-ins that run inside another framework's execution loop with
+ * no access to its allocator, or latency-critical loops where cudaMalloc's cost and implicit
+ * synchronisation are unacceptable.
+ *   Same arguments and results as cbr_forward_train, except: no ws / ws_bytes, and z_saved
+ *   is required (INVALID_ARG when NULL), because the conv output cannot live in the fixed
+ *   scratch.
+ *   Scratch: a 320 KiB array compiled into the library, held by every GPU that loads it
+ *   until the process exits.  A problem whose scratch need exceeds it returns
+ *   CBR_ERR_WORKSPACE before anything is enqueued (with Cout <= 128 the need is about
+ *   257 KiB, so supported shapes fit).
+ *   The first call on each device looks up the array's device address (one
+ *   cudaGetSymbolAddress with that device current); make that first call before any stream
+ *   capture.  Each call clears the array's arrival counters with an asynchronous memset on
+ *   `stream`.  All calls share the one array: calls that overlap on the GPU (different streams
+ *   without ordering) race and give undefined results.  No cudaMalloc, cudaFree or other
+ *   allocating routine is called.
+ */
+cbr_status_t cbr_forward_train_noalloc(const cbr_desc_t* desc, const void* x, const void* w,
+                                       const float* gamma, const float* beta, float* running_mean,
+                                       float* running_var, float momentum, float eps, void* y,
+                                       uint32_t* relu_mask, void* z_saved, float* saved_mean,
+                                       float* saved_inv_var, cbr_stream_t stream);
+
+/*
  * Synchronise `stream`, then read and clear the device error word of the current device.
  * Returns CBR_OK, CBR_ERR_TIMEOUT if a kernel abandoned a bounded wait (its outputs are then
  * undefined), or CBR_ERR_CUDA if the stream reports a CUDA error.

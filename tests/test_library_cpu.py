@@ -114,3 +114,14 @@ def test_backward_rejects_dx_aliasing_x(lib):
 @pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-device path")
 def test_no_device_is_reported(lib):
     assert _fwd(lib, _desc()) == 5
+
+
+def test_noalloc_forward_requires_z_saved(lib):
+    f = lib.cbr_forward_train_noalloc
+    vp, fp = ctypes.c_void_p, ctypes.c_float
+    f.argtypes = [ctypes.POINTER(cbr.Desc), vp, vp, vp, vp, vp, vp, fp, fp, vp, vp, vp, vp, vp, vp]
+    f.restype = ctypes.c_int32
+    d = _desc()
+    assert f(ctypes.byref(d), P, P, P, P, P, P, 0.1, 1e-5, P, P, None, P, P, None) == 1
+    bad = _desc(c_out=12)
+    assert f(ctypes.byref(bad), P, P, P, P, P, P, 0.1, 1e-5, P, P, P, P, P, None) == 1
