@@ -25,6 +25,7 @@ struct HaloGeom {
   int um;            // output rows per unit (U * 128)
   int upi;           // units per image
   int total_units;
+  int box_rows;      // halo rows per TMA box (the halo is fetched as ceil(hr/box_rows) boxes)
 };
 
 struct FpropArgs {

@@ -51,7 +51,7 @@ bool make_plan(WgPlan& P, int taps, int c_in, int nout) {
     P.ta[gi] = 2 * gi;
     P.tb[gi] = std::min(2 * gi + 1, taps - 1);
   }
-  const int gcap = 512 / nout;
+  const int gcap = std::min(512 / nout, 16);  // TMEM columns; at most 16 groups per CTA
   const int nsub = (ngroups + gcap - 1) / gcap;
   const int nchunk = (c_in + 63) / 64;
   if (nsub * nchunk > kMaxSplits) return false;
@@ -142,13 +142,14 @@ __global__ void __launch_bounds__(kWgThreads, 1)
         const int n = u / g.upi;
         const int m0 = (u - n * g.upi) * g.um;
         const uint32_t s = it & 1, ph = (it >> 1) & 1;
-        if (!mbar_wait(bar_x_empty + 8 * s, ph ^ 1)) {
+        if (!mbar_wait_backoff(bar_x_empty + 8 * s, ph ^ 1, 128)) {
           hc::set_abort(abort_flag, a.err, kErrWaitHalo);
           break;
         }
         mbar_arrive_expect_tx(bar_x_full + 8 * s, tx);
-        tma_load_4d(x_addr + s * L.halo_stride, &map_x, chunk * 64, -g.pad, m0 / g.wp - g.pad, n,
-                    bar_x_full + 8 * s);
+        for (int r0 = 0; r0 < g.hr; r0 += g.box_rows)
+          tma_load_4d(x_addr + s * L.halo_stride + (uint32_t)r0 * g.wp * 128, &map_x, chunk * 64, -g.pad,
+                      m0 / g.wp - g.pad + r0, n, bar_x_full + 8 * s);
       }
       for (uint32_t k = (it > 2 ? it - 2 : 0); k < it; ++k)
         mbar_wait(bar_x_full + 8 * (k & 1), (k >> 1) & 1);
@@ -156,6 +157,14 @@ __global__ void __launch_bounds__(kWgThreads, 1)
   } else if (warp == 1) {
     if (lane == 0) {
       const uint32_t idesc = make_idesc_f16(128, NOUT, BF16, true, true);
+      // per-group A descriptor with a zero start address: LBO = the two taps' row distance
+      uint64_t a_grp[16];
+      for (int gl = 0; gl < ng && gl < 16; ++gl) {
+        const int ta = P.ta[g0 + gl], tb = P.tb[g0 + gl];
+        const int sha = (ta / g.s) * g.wp + ta % g.s;
+        const int shb = (tb / g.s) * g.wp + tb % g.s;
+        a_grp[gl] = make_sw128_desc((uint32_t)sha * 128u, (uint32_t)(shb - sha) * 128u, 1024, 0);
+      }
       uint32_t it = 0;
       bool first = true;
       for (int u = ustart; u < g.total_units && !hc::is_aborted(abort_flag); u += ustride, ++it) {
@@ -170,16 +179,14 @@ __global__ void __launch_bounds__(kWgThreads, 1)
         tc_fence_after();
         const uint32_t xh = x_addr + s * L.halo_stride;
         const uint32_t dzs = dz_addr + s * L.dz_stride;
+        uint64_t adesc[kMaxGroups < 16 ? kMaxGroups : 16];
+        for (int gl = 0; gl < ng; ++gl) adesc[gl] = a_grp[gl] + (uint64_t)(((xh + (uint32_t)off * 128u)) >> 4);
+        const uint64_t b0 = make_sw128_desc(dzs, g.um * 128, 1024, 0);
         for (int kk = 0; kk < g.um / 16; ++kk) {
-          const uint64_t bd = make_sw128_desc(dzs + kk * 2048, g.um * 128, 1024, 0);
-          for (int gl = 0; gl < ng; ++gl) {
-            const int ta = P.ta[g0 + gl], tb = P.tb[g0 + gl];
-            const int sha = (ta / g.s) * g.wp + ta % g.s;
-            const int shb = (tb / g.s) * g.wp + tb % g.s;
-            const uint64_t ad = make_sw128_desc(xh + (uint32_t)(off + kk * 16 + sha) * 128u,
-                                                (uint32_t)(shb - sha) * 128u, 1024, 0);
-            mma_f16_ss(tmem_base + gl * NOUT, ad, bd, idesc, (first && kk == 0) ? 0u : 1u);
-          }
+          const uint64_t bd = desc_add(b0, kk * 2048);
+          for (int gl = 0; gl < ng; ++gl)
+            mma_f16_ss(tmem_base + gl * NOUT, desc_add(adesc[gl], kk * 2048), bd, idesc,
+                       (first && kk == 0) ? 0u : 1u);
         }
         mma_commit(bar_x_empty + 8 * s);
         mma_commit(bar_dz_empty + 8 * s);
@@ -197,7 +204,7 @@ __global__ void __launch_bounds__(kWgThreads, 1)
       const int n = u / g.upi;
       const int m0 = (u - n * g.upi) * g.um;
       const uint32_t s = it & 1, ph = (it >> 1) & 1;
-      if (!mbar_wait(bar_dz_empty + 8 * s, ph ^ 1)) {
+      if (!mbar_wait_backoff(bar_dz_empty + 8 * s, ph ^ 1, 128)) {
         hc::set_abort(abort_flag, a.err, kErrWaitOperand);
         break;
       }
@@ -208,7 +215,7 @@ __global__ void __launch_bounds__(kWgThreads, 1)
       fence_proxy_async_smem();
       mbar_arrive(bar_dz_full + 8 * s);
     }
-    const bool ok = mbar_wait(bar_acc_full, 0);
+    const bool ok = mbar_wait_backoff(bar_acc_full, 0, 1024);
     if (!ok) hc::set_abort(abort_flag, a.err, kErrWaitMma);
     tc_fence_after();
     if (ok) {
@@ -238,29 +245,57 @@ __global__ void __launch_bounds__(kWgThreads, 1)
   }
 }
 
-// dW[k][tap][c] = sum over the CTAs of its split (fixed order, fp64 accumulation).
-__global__ void wgrad_reduce_kernel(const float* __restrict__ part, float* __restrict__ dw,
-                                    const WgPlan P, int grid, int cout, int cin, int taps, int nout) {
+// dW[k][tap][c] = sum over the CTAs of its split, in a fixed order with fp64 accumulation.
+// A block owns 64 consecutive outputs (k fastest, so partial reads are coalesced) and four
+// slices of the CTA list; the slices are combined in slice order.
+constexpr int kRedOut = 64, kRedSlices = 4;
+
+__global__ void __launch_bounds__(kRedOut * kRedSlices)
+    wgrad_reduce_kernel(const float* __restrict__ part, float* __restrict__ dw, const WgPlan P,
+                        int grid, int cout, int cin, int taps, int nout) {
+  __shared__ double red[kRedSlices][kRedOut];
   const long long total = (long long)taps * cin * cout;
-  for (long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
-       idx += (long long)gridDim.x * blockDim.x) {
-    const int k = (int)(idx % cout);
-    const int c = (int)((idx / cout) % cin);
-    const int tap = (int)(idx / ((long long)cout * cin));
+  const int j = threadIdx.x % kRedOut, sl = threadIdx.x / kRedOut;
+  const long long idx = (long long)blockIdx.x * kRedOut + j;
+  int split = 0, gl = 0, row = 0, k = 0, c = 0, tap = 0;
+  if (idx < total) {
+    k = (int)(idx % cout);
+    c = (int)((idx / cout) % cin);
+    tap = (int)(idx / ((long long)cout * cin));
     const int chunk = c >> 6, cl = c & 63;
-    int grp = 0, row = 0;
+    int grp = 0;
     for (int gi = 0; gi < P.ngroups; ++gi) {
       if (P.ta[gi] == tap) { grp = gi; row = cl; break; }
       if (P.tb[gi] == tap) { grp = gi; row = 64 + cl; break; }
     }
-    int split = 0;
     for (int s = 0; s < P.nsplit; ++s)
       if (P.split_chunk[s] == chunk && grp >= P.split_g0[s] && grp < P.split_g0[s] + P.split_ng[s]) split = s;
-    const int gl = grp - P.split_g0[split];
-    double acc = 0.0;
-    for (int b = split; b < grid; b += P.nsplit)
-      acc += (double)__ldg(part + (((size_t)b * P.gmax + gl) * 128 + row) * nout + k);
-    dw[((size_t)k * taps + tap) * cin + c] = (float)acc;
+    gl = grp - P.split_g0[split];
+  }
+  double acc = 0.0;
+  if (idx < total) {
+    const size_t stride_b = (size_t)P.gmax * 128 * nout;
+    const float* base = part + ((size_t)gl * 128 + row) * nout + k;
+    const int nb = (grid - split + P.nsplit - 1) / P.nsplit;  // CTAs of this split
+    int t = sl;
+    for (; t + 3 * kRedSlices < nb; t += 4 * kRedSlices) {
+      const float v0 = __ldg(base + (size_t)(split + (t + 0 * kRedSlices) * P.nsplit) * stride_b);
+      const float v1 = __ldg(base + (size_t)(split + (t + 1 * kRedSlices) * P.nsplit) * stride_b);
+      const float v2 = __ldg(base + (size_t)(split + (t + 2 * kRedSlices) * P.nsplit) * stride_b);
+      const float v3 = __ldg(base + (size_t)(split + (t + 3 * kRedSlices) * P.nsplit) * stride_b);
+      acc += (double)v0;
+      acc += (double)v1;
+      acc += (double)v2;
+      acc += (double)v3;
+    }
+    for (; t < nb; t += kRedSlices) acc += (double)__ldg(base + (size_t)(split + t * P.nsplit) * stride_b);
+  }
+  red[sl][j] = acc;
+  __syncthreads();
+  if (sl == 0 && idx < total) {
+    double t = red[0][j];
+    for (int q = 1; q < kRedSlices; ++q) t += red[q][j];
+    dw[((size_t)k * taps + tap) * cin + c] = (float)t;
   }
 }
 
@@ -299,7 +334,7 @@ int launch_wgrad(const WgradArgs& w, int c_in, int c_out, bool bf16, const void*
   {
     const uint64_t dims[4] = {(uint64_t)c_in, (uint64_t)g.w, (uint64_t)g.h, (uint64_t)g.n_img};
     const uint64_t strides[3] = {(uint64_t)c_in * 2, (uint64_t)g.w * c_in * 2, (uint64_t)g.h * g.w * c_in * 2};
-    const uint32_t box[4] = {64, (uint32_t)g.wp, (uint32_t)g.hr, 1};
+    const uint32_t box[4] = {64, (uint32_t)g.wp, (uint32_t)g.box_rows, 1};
     if (!encode_tiled(&mx, dt, 4, x, dims, strides, box)) return 6;
   }
   // every CTA gets at least one unit, so every partial it writes is initialised
@@ -325,8 +360,9 @@ int launch_wgrad(const WgradArgs& w, int c_in, int c_out, bool bf16, const void*
   if (rc) return rc;
   if (between) between(ctx);
   const long long total = (long long)taps * c_in * c_out;
-  const int rgrid = (int)std::min<long long>((total + 255) / 256, 4LL * num_sms);
-  wgrad_reduce_kernel<<<rgrid, 256, 0, st>>>(a.part, w.dw, a.plan, grid, c_out, c_in, taps, nout);
+  const int rgrid = (int)((total + kRedOut - 1) / kRedOut);
+  wgrad_reduce_kernel<<<rgrid, kRedOut * kRedSlices, 0, st>>>(a.part, w.dw, a.plan, grid, c_out, c_in,
+                                                              taps, nout);
   return cudaGetLastError() == cudaSuccess ? 0 : 6;
 }
 
@@ -336,6 +372,8 @@ int launch_dgrad(const DgradArgs& d, int c_in, int c_out, bool bf16, const void*
   a.g = d.g;
   a.out = d.dx;
   a.out_c = c_in;
+  a.out_shift = __builtin_ctz((unsigned)(c_in * 2 / 16));
+  if ((c_in * 2 / 16) & (c_in * 2 / 16 - 1)) return 3;  // stored chunks per pixel: a power of two
   a.mode = kFpropPlain;
   a.err = d.err;
   a.dz = DzSrc{d.dy, d.z, d.y, d.mask, d.coef, d.g.h, d.g.w, c_out};

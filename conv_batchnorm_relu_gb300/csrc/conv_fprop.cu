@@ -17,6 +17,7 @@ int launch_fprop(const FpropArgs& f, int c_in, int c_out, bool bf16, const void*
   a.g = f.g;
   a.out = f.z;
   a.out_c = c_out;
+  a.out_shift = __builtin_ctz((unsigned)(c_out * 2 / 16));
   a.mode = f.mode;
   a.part = f.part;
   a.ticket = f.ticket;
@@ -44,7 +45,7 @@ int launch_fprop(const FpropArgs& f, int c_in, int c_out, bool bf16, const void*
   {
     const uint64_t dims[4] = {(uint64_t)c_in, (uint64_t)g.w, (uint64_t)g.h, (uint64_t)g.n_img};
     const uint64_t strides[3] = {(uint64_t)c_in * 2, (uint64_t)g.w * c_in * 2, (uint64_t)g.h * g.w * c_in * 2};
-    const uint32_t box[4] = {64, (uint32_t)g.wp, (uint32_t)g.hr, 1};
+    const uint32_t box[4] = {64, (uint32_t)g.wp, (uint32_t)g.box_rows, 1};
     if (!encode_tiled(&mx, dt, 4, x, dims, strides, box)) return 6;
   }
   {

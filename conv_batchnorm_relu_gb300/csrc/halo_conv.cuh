@@ -9,7 +9,8 @@
 //   warps [0, A)       A producers (one halo stage per (unit, 64-channel chunk))
 //   warp  A            TMEM owner and single-thread tcgen05.mma issuer
 //   warp  A+1          TMA producer for the filter slabs (resident when they fit in smem)
-//   warps A+2 .. A+5   epilogue: TMEM -> registers -> staged tile -> stats / store
+//   warps A+2 .. A+9   epilogue, two warps per TMEM lane quadrant (each takes half of the
+//                      columns): TMEM -> registers -> staged tile -> stats / store
 // Pipelines: 2 halo stages, 2 TMEM accumulator stages (U*NOUT fp32 columns each), and a
 // 2-deep filter ring when the filter is streamed.  All waits are bounded (ptx.cuh).
 #pragma once
@@ -25,6 +26,7 @@ struct ConvArgs {
   HaloGeom g;
   void* out;                // [n][p][q][out_c] storage dtype: z, y (inference) or dx
   int out_c;                // channels stored per output pixel (<= NOUT)
+  int out_shift;            // log2 of the 16-byte chunks per stored output pixel
   int mode;                 // FpropMode (fprop only)
   // forward statistics / finalize
   float* part;
@@ -47,7 +49,8 @@ struct ConvArgs {
 
 namespace hc {
 
-constexpr int kEpiThreads = 128;
+constexpr int kEpiWarps = 8;
+constexpr int kEpiThreads = 32 * kEpiWarps;
 constexpr int kStreamStages = 2;
 
 constexpr int pow2_at_least(int v) {
@@ -62,7 +65,7 @@ struct Roles {
   static constexpr int kMmaWarp = kAWarps;
   static constexpr int kWWarp = kAWarps + 1;
   static constexpr int kEpiWarp0 = kAWarps + 2;
-  static constexpr int kThreads = (kAWarps + 6) * 32;
+  static constexpr int kThreads = (kAWarps + 2 + kEpiWarps) * 32;
 };
 
 // Bytes of one filter slab (one 64-channel K chunk x one tap).
@@ -71,7 +74,7 @@ __host__ __device__ constexpr int wslab_bytes(int kind, int nout) {
 }
 
 struct Layout {
-  uint32_t halo_stride, off_w, off_stage, off_bar, total, wslab;
+  uint32_t halo_stride, off_w, off_stage, off_rowtab, off_bar, total, wslab;
   int nsw;
 };
 
@@ -84,7 +87,8 @@ __host__ __device__ inline Layout layout(const HaloGeom& g, int kind, int nch, i
   L.off_w = 2 * L.halo_stride;
   L.off_stage = L.off_w + (uint32_t)L.nsw * L.wslab;
   const uint32_t stage = 128u * nout * 2;
-  L.off_bar = (L.off_stage + stage + 15u) & ~15u;
+  L.off_rowtab = L.off_stage + stage;                 // int32[128]: global row of each tile row
+  L.off_bar = (L.off_rowtab + 512u + 15u) & ~15u;
   const uint32_t nbar = 8 + 2 * L.nsw + 1;
   L.total = L.off_bar + nbar * 8 + 16;
   return L;
@@ -95,6 +99,26 @@ __device__ __forceinline__ bool is_aborted(volatile int* flag) { return *flag !=
 __device__ __forceinline__ void set_abort(volatile int* flag, uint32_t* err, uint32_t bits) {
   *flag = 1;
   report_error(err, bits);
+}
+
+// Warp reduce-scatter: on entry each lane holds L values (L = 16 or 32 channels of its own
+// row); on exit v[0] of every lane holds the sum over the 32 lanes of channel (lane >> s),
+// s = log2(32 / L).  log2(L) butterfly steps each halve the channel set a lane keeps.
+template <int L>
+__device__ __forceinline__ void reduce_scatter(float (&v)[L], int lane) {
+  int o = 16;
+#pragma unroll
+  for (int len = L; len > 1; len >>= 1, o >>= 1) {
+    const bool hi = (lane & o) != 0;
+#pragma unroll
+    for (int j = 0; j < len / 2; ++j) {
+      const float send = hi ? v[j] : v[j + len / 2];
+      const float keep = hi ? v[j + len / 2] : v[j];
+      v[j] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+    }
+  }
+#pragma unroll
+  for (; o >= 1; o >>= 1) v[0] += __shfl_xor_sync(0xffffffffu, v[0], o);
 }
 
 // Offset of chunk c of staged row `row` (pitch = NOUT*2 bytes).
@@ -111,9 +135,7 @@ __global__ void __launch_bounds__(Roles<KIND>::kThreads, 1)
   using R = Roles<KIND>;
   constexpr int kThreads = R::kThreads;
   constexpr int kPitch = NOUT * 2;
-  constexpr int kChunks = kPitch / 16;
   constexpr int kTmemCols = pow2_at_least(2 * U * NOUT);
-  constexpr int kPairs = NOUT / 2;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -177,13 +199,15 @@ __global__ void __launch_bounds__(Roles<KIND>::kThreads, 1)
           const int h_lo = m0 / g.wp - g.pad;
           for (int ch = 0; ch < NCH; ++ch, ++it) {
             const uint32_t s = it & 1, ph = (it >> 1) & 1;
-            if (!mbar_wait(bar_halo_empty + 8 * s, ph ^ 1)) {
+            if (!mbar_wait_backoff(bar_halo_empty + 8 * s, ph ^ 1, 128)) {
               set_abort(abort_flag, a.err, kErrWaitHalo);
               break;
             }
             mbar_arrive_expect_tx(bar_halo_full + 8 * s, tx);
-            tma_load_4d(halo_addr + s * L.halo_stride, &map_x, ch * 64, -g.pad, h_lo, n,
-                        bar_halo_full + 8 * s);
+            // several smaller boxes in flight instead of one large one (lower latency)
+            for (int r0 = 0; r0 < g.hr; r0 += g.box_rows)
+              tma_load_4d(halo_addr + s * L.halo_stride + (uint32_t)r0 * g.wp * 128, &map_x, ch * 64,
+                          -g.pad, h_lo + r0, n, bar_halo_full + 8 * s);
           }
         }
         // never leave the CTA with a copy in flight
@@ -201,7 +225,7 @@ __global__ void __launch_bounds__(Roles<KIND>::kThreads, 1)
         bool bad = false;
         for (int ch = 0; ch < NCH; ++ch, ++it) {
           const uint32_t s = it & 1, ph = (it >> 1) & 1;
-          if (!mbar_wait(bar_halo_empty + 8 * s, ph ^ 1)) {
+          if (!mbar_wait_backoff(bar_halo_empty + 8 * s, ph ^ 1, 128)) {
             set_abort(abort_flag, a.err, kErrWaitOperand);
             bad = true;
             break;
@@ -239,7 +263,7 @@ __global__ void __launch_bounds__(Roles<KIND>::kThreads, 1)
           for (int ch = 0; ch < NCH && !bad; ++ch)
             for (int tap = 0; tap < rs; ++tap, ++it) {
               const uint32_t s = it % kStreamStages, ph = (it / kStreamStages) & 1;
-              if (!mbar_wait(bar_w_empty + 8 * s, ph ^ 1)) {
+              if (!mbar_wait_backoff(bar_w_empty + 8 * s, ph ^ 1, 64)) {
                 set_abort(abort_flag, a.err, kErrWaitWeights);
                 bad = true;
                 break;
@@ -280,17 +304,23 @@ __global__ void __launch_bounds__(Roles<KIND>::kThreads, 1)
           }
           tc_fence_after();
           const uint32_t hbase = halo_addr + hs * L.halo_stride;
+          // A descriptors: one base per unit, taps and tiles are start-address offsets
+          const uint64_t a_base = make_sw128_desc(hbase + (uint32_t)off * 128u, 16, 1024, 0);
+          const uint64_t b_base = kBMn ? make_sw128_desc(w_addr, 8192, 1024, 0) : make_sw128_desc(w_addr, 16, 1024, 0);
+          int r = 0, sx = 0;
           for (int tap = 0; tap < rs; ++tap) {
-            const int r = tap / g.s, sx = tap - r * g.s;
-            uint32_t wslab, ws = 0;
+            uint32_t wslab_off, ws = 0;
             if (WRES) {
               const int i = ch * rs + tap;
-              if (first && !mbar_wait(bar_w_full + 8 * i, 0)) {
-                set_abort(abort_flag, a.err, kErrWaitWeights);
-                bad = true;
-                break;
+              if (first) {
+                if (!mbar_wait(bar_w_full + 8 * i, 0)) {
+                  set_abort(abort_flag, a.err, kErrWaitWeights);
+                  bad = true;
+                  break;
+                }
+                tc_fence_after();
               }
-              wslab = w_addr + i * L.wslab;
+              wslab_off = (uint32_t)i * L.wslab;
             } else {
               ws = wit % kStreamStages;
               if (!mbar_wait(bar_w_full + 8 * ws, (wit / kStreamStages) & 1)) {
@@ -298,18 +328,21 @@ __global__ void __launch_bounds__(Roles<KIND>::kThreads, 1)
                 bad = true;
                 break;
               }
-              wslab = w_addr + ws * L.wslab;
+              tc_fence_after();
+              wslab_off = ws * L.wslab;
             }
-            tc_fence_after();
-            const uint32_t a_row0 = hbase + (uint32_t)(off + r * g.wp + sx) * 128u;
+            const uint64_t a_tap = desc_add(a_base, (uint32_t)(r * g.wp + sx) * 128u);
+            const uint64_t b_tap = desc_add(b_base, wslab_off);
             for (int t = 0; t < ntiles; ++t) {
+              const uint64_t a_t = desc_add(a_tap, (uint32_t)t * 128u * 128u);
 #pragma unroll
-              for (int kk = 0; kk < 4; ++kk) {
-                const uint64_t ad = make_sw128_desc(a_row0 + t * 128 * 128 + kk * 32, 16, 1024, 0);
-                const uint64_t bd = kBMn ? make_sw128_desc(wslab + kk * 2048, 8192, 1024, 0)
-                                         : make_sw128_desc(wslab + kk * 32, 16, 1024, 0);
-                mma_f16_ss(d0 + t * NOUT, ad, bd, idesc, (ch | tap | kk) != 0);
-              }
+              for (int kk = 0; kk < 4; ++kk)
+                mma_f16_ss(d0 + t * NOUT, desc_add(a_t, kk * 32), desc_add(b_tap, kBMn ? kk * 2048 : kk * 32),
+                           idesc, (ch | tap | kk) != 0);
+            }
+            if (++sx == g.s) {
+              sx = 0;
+              ++r;
             }
             if (!WRES) {
               mma_commit(bar_w_empty + 8 * ws);
@@ -328,16 +361,24 @@ __global__ void __launch_bounds__(Roles<KIND>::kThreads, 1)
     }
   } else {
     // ------------------------------------------------------------ epilogue
-    const int quad = warp & 3;                       // TMEM lanes 32*quad .. +31
-    const int e = quad * 32 + lane;                  // M-tile row owned by this thread
-    const int et = threadIdx.x - 32 * R::kEpiWarp0;  // rank among epilogue threads
-    constexpr int kPL = (kPairs + 31) / 32;
-    float s1[2 * kPL], s2[2 * kPL];
+    constexpr int kHalves = NOUT >= 64 ? 2 : 1;
+    constexpr int kCPH = NOUT / kHalves;        // channels per half
+    constexpr int kSB = kCPH < 32 ? kCPH : 32;  // channels per reduce block
+    constexpr int kNB = kCPH / kSB;             // reduce blocks per half
+    constexpr int kSh = kSB == 32 ? 0 : 1;      // lane -> channel shift after reduce-scatter
+    const int ew = warp - R::kEpiWarp0;         // 0..7
+    const int quad = warp & 3;                  // TMEM lanes 32*quad .. +31
+    const int half = ew >> 2;
+    const int e = quad * 32 + lane;             // M-tile row owned by this thread
+    const int et = threadIdx.x - 32 * R::kEpiWarp0;
+    int* rowtab = reinterpret_cast<int*>(smem + L.off_rowtab);
+    float s1[kNB], s2[kNB];
 #pragma unroll
-    for (int i = 0; i < 2 * kPL; ++i) s1[i] = s2[i] = 0.f;
+    for (int b = 0; b < kNB; ++b) s1[b] = s2[b] = 0.f;
     const bool stats = KIND == kKindFprop && a.mode == kFpropStats;
     const bool bias_relu = KIND == kKindFprop && a.mode == kFpropBiasRelu;
-    const int out_chunks = a.out_c * 2 / 16;
+    const int osh = a.out_shift;
+    const size_t opitch = (size_t)a.out_c * 2;
     uint8_t* obase = static_cast<uint8_t*>(a.out);
     uint32_t ait = 0;
     for (int u = blockIdx.x; u < g.total_units && !is_aborted(abort_flag); u += gridDim.x) {
@@ -345,89 +386,76 @@ __global__ void __launch_bounds__(Roles<KIND>::kThreads, 1)
       const int m0 = (u - n * g.upi) * g.um;
       const int ntiles = min(U, (rows_img - m0 + 127) / 128);
       const uint32_t as = ait & 1, aph = (ait >> 1) & 1;
-      bool ok = mbar_wait(bar_acc_full + 8 * as, aph);
+      bool ok = mbar_wait_backoff(bar_acc_full + 8 * as, aph, 256);
       if (!ok) set_abort(abort_flag, a.err, kErrWaitMma);
-      // uniform decision across the 128 epilogue threads (they share named barriers below)
+      // uniform decision across the epilogue threads (they share named barriers below)
       if (!named_bar_and(2, kEpiThreads, ok && !is_aborted(abort_flag))) break;
       tc_fence_after();
       for (int t = 0; t < ntiles; ++t) {
-        uint32_t pk[NOUT / 2];
+        const int mt = m0 + t * 128;
+        const int m = mt + e;
+        const int p = m / g.wp, q = m - p * g.wp;
+        const bool valid = (p < g.p) && (q < g.q);
+        if (half < kHalves) {
 #pragma unroll
-        for (int c16 = 0; c16 < NOUT / 16; ++c16) {
-          uint32_t r[16];
-          tmem_ld16(tmem_base + ((uint32_t)(quad * 32) << 16) + as * (U * NOUT) + t * NOUT + c16 * 16, r);
-          tmem_ld_wait();
+          for (int b = 0; b < kNB; ++b) {
+            const int c0 = half * kCPH + b * kSB;
+            uint32_t r[kSB];
 #pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            float lo = __uint_as_float(r[2 * i]), hi = __uint_as_float(r[2 * i + 1]);
-            if (bias_relu) {
-              lo = fmaxf(lo + __ldg(a.bias + c16 * 16 + 2 * i), 0.f);
-              hi = fmaxf(hi + __ldg(a.bias + c16 * 16 + 2 * i + 1), 0.f);
+            for (int q16 = 0; q16 < kSB / 16; ++q16)
+              tmem_ld16(tmem_base + ((uint32_t)(quad * 32) << 16) + as * (U * NOUT) + t * NOUT + c0 + q16 * 16,
+                        *reinterpret_cast<uint32_t(*)[16]>(r + q16 * 16));
+            tmem_ld_wait();
+            float v[kSB];
+#pragma unroll
+            for (int i = 0; i < kSB; ++i) {
+              float x = __uint_as_float(r[i]);
+              if (bias_relu) x = fmaxf(x + __ldg(a.bias + c0 + i), 0.f);
+              v[i] = valid ? x : 0.f;
             }
-            pk[c16 * 8 + i] = pack2<BF16>(lo, hi);
+#pragma unroll
+            for (int cc = 0; cc < kSB / 8; ++cc)
+              st_shared_v4(stage_addr + stage_off<kPitch>(e, c0 / 8 + cc),
+                           make_uint4(pack2<BF16>(v[8 * cc + 0], v[8 * cc + 1]), pack2<BF16>(v[8 * cc + 2], v[8 * cc + 3]),
+                                      pack2<BF16>(v[8 * cc + 4], v[8 * cc + 5]), pack2<BF16>(v[8 * cc + 6], v[8 * cc + 7])));
+            if (stats) {
+              float sq[kSB];
+#pragma unroll
+              for (int i = 0; i < kSB; ++i) sq[i] = v[i] * v[i];
+              reduce_scatter<kSB>(v, lane);
+              reduce_scatter<kSB>(sq, lane);
+              s1[b] += v[0];
+              s2[b] += sq[0];
+            }
           }
         }
         if (t == ntiles - 1) {
           tc_fence_before();
           mbar_arrive(bar_acc_empty + 8 * as);
         }
-        const int mt = m0 + t * 128;
-        {
-          const int m = mt + e;
-          const int p = m / g.wp, q = m - p * g.wp;
-          const bool valid = (p < g.p) && (q < g.q);
-#pragma unroll
-          for (int c = 0; c < kChunks; ++c) {
-            const uint4 v = valid ? make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3])
-                                  : make_uint4(0, 0, 0, 0);
-            st_shared_v4(stage_addr + stage_off<kPitch>(e, c), v);
-          }
-        }
+        if (half == 0) rowtab[e] = valid ? (int)(((long long)n * g.p + p) * g.q + q) : -1;
         named_bar_sync(1, kEpiThreads);
-        if (stats) {
-          for (int row = quad * 32; row < quad * 32 + 32; ++row) {
-#pragma unroll
-            for (int k = 0; k < kPL; ++k) {
-              const int j = lane + 32 * k;
-              if (j < kPairs) {
-                const int c = 2 * j;
-                const uint32_t o = stage_off<kPitch>(row, c >> 3) + (c & 7) * 2;
-                const float2 v = unpack2<BF16>(ld_shared_b32(stage_addr + o));
-                s1[2 * k] += v.x;
-                s1[2 * k + 1] += v.y;
-                s2[2 * k] = fmaf(v.x, v.x, s2[2 * k]);
-                s2[2 * k + 1] = fmaf(v.y, v.y, s2[2 * k + 1]);
-              }
-            }
-          }
-        }
         // coalesced copy-out of the valid rows
-        for (int i = et; i < 128 * out_chunks; i += kEpiThreads) {
-          const int row = i / out_chunks, c = i - row * out_chunks;
-          const int m = mt + row;
-          const int p = m / g.wp, q = m - p * g.wp;
-          if (p < g.p && q < g.q) {
-            const size_t gi = ((size_t)n * g.p + p) * g.q + q;
-            st_global_v4(obase + gi * (size_t)a.out_c * 2 + c * 16,
+        const int nchunk = 128 << osh;
+        for (int i = et; i < nchunk; i += kEpiThreads) {
+          const int row = i >> osh, c = i & ((1 << osh) - 1);
+          const int gr = rowtab[row];
+          if (gr >= 0)
+            st_global_v4(obase + (size_t)gr * opitch + c * 16,
                          ld_shared_v4(stage_addr + stage_off<kPitch>(row, c)));
-          }
         }
         named_bar_sync(1, kEpiThreads);
       }
       ++ait;
     }
-    if (stats) {
-      // per-warp partials -> smem; the staging buffer is free behind the last named barrier
+    if (stats && half < kHalves && (lane & ((1 << kSh) - 1)) == 0) {
+      // per-(quad) partials -> smem; the staging buffer is free behind the last named barrier
       float* red = reinterpret_cast<float*>(smem + L.off_stage);
 #pragma unroll
-      for (int k = 0; k < kPL; ++k) {
-        const int j = lane + 32 * k;
-        if (j < kPairs) {
-          red[(quad * 2 + 0) * NOUT + 2 * j] = s1[2 * k];
-          red[(quad * 2 + 0) * NOUT + 2 * j + 1] = s1[2 * k + 1];
-          red[(quad * 2 + 1) * NOUT + 2 * j] = s2[2 * k];
-          red[(quad * 2 + 1) * NOUT + 2 * j + 1] = s2[2 * k + 1];
-        }
+      for (int b = 0; b < kNB; ++b) {
+        const int c = half * kCPH + b * kSB + (lane >> kSh);
+        red[(quad * 2 + 0) * NOUT + c] = s1[b];
+        red[(quad * 2 + 1) * NOUT + c] = s2[b];
       }
     }
   }
@@ -510,6 +538,11 @@ inline bool finish_geom(HaloGeom& g, int U) {
   g.q = g.w + 2 * g.pad - g.s + 1;
   if (g.p <= 0 || g.q <= 0 || g.wp > 256) return false;
   g.hr = (g.wp - 1 + g.um - 1 + (g.r - 1) * g.wp + g.s - 1) / g.wp + 1;
+#ifndef CBR_HALO_BOX_ROWS
+#define CBR_HALO_BOX_ROWS 1
+#endif
+  g.box_rows = CBR_HALO_BOX_ROWS < g.hr ? CBR_HALO_BOX_ROWS : g.hr;
+  g.hr = (g.hr + g.box_rows - 1) / g.box_rows * g.box_rows;
   if (g.hr > 256) return false;
   g.upi = (g.p * g.wp + g.um - 1) / g.um;
   g.total_units = g.n_img * g.upi;

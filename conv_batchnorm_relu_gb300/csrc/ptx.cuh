@@ -71,6 +71,20 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
   }
 }
 
+// Wait for a phase like mbar_wait, but sleep `sleep_ns` between polls.  For threads whose wait
+// is not on the critical path (epilogue, producers): a spinning warp steals issue slots from the
+// single thread that feeds the tensor cores on the same scheduler.
+__device__ __forceinline__ bool mbar_wait_backoff(uint32_t bar, uint32_t parity, uint32_t sleep_ns,
+                                                  uint64_t limit_ns = kWaitLimitNs) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (true) {
+    __nanosleep(sleep_ns);
+    if (mbar_try_wait(bar, parity)) return true;
+    if (globaltimer_ns() - t0 > limit_ns) return false;
+  }
+}
+
 // ---------------------------------------------------------------- TMA
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int c0, int c1,
                                             uint32_t bar) {
@@ -200,6 +214,12 @@ __device__ __forceinline__ uint64_t make_sw128_desc(uint32_t saddr, uint32_t lbo
   d |= static_cast<uint64_t>(base_offset & 7) << 49;
   d |= 2ull << 61;
   return d;
+}
+
+// Advance a shared-memory descriptor's start address by `bytes` (a multiple of 16; the address
+// stays below 256 KiB, so the 14-bit field cannot carry into the next one).
+__device__ __forceinline__ uint64_t desc_add(uint64_t desc, uint32_t bytes) {
+  return desc + (uint64_t)(bytes >> 4);
 }
 
 // Instruction descriptor for kind::f16 with fp32 accumulation.
