@@ -192,7 +192,89 @@ __global__ void __launch_bounds__(kRedThreads)
   }
 }
 
+// dz = a*g - d*z + e with g = dy*mask, written to HBM (used when no dgrad kernel produces it).
+template <bool BF16, bool MASKBITS>
+__global__ void __launch_bounds__(kApplyThreads)
+    dz_kernel(const DzArgs a) {
+  __shared__ float s_coef[3 * 256];
+  for (int i = threadIdx.x; i < 3 * a.c; i += kApplyThreads) s_coef[i] = a.coef[i];
+  __syncthreads();
+  const long long nvec = a.total / 8;
+  const int cvec = a.c / 8;
+  const long long stride = (long long)gridDim.x * kApplyThreads;
+  const uint8_t* dyb = static_cast<const uint8_t*>(a.dy);
+  const uint8_t* zb = static_cast<const uint8_t*>(a.z);
+  const uint8_t* yb = static_cast<const uint8_t*>(a.y);
+  uint8_t* ob = static_cast<uint8_t*>(a.dz);
+  for (long long v0 = (long long)blockIdx.x * kApplyThreads + threadIdx.x; v0 < nvec;
+       v0 += stride * kApplyUnroll) {
+    uint4 dv[kApplyUnroll], zv[kApplyUnroll], yv[kApplyUnroll];
+    uint32_t mb[kApplyUnroll];
+#pragma unroll
+    for (int k = 0; k < kApplyUnroll; ++k) {
+      const long long v = v0 + k * stride;
+      if (v < nvec) {
+        dv[k] = ld_global_nc_v4(dyb + v * 16);
+        zv[k] = ld_global_nc_v4(zb + v * 16);
+        if (MASKBITS) mb[k] = a.mask[v];
+        else yv[k] = ld_global_nc_v4(yb + v * 16);
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < kApplyUnroll; ++k) {
+      const long long v = v0 + k * stride;
+      if (v < nvec) {
+        const int c0 = (int)(v % cvec) * 8;
+        uint32_t bits;
+        if (MASKBITS) {
+          bits = mb[k];
+        } else {
+          const uint32_t yw[4] = {yv[k].x, yv[k].y, yv[k].z, yv[k].w};
+          bits = 0;
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const float2 yy = unpack2<BF16>(yw[j]);
+            bits |= (yy.x > 0.f ? 1u : 0u) << (2 * j);
+            bits |= (yy.y > 0.f ? 1u : 0u) << (2 * j + 1);
+          }
+        }
+        const uint32_t dw[4] = {dv[k].x, dv[k].y, dv[k].z, dv[k].w};
+        const uint32_t zw[4] = {zv[k].x, zv[k].y, zv[k].z, zv[k].w};
+        uint32_t o[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const float2 d = unpack2<BF16>(dw[j]);
+          const float2 z = unpack2<BF16>(zw[j]);
+          const int c = c0 + 2 * j;
+          const float g0 = (bits >> (2 * j)) & 1u ? d.x : 0.f;
+          const float g1 = (bits >> (2 * j + 1)) & 1u ? d.y : 0.f;
+          const float r0 = fmaf(s_coef[c], g0, fmaf(-s_coef[a.c + c], z.x, s_coef[2 * a.c + c]));
+          const float r1 = fmaf(s_coef[c + 1], g1, fmaf(-s_coef[a.c + c + 1], z.y, s_coef[2 * a.c + c + 1]));
+          o[j] = pack2<BF16>(r0, r1);
+        }
+        st_global_v4(ob + v * 16, make_uint4(o[0], o[1], o[2], o[3]));
+      }
+    }
+  }
+}
+
 }  // namespace
+
+int launch_dz(const DzArgs& a, bool bf16, int num_sms, cudaStream_t st) {
+  if (a.c % 8 != 0 || a.c > 256) return 3;
+  const long long nvec = a.total / 8;
+  const long long want = (nvec + kApplyThreads * kApplyUnroll - 1) / (kApplyThreads * kApplyUnroll);
+  const int grid = (int)std::max<long long>(1, std::min<long long>(want, (long long)num_sms * 8));
+  const bool bits = a.mask != nullptr;
+  if (bf16) {
+    if (bits) dz_kernel<true, true><<<grid, kApplyThreads, 0, st>>>(a);
+    else dz_kernel<true, false><<<grid, kApplyThreads, 0, st>>>(a);
+  } else {
+    if (bits) dz_kernel<false, true><<<grid, kApplyThreads, 0, st>>>(a);
+    else dz_kernel<false, false><<<grid, kApplyThreads, 0, st>>>(a);
+  }
+  return cudaGetLastError() == cudaSuccess ? 0 : 6;
+}
 
 int launch_apply(const ApplyArgs& a, bool bf16, int num_sms, cudaStream_t st) {
   if (a.c % 8 != 0 || a.c > 256) return 3;

@@ -147,14 +147,15 @@ FwdWs fwd_ws(const Shape& s, bool need_z) {
   return L;
 }
 struct BwdWs {
-  size_t coef, part, wpart, z, total;
+  size_t coef, part, wpart, dz, z, total;
 };
 BwdWs bwd_ws(const Shape& s, bool need_z) {
   BwdWs L;
   L.coef = kHdrBytes;
   L.part = align_up(L.coef + 3 * s.cout * sizeof(float), 256);
   L.wpart = align_up(L.part + bwd_reduce_partial_floats(kMaxCtas, (int)s.cout) * sizeof(float), 256);
-  L.z = align_up(L.wpart + wgrad_partial_floats(kMaxCtas, (int)s.cin, (int)s.cout, (int)(s.r * s.s)) * sizeof(float), 256);
+  L.dz = align_up(L.wpart + wgrad_partial_floats(kMaxCtas, (int)s.cin, (int)s.cout, (int)(s.r * s.s)) * sizeof(float), 256);
+  L.z = align_up(L.dz + act_bytes(s.n, s.p, s.q, s.cout, s.elt), 256);  // dz materialised for wgrad
   L.total = need_z ? align_up(L.z + act_bytes(s.n, s.p, s.q, s.cout, s.elt), 256) : L.z;
   return L;
 }
@@ -392,9 +393,28 @@ cbr_status_t cbr_backward(const cbr_desc_t* desc, const void* dy, const void* x,
   if (st) return (cbr_status_t)st;
   prof.mark();
 
+  // dz = a*(dy*mask) - d*z + e is materialised once when the TMA-fed wgrad can use it.
+  const bool dz_tma = wgrad_dz_tma_fits(make_geom(s), (int)s.cout);
+  void* dz_buf = wsb + L.dz;
+  if (dz_tma) {
+    DzArgs za{};
+    za.dy = dy;
+    za.z = z;
+    za.y = yv;
+    za.mask = mask;
+    za.coef = coef;
+    za.dz = dz_buf;
+    za.total = s.m * s.cout;
+    za.c = (int)s.cout;
+    st = launch_dz(za, s.bf16, dev->num_sms, cs);
+    if (st) return (cbr_status_t)st;
+    prof.mark();
+  }
+
   // WGrad first, then DGrad (CBR page, section 5.2 orders DGrad after WGrad because its dX
   // overwrote X there; here dx may not alias x, so the order is only kept for familiarity).
   WgradArgs wa{};
+  wa.dz_full = dz_tma ? dz_buf : nullptr;
   wa.g = make_geom(s);
   wa.dy = dy;
   wa.z = z;

@@ -124,8 +124,24 @@ struct WgradArgs {
   const float* coef;
   float* part;              // [grid][taps*cin][cout] per-CTA partial dW
   float* dw;                // [cout][r][s][cin]
+  const void* dz_full;      // materialised dz [n][p][q][cout], or null to compute it in-kernel
   uint32_t* err;
 };
+// Whether the TMA-fed wgrad (dz read from HBM) fits shared memory for this geometry.
+bool wgrad_dz_tma_fits(const HaloGeom& g, int c_out);
+
+struct DzArgs {
+  const void* dy;
+  const void* z;
+  const void* y;            // mask source when mask == null (y > 0)
+  const uint8_t* mask;
+  const float* coef;        // [3][c]
+  void* dz;                 // [m][c] output, storage dtype
+  long long total;          // elements
+  int c;
+};
+// dz = a*(dy*mask) - d*z + e, elementwise (bn_kernels.cu).
+int launch_dz(const DzArgs& a, bool bf16, int num_sms, cudaStream_t st);
 // Launches the wgrad kernel, calls `between(ctx)` (if set), then the fixed-order reduction.
 int launch_wgrad(const WgradArgs& a, int c_in, int c_out, bool bf16, const void* x, int num_sms,
                  cudaStream_t st, void (*between)(void*) = nullptr, void* ctx = nullptr);

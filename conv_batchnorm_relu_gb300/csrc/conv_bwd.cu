@@ -15,6 +15,7 @@
 // the whole kernel, writes one fp32 partial, and a second kernel sums the partials in a fixed
 // order (deterministic).
 #include <algorithm>
+#include <type_traits>
 
 #include "halo_conv.cuh"
 
@@ -71,30 +72,40 @@ bool make_plan(WgPlan& P, int taps, int c_in, int nout) {
 }
 
 struct WgLayout {
-  uint32_t halo_stride, dz_stride, off_dz, off_bar, total;
+  uint32_t halo_stride, dz_sub, dz_stride, off_dz, off_bar, total;
+  int dz_rows;  // image rows per dz tile when dz is loaded by TMA
 };
 
-__host__ __device__ inline WgLayout wg_layout(const HaloGeom& g, int nout) {
+// dz tile rows when dz comes from HBM: the unit's um padded-linear rows start at column
+// offset < wp of its first image row.
+__host__ __device__ inline int wg_dz_rows(const HaloGeom& g) { return (g.wp - 1 + g.um + g.wp - 1) / g.wp; }
+
+__host__ __device__ inline WgLayout wg_layout(const HaloGeom& g, int nout, bool dztma) {
   WgLayout L;
   L.halo_stride = (((uint32_t)g.hr * g.wp * 128) + 1023u) & ~1023u;
   const int nkc = nout > 64 ? nout / 64 : 1;
-  L.dz_stride = (uint32_t)nkc * g.um * 128;
+  L.dz_rows = wg_dz_rows(g);
+  L.dz_sub = dztma ? (((uint32_t)L.dz_rows * g.wp * 128 + 1023u) & ~1023u) : (uint32_t)g.um * 128;
+  L.dz_stride = (uint32_t)nkc * L.dz_sub;
   L.off_dz = 2 * L.halo_stride;
   L.off_bar = L.off_dz + 2 * L.dz_stride;
   L.total = L.off_bar + 12 * 8 + 16;
   return L;
 }
 
-template <int NOUT, bool BF16>
+// DZTMA: dz is read from HBM by TMA (materialised earlier), so warp 0 loads both operands and
+// no producer threads are needed; otherwise warps 2-5 compute dz from dy, z and the mask.
+template <int NOUT, bool BF16, bool DZTMA>
 __global__ void __launch_bounds__(kWgThreads, 1)
-    wgrad_kernel(const __grid_constant__ CUtensorMap map_x, const WgKArgs a) {
+    wgrad_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUtensorMap map_dz,
+                 const WgKArgs a) {
   constexpr int kNkc = NOUT > 64 ? NOUT / 64 : 1;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   const HaloGeom& g = a.g;
   const WgPlan& P = a.plan;
-  const WgLayout L = wg_layout(g, NOUT);
+  const WgLayout L = wg_layout(g, NOUT, DZTMA);
   const uint32_t sbase = smem_u32(smem);
   const uint32_t x_addr = sbase, dz_addr = sbase + L.off_dz;
   const uint32_t bar0 = sbase + L.off_bar;
@@ -136,7 +147,9 @@ __global__ void __launch_bounds__(kWgThreads, 1)
   if (warp == 0) {
     if (lane == 0) {
       prefetch_tensormap(&map_x);
-      const uint32_t tx = (uint32_t)g.hr * g.wp * 128;
+      if (DZTMA) prefetch_tensormap(&map_dz);
+      const uint32_t tx = (uint32_t)g.hr * g.wp * 128 +
+                          (DZTMA ? (uint32_t)kNkc * L.dz_rows * g.wp * 128 : 0u);
       uint32_t it = 0;
       for (int u = ustart; u < g.total_units && !hc::is_aborted(abort_flag); u += ustride, ++it) {
         const int n = u / g.upi;
@@ -146,10 +159,15 @@ __global__ void __launch_bounds__(kWgThreads, 1)
           hc::set_abort(abort_flag, a.err, kErrWaitHalo);
           break;
         }
+        // the x and dz stages are released together by the same MMA commit
         mbar_arrive_expect_tx(bar_x_full + 8 * s, tx);
         for (int r0 = 0; r0 < g.hr; r0 += g.box_rows)
           tma_load_4d(x_addr + s * L.halo_stride + (uint32_t)r0 * g.wp * 128, &map_x, chunk * 64, -g.pad,
                       m0 / g.wp - g.pad + r0, n, bar_x_full + 8 * s);
+        if (DZTMA)
+          for (int kc = 0; kc < kNkc; ++kc)
+            tma_load_4d(dz_addr + s * L.dz_stride + kc * L.dz_sub, &map_dz, kc * 64, 0, m0 / g.wp, n,
+                        bar_x_full + 8 * s);
       }
       for (uint32_t k = (it > 2 ? it - 2 : 0); k < it; ++k)
         mbar_wait(bar_x_full + 8 * (k & 1), (k >> 1) & 1);
@@ -157,13 +175,19 @@ __global__ void __launch_bounds__(kWgThreads, 1)
   } else if (warp == 1) {
     if (lane == 0) {
       const uint32_t idesc = make_idesc_f16(128, NOUT, BF16, true, true);
-      // per-group A descriptor with a zero start address: LBO = the two taps' row distance
-      uint64_t a_grp[16];
-      for (int gl = 0; gl < ng && gl < 16; ++gl) {
-        const int ta = P.ta[g0 + gl], tb = P.tb[g0 + gl];
-        const int sha = (ta / g.s) * g.wp + ta % g.s;
-        const int shb = (tb / g.s) * g.wp + tb % g.s;
-        a_grp[gl] = make_sw128_desc((uint32_t)sha * 128u, (uint32_t)(shb - sha) * 128u, 1024, 0);
+      // per-group A descriptor with a zero start address: LBO = the two taps' row distance.
+      // Kept in registers (fully unrolled over the compile-time maximum group count).
+      constexpr int kG = (512 / NOUT) < 16 ? (512 / NOUT) : 16;
+      uint64_t a_grp[kG];
+#pragma unroll
+      for (int gl = 0; gl < kG; ++gl) {
+        a_grp[gl] = 0;
+        if (gl < ng) {
+          const int ta = P.ta[g0 + gl], tb = P.tb[g0 + gl];
+          const int sha = (ta / g.s) * g.wp + ta % g.s;
+          const int shb = (tb / g.s) * g.wp + tb % g.s;
+          a_grp[gl] = make_sw128_desc((uint32_t)sha * 128u, (uint32_t)(shb - sha) * 128u, 1024, 0);
+        }
       }
       uint32_t it = 0;
       bool first = true;
@@ -172,24 +196,40 @@ __global__ void __launch_bounds__(kWgThreads, 1)
         const int m0 = (u - n * g.upi) * g.um;
         const int off = m0 - (m0 / g.wp) * g.wp;
         const uint32_t s = it & 1, ph = (it >> 1) & 1;
-        if (!mbar_wait(bar_x_full + 8 * s, ph) || !mbar_wait(bar_dz_full + 8 * s, ph)) {
+        if (!mbar_wait(bar_x_full + 8 * s, ph) || (!DZTMA && !mbar_wait(bar_dz_full + 8 * s, ph))) {
           hc::set_abort(abort_flag, a.err, kErrWaitOperand);
           break;
         }
         tc_fence_after();
         const uint32_t xh = x_addr + s * L.halo_stride;
         const uint32_t dzs = dz_addr + s * L.dz_stride;
-        uint64_t adesc[kMaxGroups < 16 ? kMaxGroups : 16];
-        for (int gl = 0; gl < ng; ++gl) adesc[gl] = a_grp[gl] + (uint64_t)(((xh + (uint32_t)off * 128u)) >> 4);
-        const uint64_t b0 = make_sw128_desc(dzs, g.um * 128, 1024, 0);
-        for (int kk = 0; kk < g.um / 16; ++kk) {
-          const uint64_t bd = desc_add(b0, kk * 2048);
-          for (int gl = 0; gl < ng; ++gl)
-            mma_f16_ss(tmem_base + gl * NOUT, desc_add(adesc[gl], kk * 2048), bd, idesc,
-                       (first && kk == 0) ? 0u : 1u);
+        const uint64_t a_unit = (uint64_t)((xh + (uint32_t)off * 128u) >> 4);
+        uint64_t bd = make_sw128_desc(dzs + (DZTMA ? (uint32_t)off * 128u : 0u), L.dz_sub, 1024, 0);
+        // The group count is fixed per CTA: dispatch once per unit to a loop with a
+        // compile-time trip count (a runtime guard around each MMA slows issue ~2x).
+        auto issue = [&](auto ng_c) {
+          constexpr int NG = decltype(ng_c)::value;
+          if constexpr (NG <= kG) {
+            uint32_t acc = first ? 0u : 1u;
+            for (int kk = 0; kk < g.um / 16; ++kk) {
+              const uint64_t ak = a_unit + (uint64_t)kk * 128;  // 16 pixel rows further
+#pragma unroll
+              for (int gl = 0; gl < NG; ++gl) mma_f16_ss(tmem_base + gl * NOUT, a_grp[gl] + ak, bd, idesc, acc);
+              bd += 128;
+              acc = 1u;
+            }
+          }
+        };
+        switch (ng) {
+#define CBR_WG_NG(k) case k: issue(std::integral_constant<int, k>{}); break;
+          CBR_WG_NG(1) CBR_WG_NG(2) CBR_WG_NG(3) CBR_WG_NG(4) CBR_WG_NG(5) CBR_WG_NG(6)
+          CBR_WG_NG(7) CBR_WG_NG(8) CBR_WG_NG(9) CBR_WG_NG(10) CBR_WG_NG(11) CBR_WG_NG(12)
+          CBR_WG_NG(13) CBR_WG_NG(14) CBR_WG_NG(15) CBR_WG_NG(16)
+#undef CBR_WG_NG
+          default: break;
         }
         mma_commit(bar_x_empty + 8 * s);
-        mma_commit(bar_dz_empty + 8 * s);
+        if (!DZTMA) mma_commit(bar_dz_empty + 8 * s);
         first = false;
       }
       mma_commit(bar_acc_full);
@@ -200,7 +240,7 @@ __global__ void __launch_bounds__(kWgThreads, 1)
     // warps 2..5: dz producers, then the epilogue
     const int tid = threadIdx.x - 64;  // 0..127
     uint32_t it = 0;
-    for (int u = ustart; u < g.total_units && !hc::is_aborted(abort_flag); u += ustride, ++it) {
+    for (int u = ustart; !DZTMA && u < g.total_units && !hc::is_aborted(abort_flag); u += ustride, ++it) {
       const int n = u / g.upi;
       const int m0 = (u - n * g.upi) * g.um;
       const uint32_t s = it & 1, ph = (it >> 1) & 1;
@@ -310,6 +350,13 @@ size_t wgrad_partial_floats(int num_sms, int c_in, int c_out, int taps) {
   return (size_t)num_sms * P.gmax * 128 * nout;
 }
 
+bool wgrad_dz_tma_fits(const HaloGeom& g_in, int c_out) {
+  HaloGeom g = g_in;
+  const int nout = nout_for(c_out);
+  if (nout != c_out || !hc::finish_geom(g, nout <= 64 ? 2 : 1)) return false;
+  return wg_layout(g, nout, true).total + 1024 <= 227 * 1024;
+}
+
 int launch_wgrad(const WgradArgs& w, int c_in, int c_out, bool bf16, const void* x, int num_sms,
                  cudaStream_t st, void (*between)(void*), void* ctx) {
   WgKArgs a{};
@@ -325,7 +372,8 @@ int launch_wgrad(const WgradArgs& w, int c_in, int c_out, bool bf16, const void*
   a.dz.q = a.g.q;
   const int taps = a.g.r * a.g.s;
   if (!make_plan(a.plan, taps, c_in, nout)) return 3;
-  const WgLayout L = wg_layout(a.g, nout);
+  const bool dztma = w.dz_full != nullptr;
+  const WgLayout L = wg_layout(a.g, nout, dztma);
   const uint32_t smem = L.total + 1024;
   if (smem > 227 * 1024) return 3;
   const CUtensorMapDataType dt = bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
@@ -337,24 +385,33 @@ int launch_wgrad(const WgradArgs& w, int c_in, int c_out, bool bf16, const void*
     const uint32_t box[4] = {64, (uint32_t)g.wp, (uint32_t)g.box_rows, 1};
     if (!encode_tiled(&mx, dt, 4, x, dims, strides, box)) return 6;
   }
+  CUtensorMap mdz{};
+  if (dztma) {
+    const uint64_t dims[4] = {(uint64_t)c_out, (uint64_t)g.q, (uint64_t)g.p, (uint64_t)g.n_img};
+    const uint64_t strides[3] = {(uint64_t)c_out * 2, (uint64_t)g.q * c_out * 2, (uint64_t)g.p * g.q * c_out * 2};
+    const uint32_t box[4] = {64, (uint32_t)g.wp, (uint32_t)L.dz_rows, 1};
+    if (!encode_tiled(&mdz, dt, 4, w.dz_full, dims, strides, box)) return 6;
+  }
   // every CTA gets at least one unit, so every partial it writes is initialised
   const int per_split = std::max(1, std::min(num_sms / a.plan.nsplit, g.total_units));
   const int grid = per_split * a.plan.nsplit;
   auto launch = [&](auto kern) -> int {
     if (!ensure_smem_attr(reinterpret_cast<const void*>(kern), 227 * 1024)) return 6;
-    kern<<<grid, kWgThreads, smem, st>>>(mx, a);
+    kern<<<grid, kWgThreads, smem, st>>>(mx, mdz, a);
     return cudaGetLastError() == cudaSuccess ? 0 : 6;
   };
   int rc;
-  switch (nout * 2 + (bf16 ? 1 : 0)) {
-    case 32: rc = launch(wgrad_kernel<16, false>); break;
-    case 33: rc = launch(wgrad_kernel<16, true>); break;
-    case 64: rc = launch(wgrad_kernel<32, false>); break;
-    case 65: rc = launch(wgrad_kernel<32, true>); break;
-    case 128: rc = launch(wgrad_kernel<64, false>); break;
-    case 129: rc = launch(wgrad_kernel<64, true>); break;
-    case 256: rc = launch(wgrad_kernel<128, false>); break;
-    case 257: rc = launch(wgrad_kernel<128, true>); break;
+  switch (nout * 4 + (bf16 ? 2 : 0) + (dztma ? 1 : 0)) {
+#define CBR_WG_CASE(N_)                                                   \
+    case N_ * 4 + 0: rc = launch(wgrad_kernel<N_, false, false>); break; \
+    case N_ * 4 + 1: rc = launch(wgrad_kernel<N_, false, true>); break;  \
+    case N_ * 4 + 2: rc = launch(wgrad_kernel<N_, true, false>); break;  \
+    case N_ * 4 + 3: rc = launch(wgrad_kernel<N_, true, true>); break;
+    CBR_WG_CASE(16)
+    CBR_WG_CASE(32)
+    CBR_WG_CASE(64)
+    CBR_WG_CASE(128)
+#undef CBR_WG_CASE
     default: return 3;
   }
   if (rc) return rc;

@@ -14,6 +14,7 @@
 // Pipelines: 2 halo stages, 2 TMEM accumulator stages (U*NOUT fp32 columns each), and a
 // 2-deep filter ring when the filter is streamed.  All waits are bounded (ptx.cuh).
 #pragma once
+#include <type_traits>
 #include "cbr_internal.h"
 #include "common.cuh"
 #include "dz_producer.cuh"
@@ -277,12 +278,25 @@ __global__ void __launch_bounds__(Roles<KIND>::kThreads, 1)
     }
   } else if (warp == R::kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
+    // One thread feeds the tensor cores, so the issue sequence is kept free of runtime
+    // conditions: a guard or data-dependent branch beside each MMA roughly halves the rate.
     if (lane == 0) {
       constexpr bool kBMn = KIND == kKindDgrad;
       const uint32_t idesc = make_idesc_f16(128, NOUT, BF16, false, kBMn);
+      const uint64_t b_base = kBMn ? make_sw128_desc(w_addr, 8192, 1024, 0) : make_sw128_desc(w_addr, 16, 1024, 0);
+      const uint64_t a_row_skip = (uint64_t)((g.wp - g.s) * 128 / 16);  // end of a filter row
+      bool bad = false;
+      if (WRES) {
+        // resident filter: every slab is waited for once, before the first unit
+        for (int i = 0; i < NCH * rs && !bad; ++i)
+          if (!mbar_wait(bar_w_full + 8 * i, 0)) {
+            set_abort(abort_flag, a.err, kErrWaitWeights);
+            bad = true;
+          }
+        tc_fence_after();
+      }
       uint32_t hit = 0, wit = 0, ait = 0;
-      bool first = true;
-      for (int u = blockIdx.x; u < g.total_units && !is_aborted(abort_flag); u += gridDim.x) {
+      for (int u = blockIdx.x; u < g.total_units && !bad && !is_aborted(abort_flag); u += gridDim.x) {
         const int n = u / g.upi;
         const int m0 = (u - n * g.upi) * g.um;
         const int off = m0 - (m0 / g.wp) * g.wp;
@@ -294,7 +308,6 @@ __global__ void __launch_bounds__(Roles<KIND>::kThreads, 1)
         }
         tc_fence_after();
         const uint32_t d0 = tmem_base + as * (U * NOUT);
-        bool bad = false;
         for (int ch = 0; ch < NCH && !bad; ++ch, ++hit) {
           const uint32_t hs = hit & 1, hph = (hit >> 1) & 1;
           if (!mbar_wait(bar_halo_full + 8 * hs, hph)) {
@@ -304,57 +317,52 @@ __global__ void __launch_bounds__(Roles<KIND>::kThreads, 1)
           }
           tc_fence_after();
           const uint32_t hbase = halo_addr + hs * L.halo_stride;
-          // A descriptors: one base per unit, taps and tiles are start-address offsets
-          const uint64_t a_base = make_sw128_desc(hbase + (uint32_t)off * 128u, 16, 1024, 0);
-          const uint64_t b_base = kBMn ? make_sw128_desc(w_addr, 8192, 1024, 0) : make_sw128_desc(w_addr, 16, 1024, 0);
-          int r = 0, sx = 0;
-          for (int tap = 0; tap < rs; ++tap) {
-            uint32_t wslab_off, ws = 0;
-            if (WRES) {
-              const int i = ch * rs + tap;
-              if (first) {
-                if (!mbar_wait(bar_w_full + 8 * i, 0)) {
+          // taps advance the A start address incrementally (one 128-byte row per tap, plus the
+          // rest of the padded row at the end of a filter row)
+          auto run_taps = [&](auto nt_c) {
+            constexpr int NT = decltype(nt_c)::value;
+            uint64_t a_tap = make_sw128_desc(hbase + (uint32_t)off * 128u, 16, 1024, 0);
+            int sx = 0;
+            for (int tap = 0; tap < rs; ++tap) {
+              uint32_t wslab_off, ws = 0;
+              if (WRES) {
+                wslab_off = (uint32_t)(ch * rs + tap) * L.wslab;
+              } else {
+                ws = wit % kStreamStages;
+                if (!mbar_wait(bar_w_full + 8 * ws, (wit / kStreamStages) & 1)) {
                   set_abort(abort_flag, a.err, kErrWaitWeights);
                   bad = true;
                   break;
                 }
                 tc_fence_after();
+                wslab_off = ws * L.wslab;
               }
-              wslab_off = (uint32_t)i * L.wslab;
-            } else {
-              ws = wit % kStreamStages;
-              if (!mbar_wait(bar_w_full + 8 * ws, (wit / kStreamStages) & 1)) {
-                set_abort(abort_flag, a.err, kErrWaitWeights);
-                bad = true;
-                break;
-              }
-              tc_fence_after();
-              wslab_off = ws * L.wslab;
-            }
-            const uint64_t a_tap = desc_add(a_base, (uint32_t)(r * g.wp + sx) * 128u);
-            const uint64_t b_tap = desc_add(b_base, wslab_off);
-            for (int t = 0; t < ntiles; ++t) {
-              const uint64_t a_t = desc_add(a_tap, (uint32_t)t * 128u * 128u);
+              const uint64_t b_tap = b_base + (uint64_t)(wslab_off >> 4);
+              const uint32_t acc0 = (ch | tap) != 0 ? 1u : 0u;
 #pragma unroll
-              for (int kk = 0; kk < 4; ++kk)
-                mma_f16_ss(d0 + t * NOUT, desc_add(a_t, kk * 32), desc_add(b_tap, kBMn ? kk * 2048 : kk * 32),
-                           idesc, (ch | tap | kk) != 0);
+              for (int t = 0; t < NT; ++t)
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)
+                  mma_f16_ss(d0 + t * NOUT, a_tap + (uint64_t)((t * 128 * 128 + kk * 32) >> 4),
+                             b_tap + (uint64_t)((kBMn ? kk * 2048 : kk * 32) >> 4), idesc, kk ? 1u : acc0);
+              const bool wrap = sx + 1 == g.s;
+              sx = wrap ? 0 : sx + 1;
+              a_tap += wrap ? 8 + a_row_skip : 8;
+              if (!WRES) {
+                mma_commit(bar_w_empty + 8 * ws);
+                ++wit;
+              }
             }
-            if (++sx == g.s) {
-              sx = 0;
-              ++r;
-            }
-            if (!WRES) {
-              mma_commit(bar_w_empty + 8 * ws);
-              ++wit;
-            }
-          }
+          };
+          if (ntiles == U)
+            run_taps(std::integral_constant<int, U>{});
+          else
+            run_taps(std::integral_constant<int, 1>{});  // ragged tail of an image (U = 2 only)
           mma_commit(bar_halo_empty + 8 * hs);
         }
         if (bad) break;
         mma_commit(bar_acc_full + 8 * as);
         ++ait;
-        first = false;
       }
       mma_commit(bar_drain);
       mbar_wait(bar_drain, 0);
