@@ -444,6 +444,7 @@ cbr_status_t cbr_backward(const cbr_desc_t* desc, const void* dy, const void* x,
     da.mask = mask;
     da.coef = coef;
     da.dx = dx;
+    da.dz_full = dz_tma ? dz_buf : nullptr;
     da.err = dev->err;
     st = launch_dgrad(da, (int)s.cin, (int)s.cout, s.bf16, w, dev->num_sms, cs);
     if (st) return (cbr_status_t)st;

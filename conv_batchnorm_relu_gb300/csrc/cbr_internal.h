@@ -110,8 +110,11 @@ struct DgradArgs {
   const uint8_t* mask;
   const float* coef;
   void* dx;
+  const void* dz_full;      // materialised dz [n][p][q][cout], or null to compute it in-kernel
   uint32_t* err;
 };
+// MMA N width used for `c` output channels: the next of 16, 32, 64, 128.
+inline int nout_for(int c) { return c <= 16 ? 16 : (c <= 32 ? 32 : (c <= 64 ? 64 : 128)); }
 int launch_dgrad(const DgradArgs& a, int c_in, int c_out, bool bf16, const void* w, int num_sms,
                  cudaStream_t st);
 

@@ -339,7 +339,6 @@ __global__ void __launch_bounds__(kRedOut * kRedSlices)
   }
 }
 
-int nout_for(int c) { return c <= 16 ? 16 : (c <= 32 ? 32 : (c <= 64 ? 64 : 128)); }
 
 }  // namespace
 
@@ -421,51 +420,6 @@ int launch_wgrad(const WgradArgs& w, int c_in, int c_out, bool bf16, const void*
   wgrad_reduce_kernel<<<rgrid, kRedOut * kRedSlices, 0, st>>>(a.part, w.dw, a.plan, grid, c_out, c_in,
                                                               taps, nout);
   return cudaGetLastError() == cudaSuccess ? 0 : 6;
-}
-
-int launch_dgrad(const DgradArgs& d, int c_in, int c_out, bool bf16, const void* w, int num_sms,
-                 cudaStream_t st) {
-  ConvArgs a{};
-  a.g = d.g;
-  a.out = d.dx;
-  a.out_c = c_in;
-  a.out_shift = __builtin_ctz((unsigned)(c_in * 2 / 16));
-  if ((c_in * 2 / 16) & (c_in * 2 / 16 - 1)) return 3;  // stored chunks per pixel: a power of two
-  a.mode = kFpropPlain;
-  a.err = d.err;
-  a.dz = DzSrc{d.dy, d.z, d.y, d.mask, d.coef, d.g.h, d.g.w, c_out};
-  const int nch = (c_out + 63) / 64;
-  const int nout = nout_for(c_in);
-  if (nch > 2 || c_in > 128) return 3;
-  const int U = nout <= 64 ? 2 : 1;
-  HaloGeom& g = a.g;
-  if (!hc::finish_geom(g, U)) return 3;
-  const bool wres = hc::layout(g, kKindDgrad, nch, nout, true).total + 1024 <= 227 * 1024;
-  const CUtensorMapDataType dt = bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
-  CUtensorMap mx{}, mw;  // dgrad builds its A operand in-kernel; mx is unused
-  {
-    const uint64_t dims[3] = {(uint64_t)c_in, (uint64_t)(g.r * g.s), (uint64_t)c_out};
-    const uint64_t strides[2] = {(uint64_t)c_in * 2, (uint64_t)g.r * g.s * c_in * 2};
-    const uint32_t box[3] = {64, 1, 64};
-    if (!encode_tiled(&mw, dt, 3, w, dims, strides, box)) return 6;
-  }
-  const int grid = std::min(g.total_units, num_sms);
-#define CBR_DGRAD_CASE(NCH_, NOUT_, U_, WRES_)                                                        \
-  if (nch == NCH_ && nout == NOUT_ && U == U_ && (WRES_ == wres)) {                                  \
-    return bf16 ? hc::launch_halo_conv<kKindDgrad, NCH_, NOUT_, U_, WRES_, true>(a, mx, mw, grid, st) \
-                : hc::launch_halo_conv<kKindDgrad, NCH_, NOUT_, U_, WRES_, false>(a, mx, mw, grid, st); \
-  }
-  CBR_DGRAD_CASE(1, 16, 2, true)
-  CBR_DGRAD_CASE(1, 32, 2, true)
-  CBR_DGRAD_CASE(1, 64, 2, true)
-  CBR_DGRAD_CASE(1, 16, 2, false)
-  CBR_DGRAD_CASE(1, 32, 2, false)
-  CBR_DGRAD_CASE(1, 64, 2, false)
-  CBR_DGRAD_CASE(2, 64, 2, false)
-  CBR_DGRAD_CASE(1, 128, 1, false)
-  CBR_DGRAD_CASE(2, 128, 1, false)
-#undef CBR_DGRAD_CASE
-  return 3;
 }
 
 }  // namespace cbr

@@ -1,0 +1,66 @@
+// DGrad: dx = stride-1 convolution of dz (P x Q, Cout channels) with the filter rotated by 180
+// degrees and its channel roles swapped (CBR page, section 5.2; padding R-1-pad).  The A
+// operand is the zero-padded dz halo: loaded by TMA from a materialised dz when the backward
+// pass has one, otherwise built in shared memory from (dy, z, mask) by four producer warps.
+#include <algorithm>
+
+#include "halo_conv.cuh"
+
+namespace cbr {
+
+int launch_dgrad(const DgradArgs& d, int c_in, int c_out, bool bf16, const void* w, int num_sms,
+                 cudaStream_t st) {
+  ConvArgs a{};
+  a.g = d.g;
+  a.out = d.dx;
+  a.out_c = c_in;
+  a.out_shift = __builtin_ctz((unsigned)(c_in * 2 / 16));
+  if ((c_in * 2 / 16) & (c_in * 2 / 16 - 1)) return 3;  // stored chunks per pixel: a power of two
+  a.mode = kFpropPlain;
+  a.err = d.err;
+  a.dz = DzSrc{d.dy, d.z, d.y, d.mask, d.coef, d.g.h, d.g.w, c_out};
+  const int nch = (c_out + 63) / 64;
+  const int nout = nout_for(c_in);
+  if (nch > 2 || c_in > 128) return 3;
+  const int U = nout <= 64 ? 2 : 1;
+  HaloGeom& g = a.g;
+  if (!hc::finish_geom(g, U)) return 3;
+  const bool wres = hc::layout(g, kKindDgrad, nch, nout, true).total + 1024 <= 227 * 1024;
+  const CUtensorMapDataType dt = bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  CUtensorMap mx{}, mw;  // mx: the materialised dz, when there is one
+  if (d.dz_full) {
+    const uint64_t dims[4] = {(uint64_t)c_out, (uint64_t)g.w, (uint64_t)g.h, (uint64_t)g.n_img};
+    const uint64_t strides[3] = {(uint64_t)c_out * 2, (uint64_t)g.w * c_out * 2, (uint64_t)g.h * g.w * c_out * 2};
+    const uint32_t box[4] = {64, (uint32_t)g.wp, (uint32_t)g.box_rows, 1};
+    if (!encode_tiled(&mx, dt, 4, d.dz_full, dims, strides, box)) return 6;
+  }
+  {
+    const uint64_t dims[3] = {(uint64_t)c_in, (uint64_t)(g.r * g.s), (uint64_t)c_out};
+    const uint64_t strides[2] = {(uint64_t)c_in * 2, (uint64_t)g.r * g.s * c_in * 2};
+    const uint32_t box[3] = {64, 1, 64};
+    if (!encode_tiled(&mw, dt, 3, w, dims, strides, box)) return 6;
+  }
+  const int grid = std::min(g.total_units, num_sms);
+#define CBR_DGRAD_KIND(K_, NCH_, NOUT_, U_, WRES_)                                               \
+  (bf16 ? hc::launch_halo_conv<K_, NCH_, NOUT_, U_, WRES_, true>(a, mx, mw, grid, st)            \
+        : hc::launch_halo_conv<K_, NCH_, NOUT_, U_, WRES_, false>(a, mx, mw, grid, st))
+#define CBR_DGRAD_CASE(NCH_, NOUT_, U_, WRES_)                                                   \
+  if (nch == NCH_ && nout == NOUT_ && U == U_ && (WRES_ == wres)) {                             \
+    return d.dz_full ? CBR_DGRAD_KIND(kKindDgradTma, NCH_, NOUT_, U_, WRES_)                    \
+                     : CBR_DGRAD_KIND(kKindDgrad, NCH_, NOUT_, U_, WRES_);                      \
+  }
+  CBR_DGRAD_CASE(1, 16, 2, true)
+  CBR_DGRAD_CASE(1, 32, 2, true)
+  CBR_DGRAD_CASE(1, 64, 2, true)
+  CBR_DGRAD_CASE(1, 16, 2, false)
+  CBR_DGRAD_CASE(1, 32, 2, false)
+  CBR_DGRAD_CASE(1, 64, 2, false)
+  CBR_DGRAD_CASE(2, 64, 2, false)
+  CBR_DGRAD_CASE(1, 128, 1, false)
+  CBR_DGRAD_CASE(2, 128, 1, false)
+#undef CBR_DGRAD_CASE
+#undef CBR_DGRAD_KIND
+  return 3;
+}
+
+}  // namespace cbr

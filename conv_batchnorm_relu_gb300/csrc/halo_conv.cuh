@@ -21,7 +21,9 @@
 
 namespace cbr {
 
-enum ConvKind : int { kKindFprop = 0, kKindDgrad = 1 };
+// Fprop: A = input halo by TMA.  Dgrad: A = dz halo built in-kernel from (dy, z, mask) by four
+// producer warps.  DgradTma: A = a materialised dz halo by TMA; filter and epilogue as Dgrad.
+enum ConvKind : int { kKindFprop = 0, kKindDgrad = 1, kKindDgradTma = 2 };
 
 struct ConvArgs {
   HaloGeom g;
@@ -62,7 +64,7 @@ constexpr int pow2_at_least(int v) {
 
 template <int KIND>
 struct Roles {
-  static constexpr int kAWarps = KIND == kKindFprop ? 1 : 4;
+  static constexpr int kAWarps = KIND == kKindDgrad ? 4 : 1;
   static constexpr int kMmaWarp = kAWarps;
   static constexpr int kWWarp = kAWarps + 1;
   static constexpr int kEpiWarp0 = kAWarps + 2;
@@ -165,7 +167,7 @@ __global__ void __launch_bounds__(Roles<KIND>::kThreads, 1)
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < 2; ++i) {
-      mbar_init(bar_halo_full + 8 * i, KIND == kKindFprop ? 1 : 32 * R::kAWarps);
+      mbar_init(bar_halo_full + 8 * i, KIND == kKindDgrad ? 32 * R::kAWarps : 1);
       mbar_init(bar_halo_empty + 8 * i, 1);
       mbar_init(bar_acc_full + 8 * i, 1);
       mbar_init(bar_acc_empty + 8 * i, kEpiThreads);
@@ -189,7 +191,7 @@ __global__ void __launch_bounds__(Roles<KIND>::kThreads, 1)
 
   if (warp < R::kAWarps) {
     // ------------------------------------------------------------ A producers
-    if constexpr (KIND == kKindFprop) {
+    if constexpr (KIND != kKindDgrad) {
       if (lane == 0) {
         prefetch_tensormap(&map_x);
         const uint32_t tx = (uint32_t)g.hr * g.wp * 128;
@@ -281,7 +283,7 @@ __global__ void __launch_bounds__(Roles<KIND>::kThreads, 1)
     // One thread feeds the tensor cores, so the issue sequence is kept free of runtime
     // conditions: a guard or data-dependent branch beside each MMA roughly halves the rate.
     if (lane == 0) {
-      constexpr bool kBMn = KIND == kKindDgrad;
+      constexpr bool kBMn = KIND != kKindFprop;
       const uint32_t idesc = make_idesc_f16(128, NOUT, BF16, false, kBMn);
       const uint64_t b_base = kBMn ? make_sw128_desc(w_addr, 8192, 1024, 0) : make_sw128_desc(w_addr, 16, 1024, 0);
       const uint64_t a_row_skip = (uint64_t)((g.wp - g.s) * 128 / 16);  // end of a filter row
