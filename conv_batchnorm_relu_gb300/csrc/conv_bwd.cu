@@ -285,60 +285,63 @@ __global__ void __launch_bounds__(kWgThreads, 1)
   }
 }
 
-// dW[k][tap][c] = sum over the CTAs of its split, in a fixed order with fp64 accumulation.
-// A block owns 64 consecutive outputs (k fastest, so partial reads are coalesced) and four
-// slices of the CTA list; the slices are combined in slice order.
-constexpr int kRedOut = 64, kRedSlices = 4;
+// dW[k][tap][c] = sum over the CTAs of its split, in a fixed order.
+// A block owns one (tap, c) pair and all NOUT filters k: thread (sl, q) loads the float4 of
+// k = 4q..4q+3 from CTAs sl, sl + S, sl + 2S, ... (S = 256 / (NOUT/4) slices, up to eight loads
+// in flight), and the slices are then combined in slice order, so the sum is deterministic.
+constexpr int kRedThreads = 256;
 
-__global__ void __launch_bounds__(kRedOut * kRedSlices)
+template <int NOUT>
+__global__ void __launch_bounds__(kRedThreads)
     wgrad_reduce_kernel(const float* __restrict__ part, float* __restrict__ dw, const WgPlan P,
-                        int grid, int cout, int cin, int taps, int nout) {
-  __shared__ double red[kRedSlices][kRedOut];
-  const long long total = (long long)taps * cin * cout;
-  const int j = threadIdx.x % kRedOut, sl = threadIdx.x / kRedOut;
-  const long long idx = (long long)blockIdx.x * kRedOut + j;
-  int split = 0, gl = 0, row = 0, k = 0, c = 0, tap = 0;
-  if (idx < total) {
-    k = (int)(idx % cout);
-    c = (int)((idx / cout) % cin);
-    tap = (int)(idx / ((long long)cout * cin));
-    const int chunk = c >> 6, cl = c & 63;
-    int grp = 0;
-    for (int gi = 0; gi < P.ngroups; ++gi) {
-      if (P.ta[gi] == tap) { grp = gi; row = cl; break; }
-      if (P.tb[gi] == tap) { grp = gi; row = 64 + cl; break; }
-    }
-    for (int s = 0; s < P.nsplit; ++s)
-      if (P.split_chunk[s] == chunk && grp >= P.split_g0[s] && grp < P.split_g0[s] + P.split_ng[s]) split = s;
-    gl = grp - P.split_g0[split];
+                        int grid, int cin, int taps) {
+  constexpr int kQ = NOUT / 4;                // float4 columns
+  constexpr int kS = kRedThreads / kQ;        // CTA slices
+  __shared__ double red[kS][NOUT];
+  const int q = threadIdx.x % kQ, sl = threadIdx.x / kQ;
+  const int c = blockIdx.x % cin, tap = blockIdx.x / cin;
+  const int chunk = c >> 6, cl = c & 63;
+  int grp = 0, row = 0;
+  for (int gi = 0; gi < P.ngroups; ++gi) {
+    if (P.ta[gi] == tap) { grp = gi; row = cl; break; }
+    if (P.tb[gi] == tap) { grp = gi; row = 64 + cl; break; }
   }
-  double acc = 0.0;
-  if (idx < total) {
-    const size_t stride_b = (size_t)P.gmax * 128 * nout;
-    const float* base = part + ((size_t)gl * 128 + row) * nout + k;
-    const int nb = (grid - split + P.nsplit - 1) / P.nsplit;  // CTAs of this split
-    int t = sl;
-    for (; t + 3 * kRedSlices < nb; t += 4 * kRedSlices) {
-      const float v0 = __ldg(base + (size_t)(split + (t + 0 * kRedSlices) * P.nsplit) * stride_b);
-      const float v1 = __ldg(base + (size_t)(split + (t + 1 * kRedSlices) * P.nsplit) * stride_b);
-      const float v2 = __ldg(base + (size_t)(split + (t + 2 * kRedSlices) * P.nsplit) * stride_b);
-      const float v3 = __ldg(base + (size_t)(split + (t + 3 * kRedSlices) * P.nsplit) * stride_b);
-      acc += (double)v0;
-      acc += (double)v1;
-      acc += (double)v2;
-      acc += (double)v3;
+  int split = 0;
+  for (int s = 0; s < P.nsplit; ++s)
+    if (P.split_chunk[s] == chunk && grp >= P.split_g0[s] && grp < P.split_g0[s] + P.split_ng[s]) split = s;
+  const int gl = grp - P.split_g0[split];
+  const size_t stride_b = (size_t)P.gmax * 128 * NOUT;
+  const float4* base = reinterpret_cast<const float4*>(part + ((size_t)gl * 128 + row) * NOUT) + q;
+  const int nb = (grid - split + P.nsplit - 1) / P.nsplit;  // CTAs of this split
+  // fp32 within a slice (a handful of terms), fp64 across slices: the FP64 rate of this part is
+  // a small fraction of its FP32 rate, so fp64 is kept to the final combine.
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int t0 = sl; t0 < nb; t0 += 8 * kS) {
+    float4 v[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int t = t0 + u * kS;
+      v[u] = t < nb ? __ldg(base + (size_t)(split + t * P.nsplit) * (stride_b / 4)) : make_float4(0.f, 0.f, 0.f, 0.f);
     }
-    for (; t < nb; t += kRedSlices) acc += (double)__ldg(base + (size_t)(split + t * P.nsplit) * stride_b);
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      acc.x += v[u].x;
+      acc.y += v[u].y;
+      acc.z += v[u].z;
+      acc.w += v[u].w;
+    }
   }
-  red[sl][j] = acc;
+  red[sl][4 * q + 0] = acc.x;
+  red[sl][4 * q + 1] = acc.y;
+  red[sl][4 * q + 2] = acc.z;
+  red[sl][4 * q + 3] = acc.w;
   __syncthreads();
-  if (sl == 0 && idx < total) {
-    double t = red[0][j];
-    for (int q = 1; q < kRedSlices; ++q) t += red[q][j];
+  for (int k = threadIdx.x; k < NOUT; k += kRedThreads) {
+    double t = red[0][k];
+    for (int s2 = 1; s2 < kS; ++s2) t += red[s2][k];
     dw[((size_t)k * taps + tap) * cin + c] = (float)t;
   }
 }
-
 
 }  // namespace
 
@@ -415,10 +418,13 @@ int launch_wgrad(const WgradArgs& w, int c_in, int c_out, bool bf16, const void*
   }
   if (rc) return rc;
   if (between) between(ctx);
-  const long long total = (long long)taps * c_in * c_out;
-  const int rgrid = (int)((total + kRedOut - 1) / kRedOut);
-  wgrad_reduce_kernel<<<rgrid, kRedOut * kRedSlices, 0, st>>>(a.part, w.dw, a.plan, grid, c_out, c_in,
-                                                              taps, nout);
+  const int rgrid = taps * c_in;
+  switch (nout) {
+    case 16: wgrad_reduce_kernel<16><<<rgrid, kRedThreads, 0, st>>>(a.part, w.dw, a.plan, grid, c_in, taps); break;
+    case 32: wgrad_reduce_kernel<32><<<rgrid, kRedThreads, 0, st>>>(a.part, w.dw, a.plan, grid, c_in, taps); break;
+    case 64: wgrad_reduce_kernel<64><<<rgrid, kRedThreads, 0, st>>>(a.part, w.dw, a.plan, grid, c_in, taps); break;
+    default: wgrad_reduce_kernel<128><<<rgrid, kRedThreads, 0, st>>>(a.part, w.dw, a.plan, grid, c_in, taps); break;
+  }
   return cudaGetLastError() == cudaSuccess ? 0 : 6;
 }
 

@@ -385,6 +385,14 @@ __global__ void __launch_bounds__(Roles<KIND>::kThreads, 1)
     float s1[kNB], s2[kNB];
 #pragma unroll
     for (int b = 0; b < kNB; ++b) s1[b] = s2[b] = 0.f;
+    // Statistics: with at most 32 channels per thread, each thread keeps per-channel sums of
+    // its own rows in registers for the whole kernel and the warp reduction runs once at the
+    // end (shuffles share the shared-memory pipe with the tensor cores' operand reads);
+    // otherwise every tile is reduced across the warp as it is produced.
+    constexpr bool kRegStats = kCPH <= 32;
+    float r1[kRegStats ? kCPH : 1], r2[kRegStats ? kCPH : 1];
+#pragma unroll
+    for (int i = 0; i < (kRegStats ? kCPH : 1); ++i) r1[i] = r2[i] = 0.f;
     const bool stats = KIND == kKindFprop && a.mode == kFpropStats;
     const bool bias_relu = KIND == kKindFprop && a.mode == kFpropBiasRelu;
     const int osh = a.out_shift;
@@ -429,13 +437,21 @@ __global__ void __launch_bounds__(Roles<KIND>::kThreads, 1)
                            make_uint4(pack2<BF16>(v[8 * cc + 0], v[8 * cc + 1]), pack2<BF16>(v[8 * cc + 2], v[8 * cc + 3]),
                                       pack2<BF16>(v[8 * cc + 4], v[8 * cc + 5]), pack2<BF16>(v[8 * cc + 6], v[8 * cc + 7])));
             if (stats) {
-              float sq[kSB];
+              if constexpr (kRegStats) {
 #pragma unroll
-              for (int i = 0; i < kSB; ++i) sq[i] = v[i] * v[i];
-              reduce_scatter<kSB>(v, lane);
-              reduce_scatter<kSB>(sq, lane);
-              s1[b] += v[0];
-              s2[b] += sq[0];
+                for (int i = 0; i < kSB; ++i) {
+                  r1[b * kSB + i] += v[i];
+                  r2[b * kSB + i] = fmaf(v[i], v[i], r2[b * kSB + i]);
+                }
+              } else {
+                float sq[kSB];
+#pragma unroll
+                for (int i = 0; i < kSB; ++i) sq[i] = v[i] * v[i];
+                reduce_scatter<kSB>(v, lane);
+                reduce_scatter<kSB>(sq, lane);
+                s1[b] += v[0];
+                s2[b] += sq[0];
+              }
             }
           }
         }
@@ -457,6 +473,23 @@ __global__ void __launch_bounds__(Roles<KIND>::kThreads, 1)
         named_bar_sync(1, kEpiThreads);
       }
       ++ait;
+    }
+    if constexpr (kRegStats) {
+      if (stats && half < kHalves) {
+#pragma unroll
+        for (int b = 0; b < kNB; ++b) {
+          float v1[kSB], v2[kSB];
+#pragma unroll
+          for (int i = 0; i < kSB; ++i) {
+            v1[i] = r1[b * kSB + i];
+            v2[i] = r2[b * kSB + i];
+          }
+          reduce_scatter<kSB>(v1, lane);
+          reduce_scatter<kSB>(v2, lane);
+          s1[b] = v1[0];
+          s2[b] = v2[0];
+        }
+      }
     }
     if (stats && half < kHalves && (lane & ((1 << kSh) - 1)) == 0) {
       // per-(quad) partials -> smem; the staging buffer is free behind the last named barrier
