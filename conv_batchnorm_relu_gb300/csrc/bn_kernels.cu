@@ -8,6 +8,9 @@
 // Both passes are HBM-bound streams over NHWC tensors: 128-bit loads of 8 channels, several
 // independent vectors in flight per thread, grid sized to the SM count.
 #include <algorithm>
+#include <map>
+#include <mutex>
+#include <utility>
 
 #include "cbr_internal.h"
 #include "common.cuh"
@@ -18,7 +21,7 @@ namespace {
 constexpr int kApplyThreads = 256;
 constexpr int kApplyUnroll = 4;
 constexpr int kRedThreads = 512;
-constexpr int kRedUnroll = 4;
+constexpr int kRedUnroll = 8;
 
 template <bool BF16, bool MASK>
 __global__ void __launch_bounds__(kApplyThreads)
@@ -66,6 +69,8 @@ __global__ void __launch_bounds__(kApplyThreads)
 template <bool BF16, bool MASKBITS>
 __global__ void __launch_bounds__(kRedThreads)
     bn_bwd_reduce_kernel(const BwdReduceArgs a) {
+  // vectors in flight per thread (the y-derived mask needs a third operand)
+  constexpr int kU = MASKBITS ? kRedUnroll : kRedUnroll / 2;
   __shared__ __align__(16) float red[kRedThreads * 16];  // reused as fp64 [8][2*c] at the end
   __shared__ uint32_t ticket;
   const int c = a.c;
@@ -83,11 +88,11 @@ __global__ void __launch_bounds__(kRedThreads)
   const uint8_t* dyb = static_cast<const uint8_t*>(a.dy);
   const uint8_t* zb = static_cast<const uint8_t*>(a.z);
   const uint8_t* yb = static_cast<const uint8_t*>(a.y);
-  for (long long v0 = gtid; v0 < nvec; v0 += stride * kRedUnroll) {
-    uint4 dyv[kRedUnroll], zv[kRedUnroll], yv[kRedUnroll];
-    uint32_t mb[kRedUnroll];
+  for (long long v0 = gtid; v0 < nvec; v0 += stride * kU) {
+    uint4 dyv[kU], zv[kU], yv[kU];
+    uint32_t mb[kU];
 #pragma unroll
-    for (int k = 0; k < kRedUnroll; ++k) {
+    for (int k = 0; k < kU; ++k) {
       const long long v = v0 + k * stride;
       if (v < nvec) {
         dyv[k] = ld_global_nc_v4(dyb + v * 16);
@@ -97,7 +102,7 @@ __global__ void __launch_bounds__(kRedThreads)
       }
     }
 #pragma unroll
-    for (int k = 0; k < kRedUnroll; ++k) {
+    for (int k = 0; k < kU; ++k) {
       const long long v = v0 + k * stride;
       if (v < nvec) {
         const uint32_t dw[4] = {dyv[k].x, dyv[k].y, dyv[k].z, dyv[k].w};
@@ -156,7 +161,9 @@ __global__ void __launch_bounds__(kRedThreads)
   const int nv4 = (2 * c) / 4;
   if (warp < kFinWarps) {
     for (int c4 = lane; c4 < nv4; c4 += 32) {
-      double s0 = 0, s1 = 0, s2 = 0, s3 = 0;
+      // fp32 over this warp's share of blocks (fixed order), fp64 across warps: this loop runs
+      // on one SM after all others and the FP64 rate is a small fraction of FP32.
+      float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
       for (int b = warp; b < (int)gridDim.x; b += kFinWarps) {
         const float4 v = __ldcg(reinterpret_cast<const float4*>(a.part + (size_t)b * 2 * c) + c4);
         s0 += v.x;
@@ -260,18 +267,43 @@ __global__ void __launch_bounds__(kApplyThreads)
 
 }  // namespace
 
+// Blocks of `kern` resident per SM, queried once per (kernel, device).
+template <typename K>
+int resident_blocks(K kern, int threads) {
+  static std::mutex mu;
+  static std::map<std::pair<const void*, int>, int> cache;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  const auto key = std::make_pair(reinterpret_cast<const void*>(kern), dev);
+  std::lock_guard<std::mutex> lock(mu);
+  auto it = cache.find(key);
+  if (it != cache.end()) return it->second;
+  int nb = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, kern, threads, 0) != cudaSuccess || nb < 1) nb = 1;
+  cache[key] = nb;
+  return nb;
+}
+
+// Streaming grid: every block resident at once (one wave), grid-stride loops inside.
+template <typename K>
+int stream_grid(K kern, int threads, long long work_items, int num_sms) {
+  const long long want = std::max<long long>(1, (work_items + threads - 1) / threads);
+  return (int)std::min<long long>(want, (long long)num_sms * resident_blocks(kern, threads));
+}
+
 int launch_dz(const DzArgs& a, bool bf16, int num_sms, cudaStream_t st) {
   if (a.c % 8 != 0 || a.c > 256) return 3;
   const long long nvec = a.total / 8;
-  const long long want = (nvec + kApplyThreads * kApplyUnroll - 1) / (kApplyThreads * kApplyUnroll);
-  const int grid = (int)std::max<long long>(1, std::min<long long>(want, (long long)num_sms * 8));
   const bool bits = a.mask != nullptr;
+  auto go = [&](auto kern) {
+    kern<<<stream_grid(kern, kApplyThreads, nvec / kApplyUnroll, num_sms), kApplyThreads, 0, st>>>(a);
+  };
   if (bf16) {
-    if (bits) dz_kernel<true, true><<<grid, kApplyThreads, 0, st>>>(a);
-    else dz_kernel<true, false><<<grid, kApplyThreads, 0, st>>>(a);
+    if (bits) go(dz_kernel<true, true>);
+    else go(dz_kernel<true, false>);
   } else {
-    if (bits) dz_kernel<false, true><<<grid, kApplyThreads, 0, st>>>(a);
-    else dz_kernel<false, false><<<grid, kApplyThreads, 0, st>>>(a);
+    if (bits) go(dz_kernel<false, true>);
+    else go(dz_kernel<false, false>);
   }
   return cudaGetLastError() == cudaSuccess ? 0 : 6;
 }
@@ -279,15 +311,16 @@ int launch_dz(const DzArgs& a, bool bf16, int num_sms, cudaStream_t st) {
 int launch_apply(const ApplyArgs& a, bool bf16, int num_sms, cudaStream_t st) {
   if (a.c % 8 != 0 || a.c > 256) return 3;
   const long long nvec = a.total / 8;
-  const long long want = (nvec + kApplyThreads * kApplyUnroll - 1) / (kApplyThreads * kApplyUnroll);
-  const int grid = (int)std::max<long long>(1, std::min<long long>(want, (long long)num_sms * 8));
   const bool mask = a.mask != nullptr;
+  auto go = [&](auto kern) {
+    kern<<<stream_grid(kern, kApplyThreads, nvec / kApplyUnroll, num_sms), kApplyThreads, 0, st>>>(a);
+  };
   if (bf16) {
-    if (mask) bn_apply_relu_kernel<true, true><<<grid, kApplyThreads, 0, st>>>(a);
-    else bn_apply_relu_kernel<true, false><<<grid, kApplyThreads, 0, st>>>(a);
+    if (mask) go(bn_apply_relu_kernel<true, true>);
+    else go(bn_apply_relu_kernel<true, false>);
   } else {
-    if (mask) bn_apply_relu_kernel<false, true><<<grid, kApplyThreads, 0, st>>>(a);
-    else bn_apply_relu_kernel<false, false><<<grid, kApplyThreads, 0, st>>>(a);
+    if (mask) go(bn_apply_relu_kernel<false, true>);
+    else go(bn_apply_relu_kernel<false, false>);
   }
   return cudaGetLastError() == cudaSuccess ? 0 : 6;
 }
@@ -297,15 +330,19 @@ size_t bwd_reduce_partial_floats(int num_sms, int c) { return (size_t)num_sms * 
 int launch_bwd_reduce(const BwdReduceArgs& a, bool bf16, int num_sms, cudaStream_t st) {
   if (a.c % 8 != 0 || a.c > 256 || (kRedThreads % (a.c / 8)) != 0) return 3;
   const long long nvec = a.m_count * (a.c / 8);
-  const long long want = (nvec + kRedThreads * kRedUnroll - 1) / (kRedThreads * kRedUnroll);
-  const int grid = (int)std::max<long long>(1, std::min<long long>(want, (long long)num_sms * 2));
   const bool bits = a.mask != nullptr;
+  // the grid is at most the resident blocks (one wave) and the number of partials it leaves
+  // is bounded by the workspace (bwd_reduce_partial_floats: two blocks per SM)
+  auto go = [&](auto kern) {
+    const int grid = std::min(stream_grid(kern, kRedThreads, nvec / kRedUnroll, num_sms), 2 * num_sms);
+    kern<<<grid, kRedThreads, 0, st>>>(a);
+  };
   if (bf16) {
-    if (bits) bn_bwd_reduce_kernel<true, true><<<grid, kRedThreads, 0, st>>>(a);
-    else bn_bwd_reduce_kernel<true, false><<<grid, kRedThreads, 0, st>>>(a);
+    if (bits) go(bn_bwd_reduce_kernel<true, true>);
+    else go(bn_bwd_reduce_kernel<true, false>);
   } else {
-    if (bits) bn_bwd_reduce_kernel<false, true><<<grid, kRedThreads, 0, st>>>(a);
-    else bn_bwd_reduce_kernel<false, false><<<grid, kRedThreads, 0, st>>>(a);
+    if (bits) go(bn_bwd_reduce_kernel<false, true>);
+    else go(bn_bwd_reduce_kernel<false, false>);
   }
   return cudaGetLastError() == cudaSuccess ? 0 : 6;
 }

@@ -75,6 +75,13 @@ __device__ __forceinline__ uint32_t swz_off(uint32_t row, uint32_t ch, uint32_t 
   return row * pitch + (((ch & ~7u) | ((ch ^ row) & 7u)) << 4);
 }
 
+// 32-byte store (sm_100+ vector width); p must be 32-byte aligned.
+__device__ __forceinline__ void st_global_v8(void* p, uint4 a, uint4 b) {
+  asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(a.x), "r"(a.y),
+               "r"(a.z), "r"(a.w), "r"(b.x), "r"(b.y), "r"(b.z), "r"(b.w)
+               : "memory");
+}
+
 __device__ __forceinline__ void st_global_v4(void* p, uint4 v) {
   asm volatile("st.global.v4.b32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z),
                "r"(v.w)

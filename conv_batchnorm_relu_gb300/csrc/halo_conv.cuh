@@ -380,8 +380,6 @@ __global__ void __launch_bounds__(Roles<KIND>::kThreads, 1)
     const int quad = warp & 3;                  // TMEM lanes 32*quad .. +31
     const int half = ew >> 2;
     const int e = quad * 32 + lane;             // M-tile row owned by this thread
-    const int et = threadIdx.x - 32 * R::kEpiWarp0;
-    int* rowtab = reinterpret_cast<int*>(smem + L.off_rowtab);
     float s1[kNB], s2[kNB];
 #pragma unroll
     for (int b = 0; b < kNB; ++b) s1[b] = s2[b] = 0.f;
@@ -395,8 +393,10 @@ __global__ void __launch_bounds__(Roles<KIND>::kThreads, 1)
     for (int i = 0; i < (kRegStats ? kCPH : 1); ++i) r1[i] = r2[i] = 0.f;
     const bool stats = KIND == kKindFprop && a.mode == kFpropStats;
     const bool bias_relu = KIND == kKindFprop && a.mode == kFpropBiasRelu;
-    const int osh = a.out_shift;
-    const size_t opitch = (size_t)a.out_c * 2;
+    const int out_c = a.out_c;
+    const size_t opitch = (size_t)out_c * 2;
+    // 32-byte stores when every 16-channel group of a row is whole and aligned
+    const bool v8 = (out_c % 16) == 0 && (reinterpret_cast<uintptr_t>(a.out) & 31) == 0;
     uint8_t* obase = static_cast<uint8_t*>(a.out);
     uint32_t ait = 0;
     for (int u = blockIdx.x; u < g.total_units && !is_aborted(abort_flag); u += gridDim.x) {
@@ -404,16 +404,19 @@ __global__ void __launch_bounds__(Roles<KIND>::kThreads, 1)
       const int m0 = (u - n * g.upi) * g.um;
       const int ntiles = min(U, (rows_img - m0 + 127) / 128);
       const uint32_t as = ait & 1, aph = (ait >> 1) & 1;
-      bool ok = mbar_wait_backoff(bar_acc_full + 8 * as, aph, 256);
-      if (!ok) set_abort(abort_flag, a.err, kErrWaitMma);
-      // uniform decision across the epilogue threads (they share named barriers below)
-      if (!named_bar_and(2, kEpiThreads, ok && !is_aborted(abort_flag))) break;
+      if (!mbar_wait_backoff(bar_acc_full + 8 * as, aph, 256)) {
+        set_abort(abort_flag, a.err, kErrWaitMma);
+        break;
+      }
       tc_fence_after();
+      // Each thread owns one accumulator row (an output pixel) and kCPH channels of it: the
+      // values go from TMEM to registers to HBM without a shared-memory round trip (shared
+      // memory bandwidth is what the tensor cores' operand reads need).
       for (int t = 0; t < ntiles; ++t) {
-        const int mt = m0 + t * 128;
-        const int m = mt + e;
+        const int m = m0 + t * 128 + e;
         const int p = m / g.wp, q = m - p * g.wp;
         const bool valid = (p < g.p) && (q < g.q);
+        uint8_t* orow = obase + (size_t)(((long long)n * g.p + p) * g.q + q) * opitch;
         if (half < kHalves) {
 #pragma unroll
           for (int b = 0; b < kNB; ++b) {
@@ -424,6 +427,11 @@ __global__ void __launch_bounds__(Roles<KIND>::kThreads, 1)
               tmem_ld16(tmem_base + ((uint32_t)(quad * 32) << 16) + as * (U * NOUT) + t * NOUT + c0 + q16 * 16,
                         *reinterpret_cast<uint32_t(*)[16]>(r + q16 * 16));
             tmem_ld_wait();
+            if (t == ntiles - 1 && b == kNB - 1) {
+              // this thread's last read of the accumulator stage
+              tc_fence_before();
+              mbar_arrive(bar_acc_empty + 8 * as);
+            }
             float v[kSB];
 #pragma unroll
             for (int i = 0; i < kSB; ++i) {
@@ -431,11 +439,22 @@ __global__ void __launch_bounds__(Roles<KIND>::kThreads, 1)
               if (bias_relu) x = fmaxf(x + __ldg(a.bias + c0 + i), 0.f);
               v[i] = valid ? x : 0.f;
             }
+            if (valid) {
+              uint4 pk[kSB / 8];
 #pragma unroll
-            for (int cc = 0; cc < kSB / 8; ++cc)
-              st_shared_v4(stage_addr + stage_off<kPitch>(e, c0 / 8 + cc),
-                           make_uint4(pack2<BF16>(v[8 * cc + 0], v[8 * cc + 1]), pack2<BF16>(v[8 * cc + 2], v[8 * cc + 3]),
-                                      pack2<BF16>(v[8 * cc + 4], v[8 * cc + 5]), pack2<BF16>(v[8 * cc + 6], v[8 * cc + 7])));
+              for (int cc = 0; cc < kSB / 8; ++cc)
+                pk[cc] = make_uint4(pack2<BF16>(v[8 * cc + 0], v[8 * cc + 1]), pack2<BF16>(v[8 * cc + 2], v[8 * cc + 3]),
+                                    pack2<BF16>(v[8 * cc + 4], v[8 * cc + 5]), pack2<BF16>(v[8 * cc + 6], v[8 * cc + 7]));
+              if (v8) {
+#pragma unroll
+                for (int cc = 0; cc < kSB / 16; ++cc)
+                  if (c0 + 16 * cc < out_c) st_global_v8(orow + (c0 + 16 * cc) * 2, pk[2 * cc], pk[2 * cc + 1]);
+              } else {
+#pragma unroll
+                for (int cc = 0; cc < kSB / 8; ++cc)
+                  if (c0 + 8 * cc < out_c) st_global_v4(orow + (c0 + 8 * cc) * 2, pk[cc]);
+              }
+            }
             if (stats) {
               if constexpr (kRegStats) {
 #pragma unroll
@@ -454,23 +473,10 @@ __global__ void __launch_bounds__(Roles<KIND>::kThreads, 1)
               }
             }
           }
-        }
-        if (t == ntiles - 1) {
+        } else if (t == ntiles - 1) {
           tc_fence_before();
           mbar_arrive(bar_acc_empty + 8 * as);
         }
-        if (half == 0) rowtab[e] = valid ? (int)(((long long)n * g.p + p) * g.q + q) : -1;
-        named_bar_sync(1, kEpiThreads);
-        // coalesced copy-out of the valid rows
-        const int nchunk = 128 << osh;
-        for (int i = et; i < nchunk; i += kEpiThreads) {
-          const int row = i >> osh, c = i & ((1 << osh) - 1);
-          const int gr = rowtab[row];
-          if (gr >= 0)
-            st_global_v4(obase + (size_t)gr * opitch + c * 16,
-                         ld_shared_v4(stage_addr + stage_off<kPitch>(row, c)));
-        }
-        named_bar_sync(1, kEpiThreads);
       }
       ++ait;
     }
@@ -529,7 +535,9 @@ __global__ void __launch_bounds__(Roles<KIND>::kThreads, 1)
       double* fin = dred + kW * 2 * COUT;                             // [2*COUT]
       constexpr int kV4 = (2 * COUT) / 4;
       for (int c4 = lane; c4 < kV4; c4 += 32) {
-        double acc0 = 0, acc1 = 0, acc2 = 0, acc3 = 0;
+        // fp32 over this warp's share of CTAs (fixed order), fp64 across warps: the FP64 rate
+        // is a small fraction of FP32 here and this loop runs on one SM after all others.
+        float acc0 = 0.f, acc1 = 0.f, acc2 = 0.f, acc3 = 0.f;
         for (int b = warp; b < (int)gridDim.x; b += kW) {
           const float4 v = __ldcg(reinterpret_cast<const float4*>(a.part + (size_t)b * 2 * COUT) + c4);
           acc0 += v.x;
