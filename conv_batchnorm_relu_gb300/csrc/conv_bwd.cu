@@ -267,12 +267,13 @@ __global__ void __launch_bounds__(kWgThreads, 1)
           uint32_t r[16];
           tmem_ld16(tmem_base + ((uint32_t)(quad * 32) << 16) + gl * NOUT + c16 * 16, r);
           tmem_ld_wait();
-          float4* dst = reinterpret_cast<float4*>(
-              a.part + (((size_t)blockIdx.x * P.gmax + gl) * 128 + e) * NOUT + c16 * 16);
+          // partial layout [cta][group][c16][v][row][4]: a warp's store is 512 contiguous bytes
+          float4* dst = reinterpret_cast<float4*>(a.part) +
+                        (((size_t)blockIdx.x * P.gmax + gl) * (NOUT / 16) + c16) * 512 + e;
 #pragma unroll
           for (int v = 0; v < 4; ++v)
-            dst[v] = make_float4(__uint_as_float(r[4 * v]), __uint_as_float(r[4 * v + 1]),
-                                 __uint_as_float(r[4 * v + 2]), __uint_as_float(r[4 * v + 3]));
+            dst[v * 128] = make_float4(__uint_as_float(r[4 * v]), __uint_as_float(r[4 * v + 1]),
+                                       __uint_as_float(r[4 * v + 2]), __uint_as_float(r[4 * v + 3]));
         }
       }
     }
@@ -285,61 +286,71 @@ __global__ void __launch_bounds__(kWgThreads, 1)
   }
 }
 
-// dW[k][tap][c] = sum over the CTAs of its split, in a fixed order.
-// A block owns one (tap, c) pair and all NOUT filters k: thread (sl, q) loads the float4 of
-// k = 4q..4q+3 from CTAs sl, sl + S, sl + 2S, ... (S = 256 / (NOUT/4) slices, up to eight loads
-// in flight), and the slices are then combined in slice order, so the sum is deterministic.
+// dW = sum over the CTAs of each split of their partials, in a fixed order.  A block owns 64
+// consecutive float4 of the per-CTA partial (the same span in every CTA, so every load is
+// coalesced) and four slices of the split's CTA list: slice sl sums CTAs sl, sl+4, ... in fp32
+// with eight loads in flight, and the four slices are combined in slice order in fp64.  Each
+// partial element is then written to its dW[k][tap][c] position.
 constexpr int kRedThreads = 256;
+constexpr int kRedSpan = 64;                  // float4 per block
+constexpr int kRedSlices = kRedThreads / kRedSpan;
 
 template <int NOUT>
 __global__ void __launch_bounds__(kRedThreads)
     wgrad_reduce_kernel(const float* __restrict__ part, float* __restrict__ dw, const WgPlan P,
                         int grid, int cin, int taps) {
-  constexpr int kQ = NOUT / 4;                // float4 columns
-  constexpr int kS = kRedThreads / kQ;        // CTA slices
-  __shared__ double red[kS][NOUT];
-  const int q = threadIdx.x % kQ, sl = threadIdx.x / kQ;
-  const int c = blockIdx.x % cin, tap = blockIdx.x / cin;
-  const int chunk = c >> 6, cl = c & 63;
-  int grp = 0, row = 0;
-  for (int gi = 0; gi < P.ngroups; ++gi) {
-    if (P.ta[gi] == tap) { grp = gi; row = cl; break; }
-    if (P.tb[gi] == tap) { grp = gi; row = 64 + cl; break; }
-  }
-  int split = 0;
-  for (int s = 0; s < P.nsplit; ++s)
-    if (P.split_chunk[s] == chunk && grp >= P.split_g0[s] && grp < P.split_g0[s] + P.split_ng[s]) split = s;
-  const int gl = grp - P.split_g0[split];
-  const size_t stride_b = (size_t)P.gmax * 128 * NOUT;
-  const float4* base = reinterpret_cast<const float4*>(part + ((size_t)gl * 128 + row) * NOUT) + q;
+  __shared__ float4 red[kRedSlices][kRedSpan];
+  constexpr int kC16 = NOUT / 16;
+  const size_t per_cta = (size_t)P.gmax * kC16 * 512;  // float4 per CTA partial
+  const int blocks_per_split = (int)((per_cta + kRedSpan - 1) / kRedSpan);
+  const int split = blockIdx.x / blocks_per_split;
+  const size_t f4 = (size_t)(blockIdx.x % blocks_per_split) * kRedSpan + threadIdx.x % kRedSpan;
+  const int sl = threadIdx.x / kRedSpan;
   const int nb = (grid - split + P.nsplit - 1) / P.nsplit;  // CTAs of this split
-  // fp32 within a slice (a handful of terms), fp64 across slices: the FP64 rate of this part is
-  // a small fraction of its FP32 rate, so fp64 is kept to the final combine.
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int t0 = sl; t0 < nb; t0 += 8 * kS) {
-    float4 v[8];
+  if (f4 < per_cta) {
+    const float4* base = reinterpret_cast<const float4*>(part) + f4;
+    for (int t0 = sl; t0 < nb; t0 += 8 * kRedSlices) {
+      float4 v[8];
 #pragma unroll
-    for (int u = 0; u < 8; ++u) {
-      const int t = t0 + u * kS;
-      v[u] = t < nb ? __ldg(base + (size_t)(split + t * P.nsplit) * (stride_b / 4)) : make_float4(0.f, 0.f, 0.f, 0.f);
-    }
+      for (int u = 0; u < 8; ++u) {
+        const int t = t0 + u * kRedSlices;
+        v[u] = t < nb ? __ldg(base + (size_t)(split + t * P.nsplit) * per_cta) : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
 #pragma unroll
-    for (int u = 0; u < 8; ++u) {
-      acc.x += v[u].x;
-      acc.y += v[u].y;
-      acc.z += v[u].z;
-      acc.w += v[u].w;
+      for (int u = 0; u < 8; ++u) {
+        acc.x += v[u].x;
+        acc.y += v[u].y;
+        acc.z += v[u].z;
+        acc.w += v[u].w;
+      }
     }
   }
-  red[sl][4 * q + 0] = acc.x;
-  red[sl][4 * q + 1] = acc.y;
-  red[sl][4 * q + 2] = acc.z;
-  red[sl][4 * q + 3] = acc.w;
+  red[sl][threadIdx.x % kRedSpan] = acc;
   __syncthreads();
-  for (int k = threadIdx.x; k < NOUT; k += kRedThreads) {
-    double t = red[0][k];
-    for (int s2 = 1; s2 < kS; ++s2) t += red[s2][k];
-    dw[((size_t)k * taps + tap) * cin + c] = (float)t;
+  if (sl != 0 || f4 >= per_cta) return;
+  double t4[4] = {0.0, 0.0, 0.0, 0.0};
+  for (int q = 0; q < kRedSlices; ++q) {
+    const float4 v = red[q][threadIdx.x];
+    t4[0] += v.x;
+    t4[1] += v.y;
+    t4[2] += v.z;
+    t4[3] += v.w;
+  }
+  // f4 -> (group, c16, v, row): see the partial layout in wgrad_kernel
+  const int row = (int)(f4 % 128);
+  const int vq = (int)((f4 / 128) % 4);
+  const int c16 = (int)((f4 / 512) % kC16);
+  const int gl = (int)(f4 / (512 * (size_t)kC16));
+  if (gl >= P.split_ng[split]) return;
+  const int grp = P.split_g0[split] + gl;
+  const int tap = row < 64 ? P.ta[grp] : P.tb[grp];
+  if (row >= 64 && P.tb[grp] == P.ta[grp]) return;  // discarded half of a self-paired tap
+  const int c = P.split_chunk[split] * 64 + (row & 63);
+  if (c >= cin) return;
+  for (int j = 0; j < 4; ++j) {
+    const int k = c16 * 16 + vq * 4 + j;
+    dw[((size_t)k * taps + tap) * cin + c] = (float)t4[j];
   }
 }
 
@@ -418,7 +429,8 @@ int launch_wgrad(const WgradArgs& w, int c_in, int c_out, bool bf16, const void*
   }
   if (rc) return rc;
   if (between) between(ctx);
-  const int rgrid = taps * c_in;
+  const size_t per_cta = (size_t)a.plan.gmax * (nout / 16) * 512;
+  const int rgrid = (int)((per_cta + kRedSpan - 1) / kRedSpan) * a.plan.nsplit;
   switch (nout) {
     case 16: wgrad_reduce_kernel<16><<<rgrid, kRedThreads, 0, st>>>(a.part, w.dw, a.plan, grid, c_in, taps); break;
     case 32: wgrad_reduce_kernel<32><<<rgrid, kRedThreads, 0, st>>>(a.part, w.dw, a.plan, grid, c_in, taps); break;
