@@ -14,8 +14,7 @@ int launch_dgrad(const DgradArgs& d, int c_in, int c_out, bool bf16, const void*
   a.g = d.g;
   a.out = d.dx;
   a.out_c = c_in;
-  a.out_shift = __builtin_ctz((unsigned)(c_in * 2 / 16));
-  if ((c_in * 2 / 16) & (c_in * 2 / 16 - 1)) return 3;  // stored chunks per pixel: a power of two
+  if (c_in % 8 != 0) return 3;  // dx rows are stored in 16-byte groups of 8 channels
   a.mode = kFpropPlain;
   a.err = d.err;
   a.dz = DzSrc{d.dy, d.z, d.y, d.mask, d.coef, d.g.h, d.g.w, c_out};

@@ -17,7 +17,6 @@ int launch_fprop(const FpropArgs& f, int c_in, int c_out, bool bf16, const void*
   a.g = f.g;
   a.out = f.z;
   a.out_c = c_out;
-  a.out_shift = __builtin_ctz((unsigned)(c_out * 2 / 16));
   a.mode = f.mode;
   a.part = f.part;
   a.ticket = f.ticket;

@@ -29,7 +29,6 @@ struct ConvArgs {
   HaloGeom g;
   void* out;                // [n][p][q][out_c] storage dtype: z, y (inference) or dx
   int out_c;                // channels stored per output pixel (<= NOUT)
-  int out_shift;            // log2 of the 16-byte chunks per stored output pixel
   int mode;                 // FpropMode (fprop only)
   // forward statistics / finalize
   float* part;
@@ -77,7 +76,7 @@ __host__ __device__ constexpr int wslab_bytes(int kind, int nout) {
 }
 
 struct Layout {
-  uint32_t halo_stride, off_w, off_stage, off_rowtab, off_bar, total, wslab;
+  uint32_t halo_stride, off_w, off_stage, off_bar, total, wslab;
   int nsw;
 };
 
@@ -90,8 +89,8 @@ __host__ __device__ inline Layout layout(const HaloGeom& g, int kind, int nch, i
   L.off_w = 2 * L.halo_stride;
   L.off_stage = L.off_w + (uint32_t)L.nsw * L.wslab;
   const uint32_t stage = 128u * nout * 2;
-  L.off_rowtab = L.off_stage + stage;                 // int32[128]: global row of each tile row
-  L.off_bar = (L.off_rowtab + 512u + 15u) & ~15u;
+  // off_stage: scratch for the end-of-kernel statistics reduction (and the finalize)
+  L.off_bar = (L.off_stage + stage + 15u) & ~15u;
   const uint32_t nbar = 8 + 2 * L.nsw + 1;
   L.total = L.off_bar + nbar * 8 + 16;
   return L;
@@ -124,20 +123,12 @@ __device__ __forceinline__ void reduce_scatter(float (&v)[L], int lane) {
   for (; o >= 1; o >>= 1) v[0] += __shfl_xor_sync(0xffffffffu, v[0], o);
 }
 
-// Offset of chunk c of staged row `row` (pitch = NOUT*2 bytes).
-template <int PITCH>
-__device__ __forceinline__ uint32_t stage_off(uint32_t row, uint32_t c) {
-  if constexpr (PITCH >= 128) return swz_off(row, c, PITCH);
-  else return row * PITCH + c * 16;
-}
-
 template <int KIND, int NCH, int NOUT, int U, bool WRES, bool BF16>
 __global__ void __launch_bounds__(Roles<KIND>::kThreads, 1)
     halo_conv_kernel(const __grid_constant__ CUtensorMap map_x,
                      const __grid_constant__ CUtensorMap map_w, const ConvArgs a) {
   using R = Roles<KIND>;
   constexpr int kThreads = R::kThreads;
-  constexpr int kPitch = NOUT * 2;
   constexpr int kTmemCols = pow2_at_least(2 * U * NOUT);
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -147,7 +138,6 @@ __global__ void __launch_bounds__(Roles<KIND>::kThreads, 1)
   const uint32_t sbase = smem_u32(smem);
   const uint32_t halo_addr = sbase;
   const uint32_t w_addr = sbase + L.off_w;
-  const uint32_t stage_addr = sbase + L.off_stage;
   const uint32_t bar0 = sbase + L.off_bar;
   const uint32_t bar_halo_full = bar0;
   const uint32_t bar_halo_empty = bar0 + 16;
