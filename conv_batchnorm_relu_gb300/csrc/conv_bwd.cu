@@ -173,7 +173,9 @@ __global__ void __launch_bounds__(kWgThreads, 1)
         mbar_wait(bar_x_full + 8 * (k & 1), (k >> 1) & 1);
     }
   } else if (warp == 1) {
-    if (lane == 0) {
+    // The whole warp runs the issue loop (warp-uniform descriptor arithmetic) and one elected
+    // lane issues each MMA and commit; control-flow decisions are voted across the warp.
+    {
       const uint32_t idesc = make_idesc_f16(128, NOUT, BF16, true, true);
       // per-group A descriptor with a zero start address: LBO = the two taps' row distance.
       // Kept in registers (fully unrolled over the compile-time maximum group count).
@@ -191,12 +193,13 @@ __global__ void __launch_bounds__(kWgThreads, 1)
       }
       uint32_t it = 0;
       bool first = true;
-      for (int u = ustart; u < g.total_units && !hc::is_aborted(abort_flag); u += ustride, ++it) {
+      for (int u = ustart; u < g.total_units && !__any_sync(0xffffffffu, hc::is_aborted(abort_flag));
+           u += ustride, ++it) {
         const int n = u / g.upi;
         const int m0 = (u - n * g.upi) * g.um;
         const int off = m0 - (m0 / g.wp) * g.wp;
         const uint32_t s = it & 1, ph = (it >> 1) & 1;
-        if (!mbar_wait(bar_x_full + 8 * s, ph) || (!DZTMA && !mbar_wait(bar_dz_full + 8 * s, ph))) {
+        if (!__all_sync(0xffffffffu, mbar_wait(bar_x_full + 8 * s, ph) && (DZTMA || mbar_wait(bar_dz_full + 8 * s, ph)))) {
           hc::set_abort(abort_flag, a.err, kErrWaitOperand);
           break;
         }
@@ -214,7 +217,7 @@ __global__ void __launch_bounds__(kWgThreads, 1)
             for (int kk = 0; kk < g.um / 16; ++kk) {
               const uint64_t ak = a_unit + (uint64_t)kk * 128;  // 16 pixel rows further
 #pragma unroll
-              for (int gl = 0; gl < NG; ++gl) mma_f16_ss(tmem_base + gl * NOUT, a_grp[gl] + ak, bd, idesc, acc);
+              for (int gl = 0; gl < NG; ++gl) mma_f16_ss_warp(tmem_base + gl * NOUT, a_grp[gl] + ak, bd, idesc, acc);
               bd += 128;
               acc = 1u;
             }
@@ -228,12 +231,12 @@ __global__ void __launch_bounds__(kWgThreads, 1)
 #undef CBR_WG_NG
           default: break;
         }
-        mma_commit(bar_x_empty + 8 * s);
-        if (!DZTMA) mma_commit(bar_dz_empty + 8 * s);
+        mma_commit_warp(bar_x_empty + 8 * s);
+        if (!DZTMA) mma_commit_warp(bar_dz_empty + 8 * s);
         first = false;
       }
-      mma_commit(bar_acc_full);
-      mma_commit(bar_drain);
+      mma_commit_warp(bar_acc_full);
+      mma_commit_warp(bar_drain);
       mbar_wait(bar_drain, 0);
     }
   } else {

@@ -270,9 +270,14 @@ __global__ void __launch_bounds__(Roles<KIND>::kThreads, 1)
     }
   } else if (warp == R::kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
-    // One thread feeds the tensor cores, so the issue sequence is kept free of runtime
-    // conditions: a guard or data-dependent branch beside each MMA roughly halves the rate.
-    if (lane == 0) {
+    // The whole warp runs the issue loop in converged control flow, so all descriptor
+    // arithmetic is warp-uniform, and one elected lane issues each tcgen05.mma and commit.
+    // (Issued from a single lane under a divergent branch, the same sequence ran 20-35%
+    // slower.)  Every decision that changes control flow is voted across the warp, so the
+    // lanes can never part (a full-mask elect.sync with absent lanes would not return).  The
+    // sequence is also kept free of runtime conditions: a guard beside each MMA halves the
+    // rate.
+    {
       constexpr bool kBMn = KIND != kKindFprop;
       const uint32_t idesc = make_idesc_f16(128, NOUT, BF16, false, kBMn);
       const uint64_t b_base = kBMn ? make_sw128_desc(w_addr, 8192, 1024, 0) : make_sw128_desc(w_addr, 16, 1024, 0);
@@ -281,20 +286,21 @@ __global__ void __launch_bounds__(Roles<KIND>::kThreads, 1)
       if (WRES) {
         // resident filter: every slab is waited for once, before the first unit
         for (int i = 0; i < NCH * rs && !bad; ++i)
-          if (!mbar_wait(bar_w_full + 8 * i, 0)) {
+          if (!__all_sync(0xffffffffu, mbar_wait(bar_w_full + 8 * i, 0))) {
             set_abort(abort_flag, a.err, kErrWaitWeights);
             bad = true;
           }
         tc_fence_after();
       }
       uint32_t hit = 0, wit = 0, ait = 0;
-      for (int u = blockIdx.x; u < g.total_units && !bad && !is_aborted(abort_flag); u += gridDim.x) {
+      for (int u = blockIdx.x; u < g.total_units && !bad && !__any_sync(0xffffffffu, is_aborted(abort_flag));
+           u += gridDim.x) {
         const int n = u / g.upi;
         const int m0 = (u - n * g.upi) * g.um;
         const int off = m0 - (m0 / g.wp) * g.wp;
         const int ntiles = min(U, (rows_img - m0 + 127) / 128);
         const uint32_t as = ait & 1, aph = (ait >> 1) & 1;
-        if (!mbar_wait(bar_acc_empty + 8 * as, aph ^ 1)) {
+        if (!__all_sync(0xffffffffu, mbar_wait(bar_acc_empty + 8 * as, aph ^ 1))) {
           set_abort(abort_flag, a.err, kErrWaitAccum);
           break;
         }
@@ -302,7 +308,7 @@ __global__ void __launch_bounds__(Roles<KIND>::kThreads, 1)
         const uint32_t d0 = tmem_base + as * (U * NOUT);
         for (int ch = 0; ch < NCH && !bad; ++ch, ++hit) {
           const uint32_t hs = hit & 1, hph = (hit >> 1) & 1;
-          if (!mbar_wait(bar_halo_full + 8 * hs, hph)) {
+          if (!__all_sync(0xffffffffu, mbar_wait(bar_halo_full + 8 * hs, hph))) {
             set_abort(abort_flag, a.err, kErrWaitHalo);
             bad = true;
             break;
@@ -321,7 +327,7 @@ __global__ void __launch_bounds__(Roles<KIND>::kThreads, 1)
                 wslab_off = (uint32_t)(ch * rs + tap) * L.wslab;
               } else {
                 ws = wit % kStreamStages;
-                if (!mbar_wait(bar_w_full + 8 * ws, (wit / kStreamStages) & 1)) {
+                if (!__all_sync(0xffffffffu, mbar_wait(bar_w_full + 8 * ws, (wit / kStreamStages) & 1))) {
                   set_abort(abort_flag, a.err, kErrWaitWeights);
                   bad = true;
                   break;
@@ -335,13 +341,13 @@ __global__ void __launch_bounds__(Roles<KIND>::kThreads, 1)
               for (int t = 0; t < NT; ++t)
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk)
-                  mma_f16_ss(d0 + t * NOUT, a_tap + (uint64_t)((t * 128 * 128 + kk * 32) >> 4),
+                  mma_f16_ss_warp(d0 + t * NOUT, a_tap + (uint64_t)((t * 128 * 128 + kk * 32) >> 4),
                              b_tap + (uint64_t)((kBMn ? kk * 2048 : kk * 32) >> 4), idesc, kk ? 1u : acc0);
               const bool wrap = sx + 1 == g.s;
               sx = wrap ? 0 : sx + 1;
               a_tap += wrap ? 8 + a_row_skip : 8;
               if (!WRES) {
-                mma_commit(bar_w_empty + 8 * ws);
+                mma_commit_warp(bar_w_empty + 8 * ws);
                 ++wit;
               }
             }
@@ -350,13 +356,13 @@ __global__ void __launch_bounds__(Roles<KIND>::kThreads, 1)
             run_taps(std::integral_constant<int, U>{});
           else
             run_taps(std::integral_constant<int, 1>{});  // ragged tail of an image (U = 2 only)
-          mma_commit(bar_halo_empty + 8 * hs);
+          mma_commit_warp(bar_halo_empty + 8 * hs);
         }
         if (bad) break;
-        mma_commit(bar_acc_full + 8 * as);
+        mma_commit_warp(bar_acc_full + 8 * as);
         ++ait;
       }
-      mma_commit(bar_drain);
+      mma_commit_warp(bar_drain);
       mbar_wait(bar_drain, 0);
     }
   } else {
