@@ -82,8 +82,15 @@ struct Prof {
     t_prof_count = 0;
     mark();
   }
+  // Under stream capture a plain event record only orders streams; the external flag makes
+  // it a timestamping event-record node of the graph.
   void mark() {
-    if (ev && used < count) cudaEventRecord(static_cast<cudaEvent_t>(ev[used++]), st);
+    if (!ev || used >= count) return;
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(st, &cs) == cudaSuccess && cs == cudaStreamCaptureStatusActive)
+      cudaEventRecordWithFlags(static_cast<cudaEvent_t>(ev[used++]), st, cudaEventRecordExternal);
+    else
+      cudaEventRecord(static_cast<cudaEvent_t>(ev[used++]), st);
   }
   ~Prof() { t_prof_used = used; }
 };

@@ -193,7 +193,9 @@ cbr_status_t cbr_stream_status(cbr_stream_t stream);
  * cbr_forward_train / cbr_backward / cbr_forward_infer call records events[0] before its
  * first kernel and events[i] after its i-th kernel (cudaEvent_t handles owned by the caller,
  * at most `count`), then clears the hook.  cbr_profile_last_count() returns how many events
- * that call recorded.  Used to time each kernel inside the real calls.
+ * that call recorded.  Used to time each kernel inside the real calls.  When the call is made
+ * while its stream is being captured into a CUDA graph, the events are recorded as external
+ * event-record nodes (cudaEventRecordExternal), so they timestamp every replay of the graph.
  */
 cbr_status_t cbr_profile_next_call(void* const* events, int32_t count);
 int32_t cbr_profile_last_count(void);
