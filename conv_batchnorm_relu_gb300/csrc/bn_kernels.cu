@@ -155,42 +155,51 @@ __global__ void __launch_bounds__(kRedThreads)
   if (ticket != gridDim.x - 1) return;
   // ------------------------------------------------------------ last block: finalize
   __threadfence();
-  constexpr int kFinWarps = 8;
-  double* dred = reinterpret_cast<double*>(red);  // [kFinWarps][2*c], c <= 256
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int nv4 = (2 * c) / 4;
-  if (warp < kFinWarps) {
-    for (int c4 = lane; c4 < nv4; c4 += 32) {
-      // fp32 over this warp's share of blocks (fixed order), fp64 across warps: this loop runs
-      // on one SM after all others and the FP64 rate is a small fraction of FP32.
-      float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
-      for (int b = warp; b < (int)gridDim.x; b += kFinWarps) {
-        const float4 v = __ldcg(reinterpret_cast<const float4*>(a.part + (size_t)b * 2 * c) + c4);
-        s0 += v.x;
-        s1 += v.y;
-        s2 += v.z;
-        s3 += v.w;
+  // One SM runs this after all the others, so it is kept short: every block partial is loaded
+  // in one batch (thread t sums float4 column t % nv4 of blocks t / nv4, + rgs, ..., in fp32
+  // and a fixed order), row groups are combined in fixed order in fp64, and the coefficient
+  // math multiplies by the host's 1/M instead of dividing (fp64 division is slow here).
+  constexpr int kLd = 16;
+  const int nv4 = (2 * c) / 4;                    // float4 columns of one partial (<= 128)
+  const int rgs = kRedThreads / nv4;              // row groups; rgs * 2c = 2048 floats
+  float* fred = red;                              // [rgs][2c]
+  double* fin = reinterpret_cast<double*>(red + rgs * 2 * c);  // [2c]
+  {
+    const int c4 = threadIdx.x % nv4, rg = threadIdx.x / nv4;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int b0 = rg; b0 < (int)gridDim.x; b0 += kLd * rgs) {
+      float4 v[kLd];
+#pragma unroll
+      for (int k = 0; k < kLd; ++k) {
+        const int b = b0 + k * rgs;
+        v[k] = b < (int)gridDim.x ? __ldcg(reinterpret_cast<const float4*>(a.part + (size_t)b * 2 * c) + c4)
+                                  : make_float4(0.f, 0.f, 0.f, 0.f);
       }
-      dred[warp * 2 * c + 4 * c4 + 0] = s0;
-      dred[warp * 2 * c + 4 * c4 + 1] = s1;
-      dred[warp * 2 * c + 4 * c4 + 2] = s2;
-      dred[warp * 2 * c + 4 * c4 + 3] = s3;
+#pragma unroll
+      for (int k = 0; k < kLd; ++k) {
+        acc.x += v[k].x;
+        acc.y += v[k].y;
+        acc.z += v[k].z;
+        acc.w += v[k].w;
+      }
     }
+    reinterpret_cast<float4*>(fred + rg * 2 * c)[c4] = acc;
+  }
+  __syncthreads();
+  for (int i = threadIdx.x; i < 2 * c; i += kRedThreads) {
+    double t = 0;
+    for (int r = 0; r < rgs; ++r) t += fred[r * 2 * c + i];
+    fin[i] = t;
   }
   __syncthreads();
   for (int ch = threadIdx.x; ch < c; ch += kRedThreads) {
-    double g = 0, gx = 0;
-    for (int w = 0; w < kFinWarps; ++w) {
-      g += dred[w * 2 * c + ch];
-      gx += dred[w * 2 * c + c + ch];
-    }
-    const double M = (double)a.m_count;
+    const double g = fin[ch], gx = fin[c + ch];
     const double inv = a.inv_std[ch];
     const double dgamma = gx * inv;  // sum g * xhat
     const double dbeta = g;
     const double ac = (double)a.gamma[ch] * inv;
-    const double dc = ac * dgamma * inv / M;
-    const double ec = -ac * dbeta / M + dc * (double)a.mean[ch];
+    const double dc = ac * dgamma * inv * a.inv_m;
+    const double ec = -ac * dbeta * a.inv_m + dc * (double)a.mean[ch];
     a.dgamma[ch] = (float)dgamma;
     a.dbeta[ch] = (float)dbeta;
     a.coef[ch] = (float)ac;
@@ -333,9 +342,11 @@ int launch_bwd_reduce(const BwdReduceArgs& a, bool bf16, int num_sms, cudaStream
   const bool bits = a.mask != nullptr;
   // the grid is at most the resident blocks (one wave) and the number of partials it leaves
   // is bounded by the workspace (bwd_reduce_partial_floats: two blocks per SM)
+  BwdReduceArgs b = a;
+  b.inv_m = 1.0 / (double)a.m_count;
   auto go = [&](auto kern) {
     const int grid = std::min(stream_grid(kern, kRedThreads, nvec / kRedUnroll, num_sms), 2 * num_sms);
-    kern<<<grid, kRedThreads, 0, st>>>(a);
+    kern<<<grid, kRedThreads, 0, st>>>(b);
   };
   if (bf16) {
     if (bits) go(bn_bwd_reduce_kernel<true, true>);

@@ -96,6 +96,7 @@ struct BwdReduceArgs {
   float* part;              // [grid][2][c]
   uint32_t* ticket;
   long long m_count;
+  double inv_m;             // 1 / m_count (set by the launcher)
   int c;
   uint32_t* err;
 };

@@ -31,6 +31,8 @@ int launch_fprop(const FpropArgs& f, int c_in, int c_out, bool bf16, const void*
   a.momentum = f.momentum;
   a.eps = f.eps;
   a.m_count = f.m_count;
+  a.inv_m = 1.0 / (double)f.m_count;
+  a.unbias = f.m_count > 1 ? (float)((double)f.m_count / (double)(f.m_count - 1)) : 1.f;
   a.err = f.err;
   HaloGeom& g = a.g;
   const int nch = c_in <= 64 ? 1 : (c_in <= 128 ? 2 : 0);

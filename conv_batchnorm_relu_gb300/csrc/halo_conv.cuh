@@ -44,6 +44,8 @@ struct ConvArgs {
   float momentum;
   float eps;
   long long m_count;
+  double inv_m;             // 1 / m_count
+  float unbias;             // m_count / (m_count - 1)
   // dgrad A operand
   DzSrc dz;
   uint32_t* err;
@@ -526,47 +528,61 @@ __global__ void __launch_bounds__(Roles<KIND>::kThreads, 1)
     if (*ticket_slot == gridDim.x - 1 && !is_aborted(abort_flag)) {
       // ---------------------------------------------------- bn_finalize (last CTA)
       __threadfence();
-      constexpr int kW = kThreads / 32;
-      double* dred = reinterpret_cast<double*>(smem + L.off_stage);  // [kW][2*COUT]
-      double* fin = dred + kW * 2 * COUT;                             // [2*COUT]
-      constexpr int kV4 = (2 * COUT) / 4;
-      for (int c4 = lane; c4 < kV4; c4 += 32) {
-        // fp32 over this warp's share of CTAs (fixed order), fp64 across warps: the FP64 rate
-        // is a small fraction of FP32 here and this loop runs on one SM after all others.
-        float acc0 = 0.f, acc1 = 0.f, acc2 = 0.f, acc3 = 0.f;
-        for (int b = warp; b < (int)gridDim.x; b += kW) {
-          const float4 v = __ldcg(reinterpret_cast<const float4*>(a.part + (size_t)b * 2 * COUT) + c4);
-          acc0 += v.x;
-          acc1 += v.y;
-          acc2 += v.z;
-          acc3 += v.w;
+      // This runs on one SM after all the others, so it is kept short: every CTA partial is
+      // loaded in one batch (thread t sums float4 column t % kV4 of CTAs t / kV4, + kRG, ...,
+      // in fp32 and a fixed order), the row groups are combined in fixed order in fp64, and
+      // the per-channel math avoids fp64 division and square root (slow at this part's FP64
+      // rate): mean and variance by fp64 multiplies with the host's 1/M, 1/sqrt in fp32.
+      constexpr int kV4 = (2 * COUT) / 4;        // float4 columns of one partial
+      // row groups, bounded by the staging region (128 x NOUT x 2 bytes) that also holds fin
+      constexpr int kRGfit = (128 * NOUT * 2 - 2 * COUT * 8) / (2 * COUT * 4);
+      constexpr int kRG = kThreads / kV4 < kRGfit ? kThreads / kV4 : kRGfit;
+      static_assert(kRG >= 1, "finalize scratch");
+      constexpr int kLd = 16;                    // loads in flight per thread
+      float* fred = reinterpret_cast<float*>(smem + L.off_stage);  // [kRG][2*COUT]
+      double* fin = reinterpret_cast<double*>(fred + kRG * 2 * COUT);
+      const int c4 = threadIdx.x % kV4, rg = threadIdx.x / kV4;
+      if (rg < kRG) {
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int b0 = rg; b0 < (int)gridDim.x; b0 += kLd * kRG) {
+          float4 v[kLd];
+#pragma unroll
+          for (int k = 0; k < kLd; ++k) {
+            const int b = b0 + k * kRG;
+            v[k] = b < (int)gridDim.x ? __ldcg(reinterpret_cast<const float4*>(a.part + (size_t)b * 2 * COUT) + c4)
+                                      : make_float4(0.f, 0.f, 0.f, 0.f);
+          }
+#pragma unroll
+          for (int k = 0; k < kLd; ++k) {
+            acc.x += v[k].x;
+            acc.y += v[k].y;
+            acc.z += v[k].z;
+            acc.w += v[k].w;
+          }
         }
-        dred[warp * 2 * COUT + 4 * c4 + 0] = acc0;
-        dred[warp * 2 * COUT + 4 * c4 + 1] = acc1;
-        dred[warp * 2 * COUT + 4 * c4 + 2] = acc2;
-        dred[warp * 2 * COUT + 4 * c4 + 3] = acc3;
+        reinterpret_cast<float4*>(fred + rg * 2 * COUT)[c4] = acc;
       }
       __syncthreads();
       for (int i = threadIdx.x; i < 2 * COUT; i += kThreads) {
         double t = 0;
-        for (int w = 0; w < kW; ++w) t += dred[w * 2 * COUT + i];
+        for (int r = 0; r < kRG; ++r) t += fred[r * 2 * COUT + i];
         fin[i] = t;
       }
       __syncthreads();
       for (int c = threadIdx.x; c < COUT; c += kThreads) {
-        const double M = (double)a.m_count;
-        const double mean = fin[c] / M;
-        double var = fin[COUT + c] / M - mean * mean;
-        var = var > 0.0 ? var : 0.0;
-        const double inv = 1.0 / sqrt(var + (double)a.eps);
-        const double gm = a.gamma[c];
-        a.saved_mean[c] = (float)mean;
-        a.saved_inv_var[c] = (float)inv;
-        a.eq[c] = (float)(gm * inv);
-        a.eq[COUT + c] = (float)((double)a.beta[c] - gm * mean * inv);
-        const double mom = a.momentum;
-        a.running_mean[c] = (float)((1.0 - mom) * a.running_mean[c] + mom * mean);
-        a.running_var[c] = (float)((1.0 - mom) * a.running_var[c] + mom * var * M / (M - 1.0));
+        const double mean = fin[c] * a.inv_m;
+        const double var_d = fin[COUT + c] * a.inv_m - mean * mean;
+        const float var = var_d > 0.0 ? (float)var_d : 0.f;
+        const float inv = rsqrtf(var + a.eps);
+        const float meanf = (float)mean;
+        const float gm = a.gamma[c];
+        a.saved_mean[c] = meanf;
+        a.saved_inv_var[c] = inv;
+        a.eq[c] = gm * inv;
+        a.eq[COUT + c] = a.beta[c] - gm * meanf * inv;
+        const float mom = a.momentum;
+        a.running_mean[c] = (1.f - mom) * a.running_mean[c] + mom * meanf;
+        a.running_var[c] = (1.f - mom) * a.running_var[c] + mom * var * a.unbias;
       }
     }
   }
