@@ -130,7 +130,8 @@ bool is_first_layer(const Shape& s) { return s.cin == 3; }
 // Shapes this build runs on the device.
 int check_supported(const Shape& s) {
   if (!(s.cout == 16 || s.cout == 32 || s.cout == 64 || s.cout == 128)) return CBR_ERR_UNSUPPORTED;
-  if (is_first_layer(s)) return CBR_ERR_UNSUPPORTED;  // first-layer kernels not built yet
+  // first layer (3 channels): im2col kernels, any stride, filters up to 8x8, rows up to 128
+  if (is_first_layer(s)) return (s.r <= 8 && s.s <= 8 && s.q <= 128) ? CBR_OK : CBR_ERR_UNSUPPORTED;
   if (s.stride != 1) return CBR_ERR_UNSUPPORTED;
   if (s.cin % 8 != 0 || s.cin > 128) return CBR_ERR_UNSUPPORTED;
   if (s.w + 2 * s.pad > 256) return CBR_ERR_UNSUPPORTED;
@@ -183,10 +184,34 @@ HaloGeom make_geom(const Shape& s) {
   return g;
 }
 
+// Forward convolution of either family (halo tiling, or the first-layer im2col kernel).
+int run_fprop(const FpropArgs& a, const Shape& s, const void* x, const void* w, int num_sms, cudaStream_t st) {
+  if (is_first_layer(s)) return launch_first_fprop(a, (int)s.stride, (int)s.cout, s.bf16, x, w, num_sms, st);
+  return launch_fprop(a, (int)s.cin, (int)s.cout, s.bf16, x, w, num_sms, st);
+}
+
+}  // namespace
+
+namespace {
+bool encode_tiled_mode(CUtensorMap* map, CUtensorMapDataType dt, int rank, const void* base,
+                       const uint64_t* dims, const uint64_t* strides_bytes, const uint32_t* box,
+                       CUtensorMapSwizzle swz);
 }  // namespace
 
 bool encode_tiled(CUtensorMap* map, CUtensorMapDataType dt, int rank, const void* base,
                   const uint64_t* dims, const uint64_t* strides_bytes, const uint32_t* box) {
+  return encode_tiled_mode(map, dt, rank, base, dims, strides_bytes, box, CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
+bool encode_tiled_plain(CUtensorMap* map, CUtensorMapDataType dt, int rank, const void* base,
+                        const uint64_t* dims, const uint64_t* strides_bytes, const uint32_t* box) {
+  return encode_tiled_mode(map, dt, rank, base, dims, strides_bytes, box, CU_TENSOR_MAP_SWIZZLE_NONE);
+}
+
+namespace {
+bool encode_tiled_mode(CUtensorMap* map, CUtensorMapDataType dt, int rank, const void* base,
+                       const uint64_t* dims, const uint64_t* strides_bytes, const uint32_t* box,
+                       CUtensorMapSwizzle swz) {
   std::call_once(g_encode_once, [] {
     cudaDriverEntryPointQueryResult q;
     void* fn = nullptr;
@@ -206,9 +231,10 @@ bool encode_tiled(CUtensorMap* map, CUtensorMapDataType dt, int rank, const void
     if (i + 1 < rank) st[i] = strides_bytes[i];
   }
   return g_encode(map, dt, (cuuint32_t)rank, const_cast<void*>(base), d, st, b, es,
-                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
+}  // namespace
 
 int forward_workspace_bytes(const void* desc, bool need_z, size_t* bytes) {
   Shape s;
@@ -313,7 +339,7 @@ cbr_status_t cbr_forward_train(const cbr_desc_t* desc, const void* x, const void
   a.m_count = s.m;
   a.err = dev->err;
   a.mode = kFpropStats;
-  st = launch_fprop(a, (int)s.cin, (int)s.cout, s.bf16, x, w, dev->num_sms, cs);
+  st = run_fprop(a, s, x, w, dev->num_sms, cs);
   if (st) return (cbr_status_t)st;
   prof.mark();
 
@@ -354,6 +380,8 @@ cbr_status_t cbr_backward(const cbr_desc_t* desc, const void* dy, const void* x,
   if ((st = check_supported(s))) return (cbr_status_t)st;
   // dgrad runs as a stride-1 conv with padding R-1-pad on both axes
   if (dx && (s.r != s.s || s.pad > s.r - 1)) return CBR_ERR_UNSUPPORTED;
+  // The first layer has no dgrad (CBR page, section 6); its wgrad kernel is not built yet.
+  if (is_first_layer(s)) return CBR_ERR_UNSUPPORTED;
   const BwdWs L = bwd_ws(s, z_saved == nullptr);
   if (ws_bytes < L.total) return CBR_ERR_WORKSPACE;
   DeviceInfo* dev = nullptr;
@@ -371,7 +399,7 @@ cbr_status_t cbr_backward(const cbr_desc_t* desc, const void* dy, const void* x,
     a.m_count = s.m;
     a.err = dev->err;
     a.mode = kFpropPlain;
-    st = launch_fprop(a, (int)s.cin, (int)s.cout, s.bf16, x, w, dev->num_sms, cs);
+    st = run_fprop(a, s, x, w, dev->num_sms, cs);
     if (st) return (cbr_status_t)st;
     prof.mark();
     z = wsb + L.z;
@@ -501,7 +529,7 @@ cbr_status_t cbr_forward_infer(const cbr_desc_t* desc, const void* x, const void
   a.m_count = s.m;
   a.err = dev->err;
   a.mode = kFpropBiasRelu;
-  st = launch_fprop(a, (int)s.cin, (int)s.cout, s.bf16, x, w_fold, dev->num_sms, cs);
+  st = run_fprop(a, s, x, w_fold, dev->num_sms, cs);
   if (st) return (cbr_status_t)st;
   prof.mark();
   return CBR_OK;

@@ -65,9 +65,15 @@ int forward_workspace_bytes(const void* desc, bool need_z, size_t* bytes);
 // Tensor-map helpers (cbr_api.cu).
 bool encode_tiled(CUtensorMap* map, CUtensorMapDataType dt, int rank, const void* base,
                   const uint64_t* dims, const uint64_t* strides_bytes, const uint32_t* box);
+// Same, without swizzle (plain row-major boxes).
+bool encode_tiled_plain(CUtensorMap* map, CUtensorMapDataType dt, int rank, const void* base,
+                  const uint64_t* dims, const uint64_t* strides_bytes, const uint32_t* box);
 
 // Launchers (one per kernel family).  Each validates only what its kernel needs beyond the
 // C-ABI checks and returns a CBR status.
+// First-layer forward (Cin = 3, any stride, R, S <= 8, Q <= 128): first_layer.cu.
+int launch_first_fprop(const FpropArgs& f, int stride, int c_out, bool bf16, const void* x, const void* w,
+                       int num_sms, cudaStream_t st);
 int launch_fprop(const FpropArgs& a, int c_in, int c_out, bool bf16, const void* x,
                  const void* w, int num_sms, cudaStream_t st);
 size_t fprop_partial_floats(int num_sms, int c_out);

@@ -1,0 +1,455 @@
+// First-layer convolution (Tech-Renaissance CBR page, section 6: the network's first CBR takes
+// the 3-channel image, 7x7 filter, stride 2, padding 3, and has no dgrad).  A 3-channel pixel
+// is 6 bytes, so the input cannot be the innermost dimension of a TMA tile; instead whole
+// input rows (W*3 contiguous elements) are staged in shared memory by TMA and four builder
+// warps assemble the im2col tile from them:
+//   - one unit = one output row (n, p): Q <= 128 pixels = the M rows of one tile;
+//   - K slot of (r, s, c) = r*24 + s*3 + c: each filter row is a 24-slot segment (S*3 <= 24
+//     values and zeros), so a row of the tile is three 128-byte K atoms (K <= 192);
+//   - the filter is laid out in the same slot order once per CTA.
+// Forward: z = im2col(x) * W^T on the tensor cores (K = 16 per MMA, ceil(R*24/16) MMAs per unit),
+// then the same epilogue as the other convolutions (statistics in registers, direct stores).
+// WGrad: dW^T = im2col(x)^T * dz, with the same tile read as an MN-major operand.
+#include <algorithm>
+#include <type_traits>
+
+#include "halo_conv.cuh"
+
+namespace cbr {
+namespace {
+
+constexpr int kFlAtoms = 3;                          // 192 K slots
+constexpr uint32_t kFlAtomBytes = 128 * 128;         // 128 rows x 128 B
+constexpr uint32_t kFlTile = kFlAtoms * kFlAtomBytes;
+constexpr int kFlBuildWarps = 4;
+constexpr int kFlEpiWarp0 = 6;                       // warp 0: x TMA, 1-4: builders, 5: MMA
+constexpr int kFlThreads = (kFlEpiWarp0 + 8) * 32;   // 448
+
+struct FirstGeom {
+  int n_img, h, w;       // x [n][h][w][3]
+  int p, q;              // output rows and columns (q <= 128)
+  int r, s, stride, pad; // r, s <= 8
+  int units;             // n_img * p
+  int xbox, nbox;        // staging boxes per input row (xbox elements each, multiple of 8)
+  int bstride;           // elements between staged boxes: r*xbox rounded up to 128 bytes (TMA
+                         // destinations in shared memory must be 128-byte aligned)
+  int nk;                // MMA K steps: ceil(r*24/16)
+  int tma;               // input rows staged by TMA (row pitch a multiple of 16 bytes), else by warp 0
+};
+
+__host__ __device__ inline uint32_t fl_xstage_bytes(const FirstGeom& g) {
+  return ((uint32_t)g.nbox * g.bstride * 2 + 1023u) & ~1023u;
+}
+
+// Build the im2col tile of output row p of image n from the staged input rows.
+__device__ __forceinline__ void fl_build_tile(uint32_t a_stage, const uint16_t* xs, const FirstGeom& g, int tid,
+                                              int nthr) {
+  const int items = g.q * g.r;
+  for (int it = tid; it < items; it += nthr) {
+    const int q = it / g.r, rr = it - q * g.r;
+    uint32_t w32[12];
+#pragma unroll
+    for (int j = 0; j < 12; ++j) w32[j] = 0;
+    const int w0 = q * g.stride - g.pad;
+#pragma unroll
+    for (int sx = 0; sx < 8; ++sx) {
+      const int w = w0 + sx;
+      if (sx < g.s && w >= 0 && w < g.w) {
+#pragma unroll
+        for (int c = 0; c < 3; ++c) {
+          const int e = w * 3 + c;
+          const int b = e / g.xbox;
+          const uint32_t v = xs[b * g.bstride + rr * g.xbox + (e - b * g.xbox)];
+          const int slot = sx * 3 + c;
+          w32[slot >> 1] |= v << ((slot & 1) * 16);
+        }
+      }
+    }
+#pragma unroll
+    for (int cj = 0; cj < 3; ++cj) {
+      const int chunk = rr * 3 + cj;
+      const uint32_t addr = a_stage + (uint32_t)(chunk >> 3) * kFlAtomBytes + (uint32_t)q * 128u +
+                            ((uint32_t)((chunk & 7) ^ (q & 7)) << 4);
+      st_shared_v4(addr, make_uint4(w32[4 * cj], w32[4 * cj + 1], w32[4 * cj + 2], w32[4 * cj + 3]));
+    }
+  }
+}
+
+// Input rows without TMA (row pitch not a multiple of 16 bytes): the whole warp copies the R
+// rows of each unit, zero outside the image, then lane 0 marks the stage full.  Waits are
+// voted across the warp so its lanes stay together.
+__device__ void fl_stage_rows_plain(const uint16_t* x, const FirstGeom& g, uint16_t* stages, uint32_t xst,
+                                    uint32_t bar_x_full, uint32_t bar_x_empty, volatile int* abort_flag,
+                                    uint32_t* err) {
+  const int lane = threadIdx.x & 31;
+  const int row = g.w * 3;
+  uint32_t it = 0;
+  for (int u = blockIdx.x; u < g.units && !__any_sync(0xffffffffu, hc::is_aborted(abort_flag)); u += gridDim.x, ++it) {
+    const int n = u / g.p, p = u - n * g.p;
+    const uint32_t s = it & 1, ph = (it >> 1) & 1;
+    if (!__all_sync(0xffffffffu, mbar_wait_backoff(bar_x_empty + 8 * s, ph ^ 1, 64))) {
+      hc::set_abort(abort_flag, err, kErrWaitHalo);
+      break;
+    }
+    uint16_t* dst = stages + s * (xst / 2);
+    for (int i = lane; i < g.r * g.xbox; i += 32) {
+      const int rr = i / g.xbox, e = i - rr * g.xbox;
+      const int h = p * g.stride - g.pad + rr;
+      dst[i] = (h >= 0 && h < g.h && e < row) ? x[((size_t)n * g.h + h) * row + e] : (uint16_t)0;
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bar_x_full + 8 * s);
+  }
+}
+
+// ------------------------------------------------------------------------------ forward
+template <int NOUT, bool BF16>
+__global__ void __launch_bounds__(kFlThreads, 1)
+    first_fprop_kernel(const __grid_constant__ CUtensorMap map_x, const ConvArgs a, const FirstGeom g,
+                       const void* wts, const void* xin) {
+  constexpr int kTmemCols = hc::pow2_at_least(2 * NOUT);
+  constexpr uint32_t kBBytes = kFlAtoms * NOUT * 128;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  const uint32_t xst = fl_xstage_bytes(g);
+  const uint32_t off_a = 2 * xst, off_b = off_a + 2 * kFlTile, off_bar = off_b + kBBytes;
+  const uint32_t sbase = smem_u32(smem);
+  const uint32_t bar0 = sbase + off_bar;
+  const uint32_t bar_x_full = bar0, bar_x_empty = bar0 + 16, bar_a_full = bar0 + 32, bar_a_empty = bar0 + 48;
+  const uint32_t bar_acc_full = bar0 + 64, bar_acc_empty = bar0 + 80, bar_drain = bar0 + 96;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + off_bar + 104);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  volatile uint32_t* ticket_slot = reinterpret_cast<volatile uint32_t*>(tmem_slot + 2);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  // zero both A stages (rows >= Q and slots never written stay zero), build the filter tile
+  for (uint32_t i = threadIdx.x; i < 2 * kFlTile / 16; i += kFlThreads)
+    st_shared_v4(sbase + off_a + i * 16, make_uint4(0, 0, 0, 0));
+  {
+    const uint16_t* wsrc = static_cast<const uint16_t*>(wts);
+    for (int i = threadIdx.x; i < NOUT * kFlAtoms * 8; i += kFlThreads) {
+      const int n = i / (kFlAtoms * 8), chunk = i - n * (kFlAtoms * 8);
+      uint32_t w32[4] = {0, 0, 0, 0};
+      const int rr = chunk / 3;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const int slot = (chunk - rr * 3) * 8 + e;  // 0..23 within the filter row
+        const int sx = slot / 3, c = slot - sx * 3;
+        if (rr < g.r && sx < g.s && n < a.out_c) {
+          const uint32_t v = wsrc[((n * g.r + rr) * g.s + sx) * 3 + c];
+          w32[e >> 1] |= v << ((e & 1) * 16);
+        }
+      }
+      st_shared_v4(sbase + off_b + (uint32_t)(chunk >> 3) * (NOUT * 128) + (uint32_t)n * 128u +
+                       ((uint32_t)((chunk & 7) ^ (n & 7)) << 4),
+                   make_uint4(w32[0], w32[1], w32[2], w32[3]));
+    }
+  }
+  fence_proxy_async_smem();
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(bar_x_full + 8 * i, 1);
+      mbar_init(bar_x_empty + 8 * i, kFlBuildWarps);
+      mbar_init(bar_a_full + 8 * i, kFlBuildWarps);
+      mbar_init(bar_a_empty + 8 * i, 1);
+      mbar_init(bar_acc_full + 8 * i, 1);
+      mbar_init(bar_acc_empty + 8 * i, hc::kEpiThreads);
+    }
+    mbar_init(bar_drain, 1);
+    *abort_flag = 0;
+    fence_mbarrier_init();
+  }
+  if (warp == 5) {
+    tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    // ---------------------------------------------------------------- input-row stager
+    if (!g.tma) {
+      fl_stage_rows_plain(static_cast<const uint16_t*>(xin), g, reinterpret_cast<uint16_t*>(smem), xst,
+                          bar_x_full, bar_x_empty, abort_flag, a.err);
+    } else if (lane == 0) {
+      prefetch_tensormap(&map_x);
+      const uint32_t tx = (uint32_t)g.nbox * g.r * g.xbox * 2;
+      uint32_t it = 0;
+      for (int u = blockIdx.x; u < g.units && !hc::is_aborted(abort_flag); u += gridDim.x, ++it) {
+        const int n = u / g.p, p = u - n * g.p;
+        const uint32_t s = it & 1, ph = (it >> 1) & 1;
+        if (!mbar_wait_backoff(bar_x_empty + 8 * s, ph ^ 1, 64)) {
+          hc::set_abort(abort_flag, a.err, kErrWaitHalo);
+          break;
+        }
+        mbar_arrive_expect_tx(bar_x_full + 8 * s, tx);
+        for (int b = 0; b < g.nbox; ++b)
+          tma_load_3d(sbase + s * xst + (uint32_t)b * g.bstride * 2, &map_x, b * g.xbox, p * g.stride - g.pad, n,
+                      bar_x_full + 8 * s);
+      }
+      for (uint32_t k = (it > 2 ? it - 2 : 0); k < it; ++k) mbar_wait(bar_x_full + 8 * (k & 1), (k >> 1) & 1);
+    }
+  } else if (warp <= kFlBuildWarps) {
+    // ---------------------------------------------------------------- im2col builders
+    const int tid = threadIdx.x - 32;
+    uint32_t it = 0;
+    for (int u = blockIdx.x; u < g.units && !hc::is_aborted(abort_flag); u += gridDim.x, ++it) {
+      const uint32_t s = it & 1, ph = (it >> 1) & 1;
+      if (!mbar_wait_backoff(bar_a_empty + 8 * s, ph ^ 1, 64) || !mbar_wait(bar_x_full + 8 * s, ph)) {
+        hc::set_abort(abort_flag, a.err, kErrWaitOperand);
+        break;
+      }
+      fl_build_tile(sbase + off_a + s * kFlTile, reinterpret_cast<const uint16_t*>(smem + s * xst), g, tid,
+                    32 * kFlBuildWarps);
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(bar_x_empty + 8 * s);
+        mbar_arrive(bar_a_full + 8 * s);
+      }
+    }
+  } else if (warp == 5) {
+    // ---------------------------------------------------------------- MMA issuer (whole warp)
+    const uint32_t idesc = make_idesc_f16(128, NOUT, BF16, false, false);
+    const uint64_t b_base = make_sw128_desc(sbase + off_b, 16, 1024, 0);
+    uint32_t it = 0;
+    for (int u = blockIdx.x; u < g.units && !__any_sync(0xffffffffu, hc::is_aborted(abort_flag));
+         u += gridDim.x, ++it) {
+      const uint32_t s = it & 1, ph = (it >> 1) & 1;
+      if (!__all_sync(0xffffffffu, mbar_wait(bar_acc_empty + 8 * s, ph ^ 1) && mbar_wait(bar_a_full + 8 * s, ph))) {
+        hc::set_abort(abort_flag, a.err, kErrWaitAccum);
+        break;
+      }
+      tc_fence_after();
+      const uint64_t a_base = make_sw128_desc(sbase + off_a + s * kFlTile, 16, 1024, 0);
+      const uint32_t d = tmem_base + s * NOUT;
+      for (int kk = 0; kk < g.nk; ++kk)
+        mma_f16_ss_warp(d, a_base + (uint64_t)(((kk >> 2) * kFlAtomBytes + (kk & 3) * 32) >> 4),
+                        b_base + (uint64_t)(((kk >> 2) * (NOUT * 128) + (kk & 3) * 32) >> 4), idesc, kk ? 1u : 0u);
+      mma_commit_warp(bar_a_empty + 8 * s);
+      mma_commit_warp(bar_acc_full + 8 * s);
+    }
+    mma_commit_warp(bar_drain);
+    mbar_wait(bar_drain, 0);
+  } else {
+    // ---------------------------------------------------------------- epilogue (8 warps)
+    constexpr int kHalves = NOUT >= 64 ? 2 : 1;
+    constexpr int kCPH = NOUT / kHalves;
+    constexpr int kSB = kCPH < 32 ? kCPH : 32;
+    constexpr int kNB = kCPH / kSB;
+    constexpr int kSh = kSB == 32 ? 0 : 1;
+    const int ew = warp - kFlEpiWarp0;
+    const int quad = warp & 3;
+    const int half = ew >> 2;
+    const int e = quad * 32 + lane;
+    float s1[kNB], s2[kNB];
+#pragma unroll
+    for (int b = 0; b < kNB; ++b) s1[b] = s2[b] = 0.f;
+    constexpr bool kRegStats = kCPH <= 32;
+    float r1[kRegStats ? kCPH : 1], r2[kRegStats ? kCPH : 1];
+#pragma unroll
+    for (int i = 0; i < (kRegStats ? kCPH : 1); ++i) r1[i] = r2[i] = 0.f;
+    const bool stats = a.mode == kFpropStats;
+    const bool bias_relu = a.mode == kFpropBiasRelu;
+    const int out_c = a.out_c;
+    const size_t opitch = (size_t)out_c * 2;
+    const bool v8 = (out_c % 16) == 0 && (reinterpret_cast<uintptr_t>(a.out) & 31) == 0;
+    uint8_t* obase = static_cast<uint8_t*>(a.out);
+    const bool valid = e < g.q;
+    uint32_t it = 0;
+    for (int u = blockIdx.x; u < g.units && !hc::is_aborted(abort_flag); u += gridDim.x, ++it) {
+      const uint32_t s = it & 1, ph = (it >> 1) & 1;
+      if (!mbar_wait_backoff(bar_acc_full + 8 * s, ph, 128)) {
+        hc::set_abort(abort_flag, a.err, kErrWaitMma);
+        break;
+      }
+      tc_fence_after();
+      uint8_t* orow = obase + ((size_t)u * g.q + e) * opitch;  // u = n * P + p
+      if (half < kHalves) {
+#pragma unroll
+        for (int b = 0; b < kNB; ++b) {
+          const int c0 = half * kCPH + b * kSB;
+          uint32_t r[kSB];
+#pragma unroll
+          for (int q16 = 0; q16 < kSB / 16; ++q16)
+            tmem_ld16(tmem_base + ((uint32_t)(quad * 32) << 16) + s * NOUT + c0 + q16 * 16,
+                      *reinterpret_cast<uint32_t(*)[16]>(r + q16 * 16));
+          tmem_ld_wait();
+          if (b == kNB - 1) {
+            tc_fence_before();
+            mbar_arrive(bar_acc_empty + 8 * s);
+          }
+          float v[kSB];
+#pragma unroll
+          for (int i = 0; i < kSB; ++i) {
+            float x = __uint_as_float(r[i]);
+            if (bias_relu) x = fmaxf(x + __ldg(a.bias + c0 + i), 0.f);
+            v[i] = valid ? x : 0.f;
+          }
+          if (valid) {
+            uint4 pk[kSB / 8];
+#pragma unroll
+            for (int cc = 0; cc < kSB / 8; ++cc)
+              pk[cc] = make_uint4(pack2<BF16>(v[8 * cc + 0], v[8 * cc + 1]), pack2<BF16>(v[8 * cc + 2], v[8 * cc + 3]),
+                                  pack2<BF16>(v[8 * cc + 4], v[8 * cc + 5]), pack2<BF16>(v[8 * cc + 6], v[8 * cc + 7]));
+            if (v8) {
+#pragma unroll
+              for (int cc = 0; cc < kSB / 16; ++cc)
+                if (c0 + 16 * cc < out_c) st_global_v8(orow + (c0 + 16 * cc) * 2, pk[2 * cc], pk[2 * cc + 1]);
+            } else {
+#pragma unroll
+              for (int cc = 0; cc < kSB / 8; ++cc)
+                if (c0 + 8 * cc < out_c) st_global_v4(orow + (c0 + 8 * cc) * 2, pk[cc]);
+            }
+          }
+          if (stats) {
+            if constexpr (kRegStats) {
+#pragma unroll
+              for (int i = 0; i < kSB; ++i) {
+                r1[b * kSB + i] += v[i];
+                r2[b * kSB + i] = fmaf(v[i], v[i], r2[b * kSB + i]);
+              }
+            } else {
+              float sq[kSB];
+#pragma unroll
+              for (int i = 0; i < kSB; ++i) sq[i] = v[i] * v[i];
+              hc::reduce_scatter<kSB>(v, lane);
+              hc::reduce_scatter<kSB>(sq, lane);
+              s1[b] += v[0];
+              s2[b] += sq[0];
+            }
+          }
+        }
+      } else {
+        tc_fence_before();
+        mbar_arrive(bar_acc_empty + 8 * s);
+      }
+    }
+    if constexpr (kRegStats) {
+      if (stats && half < kHalves) {
+#pragma unroll
+        for (int b = 0; b < kNB; ++b) {
+          float v1[kSB], v2[kSB];
+#pragma unroll
+          for (int i = 0; i < kSB; ++i) {
+            v1[i] = r1[b * kSB + i];
+            v2[i] = r2[b * kSB + i];
+          }
+          hc::reduce_scatter<kSB>(v1, lane);
+          hc::reduce_scatter<kSB>(v2, lane);
+          s1[b] = v1[0];
+          s2[b] = v2[0];
+        }
+      }
+    }
+    if (stats && half < kHalves && (lane & ((1 << kSh) - 1)) == 0) {
+      float* red = reinterpret_cast<float*>(smem + off_a);  // the A stages are free now
+#pragma unroll
+      for (int b = 0; b < kNB; ++b) {
+        const int c = half * kCPH + b * kSB + (lane >> kSh);
+        red[(quad * 2 + 0) * NOUT + c] = s1[b];
+        red[(quad * 2 + 1) * NOUT + c] = s2[b];
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (a.mode == kFpropStats)
+    hc::stats_partial_finalize<NOUT, kFlThreads, 2 * kFlTile>(a, reinterpret_cast<const float*>(smem + off_a),
+                                                               smem + off_a, ticket_slot, abort_flag);
+  if (warp == 5) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, kTmemCols);
+  }
+}
+
+// ------------------------------------------------------------------------------ host helpers
+bool first_geom(FirstGeom& g, const HaloGeom& hg, int stride) {
+  g = FirstGeom{};
+  g.n_img = hg.n_img;
+  g.h = hg.h;
+  g.w = hg.w;
+  g.r = hg.r;
+  g.s = hg.s;
+  g.pad = hg.pad;
+  g.stride = stride;
+  g.p = (g.h + 2 * g.pad - g.r) / stride + 1;
+  g.q = (g.w + 2 * g.pad - g.s) / stride + 1;
+  if (g.p <= 0 || g.q <= 0 || g.q > 128 || g.r > 8 || g.s > 8) return false;
+  g.units = g.n_img * g.p;
+  const int row = g.w * 3;
+  g.nbox = (row + 255) / 256;
+  g.xbox = ((row + g.nbox - 1) / g.nbox + 7) / 8 * 8;
+  g.nk = (g.r * 24 + 15) / 16;
+  g.tma = (row * 2) % 16 == 0;
+  if (!g.tma) {
+    g.nbox = 1;
+    g.xbox = (row + 7) / 8 * 8;
+  }
+  g.bstride = (g.r * g.xbox + 63) / 64 * 64;  // 64 elements = 128 bytes
+  return true;
+}
+
+bool first_x_map(CUtensorMap* m, const FirstGeom& g, const void* x, bool bf16) {
+  const uint64_t dims[3] = {(uint64_t)g.w * 3, (uint64_t)g.h, (uint64_t)g.n_img};
+  const uint64_t strides[2] = {(uint64_t)g.w * 3 * 2, (uint64_t)g.h * g.w * 3 * 2};
+  const uint32_t box[3] = {(uint32_t)g.xbox, (uint32_t)g.r, 1};
+  return encode_tiled_plain(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, x, dims,
+                            strides, box);
+}
+
+}  // namespace
+
+int launch_first_fprop(const FpropArgs& f, int stride, int c_out, bool bf16, const void* x, const void* w,
+                       int num_sms, cudaStream_t st) {
+  ConvArgs a{};
+  a.out = f.z;
+  a.out_c = c_out;
+  a.mode = f.mode;
+  a.part = f.part;
+  a.ticket = f.ticket;
+  a.gamma = f.gamma;
+  a.beta = f.beta;
+  a.running_mean = f.running_mean;
+  a.running_var = f.running_var;
+  a.saved_mean = f.saved_mean;
+  a.saved_inv_var = f.saved_inv_var;
+  a.eq = f.eq;
+  a.bias = f.bias;
+  a.momentum = f.momentum;
+  a.eps = f.eps;
+  a.m_count = f.m_count;
+  a.inv_m = 1.0 / (double)f.m_count;
+  a.unbias = f.m_count > 1 ? (float)((double)f.m_count / (double)(f.m_count - 1)) : 1.f;
+  a.err = f.err;
+  FirstGeom g;
+  if (!first_geom(g, f.g, stride)) return 3;
+  CUtensorMap mx{};
+  if (g.tma && !first_x_map(&mx, g, x, bf16)) return 6;
+  const int nout = nout_for(c_out);
+  if (nout != c_out) return 3;
+  const uint32_t smem = 2 * fl_xstage_bytes(g) + 2 * kFlTile + kFlAtoms * nout * 128 + 128 + 1024;
+  if (smem > 227 * 1024) return 3;
+  const int grid = std::min(g.units, num_sms);
+  auto go = [&](auto kern) {
+    if (!ensure_smem_attr(reinterpret_cast<const void*>(kern), 227 * 1024)) return 6;
+    kern<<<grid, kFlThreads, smem, st>>>(mx, a, g, w, x);
+    return cudaGetLastError() == cudaSuccess ? 0 : 6;
+  };
+  switch (nout * 2 + (bf16 ? 1 : 0)) {
+    case 16 * 2: return go(first_fprop_kernel<16, false>);
+    case 16 * 2 + 1: return go(first_fprop_kernel<16, true>);
+    case 32 * 2: return go(first_fprop_kernel<32, false>);
+    case 32 * 2 + 1: return go(first_fprop_kernel<32, true>);
+    case 64 * 2: return go(first_fprop_kernel<64, false>);
+    case 64 * 2 + 1: return go(first_fprop_kernel<64, true>);
+    case 128 * 2: return go(first_fprop_kernel<128, false>);
+    case 128 * 2 + 1: return go(first_fprop_kernel<128, true>);
+    default: return 3;
+  }
+}
+
+}  // namespace cbr

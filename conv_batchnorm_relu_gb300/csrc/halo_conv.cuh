@@ -125,6 +125,88 @@ __device__ __forceinline__ void reduce_scatter(float (&v)[L], int lane) {
   for (; o >= 1; o >>= 1) v[0] += __shfl_xor_sync(0xffffffffu, v[0], o);
 }
 
+// Forward statistics, after the main loop: `red` holds the per-TMEM-lane-quarter sums
+// [4][2][COUT] of this CTA (written by the epilogue, visible after a __syncthreads).  Every
+// thread calls this: the CTA's partial is written, a wrap-around ticket elects the last CTA,
+// and that CTA runs bn_finalize.  `scratch` (SCRATCH bytes, may alias `red`) holds the
+// finalize's working set.
+template <int COUT, int kThreads, int SCRATCH>
+__device__ void stats_partial_finalize(const ConvArgs& a, const float* red, uint8_t* scratch,
+                                       volatile uint32_t* ticket_slot, volatile int* abort_flag) {
+  for (int i = threadIdx.x; i < 2 * COUT; i += kThreads) {
+    const int st = i / COUT, c = i - st * COUT;
+    float v = red[(0 * 2 + st) * COUT + c];
+    v += red[(1 * 2 + st) * COUT + c];
+    v += red[(2 * 2 + st) * COUT + c];
+    v += red[(3 * 2 + st) * COUT + c];
+    a.part[(size_t)blockIdx.x * 2 * COUT + i] = v;
+  }
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) *ticket_slot = atomicInc(a.ticket, gridDim.x - 1);
+  __syncthreads();
+  if (*ticket_slot == gridDim.x - 1 && !is_aborted(abort_flag)) {
+    // ---------------------------------------------------- bn_finalize (last CTA)
+    __threadfence();
+    // This runs on one SM after all the others, so it is kept short: every CTA partial is
+    // loaded in one batch (thread t sums float4 column t % kV4 of CTAs t / kV4, + kRG, ...,
+    // in fp32 and a fixed order), the row groups are combined in fixed order in fp64, and
+    // the per-channel math avoids fp64 division and square root (slow at this part's FP64
+    // rate): mean and variance by fp64 multiplies with the host's 1/M, 1/sqrt in fp32.
+    constexpr int kV4 = (2 * COUT) / 4;        // float4 columns of one partial
+    // row groups, bounded by the scratch region (which also holds fin)
+    constexpr int kRGfit = (SCRATCH - 2 * COUT * 8) / (2 * COUT * 4);
+    constexpr int kRG = kThreads / kV4 < kRGfit ? kThreads / kV4 : kRGfit;
+    static_assert(kRG >= 1, "finalize scratch");
+    constexpr int kLd = 16;                    // loads in flight per thread
+    float* fred = reinterpret_cast<float*>(scratch);  // [kRG][2*COUT]
+    double* fin = reinterpret_cast<double*>(fred + kRG * 2 * COUT);
+    const int c4 = threadIdx.x % kV4, rg = threadIdx.x / kV4;
+    if (rg < kRG) {
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int b0 = rg; b0 < (int)gridDim.x; b0 += kLd * kRG) {
+        float4 v[kLd];
+#pragma unroll
+        for (int k = 0; k < kLd; ++k) {
+          const int b = b0 + k * kRG;
+          v[k] = b < (int)gridDim.x ? __ldcg(reinterpret_cast<const float4*>(a.part + (size_t)b * 2 * COUT) + c4)
+                                    : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int k = 0; k < kLd; ++k) {
+          acc.x += v[k].x;
+          acc.y += v[k].y;
+          acc.z += v[k].z;
+          acc.w += v[k].w;
+        }
+      }
+      reinterpret_cast<float4*>(fred + rg * 2 * COUT)[c4] = acc;
+    }
+    __syncthreads();
+    for (int i = threadIdx.x; i < 2 * COUT; i += kThreads) {
+      double t = 0;
+      for (int r = 0; r < kRG; ++r) t += fred[r * 2 * COUT + i];
+      fin[i] = t;
+    }
+    __syncthreads();
+    for (int c = threadIdx.x; c < COUT; c += kThreads) {
+      const double mean = fin[c] * a.inv_m;
+      const double var_d = fin[COUT + c] * a.inv_m - mean * mean;
+      const float var = var_d > 0.0 ? (float)var_d : 0.f;
+      const float inv = rsqrtf(var + a.eps);
+      const float meanf = (float)mean;
+      const float gm = a.gamma[c];
+      a.saved_mean[c] = meanf;
+      a.saved_inv_var[c] = inv;
+      a.eq[c] = gm * inv;
+      a.eq[COUT + c] = a.beta[c] - gm * meanf * inv;
+      const float mom = a.momentum;
+      a.running_mean[c] = (1.f - mom) * a.running_mean[c] + mom * meanf;
+      a.running_var[c] = (1.f - mom) * a.running_var[c] + mom * var * a.unbias;
+    }
+  }
+}
+
 template <int KIND, int NCH, int NOUT, int U, bool WRES, bool BF16>
 __global__ void __launch_bounds__(Roles<KIND>::kThreads, 1)
     halo_conv_kernel(const __grid_constant__ CUtensorMap map_x,
@@ -510,82 +592,9 @@ __global__ void __launch_bounds__(Roles<KIND>::kThreads, 1)
   tc_fence_before();
   __syncthreads();
 
-  if (KIND == kKindFprop && a.mode == kFpropStats) {
-    constexpr int COUT = NOUT;
-    const float* red = reinterpret_cast<const float*>(smem + L.off_stage);
-    for (int i = threadIdx.x; i < 2 * COUT; i += kThreads) {
-      const int st = i / COUT, c = i - st * COUT;
-      float v = red[(0 * 2 + st) * COUT + c];
-      v += red[(1 * 2 + st) * COUT + c];
-      v += red[(2 * 2 + st) * COUT + c];
-      v += red[(3 * 2 + st) * COUT + c];
-      a.part[(size_t)blockIdx.x * 2 * COUT + i] = v;
-    }
-    __threadfence();
-    __syncthreads();
-    if (threadIdx.x == 0) *ticket_slot = atomicInc(a.ticket, gridDim.x - 1);
-    __syncthreads();
-    if (*ticket_slot == gridDim.x - 1 && !is_aborted(abort_flag)) {
-      // ---------------------------------------------------- bn_finalize (last CTA)
-      __threadfence();
-      // This runs on one SM after all the others, so it is kept short: every CTA partial is
-      // loaded in one batch (thread t sums float4 column t % kV4 of CTAs t / kV4, + kRG, ...,
-      // in fp32 and a fixed order), the row groups are combined in fixed order in fp64, and
-      // the per-channel math avoids fp64 division and square root (slow at this part's FP64
-      // rate): mean and variance by fp64 multiplies with the host's 1/M, 1/sqrt in fp32.
-      constexpr int kV4 = (2 * COUT) / 4;        // float4 columns of one partial
-      // row groups, bounded by the staging region (128 x NOUT x 2 bytes) that also holds fin
-      constexpr int kRGfit = (128 * NOUT * 2 - 2 * COUT * 8) / (2 * COUT * 4);
-      constexpr int kRG = kThreads / kV4 < kRGfit ? kThreads / kV4 : kRGfit;
-      static_assert(kRG >= 1, "finalize scratch");
-      constexpr int kLd = 16;                    // loads in flight per thread
-      float* fred = reinterpret_cast<float*>(smem + L.off_stage);  // [kRG][2*COUT]
-      double* fin = reinterpret_cast<double*>(fred + kRG * 2 * COUT);
-      const int c4 = threadIdx.x % kV4, rg = threadIdx.x / kV4;
-      if (rg < kRG) {
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int b0 = rg; b0 < (int)gridDim.x; b0 += kLd * kRG) {
-          float4 v[kLd];
-#pragma unroll
-          for (int k = 0; k < kLd; ++k) {
-            const int b = b0 + k * kRG;
-            v[k] = b < (int)gridDim.x ? __ldcg(reinterpret_cast<const float4*>(a.part + (size_t)b * 2 * COUT) + c4)
-                                      : make_float4(0.f, 0.f, 0.f, 0.f);
-          }
-#pragma unroll
-          for (int k = 0; k < kLd; ++k) {
-            acc.x += v[k].x;
-            acc.y += v[k].y;
-            acc.z += v[k].z;
-            acc.w += v[k].w;
-          }
-        }
-        reinterpret_cast<float4*>(fred + rg * 2 * COUT)[c4] = acc;
-      }
-      __syncthreads();
-      for (int i = threadIdx.x; i < 2 * COUT; i += kThreads) {
-        double t = 0;
-        for (int r = 0; r < kRG; ++r) t += fred[r * 2 * COUT + i];
-        fin[i] = t;
-      }
-      __syncthreads();
-      for (int c = threadIdx.x; c < COUT; c += kThreads) {
-        const double mean = fin[c] * a.inv_m;
-        const double var_d = fin[COUT + c] * a.inv_m - mean * mean;
-        const float var = var_d > 0.0 ? (float)var_d : 0.f;
-        const float inv = rsqrtf(var + a.eps);
-        const float meanf = (float)mean;
-        const float gm = a.gamma[c];
-        a.saved_mean[c] = meanf;
-        a.saved_inv_var[c] = inv;
-        a.eq[c] = gm * inv;
-        a.eq[COUT + c] = a.beta[c] - gm * meanf * inv;
-        const float mom = a.momentum;
-        a.running_mean[c] = (1.f - mom) * a.running_mean[c] + mom * meanf;
-        a.running_var[c] = (1.f - mom) * a.running_var[c] + mom * var * a.unbias;
-      }
-    }
-  }
+  if (KIND == kKindFprop && a.mode == kFpropStats)
+    stats_partial_finalize<NOUT, kThreads, 128 * NOUT * 2>(a, reinterpret_cast<const float*>(smem + L.off_stage),
+                                                           smem + L.off_stage, ticket_slot, abort_flag);
 
   if (warp == R::kMmaWarp) {
     tc_fence_after();

@@ -21,6 +21,14 @@ CASES = {
     "k1x1": (CBRSpec("1x1", n=2, h=20, w=20, c_in=64, c_out=64, r=1, s=1, pad=0), 2006),
     "k5x5": (CBRSpec("5x5", n=2, h=16, w=16, c_in=32, c_out=64, r=5, s=5, pad=2), 2007),
     "cfg2": (CONFIGS[2], 1236),
+    # first layer (3 channels, im2col kernel): the config-4 shape on small and ragged inputs
+    "first_32x32": (CBRSpec("first small", n=2, h=32, w=32, c_in=3, c_out=64, r=7, s=7, stride=2, pad=3,
+                            x_dist="uniform2.5", first_layer=True), 2008),
+    "first_ragged_bf16": (CBRSpec("first ragged", n=3, h=45, w=61, c_in=3, c_out=16, r=7, s=7, stride=2, pad=3,
+                                  x_dist="uniform2.5", first_layer=True, dtype="bf16"), 2009),
+    "first_5x5_s1": (CBRSpec("first 5x5 s1", n=2, h=20, w=33, c_in=3, c_out=32, r=5, s=5, stride=1, pad=2,
+                             x_dist="uniform2.5", first_layer=True), 2010),
+    "first_cfg4_n2": (CONFIGS[4].with_(n=2), 2011),
 }
 
 
@@ -69,7 +77,7 @@ def test_forward_deterministic():
         assert torch.equal(a[k], b[k]), k
 
 
-@pytest.mark.parametrize("case", ["ragged_13x29", "c128_bf16"])
+@pytest.mark.parametrize("case", ["ragged_13x29", "c128_bf16", "first_32x32"])
 def test_fold_and_infer_parity(case):
     spec, seed = CASES[case]
     inp = make_inputs(spec, seed, with_dy=False)
