@@ -162,7 +162,9 @@ BwdWs bwd_ws(const Shape& s, bool need_z) {
   L.coef = kHdrBytes;
   L.part = align_up(L.coef + 3 * s.cout * sizeof(float), 256);
   L.wpart = align_up(L.part + bwd_reduce_partial_floats(kMaxCtas, (int)s.cout) * sizeof(float), 256);
-  L.dz = align_up(L.wpart + wgrad_partial_floats(kMaxCtas, (int)s.cin, (int)s.cout, (int)(s.r * s.s)) * sizeof(float), 256);
+  const size_t wpart = is_first_layer(s) ? first_wgrad_partial_floats(kMaxCtas, (int)s.cout)
+                                         : wgrad_partial_floats(kMaxCtas, (int)s.cin, (int)s.cout, (int)(s.r * s.s));
+  L.dz = align_up(L.wpart + wpart * sizeof(float), 256);
   L.z = align_up(L.dz + act_bytes(s.n, s.p, s.q, s.cout, s.elt), 256);  // dz materialised for wgrad
   L.total = need_z ? align_up(L.z + act_bytes(s.n, s.p, s.q, s.cout, s.elt), 256) : L.z;
   return L;
@@ -380,8 +382,8 @@ cbr_status_t cbr_backward(const cbr_desc_t* desc, const void* dy, const void* x,
   if ((st = check_supported(s))) return (cbr_status_t)st;
   // dgrad runs as a stride-1 conv with padding R-1-pad on both axes
   if (dx && (s.r != s.s || s.pad > s.r - 1)) return CBR_ERR_UNSUPPORTED;
-  // The first layer has no dgrad (CBR page, section 6); its wgrad kernel is not built yet.
-  if (is_first_layer(s)) return CBR_ERR_UNSUPPORTED;
+  // The first layer has no dgrad (CBR page, section 6): dx must be NULL there.
+  if (is_first_layer(s) && dx) return CBR_ERR_UNSUPPORTED;
   const BwdWs L = bwd_ws(s, z_saved == nullptr);
   if (ws_bytes < L.total) return CBR_ERR_WORKSPACE;
   DeviceInfo* dev = nullptr;
@@ -429,7 +431,7 @@ cbr_status_t cbr_backward(const cbr_desc_t* desc, const void* dy, const void* x,
   prof.mark();
 
   // dz = a*(dy*mask) - d*z + e is materialised once when the TMA-fed wgrad can use it.
-  const bool dz_tma = wgrad_dz_tma_fits(make_geom(s), (int)s.cout);
+  const bool dz_tma = is_first_layer(s) || wgrad_dz_tma_fits(make_geom(s), (int)s.cout);
   void* dz_buf = wsb + L.dz;
   if (dz_tma) {
     DzArgs za{};
@@ -444,6 +446,16 @@ cbr_status_t cbr_backward(const cbr_desc_t* desc, const void* dy, const void* x,
     st = launch_dz(za, s.bf16, dev->num_sms, cs);
     if (st) return (cbr_status_t)st;
     prof.mark();
+  }
+
+  if (is_first_layer(s)) {
+    // first layer: the im2col wgrad over the materialised dz; no dgrad (CBR page, section 6)
+    st = launch_first_wgrad(make_geom(s), (int)s.stride, (int)s.cout, s.bf16, x, dz_buf,
+                            reinterpret_cast<float*>(wsb + L.wpart), dw, dev->err, dev->num_sms, cs,
+                            [](void* p) { static_cast<Prof*>(p)->mark(); }, &prof);
+    if (st) return (cbr_status_t)st;
+    prof.mark();
+    return CBR_OK;
   }
 
   // WGrad first, then DGrad (CBR page, section 5.2 orders DGrad after WGrad because its dX

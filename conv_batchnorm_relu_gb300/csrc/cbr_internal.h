@@ -74,6 +74,11 @@ bool encode_tiled_plain(CUtensorMap* map, CUtensorMapDataType dt, int rank, cons
 // First-layer forward (Cin = 3, any stride, R, S <= 8, Q <= 128): first_layer.cu.
 int launch_first_fprop(const FpropArgs& f, int stride, int c_out, bool bf16, const void* x, const void* w,
                        int num_sms, cudaStream_t st);
+// First-layer wgrad (dz read by TMA) and its fixed-order partial reduction: first_layer.cu.
+int launch_first_wgrad(const HaloGeom& hg, int stride, int c_out, bool bf16, const void* x, const void* dz,
+                       float* part, float* dw, uint32_t* err, int num_sms, cudaStream_t st,
+                       void (*between)(void*) = nullptr, void* ctx = nullptr);
+size_t first_wgrad_partial_floats(int num_sms, int c_out);
 int launch_fprop(const FpropArgs& a, int c_in, int c_out, bool bf16, const void* x,
                  const void* w, int num_sms, cudaStream_t st);
 size_t fprop_partial_floats(int num_sms, int c_out);

@@ -366,6 +366,248 @@ __global__ void __launch_bounds__(kFlThreads, 1)
   }
 }
 
+// ------------------------------------------------------------------------------ wgrad
+// D[slot][k] = sum over the CTA's units of sum_q tile[q][slot] * dz[n,p,q][k]: the im2col tile
+// is the MN-major A operand (M = K slot, two M = 128 tiles, so a fourth zero atom), the TMA-
+// loaded dz rows of the unit are the MN-major B operand, the reduction runs over the unit's 128
+// pixel rows (rows >= Q are zero in both).  Accumulators stay in TMEM for the whole kernel;
+// warps 6-9 store them as this CTA's fp32 partial ([m tile][c16][v][row][4]).
+constexpr uint32_t kFlWgTile = 4 * kFlAtomBytes;
+constexpr int kFlWgThreads = (kFlEpiWarp0 + 4) * 32;  // 320
+
+template <int NOUT, bool BF16>
+__global__ void __launch_bounds__(kFlWgThreads, 1)
+    first_wgrad_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUtensorMap map_dz,
+                       const FirstGeom g, const void* xin, float* part, uint32_t* err) {
+  constexpr int kNkc = NOUT > 64 ? NOUT / 64 : 1;
+  constexpr uint32_t kDzSub = 128 * 128;               // one 64-channel atom of the dz tile
+  constexpr uint32_t kDzStage = kNkc * kDzSub;
+  constexpr int kTmemCols = hc::pow2_at_least(2 * NOUT);
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  const uint32_t xst = fl_xstage_bytes(g);
+  const uint32_t off_a = 2 * xst, off_dz = off_a + 2 * kFlWgTile, off_bar = off_dz + 2 * kDzStage;
+  const uint32_t sbase = smem_u32(smem);
+  const uint32_t bar0 = sbase + off_bar;
+  const uint32_t bar_x_full = bar0, bar_x_empty = bar0 + 16, bar_a_full = bar0 + 32, bar_a_empty = bar0 + 48;
+  const uint32_t bar_dz_full = bar0 + 64, bar_acc_full = bar0 + 80, bar_drain = bar0 + 88;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + off_bar + 96);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  // zero the A stages (rows >= Q, unwritten slots, the fourth atom) and the dz stages (rows >= Q)
+  for (uint32_t i = threadIdx.x; i < (2 * kFlWgTile + 2 * kDzStage) / 16; i += kFlWgThreads)
+    st_shared_v4(sbase + off_a + i * 16, make_uint4(0, 0, 0, 0));
+  fence_proxy_async_smem();
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(bar_x_full + 8 * i, 1);
+      mbar_init(bar_x_empty + 8 * i, kFlBuildWarps);
+      mbar_init(bar_a_full + 8 * i, kFlBuildWarps);
+      mbar_init(bar_a_empty + 8 * i, 1);
+      mbar_init(bar_dz_full + 8 * i, 1);
+    }
+    mbar_init(bar_acc_full, 1);
+    mbar_init(bar_drain, 1);
+    *abort_flag = 0;
+    fence_mbarrier_init();
+  }
+  if (warp == 5) {
+    tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    // ------------------------------------------------- input rows (x) and dz rows of each unit
+    // One loop per unit for the whole warp: the input rows (TMA from lane 0, or a copy by all
+    // lanes when the row pitch rules TMA out), then the unit's dz rows (TMA from lane 0).
+    if (lane == 0) {
+      if (g.tma) prefetch_tensormap(&map_x);
+      prefetch_tensormap(&map_dz);
+    }
+    const uint32_t tx = (uint32_t)g.nbox * g.r * g.xbox * 2;
+    const uint16_t* xg = static_cast<const uint16_t*>(xin);
+    const int row = g.w * 3;
+    uint32_t it = 0;
+    for (int u = blockIdx.x; u < g.units && !__any_sync(0xffffffffu, hc::is_aborted(abort_flag));
+         u += gridDim.x, ++it) {
+      const int n = u / g.p, p = u - n * g.p;
+      const uint32_t s = it & 1, ph = (it >> 1) & 1;
+      if (!__all_sync(0xffffffffu, mbar_wait_backoff(bar_x_empty + 8 * s, ph ^ 1, 64))) {
+        hc::set_abort(abort_flag, err, kErrWaitHalo);
+        break;
+      }
+      if (g.tma) {
+        if (lane == 0) {
+          mbar_arrive_expect_tx(bar_x_full + 8 * s, tx);
+          for (int b = 0; b < g.nbox; ++b)
+            tma_load_3d(sbase + s * xst + (uint32_t)b * g.bstride * 2, &map_x, b * g.xbox, p * g.stride - g.pad, n,
+                        bar_x_full + 8 * s);
+        }
+      } else {
+        uint16_t* dst = reinterpret_cast<uint16_t*>(smem + s * xst);
+        for (int i = lane; i < g.r * g.xbox; i += 32) {
+          const int rr = i / g.xbox, e = i - rr * g.xbox;
+          const int h = p * g.stride - g.pad + rr;
+          dst[i] = (h >= 0 && h < g.h && e < row) ? xg[((size_t)n * g.h + h) * row + e] : (uint16_t)0;
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_x_full + 8 * s);
+      }
+      // the dz stage is free once the MMAs of the unit that last used it have completed
+      if (!__all_sync(0xffffffffu, mbar_wait_backoff(bar_a_empty + 8 * s, ph ^ 1, 64))) {
+        hc::set_abort(abort_flag, err, kErrWaitOperand);
+        break;
+      }
+      if (lane == 0) {
+        mbar_arrive_expect_tx(bar_dz_full + 8 * s, (uint32_t)kNkc * g.q * 128);
+        for (int kc = 0; kc < kNkc; ++kc)
+          tma_load_2d(sbase + off_dz + s * kDzStage + kc * kDzSub, &map_dz, kc * 64, u * g.q, bar_dz_full + 8 * s);
+      }
+    }
+    if (lane == 0)
+      for (uint32_t k = (it > 2 ? it - 2 : 0); k < it; ++k) {
+        if (g.tma) mbar_wait(bar_x_full + 8 * (k & 1), (k >> 1) & 1);
+        mbar_wait(bar_dz_full + 8 * (k & 1), (k >> 1) & 1);
+      }
+  } else if (warp <= kFlBuildWarps) {
+    // ------------------------------------------------- im2col builders
+    const int tid = threadIdx.x - 32;
+    uint32_t it = 0;
+    for (int u = blockIdx.x; u < g.units && !hc::is_aborted(abort_flag); u += gridDim.x, ++it) {
+      const uint32_t s = it & 1, ph = (it >> 1) & 1;
+      if (!mbar_wait_backoff(bar_a_empty + 8 * s, ph ^ 1, 64) || !mbar_wait(bar_x_full + 8 * s, ph)) {
+        hc::set_abort(abort_flag, err, kErrWaitOperand);
+        break;
+      }
+      fl_build_tile(sbase + off_a + s * kFlWgTile, reinterpret_cast<const uint16_t*>(smem + s * xst), g, tid,
+                    32 * kFlBuildWarps);
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(bar_x_empty + 8 * s);
+        mbar_arrive(bar_a_full + 8 * s);
+      }
+    }
+  } else if (warp == 5) {
+    // ------------------------------------------------- MMA issuer (whole warp, elected lane)
+    const uint32_t idesc = make_idesc_f16(128, NOUT, BF16, true, true);
+    uint32_t it = 0;
+    for (int u = blockIdx.x; u < g.units && !__any_sync(0xffffffffu, hc::is_aborted(abort_flag));
+         u += gridDim.x, ++it) {
+      const uint32_t s = it & 1, ph = (it >> 1) & 1;
+      if (!__all_sync(0xffffffffu, mbar_wait(bar_a_full + 8 * s, ph) && mbar_wait(bar_dz_full + 8 * s, ph))) {
+        hc::set_abort(abort_flag, err, kErrWaitOperand);
+        break;
+      }
+      tc_fence_after();
+      const uint64_t a0 = make_sw128_desc(sbase + off_a + s * kFlWgTile, kFlAtomBytes, 1024, 0);
+      const uint64_t b0 = make_sw128_desc(sbase + off_dz + s * kDzStage, kDzSub, 1024, 0);
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk)
+#pragma unroll
+        for (int mt = 0; mt < 2; ++mt)
+          mma_f16_ss_warp(tmem_base + mt * NOUT, a0 + (uint64_t)((mt * 2 * kFlAtomBytes + kk * 2048) >> 4),
+                          b0 + (uint64_t)((kk * 2048) >> 4), idesc, (it | kk) ? 1u : 0u);
+      mma_commit_warp(bar_a_empty + 8 * s);
+    }
+    mma_commit_warp(bar_acc_full);
+    mma_commit_warp(bar_drain);
+    mbar_wait(bar_drain, 0);
+  } else {
+    // ------------------------------------------------- epilogue: TMEM -> fp32 partial
+    const bool ok = mbar_wait_backoff(bar_acc_full, 0, 1024);
+    if (!ok) hc::set_abort(abort_flag, err, kErrWaitMma);
+    tc_fence_after();
+    // a CTA without units never issued an MMA: its partial is zero
+    const bool any = (int)blockIdx.x < g.units;
+    if (ok) {
+      const int quad = warp & 3;
+      const int e = quad * 32 + lane;
+#pragma unroll
+      for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+        for (int c16 = 0; c16 < NOUT / 16; ++c16) {
+          uint32_t r[16];
+          tmem_ld16(tmem_base + ((uint32_t)(quad * 32) << 16) + mt * NOUT + c16 * 16, r);
+          tmem_ld_wait();
+          float4* dst = reinterpret_cast<float4*>(part) + (((size_t)blockIdx.x * 2 + mt) * (NOUT / 16) + c16) * 512 + e;
+#pragma unroll
+          for (int v = 0; v < 4; ++v)
+            dst[v * 128] = any ? make_float4(__uint_as_float(r[4 * v]), __uint_as_float(r[4 * v + 1]),
+                                             __uint_as_float(r[4 * v + 2]), __uint_as_float(r[4 * v + 3]))
+                               : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 5) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, kTmemCols);
+  }
+}
+
+// dW[k][r][s][c] = sum over CTAs (fixed order: fp32 within four CTA slices, fp64 across them) of
+// partial element (m tile, c16, v, row) with K slot = m tile*128 + row = r*24 + s*3 + c.
+constexpr int kFlRedSpan = 64, kFlRedSlices = 4;
+
+template <int NOUT>
+__global__ void __launch_bounds__(kFlRedSpan * kFlRedSlices)
+    first_wgrad_reduce_kernel(const float* __restrict__ part, float* __restrict__ dw, int grid, int R, int S) {
+  __shared__ float4 red[kFlRedSlices][kFlRedSpan];
+  const size_t per_cta = (size_t)2 * (NOUT / 16) * 512;  // float4
+  const size_t f4 = (size_t)blockIdx.x * kFlRedSpan + threadIdx.x % kFlRedSpan;
+  const int sl = threadIdx.x / kFlRedSpan;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (f4 < per_cta) {
+    const float4* base = reinterpret_cast<const float4*>(part) + f4;
+    for (int t0 = sl; t0 < grid; t0 += 8 * kFlRedSlices) {
+      float4 v[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const int t = t0 + k * kFlRedSlices;
+        v[k] = t < grid ? __ldg(base + (size_t)t * per_cta) : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        acc.x += v[k].x;
+        acc.y += v[k].y;
+        acc.z += v[k].z;
+        acc.w += v[k].w;
+      }
+    }
+  }
+  red[sl][threadIdx.x % kFlRedSpan] = acc;
+  __syncthreads();
+  if (sl != 0 || f4 >= per_cta) return;
+  double t4[4] = {0.0, 0.0, 0.0, 0.0};
+  for (int q = 0; q < kFlRedSlices; ++q) {
+    const float4 v = red[q][threadIdx.x];
+    t4[0] += v.x;
+    t4[1] += v.y;
+    t4[2] += v.z;
+    t4[3] += v.w;
+  }
+  const int row = (int)(f4 % 128);
+  const int vq = (int)((f4 / 128) % 4);
+  const int c16 = (int)((f4 / 512) % (NOUT / 16));
+  const int mt = (int)(f4 / (512 * (size_t)(NOUT / 16)));
+  const int slot = mt * 128 + row;
+  const int r = slot / 24, o = slot - r * 24;
+  const int sx = o / 3, c = o - sx * 3;
+  if (r >= R || sx >= S) return;
+  for (int j = 0; j < 4; ++j) {
+    const int k = c16 * 16 + vq * 4 + j;
+    dw[((size_t)(k * R + r) * S + sx) * 3 + c] = (float)t4[j];
+  }
+}
+
 // ------------------------------------------------------------------------------ host helpers
 bool first_geom(FirstGeom& g, const HaloGeom& hg, int stride) {
   g = FirstGeom{};
@@ -448,6 +690,53 @@ int launch_first_fprop(const FpropArgs& f, int stride, int c_out, bool bf16, con
     case 64 * 2 + 1: return go(first_fprop_kernel<64, true>);
     case 128 * 2: return go(first_fprop_kernel<128, false>);
     case 128 * 2 + 1: return go(first_fprop_kernel<128, true>);
+    default: return 3;
+  }
+}
+
+
+size_t first_wgrad_partial_floats(int num_sms, int c_out) { return (size_t)num_sms * 2 * 128 * nout_for(c_out); }
+
+int launch_first_wgrad(const HaloGeom& hg, int stride, int c_out, bool bf16, const void* x, const void* dz,
+                       float* part, float* dw, uint32_t* err, int num_sms, cudaStream_t st,
+                       void (*between)(void*), void* ctx) {
+  FirstGeom g;
+  if (!first_geom(g, hg, stride)) return 3;
+  const int nout = nout_for(c_out);
+  if (nout != c_out) return 3;
+  CUtensorMap mx{}, mdz;
+  if (g.tma && !first_x_map(&mx, g, x, bf16)) return 6;
+  {
+    const uint64_t dims[2] = {(uint64_t)c_out, (uint64_t)g.units * g.q};
+    const uint64_t strides[1] = {(uint64_t)c_out * 2};
+    const uint32_t box[2] = {64, (uint32_t)g.q};
+    if (!encode_tiled(&mdz, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, dz, dims,
+                      strides, box))
+      return 6;
+  }
+  const int nkc = nout > 64 ? nout / 64 : 1;
+  const uint32_t smem = 2 * fl_xstage_bytes(g) + 2 * kFlWgTile + 2 * nkc * 128 * 128 + 128 + 1024;
+  if (smem > 227 * 1024) return 3;
+  const int grid = num_sms;  // every CTA writes a partial (zero when it has no unit)
+  auto go = [&](auto kern, auto red) {
+    if (!ensure_smem_attr(reinterpret_cast<const void*>(kern), 227 * 1024)) return 6;
+    kern<<<grid, kFlWgThreads, smem, st>>>(mx, mdz, g, x, part, err);
+    if (cudaGetLastError() != cudaSuccess) return 6;
+    if (between) between(ctx);
+    const size_t per_cta = (size_t)2 * (nout / 16) * 512;
+    const int rgrid = (int)((per_cta + kFlRedSpan - 1) / kFlRedSpan);
+    red<<<rgrid, kFlRedSpan * kFlRedSlices, 0, st>>>(part, dw, grid, g.r, g.s);
+    return cudaGetLastError() == cudaSuccess ? 0 : 6;
+  };
+  switch (nout * 2 + (bf16 ? 1 : 0)) {
+    case 16 * 2: return go(first_wgrad_kernel<16, false>, first_wgrad_reduce_kernel<16>);
+    case 16 * 2 + 1: return go(first_wgrad_kernel<16, true>, first_wgrad_reduce_kernel<16>);
+    case 32 * 2: return go(first_wgrad_kernel<32, false>, first_wgrad_reduce_kernel<32>);
+    case 32 * 2 + 1: return go(first_wgrad_kernel<32, true>, first_wgrad_reduce_kernel<32>);
+    case 64 * 2: return go(first_wgrad_kernel<64, false>, first_wgrad_reduce_kernel<64>);
+    case 64 * 2 + 1: return go(first_wgrad_kernel<64, true>, first_wgrad_reduce_kernel<64>);
+    case 128 * 2: return go(first_wgrad_kernel<128, false>, first_wgrad_reduce_kernel<128>);
+    case 128 * 2 + 1: return go(first_wgrad_kernel<128, true>, first_wgrad_reduce_kernel<128>);
     default: return 3;
   }
 }

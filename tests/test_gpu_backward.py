@@ -94,3 +94,35 @@ def test_backward_deterministic():
     _, _, b = run_step(spec, seed)
     for k in ("dx", "dw", "dgamma", "dbeta"):
         assert torch.equal(a[k], b[k]), k
+
+
+# First layer (3 channels, 7x7 stride 2 on the config-4 shape, and ragged / stride-1 variants):
+# masked BN reduction, dz pass and the im2col wgrad; there is no dgrad (dx is not requested).
+FIRST_CASES = {
+    "first_32x32": (CBRSpec("first small", n=2, h=32, w=32, c_in=3, c_out=64, r=7, s=7, stride=2, pad=3,
+                            x_dist="uniform2.5", first_layer=True), 2008),
+    "first_ragged_bf16": (CBRSpec("first ragged", n=3, h=45, w=61, c_in=3, c_out=16, r=7, s=7, stride=2, pad=3,
+                                  x_dist="uniform2.5", first_layer=True, dtype="bf16"), 2009),
+    "first_5x5_s1": (CBRSpec("first 5x5 s1", n=2, h=20, w=33, c_in=3, c_out=32, r=5, s=5, stride=1, pad=2,
+                             x_dist="uniform2.5", first_layer=True), 2010),
+    "first_cfg4_n2": (CONFIGS[4].with_(n=2), 2011),
+}
+
+
+@pytest.mark.parametrize("case", list(FIRST_CASES))
+def test_first_layer_backward_parity(case):
+    spec, seed = FIRST_CASES[case]
+    inp, _, bwd = run_step(spec, seed, need_dx=False)
+    assert bwd["dx"] is None
+    o, ref, rb = oracle_step(spec, inp, need_dx=False)
+    check_backward(spec, bwd, o, ref, rb, need_dx=False)
+
+
+def test_first_layer_recompute_z_and_determinism():
+    spec, seed = FIRST_CASES["first_32x32"]
+    _, _, a = run_step(spec, seed, save_z=True, need_dx=False)
+    _, _, b = run_step(spec, seed, save_z=False, need_dx=False)
+    _, _, c = run_step(spec, seed, save_z=True, need_dx=False)
+    for k in ("dw", "dgamma", "dbeta"):
+        assert torch.equal(a[k], b[k]), k
+        assert torch.equal(a[k], c[k]), k
