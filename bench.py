@@ -262,8 +262,10 @@ def run_cbr(args, world, rank, local):
         e.record(stream)
     step(g["x"], g["dy"], None, probe)
     used_b = cbr.profile_last_count() - 1
-    bwd_names = [k for k in BWD_KERNELS_DZ if (used_b == 5 or k != "bn_dz") and (need_dx or k != "conv_dgrad")]
-    bwd_names = bwd_names[:used_b]
+    cand = [k for k in BWD_KERNELS_DZ if need_dx or k != "conv_dgrad"]
+    if len(cand) != used_b:  # no dz pass: dz built inside the convolutions
+        cand = [k for k in cand if k != "bn_dz"]
+    bwd_names = cand[:used_b]
 
     # One step (L2 flush, forward, backward) is captured as a CUDA graph of the library's own
     # launches and replayed K times, so no host work falls between the kernels of a timed step.

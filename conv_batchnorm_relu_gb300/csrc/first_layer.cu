@@ -24,53 +24,56 @@ constexpr uint32_t kFlTile = kFlAtoms * kFlAtomBytes;
 constexpr int kFlBuildWarps = 4;
 constexpr int kFlEpiWarp0 = 6;                       // warp 0: x TMA, 1-4: builders, 5: MMA
 constexpr int kFlThreads = (kFlEpiWarp0 + 8) * 32;   // 448
+constexpr int kFlXStages = 4;                        // staged input rows in flight
 
 struct FirstGeom {
   int n_img, h, w;       // x [n][h][w][3]
   int p, q;              // output rows and columns (q <= 128)
   int r, s, stride, pad; // r, s <= 8
   int units;             // n_img * p
-  int xbox, nbox;        // staging boxes per input row (xbox elements each, multiple of 8)
-  int bstride;           // elements between staged boxes: r*xbox rounded up to 128 bytes (TMA
-                         // destinations in shared memory must be 128-byte aligned)
+  int rowp;              // bytes per staged row: 64-byte zero margin, the row, a zero tail
   int nk;                // MMA K steps: ceil(r*24/16)
   int tma;               // input rows staged by TMA (row pitch a multiple of 16 bytes), else by warp 0
 };
 
 __host__ __device__ inline uint32_t fl_xstage_bytes(const FirstGeom& g) {
-  return ((uint32_t)g.nbox * g.bstride * 2 + 1023u) & ~1023u;
+  return ((uint32_t)g.r * g.rowp + 1023u) & ~1023u;
 }
 
-// Build the im2col tile of output row p of image n from the staged input rows.
-__device__ __forceinline__ void fl_build_tile(uint32_t a_stage, const uint16_t* xs, const FirstGeom& g, int tid,
-                                              int nthr) {
-  const int items = g.q * g.r;
-  for (int it = tid; it < items; it += nthr) {
-    const int q = it / g.r, rr = it - q * g.r;
-    uint32_t w32[12];
+// Staged input rows: row rr of a unit (input row p*stride - pad + rr) sits at rr*rowp + 64
+// bytes, contiguous over W*3 elements, with zeros before it (the margin covers the left
+// padding) and after it (TMA out-of-bounds fill, or never written) and zeros throughout when
+// the input row is outside the image.  With TMA the x tensor is viewed in 8-byte units, so one
+// box {rowp/8 units starting 8 units before the row, R rows} stages a whole unit.  So the S*3 values of filter row rr for output pixel q
+// are one contiguous run that needs no bounds check.
+//
+// Build the im2col tile: thread q (< Q) writes row q, one 24-slot segment per filter row (the
+// run read as 12 aligned 32-bit words and realigned by a funnel shift, values past S*3 zero).
+__device__ __forceinline__ void fl_build_tile(uint32_t a_stage, const uint8_t* xs, const FirstGeom& g, int q) {
+  if (q >= g.q) return;
+  const int e0 = (q * g.stride - g.pad) * 3;  // first element of the run, >= -3*pad
+  const int nval = g.s * 3;
+  for (int rr = 0; rr < g.r; ++rr) {
+    const uint8_t* run = xs + rr * g.rowp + 64 + 2 * e0;
+    const uint32_t* w = reinterpret_cast<const uint32_t*>(reinterpret_cast<uintptr_t>(run) & ~static_cast<uintptr_t>(3));
+    const uint32_t sh = (reinterpret_cast<uintptr_t>(run) & 2) ? 16u : 0u;
+    uint32_t v[13];
 #pragma unroll
-    for (int j = 0; j < 12; ++j) w32[j] = 0;
-    const int w0 = q * g.stride - g.pad;
+    for (int j = 0; j < 13; ++j) v[j] = w[j];
+    uint32_t o[12];
 #pragma unroll
-    for (int sx = 0; sx < 8; ++sx) {
-      const int w = w0 + sx;
-      if (sx < g.s && w >= 0 && w < g.w) {
-#pragma unroll
-        for (int c = 0; c < 3; ++c) {
-          const int e = w * 3 + c;
-          const int b = e / g.xbox;
-          const uint32_t v = xs[b * g.bstride + rr * g.xbox + (e - b * g.xbox)];
-          const int slot = sx * 3 + c;
-          w32[slot >> 1] |= v << ((slot & 1) * 16);
-        }
-      }
+    for (int j = 0; j < 12; ++j) {
+      uint32_t x = __funnelshift_r(v[j], v[j + 1], sh);
+      if (2 * j >= nval) x = 0;
+      else if (2 * j + 1 >= nval) x &= 0xffffu;
+      o[j] = x;
     }
 #pragma unroll
     for (int cj = 0; cj < 3; ++cj) {
       const int chunk = rr * 3 + cj;
       const uint32_t addr = a_stage + (uint32_t)(chunk >> 3) * kFlAtomBytes + (uint32_t)q * 128u +
                             ((uint32_t)((chunk & 7) ^ (q & 7)) << 4);
-      st_shared_v4(addr, make_uint4(w32[4 * cj], w32[4 * cj + 1], w32[4 * cj + 2], w32[4 * cj + 3]));
+      st_shared_v4(addr, make_uint4(o[4 * cj], o[4 * cj + 1], o[4 * cj + 2], o[4 * cj + 3]));
     }
   }
 }
@@ -86,16 +89,17 @@ __device__ void fl_stage_rows_plain(const uint16_t* x, const FirstGeom& g, uint1
   uint32_t it = 0;
   for (int u = blockIdx.x; u < g.units && !__any_sync(0xffffffffu, hc::is_aborted(abort_flag)); u += gridDim.x, ++it) {
     const int n = u / g.p, p = u - n * g.p;
-    const uint32_t s = it & 1, ph = (it >> 1) & 1;
+    const uint32_t s = it % kFlXStages, ph = (it / kFlXStages) & 1;
     if (!__all_sync(0xffffffffu, mbar_wait_backoff(bar_x_empty + 8 * s, ph ^ 1, 64))) {
       hc::set_abort(abort_flag, err, kErrWaitHalo);
       break;
     }
-    uint16_t* dst = stages + s * (xst / 2);
-    for (int i = lane; i < g.r * g.xbox; i += 32) {
-      const int rr = i / g.xbox, e = i - rr * g.xbox;
+    uint8_t* dst = reinterpret_cast<uint8_t*>(stages) + s * xst;
+    for (int i = lane; i < g.r * row; i += 32) {
+      const int rr = i / row, e = i - rr * row;
       const int h = p * g.stride - g.pad + rr;
-      dst[i] = (h >= 0 && h < g.h && e < row) ? x[((size_t)n * g.h + h) * row + e] : (uint16_t)0;
+      *reinterpret_cast<uint16_t*>(dst + rr * g.rowp + 64 + 2 * e) =
+          (h >= 0 && h < g.h) ? x[((size_t)n * g.h + h) * row + e] : (uint16_t)0;
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(bar_x_full + 8 * s);
@@ -113,19 +117,20 @@ __global__ void __launch_bounds__(kFlThreads, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   const uint32_t xst = fl_xstage_bytes(g);
-  const uint32_t off_a = 2 * xst, off_b = off_a + 2 * kFlTile, off_bar = off_b + kBBytes;
+  const uint32_t off_a = kFlXStages * xst, off_b = off_a + 2 * kFlTile, off_bar = off_b + kBBytes;
   const uint32_t sbase = smem_u32(smem);
   const uint32_t bar0 = sbase + off_bar;
-  const uint32_t bar_x_full = bar0, bar_x_empty = bar0 + 16, bar_a_full = bar0 + 32, bar_a_empty = bar0 + 48;
-  const uint32_t bar_acc_full = bar0 + 64, bar_acc_empty = bar0 + 80, bar_drain = bar0 + 96;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + off_bar + 104);
+  const uint32_t bar_x_full = bar0, bar_x_empty = bar0 + 32, bar_a_full = bar0 + 64, bar_a_empty = bar0 + 80;
+  const uint32_t bar_acc_full = bar0 + 96, bar_acc_empty = bar0 + 112, bar_drain = bar0 + 128;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + off_bar + 136);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   volatile uint32_t* ticket_slot = reinterpret_cast<volatile uint32_t*>(tmem_slot + 2);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-  // zero both A stages (rows >= Q and slots never written stay zero), build the filter tile
-  for (uint32_t i = threadIdx.x; i < 2 * kFlTile / 16; i += kFlThreads)
-    st_shared_v4(sbase + off_a + i * 16, make_uint4(0, 0, 0, 0));
+  // zero the x stages (row margins and tails stay zero) and both A stages (rows >= Q and slots
+  // never written stay zero), build the filter tile
+  for (uint32_t i = threadIdx.x; i < (off_a + 2 * kFlTile) / 16; i += kFlThreads)
+    st_shared_v4(sbase + i * 16, make_uint4(0, 0, 0, 0));
   {
     const uint16_t* wsrc = static_cast<const uint16_t*>(wts);
     for (int i = threadIdx.x; i < NOUT * kFlAtoms * 8; i += kFlThreads) {
@@ -148,9 +153,11 @@ __global__ void __launch_bounds__(kFlThreads, 1)
   }
   fence_proxy_async_smem();
   if (threadIdx.x == 0) {
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < kFlXStages; ++i) {
       mbar_init(bar_x_full + 8 * i, 1);
       mbar_init(bar_x_empty + 8 * i, kFlBuildWarps);
+    }
+    for (int i = 0; i < 2; ++i) {
       mbar_init(bar_a_full + 8 * i, kFlBuildWarps);
       mbar_init(bar_a_empty + 8 * i, 1);
       mbar_init(bar_acc_full + 8 * i, 1);
@@ -176,21 +183,20 @@ __global__ void __launch_bounds__(kFlThreads, 1)
                           bar_x_full, bar_x_empty, abort_flag, a.err);
     } else if (lane == 0) {
       prefetch_tensormap(&map_x);
-      const uint32_t tx = (uint32_t)g.nbox * g.r * g.xbox * 2;
+      const uint32_t tx = (uint32_t)g.r * g.rowp;
       uint32_t it = 0;
       for (int u = blockIdx.x; u < g.units && !hc::is_aborted(abort_flag); u += gridDim.x, ++it) {
         const int n = u / g.p, p = u - n * g.p;
-        const uint32_t s = it & 1, ph = (it >> 1) & 1;
+        const uint32_t s = it % kFlXStages, ph = (it / kFlXStages) & 1;
         if (!mbar_wait_backoff(bar_x_empty + 8 * s, ph ^ 1, 64)) {
           hc::set_abort(abort_flag, a.err, kErrWaitHalo);
           break;
         }
         mbar_arrive_expect_tx(bar_x_full + 8 * s, tx);
-        for (int b = 0; b < g.nbox; ++b)
-          tma_load_3d(sbase + s * xst + (uint32_t)b * g.bstride * 2, &map_x, b * g.xbox, p * g.stride - g.pad, n,
-                      bar_x_full + 8 * s);
+        tma_load_3d(sbase + s * xst, &map_x, -8, p * g.stride - g.pad, n, bar_x_full + 8 * s);
       }
-      for (uint32_t k = (it > 2 ? it - 2 : 0); k < it; ++k) mbar_wait(bar_x_full + 8 * (k & 1), (k >> 1) & 1);
+      for (uint32_t k = (it > kFlXStages ? it - kFlXStages : 0); k < it; ++k)
+        mbar_wait(bar_x_full + 8 * (k % kFlXStages), (k / kFlXStages) & 1);
     }
   } else if (warp <= kFlBuildWarps) {
     // ---------------------------------------------------------------- im2col builders
@@ -198,16 +204,16 @@ __global__ void __launch_bounds__(kFlThreads, 1)
     uint32_t it = 0;
     for (int u = blockIdx.x; u < g.units && !hc::is_aborted(abort_flag); u += gridDim.x, ++it) {
       const uint32_t s = it & 1, ph = (it >> 1) & 1;
-      if (!mbar_wait_backoff(bar_a_empty + 8 * s, ph ^ 1, 64) || !mbar_wait(bar_x_full + 8 * s, ph)) {
+      const uint32_t sx = it % kFlXStages, phx = (it / kFlXStages) & 1;
+      if (!mbar_wait_backoff(bar_a_empty + 8 * s, ph ^ 1, 64) || !mbar_wait(bar_x_full + 8 * sx, phx)) {
         hc::set_abort(abort_flag, a.err, kErrWaitOperand);
         break;
       }
-      fl_build_tile(sbase + off_a + s * kFlTile, reinterpret_cast<const uint16_t*>(smem + s * xst), g, tid,
-                    32 * kFlBuildWarps);
+      fl_build_tile(sbase + off_a + s * kFlTile, smem + sx * xst, g, tid);
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) {
-        mbar_arrive(bar_x_empty + 8 * s);
+        mbar_arrive(bar_x_empty + 8 * sx);
         mbar_arrive(bar_a_full + 8 * s);
       }
     }
@@ -374,12 +380,15 @@ __global__ void __launch_bounds__(kFlThreads, 1)
 // warps 6-9 store them as this CTA's fp32 partial ([m tile][c16][v][row][4]).
 constexpr uint32_t kFlWgTile = 4 * kFlAtomBytes;
 constexpr int kFlWgThreads = (kFlEpiWarp0 + 4) * 32;  // 320
+// four staged units in flight, two at NOUT = 128 (its dz stages take the room)
+constexpr int fl_wg_xstages(int nout) { return nout > 64 ? 2 : kFlXStages; }
 
 template <int NOUT, bool BF16>
 __global__ void __launch_bounds__(kFlWgThreads, 1)
     first_wgrad_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUtensorMap map_dz,
                        const FirstGeom g, const void* xin, float* part, uint32_t* err) {
   constexpr int kNkc = NOUT > 64 ? NOUT / 64 : 1;
+  constexpr int kXS = fl_wg_xstages(NOUT);  // staged input rows in flight
   constexpr uint32_t kDzSub = 128 * 128;               // one 64-channel atom of the dz tile
   constexpr uint32_t kDzStage = kNkc * kDzSub;
   constexpr int kTmemCols = hc::pow2_at_least(2 * NOUT);
@@ -387,23 +396,26 @@ __global__ void __launch_bounds__(kFlWgThreads, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   const uint32_t xst = fl_xstage_bytes(g);
-  const uint32_t off_a = 2 * xst, off_dz = off_a + 2 * kFlWgTile, off_bar = off_dz + 2 * kDzStage;
+  const uint32_t off_a = kXS * xst, off_dz = off_a + 2 * kFlWgTile, off_bar = off_dz + 2 * kDzStage;
   const uint32_t sbase = smem_u32(smem);
   const uint32_t bar0 = sbase + off_bar;
-  const uint32_t bar_x_full = bar0, bar_x_empty = bar0 + 16, bar_a_full = bar0 + 32, bar_a_empty = bar0 + 48;
-  const uint32_t bar_dz_full = bar0 + 64, bar_acc_full = bar0 + 80, bar_drain = bar0 + 88;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + off_bar + 96);
+  const uint32_t bar_x_full = bar0, bar_x_empty = bar0 + 32, bar_a_full = bar0 + 64, bar_a_empty = bar0 + 80;
+  const uint32_t bar_dz_full = bar0 + 96, bar_acc_full = bar0 + 112, bar_drain = bar0 + 120;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + off_bar + 128);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-  // zero the A stages (rows >= Q, unwritten slots, the fourth atom) and the dz stages (rows >= Q)
-  for (uint32_t i = threadIdx.x; i < (2 * kFlWgTile + 2 * kDzStage) / 16; i += kFlWgThreads)
-    st_shared_v4(sbase + off_a + i * 16, make_uint4(0, 0, 0, 0));
+  // zero the x stages (row margins and tails), the A stages (rows >= Q, unwritten slots, the
+  // fourth atom) and the dz stages (rows >= Q)
+  for (uint32_t i = threadIdx.x; i < off_bar / 16; i += kFlWgThreads)
+    st_shared_v4(sbase + i * 16, make_uint4(0, 0, 0, 0));
   fence_proxy_async_smem();
   if (threadIdx.x == 0) {
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < kXS; ++i) {
       mbar_init(bar_x_full + 8 * i, 1);
       mbar_init(bar_x_empty + 8 * i, kFlBuildWarps);
+    }
+    for (int i = 0; i < 2; ++i) {
       mbar_init(bar_a_full + 8 * i, kFlBuildWarps);
       mbar_init(bar_a_empty + 8 * i, 1);
       mbar_init(bar_dz_full + 8 * i, 1);
@@ -430,7 +442,7 @@ __global__ void __launch_bounds__(kFlWgThreads, 1)
       if (g.tma) prefetch_tensormap(&map_x);
       prefetch_tensormap(&map_dz);
     }
-    const uint32_t tx = (uint32_t)g.nbox * g.r * g.xbox * 2;
+    const uint32_t tx = (uint32_t)g.r * g.rowp;
     const uint16_t* xg = static_cast<const uint16_t*>(xin);
     const int row = g.w * 3;
     uint32_t it = 0;
@@ -438,26 +450,26 @@ __global__ void __launch_bounds__(kFlWgThreads, 1)
          u += gridDim.x, ++it) {
       const int n = u / g.p, p = u - n * g.p;
       const uint32_t s = it & 1, ph = (it >> 1) & 1;
-      if (!__all_sync(0xffffffffu, mbar_wait_backoff(bar_x_empty + 8 * s, ph ^ 1, 64))) {
+      const uint32_t sx = it % kXS, phx = (it / kXS) & 1;
+      if (!__all_sync(0xffffffffu, mbar_wait_backoff(bar_x_empty + 8 * sx, phx ^ 1, 64))) {
         hc::set_abort(abort_flag, err, kErrWaitHalo);
         break;
       }
       if (g.tma) {
         if (lane == 0) {
-          mbar_arrive_expect_tx(bar_x_full + 8 * s, tx);
-          for (int b = 0; b < g.nbox; ++b)
-            tma_load_3d(sbase + s * xst + (uint32_t)b * g.bstride * 2, &map_x, b * g.xbox, p * g.stride - g.pad, n,
-                        bar_x_full + 8 * s);
+          mbar_arrive_expect_tx(bar_x_full + 8 * sx, tx);
+          tma_load_3d(sbase + sx * xst, &map_x, -8, p * g.stride - g.pad, n, bar_x_full + 8 * sx);
         }
       } else {
-        uint16_t* dst = reinterpret_cast<uint16_t*>(smem + s * xst);
-        for (int i = lane; i < g.r * g.xbox; i += 32) {
-          const int rr = i / g.xbox, e = i - rr * g.xbox;
+        uint8_t* dst = smem + sx * xst;
+        for (int i = lane; i < g.r * row; i += 32) {
+          const int rr = i / row, e = i - rr * row;
           const int h = p * g.stride - g.pad + rr;
-          dst[i] = (h >= 0 && h < g.h && e < row) ? xg[((size_t)n * g.h + h) * row + e] : (uint16_t)0;
+          *reinterpret_cast<uint16_t*>(dst + rr * g.rowp + 64 + 2 * e) =
+              (h >= 0 && h < g.h) ? xg[((size_t)n * g.h + h) * row + e] : (uint16_t)0;
         }
         __syncwarp();
-        if (lane == 0) mbar_arrive(bar_x_full + 8 * s);
+        if (lane == 0) mbar_arrive(bar_x_full + 8 * sx);
       }
       // the dz stage is free once the MMAs of the unit that last used it have completed
       if (!__all_sync(0xffffffffu, mbar_wait_backoff(bar_a_empty + 8 * s, ph ^ 1, 64))) {
@@ -470,27 +482,28 @@ __global__ void __launch_bounds__(kFlWgThreads, 1)
           tma_load_2d(sbase + off_dz + s * kDzStage + kc * kDzSub, &map_dz, kc * 64, u * g.q, bar_dz_full + 8 * s);
       }
     }
-    if (lane == 0)
-      for (uint32_t k = (it > 2 ? it - 2 : 0); k < it; ++k) {
-        if (g.tma) mbar_wait(bar_x_full + 8 * (k & 1), (k >> 1) & 1);
-        mbar_wait(bar_dz_full + 8 * (k & 1), (k >> 1) & 1);
-      }
+    if (lane == 0) {
+      if (g.tma)
+        for (uint32_t k = (it > kXS ? it - kXS : 0); k < it; ++k)
+          mbar_wait(bar_x_full + 8 * (k % kXS), (k / kXS) & 1);
+      for (uint32_t k = (it > 2 ? it - 2 : 0); k < it; ++k) mbar_wait(bar_dz_full + 8 * (k & 1), (k >> 1) & 1);
+    }
   } else if (warp <= kFlBuildWarps) {
     // ------------------------------------------------- im2col builders
     const int tid = threadIdx.x - 32;
     uint32_t it = 0;
     for (int u = blockIdx.x; u < g.units && !hc::is_aborted(abort_flag); u += gridDim.x, ++it) {
       const uint32_t s = it & 1, ph = (it >> 1) & 1;
-      if (!mbar_wait_backoff(bar_a_empty + 8 * s, ph ^ 1, 64) || !mbar_wait(bar_x_full + 8 * s, ph)) {
+      const uint32_t sx = it % kXS, phx = (it / kXS) & 1;
+      if (!mbar_wait_backoff(bar_a_empty + 8 * s, ph ^ 1, 64) || !mbar_wait(bar_x_full + 8 * sx, phx)) {
         hc::set_abort(abort_flag, err, kErrWaitOperand);
         break;
       }
-      fl_build_tile(sbase + off_a + s * kFlWgTile, reinterpret_cast<const uint16_t*>(smem + s * xst), g, tid,
-                    32 * kFlBuildWarps);
+      fl_build_tile(sbase + off_a + s * kFlWgTile, smem + sx * xst, g, tid);
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) {
-        mbar_arrive(bar_x_empty + 8 * s);
+        mbar_arrive(bar_x_empty + 8 * sx);
         mbar_arrive(bar_a_full + 8 * s);
       }
     }
@@ -623,24 +636,25 @@ bool first_geom(FirstGeom& g, const HaloGeom& hg, int stride) {
   if (g.p <= 0 || g.q <= 0 || g.q > 128 || g.r > 8 || g.s > 8) return false;
   g.units = g.n_img * g.p;
   const int row = g.w * 3;
-  g.nbox = (row + 255) / 256;
-  g.xbox = ((row + g.nbox - 1) / g.nbox + 7) / 8 * 8;
+  // staged row: 8 zero units (64 bytes, at least 3*pad elements), the row, a zero tail that
+  // covers the right padding and the 26 elements a run read may pass its last value
+  if (3 * g.pad > 30) return false;
+  const int data_units = (row + 3) / 4;
+  const int tail_units = (3 * g.pad + 32 + 3) / 4;
+  const int wunits = (8 + data_units + tail_units + 1) / 2 * 2;
+  g.rowp = wunits * 8;
   g.nk = (g.r * 24 + 15) / 16;
-  g.tma = (row * 2) % 16 == 0;
-  if (!g.tma) {
-    g.nbox = 1;
-    g.xbox = (row + 7) / 8 * 8;
-  }
-  g.bstride = (g.r * g.xbox + 63) / 64 * 64;  // 64 elements = 128 bytes
+  g.tma = (row * 2) % 16 == 0 && wunits <= 256;
   return true;
 }
 
 bool first_x_map(CUtensorMap* m, const FirstGeom& g, const void* x, bool bf16) {
-  const uint64_t dims[3] = {(uint64_t)g.w * 3, (uint64_t)g.h, (uint64_t)g.n_img};
+  // x viewed in 8-byte units (4 elements): a whole staged row is one box row
+  (void)bf16;
+  const uint64_t dims[3] = {(uint64_t)g.w * 3 / 4, (uint64_t)g.h, (uint64_t)g.n_img};
   const uint64_t strides[2] = {(uint64_t)g.w * 3 * 2, (uint64_t)g.h * g.w * 3 * 2};
-  const uint32_t box[3] = {(uint32_t)g.xbox, (uint32_t)g.r, 1};
-  return encode_tiled_plain(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, x, dims,
-                            strides, box);
+  const uint32_t box[3] = {(uint32_t)g.rowp / 8, (uint32_t)g.r, 1};
+  return encode_tiled_plain(m, CU_TENSOR_MAP_DATA_TYPE_UINT64, 3, x, dims, strides, box);
 }
 
 }  // namespace
@@ -673,7 +687,7 @@ int launch_first_fprop(const FpropArgs& f, int stride, int c_out, bool bf16, con
   if (g.tma && !first_x_map(&mx, g, x, bf16)) return 6;
   const int nout = nout_for(c_out);
   if (nout != c_out) return 3;
-  const uint32_t smem = 2 * fl_xstage_bytes(g) + 2 * kFlTile + kFlAtoms * nout * 128 + 128 + 1024;
+  const uint32_t smem = kFlXStages * fl_xstage_bytes(g) + 2 * kFlTile + kFlAtoms * nout * 128 + 256 + 1024;
   if (smem > 227 * 1024) return 3;
   const int grid = std::min(g.units, num_sms);
   auto go = [&](auto kern) {
@@ -715,7 +729,7 @@ int launch_first_wgrad(const HaloGeom& hg, int stride, int c_out, bool bf16, con
       return 6;
   }
   const int nkc = nout > 64 ? nout / 64 : 1;
-  const uint32_t smem = 2 * fl_xstage_bytes(g) + 2 * kFlWgTile + 2 * nkc * 128 * 128 + 128 + 1024;
+  const uint32_t smem = fl_wg_xstages(nout) * fl_xstage_bytes(g) + 2 * kFlWgTile + 2 * nkc * 128 * 128 + 256 + 1024;
   if (smem > 227 * 1024) return 3;
   const int grid = num_sms;  // every CTA writes a partial (zero when it has no unit)
   auto go = [&](auto kern, auto red) {
