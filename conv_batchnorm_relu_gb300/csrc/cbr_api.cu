@@ -210,6 +210,16 @@ bool encode_tiled_plain(CUtensorMap* map, CUtensorMapDataType dt, int rank, cons
   return encode_tiled_mode(map, dt, rank, base, dims, strides_bytes, box, CU_TENSOR_MAP_SWIZZLE_NONE);
 }
 
+bool encode_tiled_span(CUtensorMap* map, CUtensorMapDataType dt, int rank, const void* base,
+                       const uint64_t* dims, const uint64_t* strides_bytes, const uint32_t* box,
+                       int swizzle_bytes) {
+  const CUtensorMapSwizzle swz = swizzle_bytes == 128  ? CU_TENSOR_MAP_SWIZZLE_128B
+                                 : swizzle_bytes == 64 ? CU_TENSOR_MAP_SWIZZLE_64B
+                                 : swizzle_bytes == 32 ? CU_TENSOR_MAP_SWIZZLE_32B
+                                                       : CU_TENSOR_MAP_SWIZZLE_NONE;
+  return encode_tiled_mode(map, dt, rank, base, dims, strides_bytes, box, swz);
+}
+
 namespace {
 bool encode_tiled_mode(CUtensorMap* map, CUtensorMapDataType dt, int rank, const void* base,
                        const uint64_t* dims, const uint64_t* strides_bytes, const uint32_t* box,

@@ -69,6 +69,11 @@ bool encode_tiled(CUtensorMap* map, CUtensorMapDataType dt, int rank, const void
 bool encode_tiled_plain(CUtensorMap* map, CUtensorMapDataType dt, int rank, const void* base,
                   const uint64_t* dims, const uint64_t* strides_bytes, const uint32_t* box);
 
+// Same, with the swizzle span given in bytes (128, 64, 32; anything else: none).
+bool encode_tiled_span(CUtensorMap* map, CUtensorMapDataType dt, int rank, const void* base,
+                       const uint64_t* dims, const uint64_t* strides_bytes, const uint32_t* box,
+                       int swizzle_bytes);
+
 // Launchers (one per kernel family).  Each validates only what its kernel needs beyond the
 // C-ABI checks and returns a CBR status.
 // First-layer forward (Cin = 3, any stride, R, S <= 8, Q <= 128): first_layer.cu.

@@ -34,6 +34,17 @@ struct FirstGeom {
   int rowp;              // bytes per staged row: 64-byte zero margin, the row, a zero tail
   int nk;                // MMA K steps: ceil(r*24/16)
   int tma;               // input rows staged by TMA (row pitch a multiple of 16 bytes), else by warp 0
+  // implicit-im2col forward (stride 1 or 2): input rows padded to 16-byte pixel groups
+  int imp;               // the geometry fits the implicit path
+  int gpx;               // pixels per 16-byte group (= stride)
+  int cpx;               // channel slots per pixel (8 / gpx; 3 values then zeros)
+  int jm;                // groups of left margin: ceil(pad / gpx)
+  int lead;              // zero-weight pixels ahead of tap 0 in a run: gpx*jm - pad
+  int nmr;               // MMAs per filter row (two groups = K 16 each)
+  int rowb;              // bytes per padded row: (128 + 2*nmr) groups
+  int xal4;              // x is 4-byte aligned
+  int rawtma;            // input rows copied whole into shared memory (row bytes and x 16-byte aligned)
+  int rawb;              // bytes of one such row (w * 6)
 };
 
 __host__ __device__ inline uint32_t fl_xstage_bytes(const FirstGeom& g) {
@@ -49,24 +60,30 @@ __host__ __device__ inline uint32_t fl_xstage_bytes(const FirstGeom& g) {
 //
 // Build the im2col tile: thread q (< Q) writes row q, one 24-slot segment per filter row (the
 // run read as 12 aligned 32-bit words and realigned by a funnel shift, values past S*3 zero).
-__device__ __forceinline__ void fl_build_tile(uint32_t a_stage, const uint8_t* xs, const FirstGeom& g, int q) {
+__device__ __forceinline__ void fl_build_tile(uint32_t a_stage, uint32_t xs, const FirstGeom& g, int q) {
   if (q >= g.q) return;
   const int e0 = (q * g.stride - g.pad) * 3;  // first element of the run, >= -3*pad
   const int nval = g.s * 3;
-  for (int rr = 0; rr < g.r; ++rr) {
-    const uint8_t* run = xs + rr * g.rowp + 64 + 2 * e0;
-    const uint32_t* w = reinterpret_cast<const uint32_t*>(reinterpret_cast<uintptr_t>(run) & ~static_cast<uintptr_t>(3));
-    const uint32_t sh = (reinterpret_cast<uintptr_t>(run) & 2) ? 16u : 0u;
-    uint32_t v[13];
+  uint32_t keep[12];                          // values past S*3 are zero
 #pragma unroll
-    for (int j = 0; j < 13; ++j) v[j] = w[j];
+  for (int j = 0; j < 12; ++j) keep[j] = 2 * j >= nval ? 0u : (2 * j + 1 >= nval ? 0xffffu : 0xffffffffu);
+  const uint32_t run0 = xs + 64 + 2 * e0;
+  const uint32_t sh = (run0 & 2) ? 16u : 0u;
+  uint32_t wa = run0 & ~3u;
+  // Software-pipelined over filter rows: the next row's words are loaded
+  // before this row's stores, so one builder warp per sub-partition keeps
+  // its shared-memory loads in flight.
+  uint32_t v[13];
+#pragma unroll
+  for (int j = 0; j < 13; ++j) asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v[j]) : "r"(wa + 4 * j));
+  for (int rr = 0; rr < g.r; ++rr) {
     uint32_t o[12];
 #pragma unroll
-    for (int j = 0; j < 12; ++j) {
-      uint32_t x = __funnelshift_r(v[j], v[j + 1], sh);
-      if (2 * j >= nval) x = 0;
-      else if (2 * j + 1 >= nval) x &= 0xffffu;
-      o[j] = x;
+    for (int j = 0; j < 12; ++j) o[j] = __funnelshift_r(v[j], v[j + 1], sh) & keep[j];
+    if (rr + 1 < g.r) {
+      wa += g.rowp;
+#pragma unroll
+      for (int j = 0; j < 13; ++j) asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v[j]) : "r"(wa + 4 * j));
     }
 #pragma unroll
     for (int cj = 0; cj < 3; ++cj) {
@@ -209,7 +226,7 @@ __global__ void __launch_bounds__(kFlThreads, 1)
         hc::set_abort(abort_flag, a.err, kErrWaitOperand);
         break;
       }
-      fl_build_tile(sbase + off_a + s * kFlTile, smem + sx * xst, g, tid);
+      fl_build_tile(sbase + off_a + s * kFlTile, sbase + sx * xst, g, tid);
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) {
@@ -372,6 +389,516 @@ __global__ void __launch_bounds__(kFlThreads, 1)
   }
 }
 
+
+// ------------------------------------------------------------------------------ forward, implicit im2col
+// Stride 1 or 2 (Tech-Renaissance CBR page, section 6, the 7x7 stride-2 first layer): pad each
+// pixel to 8/stride channel slots, so `stride` adjacent pixels fill one 16-byte group and the
+// run of filter row rr for output pixel q starts at group q + const of the padded input row.
+// The im2col tile of a filter row is then the padded row itself read through a descriptor
+// without swizzle whose 8-row core matrices step 16 bytes per M row (one output pixel) and 16
+// bytes per K group: core matrices overlap, and no tile is ever assembled.  One unit (an
+// output row) is R * nmr MMAs.  Each CTA takes a contiguous range of output rows, so
+// consecutive units share R - stride input rows: a ring of padded rows is converted once per
+// input row by four warps reading x from global memory.  The epilogue stages each warp's
+// 32 x (channels) block swizzled in shared memory and writes it with one TMA store.
+constexpr int kImpRing = 16;                          // padded input rows in the ring (>= 2R)
+constexpr int kImpRaw = 8;                            // raw input rows in flight (bulk copies)
+constexpr int kImpProdWarp = 0;                       // warp 0: bulk copies of raw input rows
+constexpr int kImpConv0 = 1, kImpConvWarps = 4;       // warps 1-4 convert input rows
+constexpr int kImpMmaWarp = 5;
+constexpr int kImpEpiWarp0 = 6;                       // warps 6-13: epilogue
+constexpr int kImpThreads = (kImpEpiWarp0 + 8) * 32;  // 448
+constexpr uint32_t kImpStageBytes = 32 * 128;         // one epilogue warp's staging buffer
+constexpr int kImpGroupsPerLane = 5;                  // ceil(max groups per row / 32)
+
+__host__ __device__ inline uint32_t imp_align(uint32_t v) { return (v + 1023u) & ~1023u; }
+
+struct ImpLayout {
+  uint32_t off_raw, off_b, off_stage, off_bar, total;
+};
+
+template <int NOUT>
+__host__ __device__ inline ImpLayout imp_layout(const FirstGeom& g) {
+  ImpLayout L;
+  L.off_raw = imp_align((uint32_t)kImpRing * g.rowb);
+  L.off_b = imp_align(L.off_raw + (g.rawtma ? (uint32_t)kImpRaw * g.rawb : 0u));
+  L.off_stage = L.off_b + imp_align((uint32_t)(g.r * g.nmr) * NOUT * 32);
+  L.off_bar = L.off_stage + 8 * 2 * kImpStageBytes;
+  L.total = L.off_bar + 512;
+  return L;
+}
+
+// First filter row that unit (n, p) appends to the ring, given the unit before it in the
+// CTA's range: R - stride when the two are consecutive rows of one image, else 0 (all R rows).
+__device__ __forceinline__ int imp_first_new(const FirstGeom& g, int prev_n, int prev_p, int n, int p) {
+  return (n == prev_n && p == prev_p + 1 && g.stride < g.r) ? g.r - g.stride : 0;
+}
+
+// Padded row of input row h of image n: group t holds pixels gpx*(t - jm) + i (i < gpx), each as
+// cpx slots (the 3 channels, then zeros); zeros outside the image.  One warp, lane = group mod 32.
+// Every load of the row is issued before the first is used (one memory latency per row): the
+// common groups (a whole aligned pixel pair inside the image) load from a clamped, always-valid
+// address and are zeroed by a select; groups at a ragged edge take a second, element-wise pass.
+__device__ __forceinline__ void imp_convert_row(const uint16_t* x, const FirstGeom& g, int n, int h, uint32_t dst,
+                                                int lane) {
+  const int ngroups = g.rowb / 16;
+  const bool row_in = h >= 0 && h < g.h;
+  const size_t pix0 = ((size_t)n * g.h + (row_in ? h : 0)) * g.w;
+  const uint16_t* xr = x + pix0 * 3;
+  uint4 o[kImpGroupsPerLane];
+  if (g.gpx == 2) {
+    const bool al4 = g.xal4 && (pix0 & 1) == 0;  // then pixel pairs start 4-byte aligned
+    // a 4-byte aligned base for the unconditional loads (x aligned down when it is not)
+    const uint32_t* xw = al4 ? reinterpret_cast<const uint32_t*>(xr)
+                             : reinterpret_cast<const uint32_t*>(reinterpret_cast<uintptr_t>(x) & ~static_cast<uintptr_t>(3));
+    uint32_t w[kImpGroupsPerLane][3];
+    bool edge[kImpGroupsPerLane];
+#pragma unroll
+    for (int k = 0; k < kImpGroupsPerLane; ++k) {
+      const int t = lane + 32 * k;
+      const int w0 = 2 * (t - g.jm);
+      const bool in = row_in && t < ngroups && w0 + 1 >= 0 && w0 < g.w;  // some pixel inside the image
+      const bool fast = in && al4 && w0 >= 0 && w0 + 1 < g.w;
+      edge[k] = in && !fast;
+      const uint32_t* pa = xw + (fast ? 3 * (w0 >> 1) : 0);
+      w[k][0] = __ldg(pa);
+      w[k][1] = __ldg(pa + 1);
+      w[k][2] = __ldg(pa + 2);
+      if (!fast) w[k][0] = w[k][1] = w[k][2] = 0u;
+    }
+#pragma unroll
+    for (int k = 0; k < kImpGroupsPerLane; ++k) {
+      if (edge[k]) {
+        const int w0 = 2 * (lane + 32 * k - g.jm);
+        uint32_t v[6];
+#pragma unroll
+        for (int e = 0; e < 6; ++e) {
+          const int px = w0 + e / 3;
+          v[e] = (px >= 0 && px < g.w) ? (uint32_t)__ldg(xr + px * 3 + e % 3) : 0u;
+        }
+        w[k][0] = v[0] | (v[1] << 16);
+        w[k][1] = v[2] | (v[3] << 16);
+        w[k][2] = v[4] | (v[5] << 16);
+      }
+      o[k] = make_uint4(w[k][0], w[k][1] & 0xffffu, (w[k][1] >> 16) | (w[k][2] << 16), w[k][2] >> 16);
+    }
+  } else {
+#pragma unroll
+    for (int k = 0; k < kImpGroupsPerLane; ++k) {
+      const int t = lane + 32 * k;
+      const int px = t - g.jm;
+      const bool in = row_in && t < ngroups && px >= 0 && px < g.w;
+      const uint16_t* pa = xr + (in ? px * 3 : 0);
+      uint32_t v[3];
+#pragma unroll
+      for (int c = 0; c < 3; ++c) v[c] = in ? (uint32_t)__ldg(pa + c) : 0u;
+      o[k] = make_uint4(v[0] | (v[1] << 16), v[2], 0u, 0u);
+    }
+  }
+#pragma unroll
+  for (int k = 0; k < kImpGroupsPerLane; ++k) {
+    const int t = lane + 32 * k;
+    if (t < ngroups) st_shared_v4(dst + 16u * t, o[k]);
+  }
+}
+
+// The same padded row from a raw input row already in shared memory (w * 3 contiguous values,
+// w a multiple of 8 so pixel pairs never straddle the row end).
+__device__ __forceinline__ void imp_convert_row_smem(uint32_t raw, const FirstGeom& g, int h, uint32_t dst,
+                                                     int lane) {
+  const int ngroups = g.rowb / 16;
+  const bool row_in = h >= 0 && h < g.h;
+  uint4 o[kImpGroupsPerLane];
+  if (g.gpx == 2) {
+    uint32_t w[kImpGroupsPerLane][3];
+#pragma unroll
+    for (int k = 0; k < kImpGroupsPerLane; ++k) {
+      const int pi = lane + 32 * k - g.jm;  // pixel pair
+      const bool in = row_in && lane + 32 * k < ngroups && pi >= 0 && 2 * pi < g.w;
+      const uint32_t a = raw + 12u * (uint32_t)(in ? pi : 0);
+#pragma unroll
+      for (int j = 0; j < 3; ++j) asm volatile("ld.shared.b32 %0, [%1];" : "=r"(w[k][j]) : "r"(a + 4 * j));
+      if (!in) w[k][0] = w[k][1] = w[k][2] = 0u;
+    }
+#pragma unroll
+    for (int k = 0; k < kImpGroupsPerLane; ++k)
+      o[k] = make_uint4(w[k][0], w[k][1] & 0xffffu, (w[k][1] >> 16) | (w[k][2] << 16), w[k][2] >> 16);
+  } else {
+#pragma unroll
+    for (int k = 0; k < kImpGroupsPerLane; ++k) {
+      const int px = lane + 32 * k - g.jm;
+      const bool in = row_in && lane + 32 * k < ngroups && px >= 0 && px < g.w;
+      const uint32_t a = raw + 6u * (uint32_t)(in ? px : 0);
+      uint32_t v[3];
+#pragma unroll
+      for (int c = 0; c < 3; ++c)
+        asm volatile("{ .reg .b16 t; ld.shared.b16 t, [%1]; cvt.u32.u16 %0, t; }" : "=r"(v[c]) : "r"(a + 2 * c));
+      o[k] = in ? make_uint4(v[0] | (v[1] << 16), v[2], 0u, 0u) : make_uint4(0u, 0u, 0u, 0u);
+    }
+  }
+#pragma unroll
+  for (int k = 0; k < kImpGroupsPerLane; ++k) {
+    const int t = lane + 32 * k;
+    if (t < ngroups) st_shared_v4(dst + 16u * t, o[k]);
+  }
+}
+
+template <int NOUT, bool BF16>
+__global__ void __launch_bounds__(kImpThreads, 1)
+    first_fprop_imp_kernel(const __grid_constant__ CUtensorMap map_z, const ConvArgs a, const FirstGeom g,
+                           const void* wts, const void* xin) {
+  constexpr int kTmemCols = hc::pow2_at_least(2 * NOUT);
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  const ImpLayout L = imp_layout<NOUT>(g);
+  const uint32_t sbase = smem_u32(smem);
+  const uint32_t bar0 = sbase + L.off_bar;
+  const uint32_t bar_row_full = bar0, bar_row_empty = bar0 + 8 * kImpRing;
+  const uint32_t bar_raw_full = bar0 + 16 * kImpRing, bar_raw_empty = bar_raw_full + 8 * kImpRaw;
+  const uint32_t bar_acc_full = bar_raw_empty + 8 * kImpRaw, bar_acc_empty = bar_acc_full + 16;
+  const uint32_t bar_drain = bar_acc_full + 32;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L.off_bar + 16 * kImpRing + 16 * kImpRaw + 40);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  volatile uint32_t* ticket_slot = reinterpret_cast<volatile uint32_t*>(tmem_slot + 2);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nk = g.r * g.nmr;
+  // contiguous unit range of this CTA
+  const int u_begin = (int)(((long long)blockIdx.x * g.units) / gridDim.x);
+  const int u_end = (int)(((long long)(blockIdx.x + 1) * g.units) / gridDim.x);
+
+  // filter as the B operand, K-major without swizzle: MMA t = rr*nmr + m reads groups 2m, 2m+1
+  // of filter row rr; 16 bytes of (group kc, output channel o) at t*NOUT*32 + kc*NOUT*16 + o*16
+  {
+    const uint16_t* wsrc = static_cast<const uint16_t*>(wts);
+    for (int i = threadIdx.x; i < nk * 2 * NOUT; i += kImpThreads) {
+      const int t = i / (2 * NOUT), rem = i - t * 2 * NOUT;
+      const int kc = rem / NOUT, o = rem - kc * NOUT;
+      const int rr = t / g.nmr, jj = 2 * (t - rr * g.nmr) + kc;
+      uint32_t w32[4] = {0, 0, 0, 0};
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const int gp = e / g.cpx, c = e - gp * g.cpx;
+        const int sx = g.gpx * jj + gp - g.lead;
+        if (sx >= 0 && sx < g.s && c < 3 && o < a.out_c)
+          w32[e >> 1] |= (uint32_t)wsrc[((o * g.r + rr) * g.s + sx) * 3 + c] << ((e & 1) * 16);
+      }
+      st_shared_v4(sbase + L.off_b + (uint32_t)t * (NOUT * 32) + (uint32_t)kc * (NOUT * 16) + (uint32_t)o * 16u,
+                   make_uint4(w32[0], w32[1], w32[2], w32[3]));
+    }
+  }
+  fence_proxy_async_smem();
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kImpRing; ++i) {
+      mbar_init(bar_row_full + 8 * i, 1);
+      mbar_init(bar_row_empty + 8 * i, 1);
+    }
+    for (int i = 0; i < kImpRaw; ++i) {
+      mbar_init(bar_raw_full + 8 * i, 1);
+      mbar_init(bar_raw_empty + 8 * i, 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(bar_acc_full + 8 * i, 1);
+      mbar_init(bar_acc_empty + 8 * i, 8);  // lane 0 of each epilogue warp
+    }
+    mbar_init(bar_drain, 1);
+    *abort_flag = 0;
+    fence_mbarrier_init();
+  }
+  if (warp == kImpMmaWarp) {
+    tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == kImpProdWarp) {
+    // ---------------------------------------------------------------- raw input rows (bulk copies)
+    if (g.rawtma && lane == 0) {
+      const uint8_t* xb = static_cast<const uint8_t*>(xin);
+      int prev_n = -1, prev_p = -2;
+      uint32_t i = 0;
+      bool ok = true;
+      for (int u = u_begin; u < u_end && ok && !hc::is_aborted(abort_flag); ++u) {
+        const int n = u / g.p, p = u - n * g.p;
+        const int f = imp_first_new(g, prev_n, prev_p, n, p);
+        prev_n = n;
+        prev_p = p;
+        for (int rr = f; rr < g.r; ++rr, ++i) {
+          const uint32_t rs = i % kImpRaw;
+          if (!mbar_wait_backoff(bar_raw_empty + 8 * rs, ((i / kImpRaw) & 1) ^ 1, 32)) {
+            hc::set_abort(abort_flag, a.err, kErrWaitHalo);
+            ok = false;
+            break;
+          }
+          const int h = p * g.stride - g.pad + rr;
+          if (h >= 0 && h < g.h) {
+            mbar_arrive_expect_tx(bar_raw_full + 8 * rs, (uint32_t)g.rawb);
+            bulk_load_1d(sbase + L.off_raw + rs * g.rawb, xb + ((size_t)n * g.h + h) * g.rawb, (uint32_t)g.rawb,
+                         bar_raw_full + 8 * rs);
+          } else {
+            mbar_arrive(bar_raw_full + 8 * rs);  // a zero row: nothing to copy
+          }
+        }
+      }
+    }
+  } else if (warp < kImpConv0 + kImpConvWarps) {
+    // ---------------------------------------------------------------- input-row converters
+    const int cw = warp - kImpConv0;
+    const uint16_t* x = static_cast<const uint16_t*>(xin);
+    int prev_n = -1, prev_p = -2;
+    uint32_t i = 0;
+    bool ok = true;
+    for (int u = u_begin; u < u_end && ok && !__any_sync(0xffffffffu, hc::is_aborted(abort_flag)); ++u) {
+      const int n = u / g.p, p = u - n * g.p;
+      const int f = imp_first_new(g, prev_n, prev_p, n, p);
+      prev_n = n;
+      prev_p = p;
+      for (int rr = f; rr < g.r; ++rr, ++i) {
+        if ((int)(i % kImpConvWarps) != cw) continue;
+        const uint32_t slot = i % kImpRing, fill = i / kImpRing, rs = i % kImpRaw;
+        bool got = mbar_wait_backoff(bar_row_empty + 8 * slot, (fill & 1) ^ 1, 32);
+        if (g.rawtma) got = got && mbar_wait_backoff(bar_raw_full + 8 * rs, (i / kImpRaw) & 1, 32);
+        if (!__all_sync(0xffffffffu, got)) {
+          hc::set_abort(abort_flag, a.err, kErrWaitHalo);
+          ok = false;
+          break;
+        }
+        const int h = p * g.stride - g.pad + rr;
+        if (g.rawtma)
+          imp_convert_row_smem(sbase + L.off_raw + rs * g.rawb, g, h, sbase + slot * g.rowb, lane);
+        else
+          imp_convert_row(x, g, n, h, sbase + slot * g.rowb, lane);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          if (g.rawtma) mbar_arrive(bar_raw_empty + 8 * rs);
+          mbar_arrive(bar_row_full + 8 * slot);
+        }
+      }
+    }
+  } else if (warp == kImpMmaWarp) {
+    // ---------------------------------------------------------------- MMA issuer (whole warp)
+    // The R x nmr MMAs of a unit run with compile-time trip counts for the common filters
+    // (a runtime-bounded loop around the elected-lane MMA issues several times slower).
+    const uint32_t idesc = make_idesc_f16(128, NOUT, BF16, false, false);
+    const uint32_t ring = sbase, bmat = sbase + L.off_b;
+    auto run_units = [&](auto kr, auto km) {
+      constexpr int KR = decltype(kr)::value, KM = decltype(km)::value;
+      const int R = KR ? KR : g.r, M = KM ? KM : g.nmr;
+      int n = u_begin / g.p, p = u_begin - n * g.p;
+      int f = 0;  // first new filter row of the current unit (the first unit appends all R)
+      uint32_t iend = 0, it = 0;
+      for (int u = u_begin; u < u_end; ++u, ++it) {
+        if ((it & 7) == 7 && __any_sync(0xffffffffu, hc::is_aborted(abort_flag))) break;
+        const uint32_t inew = iend;
+        iend += (uint32_t)(R - f);
+        const uint32_t s = it & 1, ph = (it >> 1) & 1;
+        // the unit's barriers are tested back to back (their latencies overlap); only one
+        // that is not complete yet is then waited for
+        bool ready = mbar_test(bar_acc_empty + 8 * s, ph ^ 1);
+        for (uint32_t j = inew; j < iend; ++j) ready &= mbar_test(bar_row_full + 8 * (j % kImpRing), (j / kImpRing) & 1);
+        if (!__all_sync(0xffffffffu, ready)) {
+          bool ok = mbar_wait(bar_acc_empty + 8 * s, ph ^ 1);
+          for (uint32_t j = inew; j < iend && ok; ++j)
+            ok = mbar_wait(bar_row_full + 8 * (j % kImpRing), (j / kImpRing) & 1);
+          if (!__all_sync(0xffffffffu, ok)) {
+            hc::set_abort(abort_flag, a.err, kErrWaitAccum);
+            break;
+          }
+        }
+        tc_fence_after();
+        const uint32_t d = tmem_base + s * NOUT;
+        const uint32_t row0 = iend - (uint32_t)R;
+        if constexpr (KR != 0 && KM != 0) {
+#pragma unroll
+          for (int rr = 0; rr < KR; ++rr) {
+            const uint32_t arow = ring + ((row0 + rr) % kImpRing) * g.rowb;
+#pragma unroll
+            for (int m = 0; m < KM; ++m)
+              mma_f16_ss_warp(d, make_noswz_desc(arow + 32u * m, 16, 128),
+                              make_noswz_desc(bmat + (uint32_t)(rr * KM + m) * (NOUT * 32), NOUT * 16, 128), idesc,
+                              (rr | m) ? 1u : 0u);
+          }
+        } else {
+          uint32_t acc = 0;
+          for (int rr = 0; rr < R; ++rr) {
+            const uint32_t arow = ring + ((row0 + rr) % kImpRing) * g.rowb;
+            for (int m = 0; m < M; ++m, acc = 1u)
+              mma_f16_ss_warp(d, make_noswz_desc(arow + 32u * m, 16, 128),
+                              make_noswz_desc(bmat + (uint32_t)(rr * M + m) * (NOUT * 32), NOUT * 16, 128), idesc, acc);
+          }
+        }
+        mma_commit_warp(bar_acc_full + 8 * s);  // the epilogue also releases the unit's rows
+        const int pn = n, pp = p;
+        if (++p == g.p) {
+          p = 0;
+          ++n;
+        }
+        f = imp_first_new(g, pn, pp, n, p);
+      }
+    };
+    if (g.r == 7 && g.nmr == 2)
+      run_units(std::integral_constant<int, 7>{}, std::integral_constant<int, 2>{});
+    else if (g.r == 5 && g.nmr == 3)
+      run_units(std::integral_constant<int, 5>{}, std::integral_constant<int, 3>{});
+    else
+      run_units(std::integral_constant<int, 0>{}, std::integral_constant<int, 0>{});
+    mma_commit_warp(bar_drain);
+    mbar_wait(bar_drain, 0);
+  } else {
+    // ---------------------------------------------------------------- epilogue (8 warps)
+    constexpr int kHalves = NOUT >= 64 ? 2 : 1;
+    constexpr int kCPH = NOUT / kHalves;         // channels of one warp's block
+    constexpr int kSB = kCPH < 32 ? kCPH : 32;
+    constexpr int kNB = kCPH / kSB;
+    constexpr int kSh = kSB == 32 ? 0 : 1;
+    constexpr uint32_t kSpan = kCPH * 2;         // staged row bytes = the TMA swizzle span
+    constexpr uint32_t kSwz = kSpan / 16 - 1;    // 16-byte chunk bits XOR-ed with bits 7+ of the offset
+    const int ew = warp - kImpEpiWarp0;
+    const int quad = warp & 3;
+    const int half = ew >> 2;
+    const int e = quad * 32 + lane;
+    float s1[kNB], s2[kNB];
+#pragma unroll
+    for (int b = 0; b < kNB; ++b) s1[b] = s2[b] = 0.f;
+    constexpr bool kRegStats = kCPH <= 32;
+    float r1[kRegStats ? kCPH : 1], r2[kRegStats ? kCPH : 1];
+#pragma unroll
+    for (int i = 0; i < (kRegStats ? kCPH : 1); ++i) r1[i] = r2[i] = 0.f;
+    const bool stats = a.mode == kFpropStats;
+    const bool bias_relu = a.mode == kFpropBiasRelu;
+    const bool valid = e < g.q;
+    const uint32_t stage0 = sbase + L.off_stage + (uint32_t)ew * 2 * kImpStageBytes;
+    // the unit sequence, to release ring rows: once a unit's MMAs are complete, the rows the
+    // next unit does not read are free (first epilogue warp, lane 0)
+    int n = u_begin / g.p, p = u_begin - n * g.p, f = 0;
+    uint32_t iend = 0;
+    uint32_t it = 0;
+    for (int u = u_begin; u < u_end && !hc::is_aborted(abort_flag); ++u, ++it) {
+      const uint32_t s = it & 1, ph = (it >> 1) & 1;
+      // the store that last read this unit's staging buffer (two units ago), waited for while
+      // the accumulator is still being computed
+      if (lane == 0) bulk_wait_group_read<1>();
+      if (!mbar_wait_backoff(bar_acc_full + 8 * s, ph, 128)) {
+        hc::set_abort(abort_flag, a.err, kErrWaitMma);
+        break;
+      }
+      tc_fence_after();
+      __syncwarp();
+      {
+        iend += (uint32_t)(g.r - f);
+        const int pn = n, pp = p;
+        if (++p == g.p) {
+          p = 0;
+          ++n;
+        }
+        f = imp_first_new(g, pn, pp, n, p);
+        if (ew == 0 && lane == 0 && u + 1 < u_end)
+          for (int j = 0; j < g.r - f; ++j) mbar_arrive(bar_row_empty + 8 * ((iend - g.r + j) % kImpRing));
+      }
+      if (half < kHalves) {
+        const uint32_t sb = stage0 + s * kImpStageBytes;
+#pragma unroll
+        for (int b = 0; b < kNB; ++b) {
+          const int c0 = half * kCPH + b * kSB;
+          uint32_t r[kSB];
+#pragma unroll
+          for (int q16 = 0; q16 < kSB / 16; ++q16)
+            tmem_ld16(tmem_base + ((uint32_t)(quad * 32) << 16) + s * NOUT + c0 + q16 * 16,
+                      *reinterpret_cast<uint32_t(*)[16]>(r + q16 * 16));
+          tmem_ld_wait();
+          if (b == kNB - 1) {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar_acc_empty + 8 * s);
+          }
+          float v[kSB];
+#pragma unroll
+          for (int i = 0; i < kSB; ++i) {
+            float xv = __uint_as_float(r[i]);
+            if (bias_relu) xv = fmaxf(xv + __ldg(a.bias + c0 + i), 0.f);
+            v[i] = valid ? xv : 0.f;
+          }
+#pragma unroll
+          for (int cc = 0; cc < kSB / 8; ++cc) {
+            const uint32_t logical = (uint32_t)lane * kSpan + (uint32_t)(b * kSB / 8 + cc) * 16u;
+            st_shared_v4(sb + (logical ^ (((logical >> 7) & kSwz) << 4)),
+                         make_uint4(pack2<BF16>(v[8 * cc + 0], v[8 * cc + 1]), pack2<BF16>(v[8 * cc + 2], v[8 * cc + 3]),
+                                    pack2<BF16>(v[8 * cc + 4], v[8 * cc + 5]), pack2<BF16>(v[8 * cc + 6], v[8 * cc + 7])));
+          }
+          if (stats) {
+            if constexpr (kRegStats) {
+#pragma unroll
+              for (int i = 0; i < kSB; ++i) {
+                r1[b * kSB + i] += v[i];
+                r2[b * kSB + i] = fmaf(v[i], v[i], r2[b * kSB + i]);
+              }
+            } else {
+              float sq[kSB];
+#pragma unroll
+              for (int i = 0; i < kSB; ++i) sq[i] = v[i] * v[i];
+              hc::reduce_scatter<kSB>(v, lane);
+              hc::reduce_scatter<kSB>(sq, lane);
+              s1[b] += v[0];
+              s2[b] += sq[0];
+            }
+          }
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          if (quad * 32 < g.q) tma_store_3d(&map_z, sb, half * kCPH, quad * 32, u);
+          bulk_commit_group();
+        }
+      } else {
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_acc_empty + 8 * s);
+      }
+    }
+    if (lane == 0) bulk_wait_group<0>();
+    if constexpr (kRegStats) {
+      if (stats && half < kHalves) {
+#pragma unroll
+        for (int b = 0; b < kNB; ++b) {
+          float v1[kSB], v2[kSB];
+#pragma unroll
+          for (int i = 0; i < kSB; ++i) {
+            v1[i] = r1[b * kSB + i];
+            v2[i] = r2[b * kSB + i];
+          }
+          hc::reduce_scatter<kSB>(v1, lane);
+          hc::reduce_scatter<kSB>(v2, lane);
+          s1[b] = v1[0];
+          s2[b] = v2[0];
+        }
+      }
+    }
+    if (stats && half < kHalves && (lane & ((1 << kSh) - 1)) == 0) {
+      // the ring is free: every MMA has completed
+      float* red = reinterpret_cast<float*>(smem);
+#pragma unroll
+      for (int b = 0; b < kNB; ++b) {
+        const int c = half * kCPH + b * kSB + (lane >> kSh);
+        red[(quad * 2 + 0) * NOUT + c] = s1[b];
+        red[(quad * 2 + 1) * NOUT + c] = s2[b];
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (a.mode == kFpropStats)
+    hc::stats_partial_finalize<NOUT, kImpThreads, 32768>(a, reinterpret_cast<const float*>(smem), smem, ticket_slot,
+                                                          abort_flag);
+  if (warp == kImpMmaWarp) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, kTmemCols);
+  }
+}
+
 // ------------------------------------------------------------------------------ wgrad
 // D[slot][k] = sum over the CTA's units of sum_q tile[q][slot] * dz[n,p,q][k]: the im2col tile
 // is the MN-major A operand (M = K slot, two M = 128 tiles, so a fourth zero atom), the TMA-
@@ -499,7 +1026,7 @@ __global__ void __launch_bounds__(kFlWgThreads, 1)
         hc::set_abort(abort_flag, err, kErrWaitOperand);
         break;
       }
-      fl_build_tile(sbase + off_a + s * kFlWgTile, smem + sx * xst, g, tid);
+      fl_build_tile(sbase + off_a + s * kFlWgTile, sbase + sx * xst, g, tid);
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) {
@@ -645,6 +1172,17 @@ bool first_geom(FirstGeom& g, const HaloGeom& hg, int stride) {
   g.rowp = wunits * 8;
   g.nk = (g.r * 24 + 15) / 16;
   g.tma = (row * 2) % 16 == 0 && wunits <= 256;
+  g.imp = 0;
+  if (stride == 1 || stride == 2) {
+    g.gpx = stride;
+    g.cpx = 8 / stride;
+    g.jm = (g.pad + g.gpx - 1) / g.gpx;
+    g.lead = g.gpx * g.jm - g.pad;
+    const int nch = (g.lead + g.s + g.gpx - 1) / g.gpx;  // groups of one filter row's run
+    g.nmr = (nch + 1) / 2;
+    g.rowb = (128 + 2 * g.nmr) * 16;                     // output pixel 127 reads groups < 128 + 2*nmr
+    g.imp = 128 + 2 * g.nmr <= 32 * kImpGroupsPerLane && 2 * g.r <= kImpRing;
+  }
   return true;
 }
 
@@ -687,6 +1225,46 @@ int launch_first_fprop(const FpropArgs& f, int stride, int c_out, bool bf16, con
   if (g.tma && !first_x_map(&mx, g, x, bf16)) return 6;
   const int nout = nout_for(c_out);
   if (nout != c_out) return 3;
+  if (g.imp) {
+    // implicit im2col: output written by TMA in blocks of 32 pixels x (channels / halves)
+    g.xal4 = (reinterpret_cast<uintptr_t>(x) & 3) == 0;
+    g.rawb = g.w * 6;
+    g.rawtma = (g.rawb % 16) == 0 && (reinterpret_cast<uintptr_t>(x) & 15) == 0;
+    const int cph = nout >= 64 ? nout / 2 : nout;
+    CUtensorMap mz{};
+    const uint64_t dims[3] = {(uint64_t)c_out, (uint64_t)g.q, (uint64_t)g.units};
+    const uint64_t strides[2] = {(uint64_t)c_out * 2, (uint64_t)g.q * c_out * 2};
+    const uint32_t box[3] = {(uint32_t)cph, 32, 1};
+    uint32_t total = 0;
+    switch (nout) {
+      case 16: total = imp_layout<16>(g).total; break;
+      case 32: total = imp_layout<32>(g).total; break;
+      case 64: total = imp_layout<64>(g).total; break;
+      default: total = imp_layout<128>(g).total; break;
+    }
+    const uint32_t ismem = total + 1024;
+    if (ismem <= 227 * 1024 &&
+        encode_tiled_span(&mz, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, f.z,
+                          dims, strides, box, cph * 2)) {
+      const int igrid = std::min(g.units, num_sms);
+      auto go = [&](auto kern) {
+        if (!ensure_smem_attr(reinterpret_cast<const void*>(kern), 227 * 1024)) return 6;
+        kern<<<igrid, kImpThreads, ismem, st>>>(mz, a, g, w, x);
+        return cudaGetLastError() == cudaSuccess ? 0 : 6;
+      };
+      switch (nout * 2 + (bf16 ? 1 : 0)) {
+        case 16 * 2: return go(first_fprop_imp_kernel<16, false>);
+        case 16 * 2 + 1: return go(first_fprop_imp_kernel<16, true>);
+        case 32 * 2: return go(first_fprop_imp_kernel<32, false>);
+        case 32 * 2 + 1: return go(first_fprop_imp_kernel<32, true>);
+        case 64 * 2: return go(first_fprop_imp_kernel<64, false>);
+        case 64 * 2 + 1: return go(first_fprop_imp_kernel<64, true>);
+        case 128 * 2: return go(first_fprop_imp_kernel<128, false>);
+        case 128 * 2 + 1: return go(first_fprop_imp_kernel<128, true>);
+        default: return 3;
+      }
+    }
+  }
   const uint32_t smem = kFlXStages * fl_xstage_bytes(g) + 2 * kFlTile + kFlAtoms * nout * 128 + 256 + 1024;
   if (smem > 227 * 1024) return 3;
   const int grid = std::min(g.units, num_sms);
