@@ -195,15 +195,16 @@ def run_reference(args, world, rank):
 
 
 # ----------------------------------------------------------------------------- GPU arm
-def traffic_for(kernel: str):
-    """Per-launch DRAM bytes from a committed ncu summary, if it matches the current source."""
+def traffic_for(kernel: str, config_index: int):
+    """Per-launch DRAM bytes from a committed ncu summary of this workload, if it matches the
+    current source."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
         return None
     import hashlib
     with open(p) as f:
         t = json.load(f)
-    ent = t.get(kernel)
+    ent = t.get(f"config{config_index}", {}).get(kernel)
     if not ent:
         return None
     h = hashlib.sha256()
@@ -376,7 +377,7 @@ def run_cbr(args, world, rank, local):
                        launch="one step captured as a CUDA graph of the library's launches, replayed per step"),
         "tflops": conv_flops * world / (ms * 1e-3) / 1e12,
         "roofline": {"kernel": dom, "bound": dbound, "achieved": ach, "peak": pk, "unit": unit,
-                     "frac": ach / pk, "traffic": traffic_for(dom),
+                     "frac": ach / pk, "traffic": traffic_for(dom, args.config),
                      "peak_source": f"{peak_src} ({'sustained bf16 GEMM' if dbound == 'tensor' else 'STREAM copy'})"},
         "roofline_step": {"ledger_us": round(step_roof, 2), "measured_us": round(ms * 1e3, 2),
                           "frac": round(step_roof / (ms * 1e3), 4),
