@@ -23,6 +23,8 @@ constexpr int kApplyUnroll = 4;
 constexpr int kRedThreads = 512;
 constexpr int kRedUnroll = 8;
 
+// Sweeps the tensor last element first: the convolution before it wrote z first to last, so
+// the end of z is what the L2 still holds.
 template <bool BF16, bool MASK>
 __global__ void __launch_bounds__(kApplyThreads)
     bn_apply_relu_kernel(const ApplyArgs a) {
@@ -39,13 +41,13 @@ __global__ void __launch_bounds__(kApplyThreads)
     uint4 in[kApplyUnroll];
 #pragma unroll
     for (int k = 0; k < kApplyUnroll; ++k) {
-      const long long v = v0 + k * stride;
-      if (v < nvec) in[k] = ld_global_nc_v4(zb + v * 16);
+      const long long v = nvec - 1 - (v0 + k * stride);
+      if (v >= 0) in[k] = ld_global_nc_v4(zb + v * 16);
     }
 #pragma unroll
     for (int k = 0; k < kApplyUnroll; ++k) {
-      const long long v = v0 + k * stride;
-      if (v < nvec) {
+      const long long v = nvec - 1 - (v0 + k * stride);
+      if (v >= 0) {
         const int c0 = (int)(v % cvec) * 8;
         const uint32_t w[4] = {in[k].x, in[k].y, in[k].z, in[k].w};
         uint32_t o[4];
@@ -209,6 +211,8 @@ __global__ void __launch_bounds__(kRedThreads)
 }
 
 // dz = a*g - d*z + e with g = dy*mask, written to HBM (used when no dgrad kernel produces it).
+// Sweeps last element first: the reduction before it read dy and z first to last, so their
+// ends are what the L2 still holds.
 template <bool BF16, bool MASKBITS>
 __global__ void __launch_bounds__(kApplyThreads)
     dz_kernel(const DzArgs a) {
@@ -228,8 +232,8 @@ __global__ void __launch_bounds__(kApplyThreads)
     uint32_t mb[kApplyUnroll];
 #pragma unroll
     for (int k = 0; k < kApplyUnroll; ++k) {
-      const long long v = v0 + k * stride;
-      if (v < nvec) {
+      const long long v = nvec - 1 - (v0 + k * stride);
+      if (v >= 0) {
         dv[k] = ld_global_nc_v4(dyb + v * 16);
         zv[k] = ld_global_nc_v4(zb + v * 16);
         if (MASKBITS) mb[k] = a.mask[v];
@@ -238,8 +242,8 @@ __global__ void __launch_bounds__(kApplyThreads)
     }
 #pragma unroll
     for (int k = 0; k < kApplyUnroll; ++k) {
-      const long long v = v0 + k * stride;
-      if (v < nvec) {
+      const long long v = nvec - 1 - (v0 + k * stride);
+      if (v >= 0) {
         const int c0 = (int)(v % cvec) * 8;
         uint32_t bits;
         if (MASKBITS) {

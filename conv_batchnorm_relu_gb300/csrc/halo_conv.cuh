@@ -401,11 +401,13 @@ __global__ void __launch_bounds__(Roles<KIND>::kThreads, 1)
           const uint32_t hbase = halo_addr + hs * L.halo_stride;
           // taps advance the A start address incrementally (one 128-byte row per tap, plus the
           // rest of the padded row at the end of a filter row)
-          auto run_taps = [&](auto nt_c) {
-            constexpr int NT = decltype(nt_c)::value;
+          // NT tiles; RS taps at compile time for 3x3 and 1x1 filters (0: the runtime r*s)
+          auto run_taps = [&](auto nt_c, auto rs_c) {
+            constexpr int NT = decltype(nt_c)::value, RS = decltype(rs_c)::value;
             uint64_t a_tap = make_sw128_desc(hbase + (uint32_t)off * 128u, 16, 1024, 0);
             int sx = 0;
-            for (int tap = 0; tap < rs; ++tap) {
+#pragma unroll
+            for (int tap = 0; tap < (RS ? RS : rs); ++tap) {
               uint32_t wslab_off, ws = 0;
               if (WRES) {
                 wslab_off = (uint32_t)(ch * rs + tap) * L.wslab;
@@ -436,10 +438,18 @@ __global__ void __launch_bounds__(Roles<KIND>::kThreads, 1)
               }
             }
           };
+          auto run_rs = [&](auto nt_c) {
+            if (rs == 9)
+              run_taps(nt_c, std::integral_constant<int, 9>{});
+            else if (rs == 1)
+              run_taps(nt_c, std::integral_constant<int, 1>{});
+            else
+              run_taps(nt_c, std::integral_constant<int, 0>{});
+          };
           if (ntiles == U)
-            run_taps(std::integral_constant<int, U>{});
+            run_rs(std::integral_constant<int, U>{});
           else
-            run_taps(std::integral_constant<int, 1>{});  // ragged tail of an image (U = 2 only)
+            run_rs(std::integral_constant<int, 1>{});  // ragged tail of an image (U = 2 only)
           mma_commit_warp(bar_halo_empty + 8 * hs);
         }
         if (bad) break;
