@@ -377,14 +377,20 @@ __global__ void __launch_bounds__(Roles<KIND>::kThreads, 1)
         tc_fence_after();
       }
       uint32_t hit = 0, wit = 0, ait = 0;
-      for (int u = blockIdx.x; u < g.total_units && !bad && !__any_sync(0xffffffffu, is_aborted(abort_flag));
-           u += gridDim.x) {
+      for (int u = blockIdx.x; u < g.total_units && !bad; u += gridDim.x) {
+        // another role's failed wait is noticed every 8 units (a vote per unit costs
+        // issue time that the tensor pipe then waits for)
+        if ((ait & 7) == 7 && __any_sync(0xffffffffu, is_aborted(abort_flag))) break;
         const int n = u / g.upi;
         const int m0 = (u - n * g.upi) * g.um;
         const int off = m0 - (m0 / g.wp) * g.wp;
         const int ntiles = min(U, (rows_img - m0 + 127) / 128);
         const uint32_t as = ait & 1, aph = (ait >> 1) & 1;
-        if (!__all_sync(0xffffffffu, mbar_wait(bar_acc_empty + 8 * as, aph ^ 1))) {
+        // the accumulator stage and the first halo are tested back to back (their latencies
+        // overlap); only when one is not complete yet are they waited for one by one
+        const bool ready = __all_sync(0xffffffffu, mbar_test(bar_acc_empty + 8 * as, aph ^ 1) &
+                                                       mbar_test(bar_halo_full + 8 * (hit & 1), (hit >> 1) & 1));
+        if (!ready && !__all_sync(0xffffffffu, mbar_wait(bar_acc_empty + 8 * as, aph ^ 1))) {
           set_abort(abort_flag, a.err, kErrWaitAccum);
           break;
         }
@@ -392,7 +398,7 @@ __global__ void __launch_bounds__(Roles<KIND>::kThreads, 1)
         const uint32_t d0 = tmem_base + as * (U * NOUT);
         for (int ch = 0; ch < NCH && !bad; ++ch, ++hit) {
           const uint32_t hs = hit & 1, hph = (hit >> 1) & 1;
-          if (!__all_sync(0xffffffffu, mbar_wait(bar_halo_full + 8 * hs, hph))) {
+          if (!(ch == 0 && ready) && !__all_sync(0xffffffffu, mbar_wait(bar_halo_full + 8 * hs, hph))) {
             set_abort(abort_flag, a.err, kErrWaitHalo);
             bad = true;
             break;
