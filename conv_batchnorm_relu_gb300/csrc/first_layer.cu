@@ -1148,6 +1148,323 @@ __global__ void __launch_bounds__(kFlRedSpan * kFlRedSlices)
   }
 }
 
+// ------------------------------------------------------------------------------ wgrad, implicit im2col
+// Weight gradient of the first layer for Cout = 64, stride 1 or 2, without an im2col tile
+// (Tech-Renaissance CBR page, section 5.1: dW = sum over pixels of dz x im2col(x)).  The
+// padded rows of the forward are the B operand, read MN-major through a descriptor without
+// swizzle (16 bytes per K step = one output pixel, 16 bytes per N group of 8 K slots), and a
+// pair of output rows p, p+1 is the A operand: the two 64-channel dz tiles stacked along M
+// (M = 128).  The pair reads W = R + stride input rows; input row b of the window meets filter
+// row b for row p (accumulator lanes 0-63) and filter row b - stride for row p+1 (lanes
+// 64-127), so each window row has its own accumulator block of 16*nmr columns and one MMA
+// per 16 output pixels.  Per CTA the blocks accumulate over a contiguous range of pairs; a
+// fixed-order reduction then adds the two halves and the CTAs and maps K slots to (s, c).
+constexpr int kIwRawWarp = 0, kIwDzWarp = 1, kIwConv0 = 2, kIwMmaWarp = 6, kIwRelWarp = 7, kIwEpiWarp0 = 8;
+constexpr int kIwThreads = (kIwEpiWarp0 + 4) * 32;  // 384
+constexpr int kIwDzStages = 3;
+constexpr int kIwDone = 4;                           // pair-completion barriers in flight
+
+struct IwGeom {
+  int w;      // window rows per pair: r + stride
+  int kq;     // K steps of 16 output pixels: ceil(q / 16)
+  int pp;     // pairs per image: ceil(p / 2)
+  int units;  // n_img * pp
+  int ncol;   // accumulator columns per window row: 16 * nmr
+};
+
+struct IwLayout {
+  uint32_t off_raw, off_dz, dztile, off_bar, total;
+};
+
+__host__ __device__ inline IwLayout iw_layout(const FirstGeom& g, const IwGeom& v) {
+  IwLayout L;
+  L.off_raw = imp_align((uint32_t)kImpRing * g.rowb);
+  L.off_dz = imp_align(L.off_raw + (g.rawtma ? (uint32_t)kImpRaw * g.rawb : 0u));
+  L.dztile = (uint32_t)v.kq * 16u * 128u;  // 16*kq pixels x 64 channels, SW128
+  L.off_bar = L.off_dz + kIwDzStages * 2 * L.dztile;
+  L.total = L.off_bar + 512;
+  return L;
+}
+
+// First window row that pair j of image n appends, given the pair before it in the range.
+__device__ __forceinline__ int iw_first_new(const FirstGeom& g, const IwGeom& v, int prev_n, int prev_j, int n, int j) {
+  return (n == prev_n && j == prev_j + 1 && 2 * g.stride < v.w) ? v.w - 2 * g.stride : 0;
+}
+
+template <bool BF16>
+__global__ void __launch_bounds__(kIwThreads, 1)
+    first_wgrad_imp_kernel(const __grid_constant__ CUtensorMap map_dz, const FirstGeom g, const IwGeom v,
+                           const void* xin, float* part, uint32_t* err) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  const IwLayout L = iw_layout(g, v);
+  const uint32_t sbase = smem_u32(smem);
+  const uint32_t bar0 = sbase + L.off_bar;
+  const uint32_t bar_row_full = bar0, bar_row_empty = bar0 + 8 * kImpRing;
+  const uint32_t bar_raw_full = bar0 + 16 * kImpRing, bar_raw_empty = bar_raw_full + 8 * kImpRaw;
+  const uint32_t bar_dz_full = bar_raw_empty + 8 * kImpRaw, bar_dz_empty = bar_dz_full + 8 * kIwDzStages;
+  const uint32_t bar_done = bar_dz_empty + 8 * kIwDzStages, bar_drain = bar_done + 8 * kIwDone;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + (bar_drain + 8 - sbase));
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int u_begin = (int)(((long long)blockIdx.x * v.units) / gridDim.x);
+  const int u_end = (int)(((long long)(blockIdx.x + 1) * v.units) / gridDim.x);
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kImpRing; ++i) {
+      mbar_init(bar_row_full + 8 * i, 1);
+      mbar_init(bar_row_empty + 8 * i, 1);
+    }
+    for (int i = 0; i < kImpRaw; ++i) {
+      mbar_init(bar_raw_full + 8 * i, 1);
+      mbar_init(bar_raw_empty + 8 * i, 1);
+    }
+    for (int i = 0; i < kIwDzStages; ++i) {
+      mbar_init(bar_dz_full + 8 * i, 1);
+      mbar_init(bar_dz_empty + 8 * i, 1);
+    }
+    for (int i = 0; i < kIwDone; ++i) mbar_init(bar_done + 8 * i, 1);
+    mbar_init(bar_drain, 1);
+    *abort_flag = 0;
+    fence_mbarrier_init();
+  }
+  if (warp == kIwMmaWarp) {
+    tmem_alloc(smem_u32(tmem_slot), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  // the window's input rows: pair j of image n reads rows 2*j*stride - pad + b, b < w
+  auto row_of = [&](int j, int b) { return 2 * j * g.stride - g.pad + b; };
+
+  if (warp == kIwRawWarp) {
+    // ---------------------------------------------------------------- raw input rows (bulk copies)
+    if (g.rawtma && lane == 0) {
+      const uint8_t* xb = static_cast<const uint8_t*>(xin);
+      int prev_n = -1, prev_j = -2;
+      uint32_t i = 0;
+      bool ok = true;
+      for (int u = u_begin; u < u_end && ok && !hc::is_aborted(abort_flag); ++u) {
+        const int n = u / v.pp, j = u - n * v.pp;
+        const int f = iw_first_new(g, v, prev_n, prev_j, n, j);
+        prev_n = n;
+        prev_j = j;
+        for (int b = f; b < v.w; ++b, ++i) {
+          const uint32_t rs = i % kImpRaw;
+          if (!mbar_wait_backoff(bar_raw_empty + 8 * rs, ((i / kImpRaw) & 1) ^ 1, 32)) {
+            hc::set_abort(abort_flag, err, kErrWaitHalo);
+            ok = false;
+            break;
+          }
+          const int h = row_of(j, b);
+          if (h >= 0 && h < g.h) {
+            mbar_arrive_expect_tx(bar_raw_full + 8 * rs, (uint32_t)g.rawb);
+            bulk_load_1d(sbase + L.off_raw + rs * g.rawb, xb + ((size_t)n * g.h + h) * g.rawb, (uint32_t)g.rawb,
+                         bar_raw_full + 8 * rs);
+          } else {
+            mbar_arrive(bar_raw_full + 8 * rs);
+          }
+        }
+      }
+    }
+  } else if (warp == kIwDzWarp) {
+    // ---------------------------------------------------------------- dz tiles of the pair (TMA)
+    if (lane == 0) {
+      prefetch_tensormap(&map_dz);
+      uint32_t it = 0;
+      for (int u = u_begin; u < u_end && !hc::is_aborted(abort_flag); ++u, ++it) {
+        const int n = u / v.pp, j = u - n * v.pp;
+        const uint32_t s = it % kIwDzStages;
+        if (!mbar_wait_backoff(bar_dz_empty + 8 * s, ((it / kIwDzStages) & 1) ^ 1, 32)) {
+          hc::set_abort(abort_flag, err, kErrWaitOperand);
+          break;
+        }
+        // row 2j+1 past the image's last row loads as zeros (out-of-bounds fill), as do pixels
+        // q >= Q of the last K step
+        mbar_arrive_expect_tx(bar_dz_full + 8 * s, 2 * L.dztile);
+        const uint32_t dst = sbase + L.off_dz + s * 2 * L.dztile;
+        tma_load_4d(dst, &map_dz, 0, 0, 2 * j, n, bar_dz_full + 8 * s);
+        tma_load_4d(dst + L.dztile, &map_dz, 0, 0, 2 * j + 1, n, bar_dz_full + 8 * s);
+      }
+    }
+  } else if (warp < kIwConv0 + kImpConvWarps) {
+    // ---------------------------------------------------------------- input-row converters
+    const int cw = warp - kIwConv0;
+    const uint16_t* x = static_cast<const uint16_t*>(xin);
+    int prev_n = -1, prev_j = -2;
+    uint32_t i = 0;
+    bool ok = true;
+    for (int u = u_begin; u < u_end && ok && !__any_sync(0xffffffffu, hc::is_aborted(abort_flag)); ++u) {
+      const int n = u / v.pp, j = u - n * v.pp;
+      const int f = iw_first_new(g, v, prev_n, prev_j, n, j);
+      prev_n = n;
+      prev_j = j;
+      for (int b = f; b < v.w; ++b, ++i) {
+        if ((int)(i % kImpConvWarps) != cw) continue;
+        const uint32_t slot = i % kImpRing, fill = i / kImpRing, rs = i % kImpRaw;
+        bool got = mbar_wait_backoff(bar_row_empty + 8 * slot, (fill & 1) ^ 1, 32);
+        if (g.rawtma) got = got && mbar_wait_backoff(bar_raw_full + 8 * rs, (i / kImpRaw) & 1, 32);
+        if (!__all_sync(0xffffffffu, got)) {
+          hc::set_abort(abort_flag, err, kErrWaitHalo);
+          ok = false;
+          break;
+        }
+        const int h = row_of(j, b);
+        if (g.rawtma)
+          imp_convert_row_smem(sbase + L.off_raw + rs * g.rawb, g, h, sbase + slot * g.rowb, lane);
+        else
+          imp_convert_row(x, g, n, h, sbase + slot * g.rowb, lane);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          if (g.rawtma) mbar_arrive(bar_raw_empty + 8 * rs);
+          mbar_arrive(bar_row_full + 8 * slot);
+        }
+      }
+    }
+  } else if (warp == kIwMmaWarp) {
+    // ---------------------------------------------------------------- MMA issuer (whole warp)
+    const uint32_t idesc = make_idesc_f16(128, (uint32_t)v.ncol, BF16, true, true);
+    auto run_units = [&](auto w_c, auto kq_c) {
+      constexpr int KW = decltype(w_c)::value, KQ = decltype(kq_c)::value;
+      const int WR = KW ? KW : v.w, NQ = KQ ? KQ : v.kq;
+      int n = u_begin / v.pp, j = u_begin - n * v.pp, f = 0;
+      uint32_t iend = 0, it = 0;
+      for (int u = u_begin; u < u_end; ++u, ++it) {
+        if ((it & 7) == 7 && __any_sync(0xffffffffu, hc::is_aborted(abort_flag))) break;
+        const uint32_t inew = iend;
+        iend += (uint32_t)(WR - f);
+        const uint32_t s = it % kIwDzStages;
+        bool ok = mbar_wait(bar_dz_full + 8 * s, (it / kIwDzStages) & 1);
+        for (uint32_t r = inew; r < iend && ok; ++r)
+          ok = mbar_wait(bar_row_full + 8 * (r % kImpRing), (r / kImpRing) & 1);
+        if (!__all_sync(0xffffffffu, ok)) {
+          hc::set_abort(abort_flag, err, kErrWaitAccum);
+          break;
+        }
+        tc_fence_after();
+        const uint32_t a0 = sbase + L.off_dz + s * 2 * L.dztile;
+        const uint32_t row0 = iend - (uint32_t)WR;
+        if constexpr (KW != 0 && KQ != 0) {
+#pragma unroll
+          for (int kk = 0; kk < KQ; ++kk) {
+            const uint64_t ad = make_sw128_desc(a0 + 2048u * kk, L.dztile, 1024, 0);
+#pragma unroll
+            for (int b = 0; b < KW; ++b)
+              mma_f16_ss_warp(tmem_base + (uint32_t)(b * v.ncol),
+                              ad, make_noswz_desc(sbase + ((row0 + b) % kImpRing) * g.rowb + 256u * kk, 128, 16),
+                              idesc, (it | kk) ? 1u : 0u);
+          }
+        } else {
+          for (int kk = 0; kk < NQ; ++kk) {
+            const uint64_t ad = make_sw128_desc(a0 + 2048u * kk, L.dztile, 1024, 0);
+            for (int b = 0; b < WR; ++b)
+              mma_f16_ss_warp(tmem_base + (uint32_t)(b * v.ncol),
+                              ad, make_noswz_desc(sbase + ((row0 + b) % kImpRing) * g.rowb + 256u * kk, 128, 16),
+                              idesc, (it | kk) ? 1u : 0u);
+          }
+        }
+        mma_commit_warp(bar_done + 8 * (it % kIwDone));
+        const int pn = n, pj = j;
+        if (++j == v.pp) {
+          j = 0;
+          ++n;
+        }
+        f = iw_first_new(g, v, pn, pj, n, j);
+      }
+    };
+    if (v.w == 9 && v.kq == 7)
+      run_units(std::integral_constant<int, 9>{}, std::integral_constant<int, 7>{});
+    else
+      run_units(std::integral_constant<int, 0>{}, std::integral_constant<int, 0>{});
+    mma_commit_warp(bar_drain);
+    mbar_wait(bar_drain, 0);
+  } else if (warp == kIwRelWarp) {
+    // ---------------------------------------------------------------- releaser: once a pair's MMAs
+    // are complete, its dz stage and the window rows the next pair does not read are free
+    if (lane == 0) {
+      int n = u_begin / v.pp, j = u_begin - n * v.pp, f = 0;
+      uint32_t iend = 0, it = 0;
+      for (int u = u_begin; u < u_end && !hc::is_aborted(abort_flag); ++u, ++it) {
+        if (!mbar_wait_backoff(bar_done + 8 * (it % kIwDone), (it / kIwDone) & 1, 64)) {
+          hc::set_abort(abort_flag, err, kErrWaitMma);
+          break;
+        }
+        mbar_arrive(bar_dz_empty + 8 * (it % kIwDzStages));
+        iend += (uint32_t)(v.w - f);
+        const int pn = n, pj = j;
+        if (++j == v.pp) {
+          j = 0;
+          ++n;
+        }
+        f = iw_first_new(g, v, pn, pj, n, j);
+        if (u + 1 < u_end)
+          for (int r = 0; r < v.w - f; ++r) mbar_arrive(bar_row_empty + 8 * ((iend - v.w + r) % kImpRing));
+      }
+    }
+  } else {
+    // ---------------------------------------------------------------- partials (4 warps, once)
+    const int quad = warp & 3;
+    const bool ok = mbar_wait_backoff(bar_drain, 0, 1024);
+    tc_fence_after();
+    if (!ok) {
+      hc::set_abort(abort_flag, err, kErrWaitMma);
+    } else {
+      const int row = quad * 32 + lane;
+      float* dst = part + ((size_t)blockIdx.x * v.w * 128 + row) * v.ncol;
+      for (int b = 0; b < v.w; ++b) {
+        for (int c0 = 0; c0 < v.ncol; c0 += 16) {
+          uint32_t r[16];
+          tmem_ld16(tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)(b * v.ncol + c0), r);
+          tmem_ld_wait();
+          float4* d4 = reinterpret_cast<float4*>(dst + (size_t)b * 128 * v.ncol + c0);
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            d4[k] = make_float4(__uint_as_float(r[4 * k]), __uint_as_float(r[4 * k + 1]), __uint_as_float(r[4 * k + 2]),
+                                __uint_as_float(r[4 * k + 3]));
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kIwMmaWarp) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, 512);
+  }
+}
+
+// dW[k][r][s][c] = sum over CTAs (in fixed order: fp32 within 8 slices of the CTAs, fp64
+// across them) of the top half of window row r and the bottom half of window row r + stride,
+// K slot (group t, element e) -> s = gpx*t + e / cpx - lead, c = e % cpx (c < 3).
+constexpr int kIwRedSlices = 8;
+__global__ void __launch_bounds__(128 * kIwRedSlices / 2)
+    first_wgrad_imp_reduce_kernel(const float* __restrict__ part, float* __restrict__ dw, const FirstGeom g,
+                                  const IwGeom v, int grid) {
+  __shared__ float red[kIwRedSlices][64];
+  const int rr = blockIdx.x / 64, k = blockIdx.x % 64;  // filter row, output channel
+  const int col = threadIdx.x % 64, sl = threadIdx.x / 64;
+  const size_t per_cta = (size_t)v.w * 128 * v.ncol;
+  float acc = 0.f;
+  if (col < v.ncol) {
+    const float* top = part + ((size_t)rr * 128 + k) * v.ncol + col;
+    const float* bot = part + ((size_t)(rr + g.stride) * 128 + 64 + k) * v.ncol + col;
+    for (int c = sl; c < grid; c += kIwRedSlices) acc += __ldcg(top + c * per_cta) + __ldcg(bot + c * per_cta);
+  }
+  red[sl][col] = acc;
+  __syncthreads();
+  if (sl != 0 || col >= v.ncol) return;
+  double t = 0.0;
+  for (int q = 0; q < kIwRedSlices; ++q) t += red[q][col];
+  const int grp = col / 8, e = col % 8;
+  const int sx = g.gpx * grp + e / g.cpx - g.lead, c = e % g.cpx;
+  if (c < 3 && sx >= 0 && sx < g.s) dw[((size_t)(k * g.r + rr) * g.s + sx) * 3 + c] = (float)t;
+}
+
 // ------------------------------------------------------------------------------ host helpers
 bool first_geom(FirstGeom& g, const HaloGeom& hg, int stride) {
   g = FirstGeom{};
@@ -1287,7 +1604,10 @@ int launch_first_fprop(const FpropArgs& f, int stride, int c_out, bool bf16, con
 }
 
 
-size_t first_wgrad_partial_floats(int num_sms, int c_out) { return (size_t)num_sms * 2 * 128 * nout_for(c_out); }
+size_t first_wgrad_partial_floats(int num_sms, int c_out) {
+  // builder kernel: 2 x 128 x nout per CTA; implicit kernel: at most 512 columns x 128 lanes
+  return (size_t)num_sms * std::max(2 * 128 * nout_for(c_out), 512 * 128);
+}
 
 int launch_first_wgrad(const HaloGeom& hg, int stride, int c_out, bool bf16, const void* x, const void* dz,
                        float* part, float* dw, uint32_t* err, int num_sms, cudaStream_t st,
@@ -1296,6 +1616,37 @@ int launch_first_wgrad(const HaloGeom& hg, int stride, int c_out, bool bf16, con
   if (!first_geom(g, hg, stride)) return 3;
   const int nout = nout_for(c_out);
   if (nout != c_out) return 3;
+  if (g.imp && c_out == 64) {
+    // implicit im2col (pairs of output rows, see first_wgrad_imp_kernel)
+    IwGeom v;
+    v.w = g.r + g.stride;
+    v.kq = (g.q + 15) / 16;
+    v.pp = (g.p + 1) / 2;
+    v.units = g.n_img * v.pp;
+    v.ncol = 16 * g.nmr;
+    g.xal4 = (reinterpret_cast<uintptr_t>(x) & 3) == 0;
+    g.rawb = g.w * 6;
+    g.rawtma = (g.rawb % 16) == 0 && (reinterpret_cast<uintptr_t>(x) & 15) == 0;
+    const IwLayout L = iw_layout(g, v);
+    CUtensorMap mdz4{};
+    const uint64_t dims[4] = {64, (uint64_t)g.q, (uint64_t)g.p, (uint64_t)g.n_img};
+    const uint64_t strides[3] = {128, (uint64_t)g.q * 128, (uint64_t)g.p * g.q * 128};
+    const uint32_t box[4] = {64, (uint32_t)(16 * v.kq), 1, 1};
+    if (v.w * v.ncol <= 512 && L.total + 1024 <= 227 * 1024 &&
+        encode_tiled(&mdz4, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4, dz, dims,
+                     strides, box)) {
+      const int grid = std::min(v.units, num_sms);
+      auto go = [&](auto kern) {
+        if (!ensure_smem_attr(reinterpret_cast<const void*>(kern), 227 * 1024)) return 6;
+        kern<<<grid, kIwThreads, L.total + 1024, st>>>(mdz4, g, v, x, part, err);
+        if (cudaGetLastError() != cudaSuccess) return 6;
+        if (between) between(ctx);
+        first_wgrad_imp_reduce_kernel<<<g.r * 64, 64 * kIwRedSlices, 0, st>>>(part, dw, g, v, grid);
+        return cudaGetLastError() == cudaSuccess ? 0 : 6;
+      };
+      return bf16 ? go(first_wgrad_imp_kernel<true>) : go(first_wgrad_imp_kernel<false>);
+    }
+  }
   CUtensorMap mx{}, mdz;
   if (g.tma && !first_x_map(&mx, g, x, bf16)) return 6;
   {
