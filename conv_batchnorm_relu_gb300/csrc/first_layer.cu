@@ -1334,24 +1334,51 @@ __global__ void __launch_bounds__(kIwThreads, 1)
       const int WR = KW ? KW : v.w, NQ = KQ ? KQ : v.kq;
       int n = u_begin / v.pp, j = u_begin - n * v.pp, f = 0;
       uint32_t iend = 0, it = 0;
+      bool have_ready = false;  // this pair's barriers already seen complete (look-ahead)
       for (int u = u_begin; u < u_end; ++u, ++it) {
         if ((it & 7) == 7 && __any_sync(0xffffffffu, hc::is_aborted(abort_flag))) break;
         const uint32_t inew = iend;
         iend += (uint32_t)(WR - f);
         const uint32_t s = it % kIwDzStages;
-        bool ok = mbar_wait(bar_dz_full + 8 * s, (it / kIwDzStages) & 1);
-        for (uint32_t r = inew; r < iend && ok; ++r)
-          ok = mbar_wait(bar_row_full + 8 * (r % kImpRing), (r / kImpRing) & 1);
-        if (!__all_sync(0xffffffffu, ok)) {
-          hc::set_abort(abort_flag, err, kErrWaitAccum);
-          break;
+        if (!have_ready) {
+          // the pair's barriers are tested back to back (their latencies overlap); only one
+          // that is not complete yet is then waited for
+          bool ready = mbar_test(bar_dz_full + 8 * s, (it / kIwDzStages) & 1);
+          for (uint32_t r = inew; r < iend; ++r)
+            ready &= mbar_test(bar_row_full + 8 * (r % kImpRing), (r / kImpRing) & 1);
+          if (!__all_sync(0xffffffffu, ready)) {
+            bool ok = mbar_wait(bar_dz_full + 8 * s, (it / kIwDzStages) & 1);
+            for (uint32_t r = inew; r < iend && ok; ++r)
+              ok = mbar_wait(bar_row_full + 8 * (r % kImpRing), (r / kImpRing) & 1);
+            if (!__all_sync(0xffffffffu, ok)) {
+              hc::set_abort(abort_flag, err, kErrWaitAccum);
+              break;
+            }
+          }
         }
         tc_fence_after();
         const uint32_t a0 = sbase + L.off_dz + s * 2 * L.dztile;
         const uint32_t row0 = iend - (uint32_t)WR;
+        // the next pair
+        int n2 = n, j2 = j + 1;
+        if (j2 == v.pp) {
+          j2 = 0;
+          ++n2;
+        }
+        const int f2 = iw_first_new(g, v, n, j, n2, j2);
+        bool ready_next = false;
         if constexpr (KW != 0 && KQ != 0) {
 #pragma unroll
           for (int kk = 0; kk < KQ; ++kk) {
+            if (kk == KQ - 1 && u + 1 < u_end) {
+              // look-ahead: test the next pair's barriers while this pair's MMAs queue up,
+              // so the next pair starts without a round of barrier latency
+              const uint32_t s2 = (it + 1) % kIwDzStages, iend2 = iend + (uint32_t)(WR - f2);
+              bool rn = mbar_test(bar_dz_full + 8 * s2, ((it + 1) / kIwDzStages) & 1);
+              for (uint32_t r = iend; r < iend2; ++r)
+                rn &= mbar_test(bar_row_full + 8 * (r % kImpRing), (r / kImpRing) & 1);
+              ready_next = __all_sync(0xffffffffu, rn);
+            }
             const uint64_t ad = make_sw128_desc(a0 + 2048u * kk, L.dztile, 1024, 0);
 #pragma unroll
             for (int b = 0; b < KW; ++b)
@@ -1369,12 +1396,10 @@ __global__ void __launch_bounds__(kIwThreads, 1)
           }
         }
         mma_commit_warp(bar_done + 8 * (it % kIwDone));
-        const int pn = n, pj = j;
-        if (++j == v.pp) {
-          j = 0;
-          ++n;
-        }
-        f = iw_first_new(g, v, pn, pj, n, j);
+        n = n2;
+        j = j2;
+        f = f2;
+        have_ready = ready_next;
       }
     };
     if (v.w == 9 && v.kq == 7)
