@@ -84,6 +84,13 @@ __global__ void __launch_bounds__(kRedThreads)
   float mean[8];
 #pragma unroll
   for (int e = 0; e < 8; ++e) mean[e] = a.mean[c0 + e];
+  // the per-channel inputs of the finalize, loaded up front (see below)
+  float f_inv = 0.f, f_gamma = 0.f, f_mean = 0.f;
+  if (threadIdx.x < c) {
+    f_inv = a.inv_std[threadIdx.x];
+    f_gamma = a.gamma[threadIdx.x];
+    f_mean = a.mean[threadIdx.x];
+  }
   float sg[8], sgx[8];
 #pragma unroll
   for (int e = 0; e < 8; ++e) sg[e] = sgx[e] = 0.f;
@@ -163,10 +170,10 @@ __global__ void __launch_bounds__(kRedThreads)
   // math multiplies by the host's 1/M instead of dividing (fp64 division is slow here).
   constexpr int kLd = 16;
   const int nv4 = (2 * c) / 4;                    // float4 columns of one partial (<= 128)
-  const int rgs = kRedThreads / nv4;              // row groups; rgs * 2c = 2048 floats
+  const int rgs = min(kRedThreads / nv4, 32);     // row groups (at most the fp64 tree's width)
   float* fred = red;                              // [rgs][2c]
   double* fin = reinterpret_cast<double*>(red + rgs * 2 * c);  // [2c]
-  {
+  if (threadIdx.x < rgs * nv4) {
     const int c4 = threadIdx.x % nv4, rg = threadIdx.x / nv4;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     for (int b0 = rg; b0 < (int)gridDim.x; b0 += kLd * rgs) {
@@ -188,20 +195,18 @@ __global__ void __launch_bounds__(kRedThreads)
     reinterpret_cast<float4*>(fred + rg * 2 * c)[c4] = acc;
   }
   __syncthreads();
-  for (int i = threadIdx.x; i < 2 * c; i += kRedThreads) {
-    double t = 0;
-    for (int r = 0; r < rgs; ++r) t += fred[r * 2 * c + i];
-    fin[i] = t;
-  }
+  // row groups combined in fp64 by a fixed pairwise tree
+  for (int i = threadIdx.x; i < 2 * c; i += kRedThreads) fin[i] = tree_sum<32>(fred + i, 2 * c, rgs);
   __syncthreads();
-  for (int ch = threadIdx.x; ch < c; ch += kRedThreads) {
+  if (threadIdx.x < c) {
+    const int ch = threadIdx.x;
     const double g = fin[ch], gx = fin[c + ch];
-    const double inv = a.inv_std[ch];
+    const double inv = f_inv;
     const double dgamma = gx * inv;  // sum g * xhat
     const double dbeta = g;
-    const double ac = (double)a.gamma[ch] * inv;
+    const double ac = (double)f_gamma * inv;
     const double dc = ac * dgamma * inv * a.inv_m;
-    const double ec = -ac * dbeta * a.inv_m + dc * (double)a.mean[ch];
+    const double ec = -ac * dbeta * a.inv_m + dc * (double)f_mean;
     a.dgamma[ch] = (float)dgamma;
     a.dbeta[ch] = (float)dbeta;
     a.coef[ch] = (float)ac;

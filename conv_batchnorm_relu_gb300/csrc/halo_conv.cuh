@@ -133,6 +133,16 @@ __device__ __forceinline__ void reduce_scatter(float (&v)[L], int lane) {
 template <int COUT, int kThreads, int SCRATCH>
 __device__ void stats_partial_finalize(const ConvArgs& a, const float* red, uint8_t* scratch,
                                        volatile uint32_t* ticket_slot, volatile int* abort_flag) {
+  static_assert(kThreads >= COUT, "one thread per channel in the finalize");
+  // the per-channel inputs of the finalize, loaded before the ticket by every CTA (cheap) so
+  // the last one does not wait for them after its sums
+  float gm = 0.f, bt = 0.f, rm = 0.f, rv = 0.f;
+  if (threadIdx.x < COUT) {
+    gm = a.gamma[threadIdx.x];
+    bt = a.beta[threadIdx.x];
+    rm = a.running_mean[threadIdx.x];
+    rv = a.running_var[threadIdx.x];
+  }
   for (int i = threadIdx.x; i < 2 * COUT; i += kThreads) {
     const int st = i / COUT, c = i - st * COUT;
     float v = red[(0 * 2 + st) * COUT + c];
@@ -156,7 +166,8 @@ __device__ void stats_partial_finalize(const ConvArgs& a, const float* red, uint
     constexpr int kV4 = (2 * COUT) / 4;        // float4 columns of one partial
     // row groups, bounded by the scratch region (which also holds fin)
     constexpr int kRGfit = (SCRATCH - 2 * COUT * 8) / (2 * COUT * 4);
-    constexpr int kRG = kThreads / kV4 < kRGfit ? kThreads / kV4 : kRGfit;
+    constexpr int kRG1 = kThreads / kV4 < kRGfit ? kThreads / kV4 : kRGfit;
+    constexpr int kRG = kRG1 < 32 ? kRG1 : 32;  // at most the fp64 tree's width
     static_assert(kRG >= 1, "finalize scratch");
     constexpr int kLd = 16;                    // loads in flight per thread
     float* fred = reinterpret_cast<float*>(scratch);  // [kRG][2*COUT]
@@ -183,26 +194,24 @@ __device__ void stats_partial_finalize(const ConvArgs& a, const float* red, uint
       reinterpret_cast<float4*>(fred + rg * 2 * COUT)[c4] = acc;
     }
     __syncthreads();
-    for (int i = threadIdx.x; i < 2 * COUT; i += kThreads) {
-      double t = 0;
-      for (int r = 0; r < kRG; ++r) t += fred[r * 2 * COUT + i];
-      fin[i] = t;
-    }
+    // row groups combined in fp64 by a fixed pairwise tree (a dependent chain of fp64 adds is
+    // slow at this part's FP64 latency)
+    for (int i = threadIdx.x; i < 2 * COUT; i += kThreads) fin[i] = tree_sum<kRG>(fred + i, 2 * COUT);
     __syncthreads();
-    for (int c = threadIdx.x; c < COUT; c += kThreads) {
+    if (threadIdx.x < COUT) {
+      const int c = threadIdx.x;
       const double mean = fin[c] * a.inv_m;
       const double var_d = fin[COUT + c] * a.inv_m - mean * mean;
       const float var = var_d > 0.0 ? (float)var_d : 0.f;
       const float inv = rsqrtf(var + a.eps);
       const float meanf = (float)mean;
-      const float gm = a.gamma[c];
       a.saved_mean[c] = meanf;
       a.saved_inv_var[c] = inv;
       a.eq[c] = gm * inv;
-      a.eq[COUT + c] = a.beta[c] - gm * meanf * inv;
+      a.eq[COUT + c] = bt - gm * meanf * inv;
       const float mom = a.momentum;
-      a.running_mean[c] = (1.f - mom) * a.running_mean[c] + mom * meanf;
-      a.running_var[c] = (1.f - mom) * a.running_var[c] + mom * var * a.unbias;
+      a.running_mean[c] = (1.f - mom) * rm + mom * meanf;
+      a.running_var[c] = (1.f - mom) * rv + mom * var * a.unbias;
     }
   }
 }
