@@ -214,7 +214,11 @@ __global__ void __launch_bounds__(kWgThreads, 1)
           constexpr int NG = decltype(ng_c)::value;
           if constexpr (NG <= kG) {
             uint32_t acc = first ? 0u : 1u;
-            for (int kk = 0; kk < g.um / 16; ++kk) {
+            // 16-pixel K steps of a unit (um = U * 128 rows, U fixed by NOUT): a compile-time
+            // trip count, like the group count
+            constexpr int KK = (NOUT <= 64 ? 2 : 1) * 8;
+#pragma unroll 4
+            for (int kk = 0; kk < KK; ++kk) {
               const uint64_t ak = a_unit + (uint64_t)kk * 128;  // 16 pixel rows further
 #pragma unroll
               for (int gl = 0; gl < NG; ++gl) mma_f16_ss_warp(tmem_base + gl * NOUT, a_grp[gl] + ak, bd, idesc, acc);
