@@ -106,6 +106,15 @@ FIRST_CASES = {
     "first_5x5_s1": (CBRSpec("first 5x5 s1", n=2, h=20, w=33, c_in=3, c_out=32, r=5, s=5, stride=1, pad=2,
                              x_dist="uniform2.5", first_layer=True), 2010),
     "first_cfg4_n2": (CONFIGS[4].with_(n=2), 2011),
+    # Cout 64 (implicit wgrad): odd width (global-load converter) with an odd number of output
+    # rows (the last pair has no second row), and stride 1; Cout 128 (forward at 128, im2col
+    # wgrad)
+    "first_odd64_bf16": (CBRSpec("first odd 64", n=2, h=29, w=37, c_in=3, c_out=64, r=7, s=7, stride=2, pad=3,
+                                 x_dist="uniform2.5", first_layer=True, dtype="bf16"), 2012),
+    "first_s1_64": (CBRSpec("first s1 64", n=2, h=20, w=24, c_in=3, c_out=64, r=5, s=5, stride=1, pad=2,
+                            x_dist="uniform2.5", first_layer=True), 2013),
+    "first_c128": (CBRSpec("first c128", n=1, h=16, w=16, c_in=3, c_out=128, r=7, s=7, stride=2, pad=3,
+                           x_dist="uniform2.5", first_layer=True), 2014),
 }
 
 
