@@ -410,6 +410,7 @@ constexpr int kImpEpiWarp0 = 6;                       // warps 6-13: epilogue
 constexpr int kImpThreads = (kImpEpiWarp0 + 8) * 32;  // 448
 constexpr uint32_t kImpStageBytes = 32 * 128;         // one epilogue warp's staging buffer
 constexpr int kImpGroupsPerLane = 5;                  // ceil(max groups per row / 32)
+constexpr int kImpAcc = 4;                            // accumulator stages in TMEM
 
 __host__ __device__ inline uint32_t imp_align(uint32_t v) { return (v + 1023u) & ~1023u; }
 
@@ -547,7 +548,7 @@ template <int NOUT, bool BF16>
 __global__ void __launch_bounds__(kImpThreads, 1)
     first_fprop_imp_kernel(const __grid_constant__ CUtensorMap map_z, const ConvArgs a, const FirstGeom g,
                            const void* wts, const void* xin) {
-  constexpr int kTmemCols = hc::pow2_at_least(2 * NOUT);
+  constexpr int kTmemCols = hc::pow2_at_least(kImpAcc * NOUT);
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -556,9 +557,9 @@ __global__ void __launch_bounds__(kImpThreads, 1)
   const uint32_t bar0 = sbase + L.off_bar;
   const uint32_t bar_row_full = bar0, bar_row_empty = bar0 + 8 * kImpRing;
   const uint32_t bar_raw_full = bar0 + 16 * kImpRing, bar_raw_empty = bar_raw_full + 8 * kImpRaw;
-  const uint32_t bar_acc_full = bar_raw_empty + 8 * kImpRaw, bar_acc_empty = bar_acc_full + 16;
-  const uint32_t bar_drain = bar_acc_full + 32;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L.off_bar + 16 * kImpRing + 16 * kImpRaw + 40);
+  const uint32_t bar_acc_full = bar_raw_empty + 8 * kImpRaw, bar_acc_empty = bar_acc_full + 8 * kImpAcc;
+  const uint32_t bar_drain = bar_acc_empty + 8 * kImpAcc;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + (bar_drain + 8 - sbase));
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   volatile uint32_t* ticket_slot = reinterpret_cast<volatile uint32_t*>(tmem_slot + 2);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -597,7 +598,7 @@ __global__ void __launch_bounds__(kImpThreads, 1)
       mbar_init(bar_raw_full + 8 * i, 1);
       mbar_init(bar_raw_empty + 8 * i, 1);
     }
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < kImpAcc; ++i) {
       mbar_init(bar_acc_full + 8 * i, 1);
       mbar_init(bar_acc_empty + 8 * i, 8);  // lane 0 of each epilogue warp
     }
@@ -646,25 +647,31 @@ __global__ void __launch_bounds__(kImpThreads, 1)
     }
   } else if (warp < kImpConv0 + kImpConvWarps) {
     // ---------------------------------------------------------------- input-row converters
+    // Rows go round-robin to the four warps (row r to warp r mod 4), so a warp's rows r - 8 and
+    // r - 16, which last used the raw slot and the ring slot of row r, were its own and were
+    // handled before r: every parity wait below is for the phase right after one this warp
+    // has already seen (a parity wait cannot tell that phase from the one before it).
     const int cw = warp - kImpConv0;
     const uint16_t* x = static_cast<const uint16_t*>(xin);
-    int prev_n = -1, prev_p = -2;
+    int n = u_begin / g.p, p = u_begin - n * g.p, f = 0;
     uint32_t i = 0;
     bool ok = true;
-    for (int u = u_begin; u < u_end && ok && !__any_sync(0xffffffffu, hc::is_aborted(abort_flag)); ++u) {
-      const int n = u / g.p, p = u - n * g.p;
-      const int f = imp_first_new(g, prev_n, prev_p, n, p);
-      prev_n = n;
-      prev_p = p;
+    for (int u = u_begin, k = 0; u < u_end && ok; ++u, ++k) {
+      if ((k & 7) == 7 && __any_sync(0xffffffffu, hc::is_aborted(abort_flag))) break;
       for (int rr = f; rr < g.r; ++rr, ++i) {
         if ((int)(i % kImpConvWarps) != cw) continue;
         const uint32_t slot = i % kImpRing, fill = i / kImpRing, rs = i % kImpRaw;
-        bool got = mbar_wait_backoff(bar_row_empty + 8 * slot, (fill & 1) ^ 1, 32);
-        if (g.rawtma) got = got && mbar_wait_backoff(bar_raw_full + 8 * rs, (i / kImpRaw) & 1, 32);
-        if (!__all_sync(0xffffffffu, got)) {
-          hc::set_abort(abort_flag, a.err, kErrWaitHalo);
-          ok = false;
-          break;
+        // the row's two barriers tested back to back; waited for only when not complete
+        bool ready = mbar_test(bar_row_empty + 8 * slot, (fill & 1) ^ 1);
+        if (g.rawtma) ready &= mbar_test(bar_raw_full + 8 * rs, (i / kImpRaw) & 1);
+        if (!__all_sync(0xffffffffu, ready)) {
+          bool got = mbar_wait_backoff(bar_row_empty + 8 * slot, (fill & 1) ^ 1, 32);
+          if (g.rawtma) got = got && mbar_wait_backoff(bar_raw_full + 8 * rs, (i / kImpRaw) & 1, 32);
+          if (!__all_sync(0xffffffffu, got)) {
+            hc::set_abort(abort_flag, a.err, kErrWaitHalo);
+            ok = false;
+            break;
+          }
         }
         const int h = p * g.stride - g.pad + rr;
         if (g.rawtma)
@@ -678,6 +685,12 @@ __global__ void __launch_bounds__(kImpThreads, 1)
           mbar_arrive(bar_row_full + 8 * slot);
         }
       }
+      const int pn = n, pp = p;
+      if (++p == g.p) {
+        p = 0;
+        ++n;
+      }
+      f = imp_first_new(g, pn, pp, n, p);
     }
   } else if (warp == kImpMmaWarp) {
     // ---------------------------------------------------------------- MMA issuer (whole warp)
@@ -695,7 +708,7 @@ __global__ void __launch_bounds__(kImpThreads, 1)
         if ((it & 7) == 7 && __any_sync(0xffffffffu, hc::is_aborted(abort_flag))) break;
         const uint32_t inew = iend;
         iend += (uint32_t)(R - f);
-        const uint32_t s = it & 1, ph = (it >> 1) & 1;
+        const uint32_t s = it % kImpAcc, ph = (it / kImpAcc) & 1;
         // the unit's barriers are tested back to back (their latencies overlap); only one
         // that is not complete yet is then waited for
         bool ready = mbar_test(bar_acc_empty + 8 * s, ph ^ 1);
@@ -778,7 +791,7 @@ __global__ void __launch_bounds__(kImpThreads, 1)
     uint32_t iend = 0;
     uint32_t it = 0;
     for (int u = u_begin; u < u_end && !hc::is_aborted(abort_flag); ++u, ++it) {
-      const uint32_t s = it & 1, ph = (it >> 1) & 1;
+      const uint32_t s = it % kImpAcc, ph = (it / kImpAcc) & 1;
       // the store that last read this unit's staging buffer (two units ago), waited for while
       // the accumulator is still being computed
       if (lane == 0) bulk_wait_group_read<1>();
@@ -800,7 +813,7 @@ __global__ void __launch_bounds__(kImpThreads, 1)
           for (int j = 0; j < g.r - f; ++j) mbar_arrive(bar_row_empty + 8 * ((iend - g.r + j) % kImpRing));
       }
       if (half < kHalves) {
-        const uint32_t sb = stage0 + s * kImpStageBytes;
+        const uint32_t sb = stage0 + (it & 1) * kImpStageBytes;
 #pragma unroll
         for (int b = 0; b < kNB; ++b) {
           const int c0 = half * kCPH + b * kSB;
