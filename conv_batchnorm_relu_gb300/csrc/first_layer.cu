@@ -704,6 +704,7 @@ __global__ void __launch_bounds__(kImpThreads, 1)
       int n = u_begin / g.p, p = u_begin - n * g.p;
       int f = 0;  // first new filter row of the current unit (the first unit appends all R)
       uint32_t iend = 0, it = 0;
+      bool have_ready = false;  // this unit's barriers already seen complete (look-ahead)
       for (int u = u_begin; u < u_end; ++u, ++it) {
         if ((it & 7) == 7 && __any_sync(0xffffffffu, hc::is_aborted(abort_flag))) break;
         const uint32_t inew = iend;
@@ -711,9 +712,14 @@ __global__ void __launch_bounds__(kImpThreads, 1)
         const uint32_t s = it % kImpAcc, ph = (it / kImpAcc) & 1;
         // the unit's barriers are tested back to back (their latencies overlap); only one
         // that is not complete yet is then waited for
-        bool ready = mbar_test(bar_acc_empty + 8 * s, ph ^ 1);
-        for (uint32_t j = inew; j < iend; ++j) ready &= mbar_test(bar_row_full + 8 * (j % kImpRing), (j / kImpRing) & 1);
-        if (!__all_sync(0xffffffffu, ready)) {
+        bool ready = have_ready;
+        if (!ready) {
+          ready = mbar_test(bar_acc_empty + 8 * s, ph ^ 1);
+          for (uint32_t j = inew; j < iend; ++j)
+            ready &= mbar_test(bar_row_full + 8 * (j % kImpRing), (j / kImpRing) & 1);
+          ready = __all_sync(0xffffffffu, ready);
+        }
+        if (!ready) {
           bool ok = mbar_wait(bar_acc_empty + 8 * s, ph ^ 1);
           for (uint32_t j = inew; j < iend && ok; ++j)
             ok = mbar_wait(bar_row_full + 8 * (j % kImpRing), (j / kImpRing) & 1);
@@ -725,9 +731,26 @@ __global__ void __launch_bounds__(kImpThreads, 1)
         tc_fence_after();
         const uint32_t d = tmem_base + s * NOUT;
         const uint32_t row0 = iend - (uint32_t)R;
+        // the next unit
+        int n2 = n, p2 = p + 1;
+        if (p2 == g.p) {
+          p2 = 0;
+          ++n2;
+        }
+        const int f2 = imp_first_new(g, n, p, n2, p2);
+        bool ready_next = false;
         if constexpr (KR != 0 && KM != 0) {
 #pragma unroll
           for (int rr = 0; rr < KR; ++rr) {
+            if (rr == KR - 1 && u + 1 < u_end) {
+              // look-ahead: test the next unit's barriers while this unit's last MMAs queue up
+              const uint32_t s2 = (it + 1) % kImpAcc, ph2 = ((it + 1) / kImpAcc) & 1;
+              const uint32_t iend2 = iend + (uint32_t)(R - f2);
+              bool rn = mbar_test(bar_acc_empty + 8 * s2, ph2 ^ 1);
+              for (uint32_t j = iend; j < iend2; ++j)
+                rn &= mbar_test(bar_row_full + 8 * (j % kImpRing), (j / kImpRing) & 1);
+              ready_next = __all_sync(0xffffffffu, rn);
+            }
             const uint32_t arow = ring + ((row0 + rr) % kImpRing) * g.rowb;
 #pragma unroll
             for (int m = 0; m < KM; ++m)
@@ -745,12 +768,10 @@ __global__ void __launch_bounds__(kImpThreads, 1)
           }
         }
         mma_commit_warp(bar_acc_full + 8 * s);  // the epilogue also releases the unit's rows
-        const int pn = n, pp = p;
-        if (++p == g.p) {
-          p = 0;
-          ++n;
-        }
-        f = imp_first_new(g, pn, pp, n, p);
+        n = n2;
+        p = p2;
+        f = f2;
+        have_ready = ready_next;
       }
     };
     if (g.r == 7 && g.nmr == 2)
