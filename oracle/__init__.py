@@ -58,9 +58,11 @@ def _load():
             lib.cbr_oracle_out_dim.argtypes = [i, i, i, i]
             lib.cbr_oracle_out_dim.restype = i
             lib.cbr_oracle_conv2d_fwd.argtypes = conv_args + [_D, _D, _D]
+            lib.cbr_oracle_conv2d_fwd_at.argtypes = conv_args + [_D, _D, i, _I32, _D]
             lib.cbr_oracle_conv2d_dgrad.argtypes = conv_args + [_D, _D, _D]
             lib.cbr_oracle_conv2d_dgrad_at.argtypes = conv_args + [_D, _D, i, _I32, _D]
             lib.cbr_oracle_conv2d_wgrad.argtypes = conv_args + [_D, _D, _D]
+            lib.cbr_oracle_conv2d_wgrad_at.argtypes = conv_args + [_D, _D, i, _I32, _D]
             lib.cbr_oracle_bn_batch_stats.argtypes = [i64, i, _D, _D, _D]
             lib.cbr_oracle_bn_relu_fwd.argtypes = [i64, i, _D, _D, _D, _D, _D, d, _D, _D, _D, _U8]
             lib.cbr_oracle_bn_finalize.argtypes = [i, i64, _D, _D, d, d, _D, _D, _D]
@@ -111,6 +113,19 @@ def conv2d_fwd(x, w, stride: int, pad: int) -> np.ndarray:
     return z
 
 
+def conv2d_fwd_at(x, w, stride: int, pad: int, pixels) -> np.ndarray:
+    """z at the listed output pixels ((n,p,q) rows) -> [len(pixels), K]."""
+    x, w = _f64(x), _f64(w)
+    N, H, W, C = x.shape
+    K, R, S, C2 = w.shape
+    assert C == C2
+    pix = np.ascontiguousarray(np.asarray(pixels, dtype=np.int32).reshape(-1, 3))
+    out = np.empty((pix.shape[0], K), dtype=np.float64)
+    _load().cbr_oracle_conv2d_fwd_at(N, H, W, C, K, R, S, stride, pad, _p(x), _p(w),
+                                     pix.shape[0], _p(pix), _p(out))
+    return out
+
+
 def conv2d_dgrad(dz, w, in_hw: tuple[int, int], stride: int, pad: int) -> np.ndarray:
     dz, w = _f64(dz), _f64(w)
     N, P, Q, K = dz.shape
@@ -145,6 +160,20 @@ def conv2d_wgrad(dz, x, filter_rs: tuple[int, int], stride: int, pad: int) -> np
     dw = np.empty((K, R, S, C), dtype=np.float64)
     _load().cbr_oracle_conv2d_wgrad(N, H, W, C, K, R, S, stride, pad, _p(dz), _p(x), _p(dw))
     return dw
+
+
+def conv2d_wgrad_at(dz, x, filter_rs: tuple[int, int], stride: int, pad: int, taps) -> np.ndarray:
+    """dW at the listed filter taps ((k,r,s) rows) -> [len(taps), C]."""
+    dz, x = _f64(dz), _f64(x)
+    N, H, W, C = x.shape
+    N2, P, Q, K = dz.shape
+    R, S = filter_rs
+    assert N == N2 and (P, Q) == (out_dim(H, R, stride, pad), out_dim(W, S, stride, pad))
+    tap = np.ascontiguousarray(np.asarray(taps, dtype=np.int32).reshape(-1, 3))
+    out = np.empty((tap.shape[0], C), dtype=np.float64)
+    _load().cbr_oracle_conv2d_wgrad_at(N, H, W, C, K, R, S, stride, pad, _p(dz), _p(x),
+                                       tap.shape[0], _p(tap), _p(out))
+    return out
 
 
 # ----------------------------------------------------------------------------- BN steps

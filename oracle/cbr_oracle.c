@@ -65,6 +65,33 @@ void cbr_oracle_conv2d_fwd(int N, int H, int W, int C, int K, int R, int S, int 
         }
 }
 
+/* The same fprop sum, evaluated only at the listed output pixels (n,p,q triples); all K
+ * channels of each listed pixel are written to z_at[i*K + k]. */
+void cbr_oracle_conv2d_fwd_at(int N, int H, int W, int C, int K, int R, int S, int stride, int pad,
+                              const double* x, const double* w, int npix, const int32_t* pix,
+                              double* z_at) {
+  (void)N;
+#pragma omp parallel for schedule(static)
+  for (int i = 0; i < npix; ++i) {
+    const int n = pix[3 * i], p = pix[3 * i + 1], q = pix[3 * i + 2];
+    for (int k = 0; k < K; ++k) {
+      double acc = 0.0;
+      for (int r = 0; r < R; ++r) {
+        const int h = p * stride - pad + r;
+        if (h < 0 || h >= H) continue;
+        for (int s = 0; s < S; ++s) {
+          const int ww = q * stride - pad + s;
+          if (ww < 0 || ww >= W) continue;
+          const double* xp = x + (((size_t)n * H + h) * W + ww) * C;
+          const double* wp = w + (((size_t)k * R + r) * S + s) * C;
+          for (int c = 0; c < C; ++c) acc += xp[c] * wp[c];
+        }
+      }
+      z_at[(size_t)i * K + k] = acc;
+    }
+  }
+}
+
 /*
  * Input gradient of the convolution ([TR] section 5.2, DGrad):
  * dx[n,h,w,c] = sum over (k,r,s) with h = p*stride-pad+r and w = q*stride-pad+s for a
@@ -159,6 +186,34 @@ void cbr_oracle_conv2d_wgrad(int N, int H, int W, int C, int K, int R, int S, in
             }
           }
       }
+}
+
+/* The same wgrad sum for the listed filter taps only ((k,r,s) triples): all C channels of
+ * each listed tap are written to dw_at[i*C + c], summed in the (n,p,q) order of the full
+ * form. */
+void cbr_oracle_conv2d_wgrad_at(int N, int H, int W, int C, int K, int R, int S, int stride, int pad,
+                                const double* dz, const double* x, int ntap, const int32_t* tap,
+                                double* dw_at) {
+  const int P = cbr_oracle_out_dim(H, R, stride, pad);
+  const int Q = cbr_oracle_out_dim(W, S, stride, pad);
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int i = 0; i < ntap; ++i) {
+    const int k = tap[3 * i], r = tap[3 * i + 1], s = tap[3 * i + 2];
+    double* out = dw_at + (size_t)i * C;
+    for (int c = 0; c < C; ++c) out[c] = 0.0;
+    for (int n = 0; n < N; ++n)
+      for (int p = 0; p < P; ++p) {
+        const int h = p * stride - pad + r;
+        if (h < 0 || h >= H) continue;
+        for (int q = 0; q < Q; ++q) {
+          const int ww = q * stride - pad + s;
+          if (ww < 0 || ww >= W) continue;
+          const double g = dz[(((size_t)n * P + p) * Q + q) * K + k];
+          const double* xp = x + (((size_t)n * H + h) * W + ww) * C;
+          for (int c = 0; c < C; ++c) out[c] += g * xp[c];
+        }
+      }
+  }
 }
 
 /*

@@ -101,34 +101,52 @@ def mask_slack(spec, o: dict, ref: dict, rb: dict, margin: float = MASK_MARGIN) 
     N, P, Q, K = pre.shape
     a = np.asarray(o["gamma"]) * ref["inv_std"]                     # dz = a*g + ...
     dy = o["dy"]
-    v = np.where(amb, np.abs(a * dy), 0.0)                           # |delta dz| at ambiguous points
     M = N * P * Q
     s1 = np.where(amb, np.abs(dy), 0.0).reshape(-1, K).sum(0)        # bound on |delta dbeta|
     s2 = np.where(amb, np.abs(dy * ref["xhat"]), 0.0).reshape(-1, K).sum(0)  # |delta dgamma|
     xh_max = np.abs(ref["xhat"]).reshape(-1, K).max(0)
     u = a * (s1 + xh_max * s2) / M                                   # |delta dz| everywhere, per channel
-    x, w = o["x"], o["w"]
-    _, H, W, C = x.shape
-    R, S = w.shape[1], w.shape[2]
-    st, pad = spec.stride, spec.pad
-    dx_sl = np.zeros_like(x)
-    dw_sl = np.zeros_like(w)
     idx = np.argwhere(amb)
-    vals = v[amb]
+    vals = np.abs(a[idx[:, 3]] * dy[amb])                            # |delta dz| at ambiguous points
+    sl = mask_slack_core(idx, vals, u, o["x"], o["w"], spec.stride, spec.pad)
+    return dict(dx=sl["dx"], dw=sl["dw"], dbeta=s1, dgamma=s2, count=int(amb.sum()))
+
+
+def mask_slack_core(idx, vals, u, x, w, stride: int, pad: int, taps=None, pixels=None) -> dict:
+    """Propagate per-point dz changes through both backward convolutions.
+
+    idx: (n, p, q, k) rows of the ambiguous output points; vals: the bound on |delta dz| at
+    each; u[k]: the bound on |delta dz| at every point of channel k (through dbeta/dgamma).
+    Returns the dx bound (all input pixels, or the listed (n, h, w) pixels; None when neither
+    pixels nor a full dx is wanted, i.e. taps given without pixels) and the dW bound (all taps,
+    or the listed (k, r, s) taps)."""
+    _, H, W, C = x.shape
+    K, R, S = w.shape[0], w.shape[1], w.shape[2]
+    want_dx = pixels is not None or taps is None
+    dx_sl = np.zeros_like(x) if want_dx else None
+    dw_sl = np.zeros_like(w)
     aw, ax = np.abs(w), np.abs(x)
     for r in range(R):
         for s_ in range(S):
-            h = idx[:, 1] * st - pad + r
-            ww = idx[:, 2] * st - pad + s_
+            h = idx[:, 1] * stride - pad + r
+            ww = idx[:, 2] * stride - pad + s_
             ok = (h >= 0) & (h < H) & (ww >= 0) & (ww < W)
             n_, k_ = idx[ok, 0], idx[ok, 3]
             vv = vals[ok][:, None]
-            np.add.at(dx_sl, (n_, h[ok], ww[ok]), vv * aw[k_, r, s_, :])
+            if want_dx:
+                np.add.at(dx_sl, (n_, h[ok], ww[ok]), vv * aw[k_, r, s_, :])
             np.add.at(dw_sl[:, r, s_, :], k_, vv * ax[n_, h[ok], ww[ok], :])
     # second order: every dz of channel k may move by u[k]
-    dx_sl += (u[:, None] * aw.reshape(K, -1, C).sum(1)).sum(0)[None, None, None, :]
+    if want_dx:
+        dx_sl += (u[:, None] * aw.reshape(K, -1, C).sum(1)).sum(0)[None, None, None, :]
     dw_sl += u[:, None, None, None] * ax.reshape(-1, C).sum(0)[None, None, None, :]
-    return dict(dx=dx_sl, dw=dw_sl, dbeta=s1, dgamma=s2, count=int(amb.sum()))
+    if pixels is not None:
+        pixels = np.asarray(pixels)
+        dx_sl = dx_sl[pixels[:, 0], pixels[:, 1], pixels[:, 2]]
+    if taps is not None:
+        taps = np.asarray(taps)
+        dw_sl = dw_sl[taps[:, 0], taps[:, 1], taps[:, 2]]
+    return dict(dx=dx_sl, dw=dw_sl)
 
 
 def max_err_ok_slack(got, ref, slack, name: str) -> float:

@@ -283,6 +283,23 @@ def test_dgrad_at_matches_full_dgrad():
         assert np.array_equal(at[i], full[n, h, ww])
 
 
+def test_fwd_at_and_wgrad_at_match_full_forms():
+    """The sampled fprop and wgrad evaluate the same sums as the full forms (stride 2 with
+    padding, so out-of-range taps and strided rows are exercised)."""
+    x, w, gamma, beta = _rand_case(18, 2, 9, 11, 3, 8, 5, 5)
+    full = oracle.conv2d_fwd(x, w, 2, 2)
+    pix = [(0, 0, 0), (1, full.shape[1] - 1, full.shape[2] - 1), (0, 2, 3), (1, 0, full.shape[2] - 1)]
+    at = oracle.conv2d_fwd_at(x, w, 2, 2, pix)
+    for i, (n, p, q) in enumerate(pix):
+        assert np.array_equal(at[i], full[n, p, q])
+    dz = _rng(19).standard_normal(full.shape)
+    dw = oracle.conv2d_wgrad(dz, x, (5, 5), 2, 2)
+    taps = [(0, 0, 0), (7, 4, 4), (3, 2, 1), (5, 0, 4)]
+    at = oracle.conv2d_wgrad_at(dz, x, (5, 5), 2, 2, taps)
+    for i, (k, r, s_) in enumerate(taps):
+        assert np.array_equal(at[i], dw[k, r, s_])
+
+
 # ------------------------------------------------------------------- mutation tests
 def test_pins_reject_planted_mistakes():
     """Plant plausible oracle mistakes on the CPU and check that a pin rejects each."""
