@@ -235,6 +235,47 @@ def traffic_for(kernel: str, config_index: int):
     return ent.get("bytes_per_launch")
 
 
+def time_inference(spec, layer, g, flush, stream, K, peaks) -> dict:
+    """The folded inference path: cbr_fold_bn once (untimed), then cbr_forward_infer timed as a
+    replayed CUDA graph [L2 flush, event, infer, event], like the training step."""
+    from conv_batchnorm_relu_gb300 import cbr
+    w_fold, b_fold = cbr.fold_bn(layer, g["w"], g["gamma"], g["beta"], g["running_mean"],
+                                 g["running_var"], spec.eps)
+    y = torch.empty((spec.n, spec.p, spec.q, spec.c_out), dtype=spec.torch_dtype, device=g["x"].device)
+    for _ in range(3):
+        cbr.forward_infer(layer, g["x"], w_fold, b_fold, out=y)
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    cap = torch.cuda.Stream()
+    cap.wait_stream(stream)
+    with torch.cuda.graph(graph, stream=cap, capture_error_mode="thread_local"):
+        flush.zero_()
+        record_external(t0, torch.cuda.current_stream())
+        cbr.forward_infer(layer, g["x"], w_fold, b_fold, out=y)
+        record_external(t1, torch.cuda.current_stream())
+    torch.cuda.synchronize()
+    for _ in range(3):
+        graph.replay()
+    torch.cuda.synchronize()
+    ms = 0.0
+    for _ in range(K):
+        graph.replay()
+        torch.cuda.synchronize()
+        ms += t0.elapsed_time(t1)
+    cbr.stream_status()
+    ms /= K
+    p = roofline.infer_pass(spec)
+    roof_us, bound = p.roof_us(peaks, sustained=True)
+    t_s = ms * 1e-3
+    return {"us": round(ms * 1e3, 2), "images_per_s": spec.n / t_s, "tflops": p.flops / t_s / 1e12,
+            "gbs": p.bytes / t_s / 1e9, "roof_us": round(roof_us, 2), "bound": bound,
+            "frac": round(roof_us / (ms * 1e3), 4), "launches_per_call": 1,
+            "note": "cbr_forward_infer alone (fold done once before timing), L2 flushed before each call"}
+
+
 def run_cbr(args, world, rank, local):
     from conv_batchnorm_relu_gb300 import build, cbr
     build.build()
@@ -458,6 +499,8 @@ def run_cbr(args, world, rank, local):
         "clocks": clocks,
         "wall_s_timed": round(t_wall, 3),
     }
+    if spec.infer:
+        line["infer"] = time_inference(spec, layer, g, flush, stream, K, peaks)
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = oracle_images_per_s(spec, budget_s=15.0, max_images=spec.n)
     print(json.dumps(line), flush=True)

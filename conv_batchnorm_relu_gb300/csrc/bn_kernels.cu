@@ -215,10 +215,17 @@ __global__ void __launch_bounds__(kRedThreads)
   }
 }
 
-// dz = a*g - d*z + e with g = dy*mask, written to HBM (used when no dgrad kernel produces it).
+__device__ __forceinline__ uint32_t fastdiv(uint32_t n, const FastDiv& f) {
+  const uint32_t t = __umulhi(f.m, n);
+  return (t + ((n - t) >> f.s1)) >> f.s2;
+}
+
+// dz = a*g - d*z + e with g = dy*mask, written to HBM once for both backward convolutions.
 // Sweeps last element first: the reduction before it read dy and z first to last, so their
-// ends are what the L2 still holds.
-template <bool BF16, bool MASKBITS>
+// ends are what the L2 still holds.  PAD: dz rows are stored with a pitch of a.pitch pixels
+// (the padded-linear row space of the halo convolutions) and the thread holding an image
+// row's last pixel also zeroes the row's pitch - q trailing pixels of its channel vector.
+template <bool BF16, bool MASKBITS, bool PAD>
 __global__ void __launch_bounds__(kApplyThreads)
     dz_kernel(const DzArgs a) {
   __shared__ float s_coef[3 * 256];
@@ -249,7 +256,15 @@ __global__ void __launch_bounds__(kApplyThreads)
     for (int k = 0; k < kApplyUnroll; ++k) {
       const long long v = nvec - 1 - (v0 + k * stride);
       if (v >= 0) {
-        const int c0 = (int)(v % cvec) * 8;
+        // PAD: v < 2^31 (checked by the launcher), so the index math runs in 32 bits
+        uint32_t pix = 0, cv;
+        if (PAD) {
+          pix = fastdiv((uint32_t)v, a.fd_cvec);
+          cv = (uint32_t)v - pix * a.fd_cvec.d;
+        } else {
+          cv = (uint32_t)(v % cvec);
+        }
+        const int c0 = (int)cv * 8;
         uint32_t bits;
         if (MASKBITS) {
           bits = mb[k];
@@ -277,7 +292,17 @@ __global__ void __launch_bounds__(kApplyThreads)
           const float r1 = fmaf(s_coef[c + 1], g1, fmaf(-s_coef[a.c + c + 1], z.y, s_coef[2 * a.c + c + 1]));
           o[j] = pack2<BF16>(r0, r1);
         }
-        st_global_v4(ob + v * 16, make_uint4(o[0], o[1], o[2], o[3]));
+        if (PAD) {
+          const uint32_t row = fastdiv(pix, a.fd_q);
+          const uint32_t qq = pix - row * a.fd_q.d;
+          const uint32_t dv32 = (row * (uint32_t)a.pitch + qq) * a.fd_cvec.d + cv;
+          st_global_v4(ob + (size_t)dv32 * 16, make_uint4(o[0], o[1], o[2], o[3]));
+          if (qq == a.fd_q.d - 1)
+            for (uint32_t t = 1; t <= (uint32_t)(a.pitch - a.q); ++t)
+              st_global_v4(ob + (size_t)(dv32 + t * a.fd_cvec.d) * 16, make_uint4(0u, 0u, 0u, 0u));
+        } else {
+          st_global_v4(ob + v * 16, make_uint4(o[0], o[1], o[2], o[3]));
+        }
       }
     }
   }
@@ -309,19 +334,29 @@ int stream_grid(K kern, int threads, long long work_items, int num_sms) {
   return (int)std::min<long long>(want, (long long)num_sms * resident_blocks(kern, threads));
 }
 
-int launch_dz(const DzArgs& a, bool bf16, int num_sms, cudaStream_t st) {
-  if (a.c % 8 != 0 || a.c > 256) return 3;
+int launch_dz(const DzArgs& a_in, bool bf16, int num_sms, cudaStream_t st) {
+  DzArgs a = a_in;
+  if (a.c % 8 != 0 || a.c > 256 || a.q < 1 || a.pitch < a.q) return 3;
   const long long nvec = a.total / 8;
   const bool bits = a.mask != nullptr;
+  const bool pad = a.pitch != a.q;
+  // padded stores index in 32 bits: every vector of the padded tensor must fit
+  if (pad && nvec / a.q * a.pitch >= (1ll << 31)) return 3;
+  a.fd_cvec = make_fastdiv((uint32_t)(a.c / 8));
+  a.fd_q = make_fastdiv((uint32_t)a.q);
   auto go = [&](auto kern) {
     kern<<<stream_grid(kern, kApplyThreads, nvec / kApplyUnroll, num_sms), kApplyThreads, 0, st>>>(a);
   };
-  if (bf16) {
-    if (bits) go(dz_kernel<true, true>);
-    else go(dz_kernel<true, false>);
-  } else {
-    if (bits) go(dz_kernel<false, true>);
-    else go(dz_kernel<false, false>);
+  const int sel = (bf16 ? 4 : 0) + (bits ? 2 : 0) + (pad ? 1 : 0);
+  switch (sel) {
+    case 0: go(dz_kernel<false, false, false>); break;
+    case 1: go(dz_kernel<false, false, true>); break;
+    case 2: go(dz_kernel<false, true, false>); break;
+    case 3: go(dz_kernel<false, true, true>); break;
+    case 4: go(dz_kernel<true, false, false>); break;
+    case 5: go(dz_kernel<true, false, true>); break;
+    case 6: go(dz_kernel<true, true, false>); break;
+    default: go(dz_kernel<true, true, true>); break;
   }
   return cudaGetLastError() == cudaSuccess ? 0 : 6;
 }

@@ -154,6 +154,16 @@ FwdWs fwd_ws(const Shape& s, bool need_z) {
   L.total = need_z ? align_up(L.z + act_bytes(s.n, s.p, s.q, s.cout, s.elt), 256) : L.z;
   return L;
 }
+// Row pitch (pixels) of the materialised dz.  The halo convolutions read it in their
+// padded-linear row space (pitch w + 2*pad, the columns past q zero), so a unit's dz tile is
+// one contiguous run of rows; the first layer's wgrad reads plain [n][p][q] rows.
+long long dz_pitch(const Shape& s) { return is_first_layer(s) ? s.q : s.w + 2 * s.pad; }
+
+// Whether dz can be materialised: the padded dz kernel indexes vectors in 32 bits.
+bool dz_materialisable(const Shape& s) {
+  return is_first_layer(s) || s.n * s.p * dz_pitch(s) * (s.cout / 8) < (1ll << 31);
+}
+
 struct BwdWs {
   size_t coef, part, wpart, dz, z, total;
 };
@@ -165,7 +175,7 @@ BwdWs bwd_ws(const Shape& s, bool need_z) {
   const size_t wpart = is_first_layer(s) ? first_wgrad_partial_floats(kMaxCtas, (int)s.cout)
                                          : wgrad_partial_floats(kMaxCtas, (int)s.cin, (int)s.cout, (int)(s.r * s.s));
   L.dz = align_up(L.wpart + wpart * sizeof(float), 256);
-  L.z = align_up(L.dz + act_bytes(s.n, s.p, s.q, s.cout, s.elt), 256);  // dz materialised for wgrad
+  L.z = align_up(L.dz + act_bytes(s.n, s.p, dz_pitch(s), s.cout, s.elt), 256);  // materialised dz
   L.total = need_z ? align_up(L.z + act_bytes(s.n, s.p, s.q, s.cout, s.elt), 256) : L.z;
   return L;
 }
@@ -440,8 +450,9 @@ cbr_status_t cbr_backward(const cbr_desc_t* desc, const void* dy, const void* x,
   if (st) return (cbr_status_t)st;
   prof.mark();
 
-  // dz = a*(dy*mask) - d*z + e is materialised once when the TMA-fed wgrad can use it.
-  const bool dz_tma = is_first_layer(s) || wgrad_dz_tma_fits(make_geom(s), (int)s.cout);
+  // dz = a*(dy*mask) - d*z + e is materialised once and read by TMA in both convolutions.
+  const bool dz_tma = dz_materialisable(s);
+  const bool wgrad_tma = dz_tma && (is_first_layer(s) || wgrad_dz_tma_fits(make_geom(s), (int)s.cout));
   void* dz_buf = wsb + L.dz;
   if (dz_tma) {
     DzArgs za{};
@@ -453,6 +464,8 @@ cbr_status_t cbr_backward(const cbr_desc_t* desc, const void* dy, const void* x,
     za.dz = dz_buf;
     za.total = s.m * s.cout;
     za.c = (int)s.cout;
+    za.q = (int)s.q;
+    za.pitch = (int)dz_pitch(s);
     st = launch_dz(za, s.bf16, dev->num_sms, cs);
     if (st) return (cbr_status_t)st;
     prof.mark();
@@ -471,7 +484,7 @@ cbr_status_t cbr_backward(const cbr_desc_t* desc, const void* dy, const void* x,
   // WGrad first, then DGrad (CBR page, section 5.2 orders DGrad after WGrad because its dX
   // overwrote X there; here dx may not alias x, so the order is only kept for familiarity).
   WgradArgs wa{};
-  wa.dz_full = dz_tma ? dz_buf : nullptr;
+  wa.dz_full = wgrad_tma ? dz_buf : nullptr;
   wa.g = make_geom(s);
   wa.dy = dy;
   wa.z = z;
@@ -502,6 +515,7 @@ cbr_status_t cbr_backward(const cbr_desc_t* desc, const void* dy, const void* x,
     da.coef = coef;
     da.dx = dx;
     da.dz_full = dz_tma ? dz_buf : nullptr;
+    da.dz_pitch = (int)dz_pitch(s);
     da.err = dev->err;
     st = launch_dgrad(da, (int)s.cin, (int)s.cout, s.bf16, w, dev->num_sms, cs);
     if (st) return (cbr_status_t)st;

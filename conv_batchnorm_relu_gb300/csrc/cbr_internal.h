@@ -127,7 +127,8 @@ struct DgradArgs {
   const uint8_t* mask;
   const float* coef;
   void* dx;
-  const void* dz_full;      // materialised dz [n][p][q][cout], or null to compute it in-kernel
+  const void* dz_full;      // materialised dz [n][p][dz_pitch][cout], or null to compute it in-kernel
+  int dz_pitch;             // row pitch of dz_full in pixels (>= q, zero beyond q)
   uint32_t* err;
 };
 // MMA N width used for `c` output channels: the next of 16, 32, 64, 128.
@@ -144,11 +145,27 @@ struct WgradArgs {
   const float* coef;
   float* part;              // [grid][taps*cin][cout] per-CTA partial dW
   float* dw;                // [cout][r][s][cin]
-  const void* dz_full;      // materialised dz [n][p][q][cout], or null to compute it in-kernel
+  // materialised dz [n][p][wp][cout] in the padded-linear row layout of the forward geometry
+  // (row pitch wp = w + 2*pad, columns q..wp-1 zero), or null to compute it in-kernel
+  const void* dz_full;
   uint32_t* err;
 };
 // Whether the TMA-fed wgrad (dz read from HBM) fits shared memory for this geometry.
 bool wgrad_dz_tma_fits(const HaloGeom& g, int c_out);
+
+// Unsigned 32-bit division by a run-time invariant divisor through a multiply-high
+// (Granlund and Montgomery, "Division by invariant integers using multiplication", PLDI 1994,
+// the round-up method): n / d = (t + ((n - t) >> s1)) >> s2 with t = umulhi(m, n), exact for
+// every 32-bit n and 1 <= d < 2^31.
+struct FastDiv {
+  uint32_t d, m, s1, s2;
+};
+inline FastDiv make_fastdiv(uint32_t d) {
+  uint32_t l = 0;
+  while ((1ull << l) < d) ++l;
+  const uint64_t m = ((1ull << 32) * ((1ull << l) - d)) / d + 1;
+  return FastDiv{d, (uint32_t)m, l ? 1u : 0u, l ? l - 1 : 0u};
+}
 
 struct DzArgs {
   const void* dy;
@@ -156,9 +173,12 @@ struct DzArgs {
   const void* y;            // mask source when mask == null (y > 0)
   const uint8_t* mask;
   const float* coef;        // [3][c]
-  void* dz;                 // [m][c] output, storage dtype
-  long long total;          // elements
+  void* dz;                 // output, storage dtype: [n][p][pitch][c] (see below)
+  long long total;          // elements of dy / z (n*p*q*c)
   int c;
+  int q;                    // output columns of one image row
+  int pitch;                // dz row pitch in pixels (>= q); columns q..pitch-1 are written as zero
+  FastDiv fd_cvec, fd_q;    // division by c/8 and by q (set by the launcher)
 };
 // dz = a*(dy*mask) - d*z + e, elementwise (bn_kernels.cu).
 int launch_dz(const DzArgs& a, bool bf16, int num_sms, cudaStream_t st);

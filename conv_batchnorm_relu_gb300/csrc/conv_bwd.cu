@@ -73,19 +73,16 @@ bool make_plan(WgPlan& P, int taps, int c_in, int nout) {
 
 struct WgLayout {
   uint32_t halo_stride, dz_sub, dz_stride, off_dz, off_bar, total;
-  int dz_rows;  // image rows per dz tile when dz is loaded by TMA
 };
 
-// dz tile rows when dz comes from HBM: the unit's um padded-linear rows start at column
-// offset < wp of its first image row.
-__host__ __device__ inline int wg_dz_rows(const HaloGeom& g) { return (g.wp - 1 + g.um + g.wp - 1) / g.wp; }
-
-__host__ __device__ inline WgLayout wg_layout(const HaloGeom& g, int nout, bool dztma) {
+// The dz tile of a unit is its um padded-linear rows, 64 channels per sub-tile: built by the
+// producer warps, or loaded by TMA from a dz materialised in the same padded-linear row layout
+// (the rows past the last image row read as zero).
+__host__ __device__ inline WgLayout wg_layout(const HaloGeom& g, int nout) {
   WgLayout L;
   L.halo_stride = (((uint32_t)g.hr * g.wp * 128) + 1023u) & ~1023u;
   const int nkc = nout > 64 ? nout / 64 : 1;
-  L.dz_rows = wg_dz_rows(g);
-  L.dz_sub = dztma ? (((uint32_t)L.dz_rows * g.wp * 128 + 1023u) & ~1023u) : (uint32_t)g.um * 128;
+  L.dz_sub = (uint32_t)g.um * 128;
   L.dz_stride = (uint32_t)nkc * L.dz_sub;
   L.off_dz = 2 * L.halo_stride;
   L.off_bar = L.off_dz + 2 * L.dz_stride;
@@ -105,7 +102,7 @@ __global__ void __launch_bounds__(kWgThreads, 1)
                                              ~static_cast<uintptr_t>(1023));
   const HaloGeom& g = a.g;
   const WgPlan& P = a.plan;
-  const WgLayout L = wg_layout(g, NOUT, DZTMA);
+  const WgLayout L = wg_layout(g, NOUT);
   const uint32_t sbase = smem_u32(smem);
   const uint32_t x_addr = sbase, dz_addr = sbase + L.off_dz;
   const uint32_t bar0 = sbase + L.off_bar;
@@ -148,8 +145,7 @@ __global__ void __launch_bounds__(kWgThreads, 1)
     if (lane == 0) {
       prefetch_tensormap(&map_x);
       if (DZTMA) prefetch_tensormap(&map_dz);
-      const uint32_t tx = (uint32_t)g.hr * g.wp * 128 +
-                          (DZTMA ? (uint32_t)kNkc * L.dz_rows * g.wp * 128 : 0u);
+      const uint32_t tx = (uint32_t)g.hr * g.wp * 128 + (DZTMA ? (uint32_t)kNkc * L.dz_sub : 0u);
       uint32_t it = 0;
       for (int u = ustart; u < g.total_units && !hc::is_aborted(abort_flag); u += ustride, ++it) {
         const int n = u / g.upi;
@@ -166,7 +162,7 @@ __global__ void __launch_bounds__(kWgThreads, 1)
                       m0 / g.wp - g.pad + r0, n, bar_x_full + 8 * s);
         if (DZTMA)
           for (int kc = 0; kc < kNkc; ++kc)
-            tma_load_4d(dz_addr + s * L.dz_stride + kc * L.dz_sub, &map_dz, kc * 64, 0, m0 / g.wp, n,
+            tma_load_3d(dz_addr + s * L.dz_stride + kc * L.dz_sub, &map_dz, kc * 64, m0, n,
                         bar_x_full + 8 * s);
       }
       for (uint32_t k = (it > 2 ? it - 2 : 0); k < it; ++k)
@@ -207,7 +203,7 @@ __global__ void __launch_bounds__(kWgThreads, 1)
         const uint32_t xh = x_addr + s * L.halo_stride;
         const uint32_t dzs = dz_addr + s * L.dz_stride;
         const uint64_t a_unit = (uint64_t)((xh + (uint32_t)off * 128u) >> 4);
-        uint64_t bd = make_sw128_desc(dzs + (DZTMA ? (uint32_t)off * 128u : 0u), L.dz_sub, 1024, 0);
+        uint64_t bd = make_sw128_desc(dzs, L.dz_sub, 1024, 0);
         // The group count is fixed per CTA: dispatch once per unit to a loop with a
         // compile-time trip count (a runtime guard around each MMA slows issue ~2x).
         auto issue = [&](auto ng_c) {
@@ -374,7 +370,7 @@ bool wgrad_dz_tma_fits(const HaloGeom& g_in, int c_out) {
   HaloGeom g = g_in;
   const int nout = nout_for(c_out);
   if (nout != c_out || !hc::finish_geom(g, nout <= 64 ? 2 : 1)) return false;
-  return wg_layout(g, nout, true).total + 1024 <= 227 * 1024;
+  return wg_layout(g, nout).total + 1024 <= 227 * 1024;
 }
 
 int launch_wgrad(const WgradArgs& w, int c_in, int c_out, bool bf16, const void* x, int num_sms,
@@ -393,7 +389,7 @@ int launch_wgrad(const WgradArgs& w, int c_in, int c_out, bool bf16, const void*
   const int taps = a.g.r * a.g.s;
   if (!make_plan(a.plan, taps, c_in, nout)) return 3;
   const bool dztma = w.dz_full != nullptr;
-  const WgLayout L = wg_layout(a.g, nout, dztma);
+  const WgLayout L = wg_layout(a.g, nout);
   const uint32_t smem = L.total + 1024;
   if (smem > 227 * 1024) return 3;
   const CUtensorMapDataType dt = bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
@@ -407,10 +403,12 @@ int launch_wgrad(const WgradArgs& w, int c_in, int c_out, bool bf16, const void*
   }
   CUtensorMap mdz{};
   if (dztma) {
-    const uint64_t dims[4] = {(uint64_t)c_out, (uint64_t)g.q, (uint64_t)g.p, (uint64_t)g.n_img};
-    const uint64_t strides[3] = {(uint64_t)c_out * 2, (uint64_t)g.q * c_out * 2, (uint64_t)g.p * g.q * c_out * 2};
-    const uint32_t box[4] = {64, (uint32_t)g.wp, (uint32_t)L.dz_rows, 1};
-    if (!encode_tiled(&mdz, dt, 4, w.dz_full, dims, strides, box)) return 6;
+    // [n][p*wp][cout]: the unit's um padded-linear rows are one box
+    const uint64_t rows = (uint64_t)g.p * g.wp;
+    const uint64_t dims[3] = {(uint64_t)c_out, rows, (uint64_t)g.n_img};
+    const uint64_t strides[2] = {(uint64_t)c_out * 2, rows * c_out * 2};
+    const uint32_t box[3] = {64, (uint32_t)g.um, 1};
+    if (!encode_tiled(&mdz, dt, 3, w.dz_full, dims, strides, box)) return 6;
   }
   // every CTA gets at least one unit, so every partial it writes is initialised
   const int per_split = std::max(1, std::min(num_sms / a.plan.nsplit, g.total_units));

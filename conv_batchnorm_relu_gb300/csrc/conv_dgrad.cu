@@ -28,8 +28,12 @@ int launch_dgrad(const DgradArgs& d, int c_in, int c_out, bool bf16, const void*
   const CUtensorMapDataType dt = bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
   CUtensorMap mx{}, mw;  // mx: the materialised dz, when there is one
   if (d.dz_full) {
-    const uint64_t dims[4] = {(uint64_t)c_out, (uint64_t)g.w, (uint64_t)g.h, (uint64_t)g.n_img};
-    const uint64_t strides[3] = {(uint64_t)c_out * 2, (uint64_t)g.w * c_out * 2, (uint64_t)g.h * g.w * c_out * 2};
+    // dz rows have a pitch of dz_pitch >= q pixels, zero past q: the halo's right padding reads
+    // those zeros (or the out-of-bounds fill past the pitch), its left padding the fill
+    const uint64_t pitch = (uint64_t)d.dz_pitch;
+    if (pitch < (uint64_t)g.w) return 3;
+    const uint64_t dims[4] = {(uint64_t)c_out, pitch, (uint64_t)g.h, (uint64_t)g.n_img};
+    const uint64_t strides[3] = {(uint64_t)c_out * 2, pitch * c_out * 2, (uint64_t)g.h * pitch * c_out * 2};
     const uint32_t box[4] = {64, (uint32_t)g.wp, (uint32_t)g.box_rows, 1};
     if (!encode_tiled(&mx, dt, 4, d.dz_full, dims, strides, box)) return 6;
   }

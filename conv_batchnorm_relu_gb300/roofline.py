@@ -61,6 +61,15 @@ def ledger(spec, need_dx: bool = True) -> list[Pass]:
     return passes
 
 
+def infer_pass(spec) -> Pass:
+    """Folded inference: x and W_fold in, y out (bias + ReLU in the conv epilogue)."""
+    e = 2
+    x = spec.n * spec.h * spec.w * spec.c_in * e
+    y = spec.n * spec.p * spec.q * spec.c_out * e
+    w = spec.c_out * spec.r * spec.s * spec.c_in * e
+    return Pass("conv_infer", x + w + y + spec.c_out * 4, spec.conv_flops())
+
+
 def step_roof_us(spec, peaks: dict, need_dx: bool = True, sustained: bool = True) -> float:
     return sum(p.roof_us(peaks, sustained)[0] for p in ledger(spec, need_dx))
 
