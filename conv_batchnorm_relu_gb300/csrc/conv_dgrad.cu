@@ -21,10 +21,16 @@ int launch_dgrad(const DgradArgs& d, int c_in, int c_out, bool bf16, const void*
   const int nch = (c_out + 63) / 64;
   const int nout = nout_for(c_in);
   if (nch > 2 || c_in > 128) return 3;
-  const int U = nout <= 64 ? 2 : 1;
+  // two M tiles per unit wherever the streamed-filter layout fits (see launch_fprop)
+  int U = 2;
   HaloGeom& g = a.g;
   if (!hc::finish_geom(g, U)) return 3;
-  const bool wres = hc::layout(g, kKindDgrad, nch, nout, true).total + 1024 <= 227 * 1024;
+  if (nout > 64 && hc::layout(g, kKindDgrad, nch, nout, false).total + 1024 > 227 * 1024) {
+    U = 1;
+    g = d.g;
+    if (!hc::finish_geom(g, U)) return 3;
+  }
+  bool wres = hc::layout(g, kKindDgrad, nch, nout, true).total + 1024 <= 227 * 1024;
   const CUtensorMapDataType dt = bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
   CUtensorMap mx{}, mw;  // mx: the materialised dz, when there is one
   if (d.dz_full) {
@@ -52,15 +58,20 @@ int launch_dgrad(const DgradArgs& d, int c_in, int c_out, bool bf16, const void*
     return d.dz_full ? CBR_DGRAD_KIND(kKindDgradTma, NCH_, NOUT_, U_, WRES_)                    \
                      : CBR_DGRAD_KIND(kKindDgrad, NCH_, NOUT_, U_, WRES_);                      \
   }
-  CBR_DGRAD_CASE(1, 16, 2, true)
-  CBR_DGRAD_CASE(1, 32, 2, true)
-  CBR_DGRAD_CASE(1, 64, 2, true)
-  CBR_DGRAD_CASE(1, 16, 2, false)
-  CBR_DGRAD_CASE(1, 32, 2, false)
-  CBR_DGRAD_CASE(1, 64, 2, false)
-  CBR_DGRAD_CASE(2, 64, 2, false)
-  CBR_DGRAD_CASE(1, 128, 1, false)
-  CBR_DGRAD_CASE(2, 128, 1, false)
+  // a resident filter where an instantiation has one, else the streamed filter
+  for (int pass = 0; pass < 2; ++pass, wres = false) {
+    CBR_DGRAD_CASE(1, 16, 2, true)
+    CBR_DGRAD_CASE(1, 32, 2, true)
+    CBR_DGRAD_CASE(1, 64, 2, true)
+    CBR_DGRAD_CASE(1, 16, 2, false)
+    CBR_DGRAD_CASE(1, 32, 2, false)
+    CBR_DGRAD_CASE(1, 64, 2, false)
+    CBR_DGRAD_CASE(2, 64, 2, false)
+    CBR_DGRAD_CASE(1, 128, 2, false)
+    CBR_DGRAD_CASE(2, 128, 2, false)
+    CBR_DGRAD_CASE(1, 128, 1, false)
+    CBR_DGRAD_CASE(2, 128, 1, false)
+  }
 #undef CBR_DGRAD_CASE
 #undef CBR_DGRAD_KIND
   return 3;

@@ -37,9 +37,17 @@ int launch_fprop(const FpropArgs& f, int c_in, int c_out, bool bf16, const void*
   HaloGeom& g = a.g;
   const int nch = c_in <= 64 ? 1 : (c_in <= 128 ? 2 : 0);
   if (nch == 0) return 3;
-  const int U = c_out <= 64 ? 2 : 1;
+  // Two M tiles per unit (um = 256 rows) wherever they fit: at 128 output channels that is all
+  // 512 TMEM columns (two accumulator stages) and needs the streamed-filter layout to fit smem;
+  // each filter slab then feeds twice the MMAs.
+  int U = 2;
   if (!hc::finish_geom(g, U)) return 3;
-  const bool wres = hc::layout(g, kKindFprop, nch, c_out, true).total + 1024 <= 227 * 1024;
+  if (c_out > 64 && hc::layout(g, kKindFprop, nch, c_out, false).total + 1024 > 227 * 1024) {
+    U = 1;
+    g = f.g;
+    if (!hc::finish_geom(g, U)) return 3;
+  }
+  bool wres = hc::layout(g, kKindFprop, nch, c_out, true).total + 1024 <= 227 * 1024;
 
   const CUtensorMapDataType dt = bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
   CUtensorMap mx, mw;
@@ -62,14 +70,19 @@ int launch_fprop(const FpropArgs& f, int c_in, int c_out, bool bf16, const void*
     return bf16 ? hc::launch_halo_conv<kKindFprop, NCH_, COUT_, U_, WRES_, true>(a, mx, mw, grid, st) \
                 : hc::launch_halo_conv<kKindFprop, NCH_, COUT_, U_, WRES_, false>(a, mx, mw, grid, st); \
   }
-  CBR_FPROP_CASE(1, 16, 2, true)
-  CBR_FPROP_CASE(1, 32, 2, true)
-  CBR_FPROP_CASE(1, 64, 2, true)
-  CBR_FPROP_CASE(1, 64, 2, false)
-  CBR_FPROP_CASE(1, 128, 1, true)
-  CBR_FPROP_CASE(1, 128, 1, false)
-  CBR_FPROP_CASE(2, 64, 2, false)
-  CBR_FPROP_CASE(2, 128, 1, false)
+  // a resident filter where an instantiation has one, else the streamed filter
+  for (int pass = 0; pass < 2; ++pass, wres = false) {
+    CBR_FPROP_CASE(1, 16, 2, true)
+    CBR_FPROP_CASE(1, 32, 2, true)
+    CBR_FPROP_CASE(1, 64, 2, true)
+    CBR_FPROP_CASE(1, 64, 2, false)
+    CBR_FPROP_CASE(1, 128, 2, false)
+    CBR_FPROP_CASE(1, 128, 1, true)
+    CBR_FPROP_CASE(1, 128, 1, false)
+    CBR_FPROP_CASE(2, 64, 2, false)
+    CBR_FPROP_CASE(2, 128, 2, false)
+    CBR_FPROP_CASE(2, 128, 1, false)
+  }
 #undef CBR_FPROP_CASE
   return 3;
 }

@@ -12,7 +12,7 @@
 //   warps A+2 .. A+9   epilogue, two warps per TMEM lane quadrant (each takes half of the
 //                      columns): TMEM -> registers -> staged tile -> stats / store
 // Pipelines: 2 halo stages, 2 TMEM accumulator stages (U*NOUT fp32 columns each), and a
-// 2-deep filter ring when the filter is streamed.  All waits are bounded (ptx.cuh).
+// 3-deep filter ring when the filter is streamed.  All waits are bounded (ptx.cuh).
 #pragma once
 #include <type_traits>
 #include "cbr_internal.h"
@@ -55,7 +55,7 @@ namespace hc {
 
 constexpr int kEpiWarps = 8;
 constexpr int kEpiThreads = 32 * kEpiWarps;
-constexpr int kStreamStages = 2;
+constexpr int kStreamStages = 3;
 
 constexpr int pow2_at_least(int v) {
   int p = 32;
@@ -89,10 +89,13 @@ __host__ __device__ inline Layout layout(const HaloGeom& g, int kind, int nch, i
   L.wslab = (uint32_t)wslab_bytes(kind, nout);
   L.nsw = wres ? nch * g.r * g.s : kStreamStages;
   L.off_w = 2 * L.halo_stride;
-  L.off_stage = L.off_w + (uint32_t)L.nsw * L.wslab;
   const uint32_t stage = 128u * nout * 2;
-  // off_stage: scratch for the end-of-kernel statistics reduction (and the finalize)
-  L.off_bar = (L.off_stage + stage + 15u) & ~15u;
+  // off_stage: scratch for the end-of-kernel statistics reduction (and the finalize).  It is
+  // used only after the epilogue has drained the last accumulator, when every MMA of the CTA
+  // has completed and with it every halo load they read, so it shares the halo stages.
+  const bool alias = 2 * L.halo_stride >= stage;
+  L.off_stage = alias ? 0u : L.off_w + (uint32_t)L.nsw * L.wslab;
+  L.off_bar = ((alias ? L.off_w + (uint32_t)L.nsw * L.wslab : L.off_stage + stage) + 15u) & ~15u;
   const uint32_t nbar = 8 + 2 * L.nsw + 1;
   L.total = L.off_bar + nbar * 8 + 16;
   return L;
