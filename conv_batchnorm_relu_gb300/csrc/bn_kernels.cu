@@ -24,20 +24,27 @@ constexpr int kRedThreads = 512;
 constexpr int kRedUnroll = 8;
 
 // Sweeps the tensor last element first: the convolution before it wrote z first to last, so
-// the end of z is what the L2 still holds.
+// the end of z is what the L2 still holds.  The grid stride and the vector count are multiples
+// of the c/8 vectors of a pixel (checked by the launcher), so every vector a thread visits has
+// the same channel group and its eq_scale / eq_bias live in registers.
 template <bool BF16, bool MASK>
 __global__ void __launch_bounds__(kApplyThreads)
     bn_apply_relu_kernel(const ApplyArgs a) {
-  __shared__ float s_eq[512];
-  for (int i = threadIdx.x; i < 2 * a.c; i += kApplyThreads) s_eq[i] = a.eq[i];
-  __syncthreads();
   const long long nvec = a.total / 8;
   const int cvec = a.c / 8;
   const long long stride = (long long)gridDim.x * kApplyThreads;
+  const long long vfirst = (long long)blockIdx.x * kApplyThreads + threadIdx.x;
+  if (vfirst >= nvec) return;
+  const int c0 = (int)((nvec - 1 - vfirst) % cvec) * 8;
+  float sc[8], bi[8];
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    sc[e] = __ldg(a.eq + c0 + e);
+    bi[e] = __ldg(a.eq + a.c + c0 + e);
+  }
   const uint8_t* zb = static_cast<const uint8_t*>(a.z);
   uint8_t* yb = static_cast<uint8_t*>(a.y);
-  for (long long v0 = (long long)blockIdx.x * kApplyThreads + threadIdx.x; v0 < nvec;
-       v0 += stride * kApplyUnroll) {
+  for (long long v0 = vfirst; v0 < nvec; v0 += stride * kApplyUnroll) {
     uint4 in[kApplyUnroll];
 #pragma unroll
     for (int k = 0; k < kApplyUnroll; ++k) {
@@ -48,15 +55,14 @@ __global__ void __launch_bounds__(kApplyThreads)
     for (int k = 0; k < kApplyUnroll; ++k) {
       const long long v = nvec - 1 - (v0 + k * stride);
       if (v >= 0) {
-        const int c0 = (int)(v % cvec) * 8;
         const uint32_t w[4] = {in[k].x, in[k].y, in[k].z, in[k].w};
         uint32_t o[4];
         uint32_t bits = 0;
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
           const float2 zz = unpack2<BF16>(w[j]);
-          const float p0 = fmaf(zz.x, s_eq[c0 + 2 * j], s_eq[a.c + c0 + 2 * j]);
-          const float p1 = fmaf(zz.y, s_eq[c0 + 2 * j + 1], s_eq[a.c + c0 + 2 * j + 1]);
+          const float p0 = fmaf(zz.x, sc[2 * j], bi[2 * j]);
+          const float p1 = fmaf(zz.y, sc[2 * j + 1], bi[2 * j + 1]);
           bits |= (p0 > 0.f ? 1u : 0u) << (2 * j);
           bits |= (p1 > 0.f ? 1u : 0u) << (2 * j + 1);
           o[j] = pack2<BF16>(fmaxf(p0, 0.f), fmaxf(p1, 0.f));
@@ -228,12 +234,21 @@ __device__ __forceinline__ uint32_t fastdiv(uint32_t n, const FastDiv& f) {
 template <bool BF16, bool MASKBITS, bool PAD>
 __global__ void __launch_bounds__(kApplyThreads)
     dz_kernel(const DzArgs a) {
-  __shared__ float s_coef[3 * 256];
-  for (int i = threadIdx.x; i < 3 * a.c; i += kApplyThreads) s_coef[i] = a.coef[i];
-  __syncthreads();
   const long long nvec = a.total / 8;
   const int cvec = a.c / 8;
   const long long stride = (long long)gridDim.x * kApplyThreads;
+  // as in the apply pass, a thread's channel group is fixed: its coefficients live in registers
+  const long long vfirst = (long long)blockIdx.x * kApplyThreads + threadIdx.x;
+  if (vfirst >= nvec) return;
+  const uint32_t cv = (uint32_t)((nvec - 1 - vfirst) % cvec);
+  const int c0 = (int)cv * 8;
+  float ca[8], cd[8], ce[8];
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    ca[e] = __ldg(a.coef + c0 + e);
+    cd[e] = __ldg(a.coef + a.c + c0 + e);
+    ce[e] = __ldg(a.coef + 2 * a.c + c0 + e);
+  }
   const uint8_t* dyb = static_cast<const uint8_t*>(a.dy);
   const uint8_t* zb = static_cast<const uint8_t*>(a.z);
   const uint8_t* yb = static_cast<const uint8_t*>(a.y);
@@ -257,14 +272,7 @@ __global__ void __launch_bounds__(kApplyThreads)
       const long long v = nvec - 1 - (v0 + k * stride);
       if (v >= 0) {
         // PAD: v < 2^31 (checked by the launcher), so the index math runs in 32 bits
-        uint32_t pix = 0, cv;
-        if (PAD) {
-          pix = fastdiv((uint32_t)v, a.fd_cvec);
-          cv = (uint32_t)v - pix * a.fd_cvec.d;
-        } else {
-          cv = (uint32_t)(v % cvec);
-        }
-        const int c0 = (int)cv * 8;
+        const uint32_t pix = PAD ? fastdiv((uint32_t)v, a.fd_cvec) : 0u;
         uint32_t bits;
         if (MASKBITS) {
           bits = mb[k];
@@ -285,11 +293,10 @@ __global__ void __launch_bounds__(kApplyThreads)
         for (int j = 0; j < 4; ++j) {
           const float2 d = unpack2<BF16>(dw[j]);
           const float2 z = unpack2<BF16>(zw[j]);
-          const int c = c0 + 2 * j;
           const float g0 = (bits >> (2 * j)) & 1u ? d.x : 0.f;
           const float g1 = (bits >> (2 * j + 1)) & 1u ? d.y : 0.f;
-          const float r0 = fmaf(s_coef[c], g0, fmaf(-s_coef[a.c + c], z.x, s_coef[2 * a.c + c]));
-          const float r1 = fmaf(s_coef[c + 1], g1, fmaf(-s_coef[a.c + c + 1], z.y, s_coef[2 * a.c + c + 1]));
+          const float r0 = fmaf(ca[2 * j], g0, fmaf(-cd[2 * j], z.x, ce[2 * j]));
+          const float r1 = fmaf(ca[2 * j + 1], g1, fmaf(-cd[2 * j + 1], z.y, ce[2 * j + 1]));
           o[j] = pack2<BF16>(r0, r1);
         }
         if (PAD) {
@@ -336,7 +343,8 @@ int stream_grid(K kern, int threads, long long work_items, int num_sms) {
 
 int launch_dz(const DzArgs& a_in, bool bf16, int num_sms, cudaStream_t st) {
   DzArgs a = a_in;
-  if (a.c % 8 != 0 || a.c > 256 || a.q < 1 || a.pitch < a.q) return 3;
+  // kApplyThreads (and so the grid stride) must be a multiple of the c/8 vectors of a pixel
+  if (a.c % 8 != 0 || a.c > 256 || kApplyThreads % (a.c / 8) != 0 || a.q < 1 || a.pitch < a.q) return 3;
   const long long nvec = a.total / 8;
   const bool bits = a.mask != nullptr;
   const bool pad = a.pitch != a.q;
@@ -362,7 +370,8 @@ int launch_dz(const DzArgs& a_in, bool bf16, int num_sms, cudaStream_t st) {
 }
 
 int launch_apply(const ApplyArgs& a, bool bf16, int num_sms, cudaStream_t st) {
-  if (a.c % 8 != 0 || a.c > 256) return 3;
+  // kApplyThreads (and so the grid stride) must be a multiple of the c/8 vectors of a pixel
+  if (a.c % 8 != 0 || a.c > 256 || kApplyThreads % (a.c / 8) != 0) return 3;
   const long long nvec = a.total / 8;
   const bool mask = a.mask != nullptr;
   auto go = [&](auto kern) {
