@@ -256,7 +256,7 @@ __global__ void __launch_bounds__(Roles<KIND>::kThreads, 1)
       mbar_init(bar_halo_full + 8 * i, KIND == kKindDgrad ? 32 * R::kAWarps : 1);
       mbar_init(bar_halo_empty + 8 * i, 1);
       mbar_init(bar_acc_full + 8 * i, 1);
-      mbar_init(bar_acc_empty + 8 * i, kEpiThreads);
+      mbar_init(bar_acc_empty + 8 * i, kEpiWarps);  // one arrival per epilogue warp
     }
     for (int i = 0; i < L.nsw; ++i) {
       mbar_init(bar_w_full + 8 * i, 1);
@@ -536,9 +536,11 @@ __global__ void __launch_bounds__(Roles<KIND>::kThreads, 1)
                         *reinterpret_cast<uint32_t(*)[16]>(r + q16 * 16));
             tmem_ld_wait();
             if (t == ntiles - 1 && b == kNB - 1) {
-              // this thread's last read of the accumulator stage
+              // the warp's last read of the accumulator stage (a warp-uniform branch): every
+              // lane orders its TMEM reads before the warp sync, then one lane arrives
               tc_fence_before();
-              mbar_arrive(bar_acc_empty + 8 * as);
+              __syncwarp();
+              if (lane == 0) mbar_arrive(bar_acc_empty + 8 * as);
             }
             float v[kSB];
 #pragma unroll
@@ -583,7 +585,8 @@ __global__ void __launch_bounds__(Roles<KIND>::kThreads, 1)
           }
         } else if (t == ntiles - 1) {
           tc_fence_before();
-          mbar_arrive(bar_acc_empty + 8 * as);
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar_acc_empty + 8 * as);
         }
       }
       ++ait;
