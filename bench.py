@@ -48,6 +48,9 @@ def parse():
     ap.add_argument("--impl", default="cbr", choices=["cbr", "reference"])
     ap.add_argument("--config", type=int, default=3)
     ap.add_argument("--e2e-steps", type=int, default=20)
+    # 1: host-to-device copies on GB300 run at about 210 GB/s with 2 to 32 streams alike
+    ap.add_argument("--copy-chunks", type=int, default=1,
+                    help="e2e: host-to-device copies per input tensor and step, each on its own stream")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     return ap.parse_args()
 
@@ -398,8 +401,9 @@ def run_cbr(args, world, rank, local):
     # ---------------------------------------------------------------- e2e (public API, host buffers)
     # Every step copies its inputs (x, dy) from pinned host memory and reads its result (dW,
     # dgamma, dbeta) back into pinned host memory, inside the timed region. As a training loop's
-    # input pipeline does, step i+1's inputs are copied while step i computes: one copy stream
-    # per tensor (both copy engines), two device input buffers that alternate, events between.
+    # input pipeline does, step i+1's inputs are copied while step i computes: each input tensor
+    # is copied as --copy-chunks contiguous pieces, each piece on its own stream (several copies
+    # in flight), into two device input buffers that alternate, with events between.
     E = args.e2e_steps
     hx = inp["x"].pin_memory()
     hdy = inp["dy"].pin_memory()
@@ -410,24 +414,32 @@ def run_cbr(args, world, rank, local):
     dyd = [torch.empty_like(g["dy"]) for _ in range(2)]
     h2d = hx.numel() * hx.element_size() + hdy.numel() * hdy.element_size()
     d2h = (hdw.numel() + hdg.numel() + hdb.numel()) * 4
-    cp_x, cp_dy = torch.cuda.Stream(), torch.cuda.Stream()
-    ev_x = [torch.cuda.Event() for _ in range(2)]
-    ev_dy = [torch.cuda.Event() for _ in range(2)]
+    nck = max(1, args.copy_chunks)
+
+    def pieces(t):
+        flat = t.view(-1)
+        step_ = (flat.numel() + nck - 1) // nck
+        return [flat[k * step_:(k + 1) * step_] for k in range(nck) if k * step_ < flat.numel()]
+
+    src_pieces = pieces(hx) + pieces(hdy)
+    dst_pieces = [pieces(xd[b]) + pieces(dyd[b]) for b in range(2)]
+    cp_streams = [torch.cuda.Stream() for _ in src_pieces]
+    ev_in = [[torch.cuda.Event() for _ in src_pieces] for _ in range(2)]
     ev_free = [torch.cuda.Event() for _ in range(2)]
 
     def copy_in(i):
         b = i % 2
-        for cs_, dst, src, ev in ((cp_x, xd, hx, ev_x), (cp_dy, dyd, hdy, ev_dy)):
+        for cs_, dst, src, ev in zip(cp_streams, dst_pieces[b], src_pieces, ev_in[b]):
             if i >= 2:
                 cs_.wait_event(ev_free[b])  # step i-2 is done with buffer b
             with torch.cuda.stream(cs_):
-                dst[b].copy_(src, non_blocking=True)
-            ev[b].record(cs_)
+                dst.copy_(src, non_blocking=True)
+            ev.record(cs_)
 
     def compute(i):
         b = i % 2
-        stream.wait_event(ev_x[b])
-        stream.wait_event(ev_dy[b])
+        for ev in ev_in[b]:
+            stream.wait_event(ev)
         step(xd[b], dyd[b])
         ev_free[b].record(stream)
         hdw.copy_(bo["dw"], non_blocking=True)
@@ -494,6 +506,7 @@ def run_cbr(args, world, rank, local):
                           "note": "sum of per-pass max(FLOPs/peak, min bytes/HBM) over the measured step"},
         "passes": passes,
         "e2e": {"value": images / e2e_s, "unit": "images/s", "h2d_bytes_per_step": h2d,
+                "copy_streams": len(cp_streams),
                 "d2h_bytes_per_step": d2h},
         "gpu_launches": K * (len(kern_names)),
         "clocks": clocks,
