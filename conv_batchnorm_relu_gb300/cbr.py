@@ -65,10 +65,12 @@ def load(path: str | None = None) -> ctypes.CDLL:
             lib.cbr_fold_bn.argtypes = [D, vp, vp, vp, vp, vp, vp, fp, vp, vp, vp]
             lib.cbr_forward_infer.argtypes = [D, vp, vp, vp, vp, vp]
             lib.cbr_stream_status.argtypes = [vp]
+            lib.cbr_selftest_bounded_wait.argtypes = [i32, vp]
             lib.cbr_profile_next_call.argtypes = [ctypes.POINTER(vp), i32]
             lib.cbr_profile_last_count.restype = i32
             for f in ("cbr_workspace_size", "cbr_forward_train", "cbr_backward", "cbr_fold_bn",
-                      "cbr_forward_infer", "cbr_stream_status", "cbr_profile_next_call"):
+                      "cbr_forward_infer", "cbr_stream_status", "cbr_profile_next_call",
+                      "cbr_selftest_bounded_wait"):
                 getattr(lib, f).restype = i32
             _lib = lib
     return _lib
@@ -215,6 +217,16 @@ def stream_status(stream: int | None = None) -> None:
     """Synchronise the stream and raise if a kernel reported a device-side error."""
     _check(load().cbr_stream_status(stream if stream is not None else _stream()),
            "cbr_stream_status")
+
+
+def stream_status_code(stream: int | None = None) -> int:
+    """cbr_stream_status's raw status code (0 = CBR_OK), without raising."""
+    return load().cbr_stream_status(stream if stream is not None else _stream())
+
+
+def selftest_bounded_wait(limit_us: int) -> None:
+    """Launch the library's bounded-wait self-test on the current stream (see include/cbr.h)."""
+    _check(load().cbr_selftest_bounded_wait(int(limit_us), _stream()), "cbr_selftest_bounded_wait")
 
 
 def profile_next_call(events: list) -> None:

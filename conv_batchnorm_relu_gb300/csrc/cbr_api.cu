@@ -589,6 +589,15 @@ cbr_status_t cbr_stream_status(cbr_stream_t stream) {
   return CBR_OK;
 }
 
+cbr_status_t cbr_selftest_bounded_wait(int32_t limit_us, cbr_stream_t stream) {
+  if (limit_us < 1 || limit_us > 1000000) return CBR_ERR_INVALID_ARG;
+  DeviceInfo* dev = nullptr;
+  int st = current_device(&dev);
+  if (st) return (cbr_status_t)st;
+  st = launch_selftest_wait(dev->err, (uint64_t)limit_us * 1000ull, reinterpret_cast<cudaStream_t>(stream));
+  return (cbr_status_t)st;
+}
+
 cbr_status_t cbr_profile_next_call(void* const* events, int32_t count) {
   if (events && count <= 0) return CBR_ERR_INVALID_ARG;
   t_prof_events = events;

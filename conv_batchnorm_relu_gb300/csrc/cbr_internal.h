@@ -180,6 +180,8 @@ struct DzArgs {
   int pitch;                // dz row pitch in pixels (>= q); columns q..pitch-1 are written as zero
   FastDiv fd_cvec, fd_q;    // division by c/8 and by q (set by the launcher)
 };
+// One warp that gives up on a never-completed barrier after limit_ns (selftest.cu).
+int launch_selftest_wait(uint32_t* err, uint64_t limit_ns, cudaStream_t st);
 // dz = a*(dy*mask) - d*z + e, elementwise (bn_kernels.cu).
 int launch_dz(const DzArgs& a, bool bf16, int num_sms, cudaStream_t st);
 // Launches the wgrad kernel, calls `between(ctx)` (if set), then the fixed-order reduction.

@@ -189,6 +189,18 @@ cbr_status_t cbr_forward_train_noalloc(const cbr_desc_t* desc, const void* x, co
 cbr_status_t cbr_stream_status(cbr_stream_t stream);
 
 /*
+ * Failure-detection self-test (the pages have no counterpart; it exercises the library's own
+ * error path).  Launches one warp on `stream` that waits, with the same bounded barrier wait
+ * the library's kernels use, on a barrier nothing completes; after `limit_us` microseconds it
+ * gives up, records the timeout in the device error word and exits.  The following
+ * cbr_stream_status(stream) then returns CBR_ERR_TIMEOUT and clears the word, and the CUDA
+ * context stays usable: no fault, trap or hang is involved.  Returns CBR_ERR_INVALID_ARG unless
+ * 1 <= limit_us <= 1,000,000, CBR_ERR_DEVICE if the current device is not compute 10.3, else
+ * CBR_OK (the wait itself runs asynchronously).
+ */
+cbr_status_t cbr_selftest_bounded_wait(int32_t limit_us, cbr_stream_t stream);
+
+/*
  * Profiling hook for the calling host thread.  When `events` is non-NULL, the next
  * cbr_forward_train / cbr_backward / cbr_forward_infer call records events[0] before its
  * first kernel and events[i] after its i-th kernel (cudaEvent_t handles owned by the caller,

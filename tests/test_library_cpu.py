@@ -125,3 +125,10 @@ def test_noalloc_forward_requires_z_saved(lib):
     assert f(ctypes.byref(d), P, P, P, P, P, P, 0.1, 1e-5, P, P, None, P, P, None) == 1
     bad = _desc(c_out=12)
     assert f(ctypes.byref(bad), P, P, P, P, P, P, 0.1, 1e-5, P, P, P, P, P, None) == 1
+
+
+def test_selftest_limit_checked_before_device(lib):
+    for bad in (0, -5, 1000001):
+        assert lib.cbr_selftest_bounded_wait(bad, None) == 1
+    # a valid limit gets as far as the device check (no GPU here)
+    assert lib.cbr_selftest_bounded_wait(1000, None) == 5
