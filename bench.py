@@ -52,6 +52,8 @@ def parse():
     ap.add_argument("--copy-chunks", type=int, default=1,
                     help="e2e: host-to-device copies per input tensor and step, each on its own stream")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--recompute-z", action="store_true",
+                    help="do not keep z: the forward passes z_saved = NULL and the backward recomputes it")
     return ap.parse_args()
 
 
@@ -294,6 +296,8 @@ def run_cbr(args, world, rank, local):
     y = torch.empty((spec.n, spec.p, spec.q, spec.c_out), dtype=spec.torch_dtype, device=dev)
     fo = {"y": y, "z": torch.empty_like(y), "mask": torch.empty(cbr.mask_words(layer), dtype=torch.int32, device=dev),
           "saved_mean": torch.empty(spec.c_out, device=dev), "saved_inv_var": torch.empty(spec.c_out, device=dev)}
+    if args.recompute_z:
+        del fo["z"]
     bo = {"dw": torch.empty((spec.c_out, spec.r, spec.s, spec.c_in), dtype=torch.float32, device=dev),
           "dgamma": torch.empty(spec.c_out, device=dev), "dbeta": torch.empty(spec.c_out, device=dev)}
     if need_dx:
@@ -305,13 +309,16 @@ def run_cbr(args, world, rank, local):
         if fev:
             cbr.profile_next_call(fev)
         cbr.forward_train(layer, x, g["w"], g["gamma"], g["beta"], g["running_mean"],
-                          g["running_var"], spec.momentum, spec.eps, ws=ws_f, out=fo)
+                          g["running_var"], spec.momentum, spec.eps, ws=ws_f, out=fo,
+                          save_z=not args.recompute_z)
         if bev:
             cbr.profile_next_call(bev)
-        cbr.backward(layer, dy, x, g["w"], fo["mask"], cbr.CBR_MASK_BITS, fo["z"], g["gamma"],
+        cbr.backward(layer, dy, x, g["w"], fo["mask"], cbr.CBR_MASK_BITS, fo.get("z"), g["gamma"],
                      fo["saved_mean"], fo["saved_inv_var"], ws=ws_b, need_dx=need_dx, out=bo)
 
-    nf, nb = len(FWD_KERNELS) + 1, len(BWD_KERNELS_DZ) + 1
+    # without a kept z the backward starts with the convolution that recomputes it
+    bwd_all = (["conv_z_recompute"] if args.recompute_z else []) + BWD_KERNELS_DZ
+    nf, nb = len(FWD_KERNELS) + 1, len(bwd_all) + 1
     K = args.steps
     mk = lambda: torch.cuda.Event(enable_timing=True)
     for _ in range(args.warmup):
@@ -324,7 +331,7 @@ def run_cbr(args, world, rank, local):
         e.record(stream)
     step(g["x"], g["dy"], None, probe)
     used_b = cbr.profile_last_count() - 1
-    cand = [k for k in BWD_KERNELS_DZ if need_dx or k != "conv_dgrad"]
+    cand = [k for k in bwd_all if need_dx or k != "conv_dgrad"]
     if len(cand) != used_b:  # no dz pass: dz built inside the convolutions
         cand = [k for k in cand if k != "bn_dz"]
     bwd_names = cand[:used_b]
@@ -493,6 +500,7 @@ def run_cbr(args, world, rank, local):
         "steps": K, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": spec.dtype, "data": "synthetic",
         "config": dict(workload_config(spec, "flushed (256 MB write) between timed steps, outside the step events"),
+                       z="recomputed in the backward (z_saved = NULL)" if args.recompute_z else "kept by the caller (z_saved)",
                        launch="one step captured as a CUDA graph of the library's launches, replayed per step; "
                               "timed by two event nodes around the step; per-kernel times ('passes') from "
                               "separate replays with an event node at every kernel boundary",
