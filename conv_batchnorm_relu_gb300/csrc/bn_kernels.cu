@@ -3,9 +3,10 @@
 // B1: BN + ReLU backward reduction (CBR page, section 5.1: dY*mask before batchnorm_backward;
 //     BatchNorm CUDA page, section 3.1: dbeta = sum g, dgamma = sum g*xhat).  It also emits the
 //     per-channel coefficients of dz = gamma*inv_std*(g - dbeta/M - xhat*dgamma/M), written as
-//     dz = a*g - d*z + e, which the dgrad and wgrad kernels apply while loading their operands.
+//     dz = a*g - d*z + e.
+// dz pass: evaluates that expression once and stores dz for both backward convolutions.
 //
-// Both passes are HBM-bound streams over NHWC tensors: 128-bit loads of 8 channels, several
+// All three are HBM-bound streams over NHWC tensors: 128-bit loads of 8 channels, several
 // independent vectors in flight per thread, grid sized to the SM count.
 #include <algorithm>
 #include <map>

@@ -1,11 +1,11 @@
-// B2: data gradient (DGrad) and B3: weight gradient (WGrad) of the convolution
-// (Tech-Renaissance CBR page, section 5.2), both with the BN + ReLU backward expression
+// B3: weight gradient (WGrad) of the convolution (Tech-Renaissance CBR page, section 5.2) over
 // dz = gamma*inv_std*(g - dbeta/M - xhat*dgamma/M), g = dy*mask (section 5.1; BatchNorm CUDA
-// page, section 3.1) evaluated while building the tensor-core operand tiles, so dz never
-// touches HBM.
+// page, section 3.1).  dz is normally materialised once by the dz pass (bn_kernels.cu) in the
+// padded-linear row layout and loaded here by TMA; for shapes too large for that pass, producer
+// warps evaluate it from (dy, z, mask) while building the operand tile instead.
 //
-// DGrad is the stride-1 convolution of dz with the tap-flipped filter and padding R-1-pad; it
-// runs on the shared halo-conv template with 4 dz-producer warps and the filter read MN-major.
+// DGrad (B2, conv_dgrad.cu) is the stride-1 convolution of dz with the tap-flipped filter and
+// padding R-1-pad on the shared halo-conv template, with the filter read MN-major.
 //
 // WGrad: dW[k][r][s][c] = sum over pixels of dz[pixel][k] * x[pixel shifted by (r,s)][c].  The
 // reduction dimension is the pixel, so both operands are MN-major pixel-row tiles: A is the

@@ -1,7 +1,8 @@
 // DGrad: dx = stride-1 convolution of dz (P x Q, Cout channels) with the filter rotated by 180
 // degrees and its channel roles swapped (CBR page, section 5.2; padding R-1-pad).  The A
-// operand is the zero-padded dz halo: loaded by TMA from a materialised dz when the backward
-// pass has one, otherwise built in shared memory from (dy, z, mask) by four producer warps.
+// operand is the zero-padded dz halo: loaded by TMA from the materialised dz (its stored zero
+// columns past q and the out-of-bounds fill supply the padding), or, for shapes too large for
+// the dz pass, built in shared memory from (dy, z, mask) by four producer warps.
 #include <algorithm>
 
 #include "halo_conv.cuh"

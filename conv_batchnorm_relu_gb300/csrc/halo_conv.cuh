@@ -1,16 +1,17 @@
 // Generic stride-1 implicit-GEMM convolution over a halo tile, on tcgen05 tensor cores.
 //
 // Used for the forward convolution (A = input activations, loaded by TMA) and for the data
-// gradient (A = dz, computed in-kernel from dy, z and the ReLU mask by producer warps; the
-// filter is the forward filter read MN-major with flipped taps).  See HaloGeom for the
-// padded-linear row space in which every filter tap is a row-shifted view of one halo tile.
+// gradient (A = dz: loaded by TMA from the materialised dz, or, for shapes too large for the
+// dz pass, computed from dy, z and the ReLU mask by producer warps; the filter is the forward
+// filter read MN-major with flipped taps).  See HaloGeom for the padded-linear row space in
+// which every filter tap is a row-shifted view of one halo tile.
 //
 // Warp roles (A = number of A-producer warps: 1 for TMA, 4 for the dz producer):
 //   warps [0, A)       A producers (one halo stage per (unit, 64-channel chunk))
 //   warp  A            TMEM owner and single-thread tcgen05.mma issuer
 //   warp  A+1          TMA producer for the filter slabs (resident when they fit in smem)
 //   warps A+2 .. A+9   epilogue, two warps per TMEM lane quadrant (each takes half of the
-//                      columns): TMEM -> registers -> staged tile -> stats / store
+//                      columns): TMEM -> registers -> stats / store
 // Pipelines: 2 halo stages, 2 TMEM accumulator stages (U*NOUT fp32 columns each), and a
 // 3-deep filter ring when the filter is streamed.  All waits are bounded (ptx.cuh).
 #pragma once

@@ -37,7 +37,8 @@
  *   - No call throws; the library holds no per-call state.
  *   - Supported shapes (else CBR_ERR_UNSUPPORTED): Cout in {16, 32, 64, 128}; and either
  *     stride 1 with Cin a multiple of 8, Cin <= 128, W + 2*pad <= 256; or the first-layer
- *     form Cin = 3 (any stride, R*S*3 <= 160).  Cout % 8 != 0 is CBR_ERR_INVALID_ARG
+ *     form Cin = 3 (any stride, R <= 8, S <= 8, pad <= 10, Q <= 128).  Cout % 8 != 0 is
+ *     CBR_ERR_INVALID_ARG
  *     (CBR page, section 8: output channels must be a multiple of 8).
  */
 #ifndef CBR_H_
