@@ -130,6 +130,11 @@ cbr_status_t cbr_forward_train(const cbr_desc_t* desc, const void* x, const void
  *                                  (section 5.2's write-after-read hazard): INVALID_ARG.
  *   dw [c_out][r][s][c_in]         fp32, written
  *   dgamma, dbeta [c_out]          fp32, written
+ *   ws, ws_bytes                   workspace (see cbr_workspace_size); it also holds dz, which
+ *                                  is evaluated once and read by both convolutions
+ * Errors: INVALID_ARG (null required pointer, bad desc or mask_kind, dx overlapping x),
+ * MISALIGNED, UNSUPPORTED (also: dx requested with a non-square filter or pad > R-1, or for
+ * the 3-channel first layer), WORKSPACE, DEVICE, CUDA.
  */
 cbr_status_t cbr_backward(const cbr_desc_t* desc, const void* dy, const void* x, const void* w,
                           const void* y_or_relu_mask, int32_t mask_kind, const void* z_saved,
