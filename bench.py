@@ -5,13 +5,16 @@ Tech-Renaissance CBR page, section 1).  One step = cbr_forward_train + cbr_backw
 hot path: conv+genstats+finalize, apply+ReLU+mask, masked BN reduction, wgrad, dgrad).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl cbr|reference] [--config ID]
+                    [--e2e-steps E] [--copy-chunks C] [--recompute-z] [--no-cpu-baseline]
 
 Prints ONE JSON line on rank 0.  Timing: one step (L2 flush, then forward + backward through
-the library's public calls) is captured once as a CUDA graph and replayed per timed step;
-the library's profiling hook records its events as event-record nodes, so the step and each
-kernel are timed on the device with no host work between kernels.  The L2 flush precedes
-the step's first event.  Clocks are sampled with nvidia-smi during the timed region.  The
-e2e figure calls the public API directly (no graph), with host copies inside the timed region.
+the library's public calls) is captured once as a CUDA graph and replayed per timed step,
+timed by two event-record nodes around it; per-kernel times come from separate replays with
+the library's profiling events at every kernel boundary.  The L2 flush precedes the step's
+first event.  Clocks are sampled with nvidia-smi during the timed region.  The e2e figure
+calls the public API directly (no graph), with host copies inside the timed region.  For the
+128-channel workload (--config 5) the folded inference call is timed as well.
+`--recompute-z` runs the step without a kept z (the backward recomputes it).
 `--impl reference` times the CPU oracle on the host cores instead (the reference arm).
 Multi-GPU runs are independent replicas (weak scaling; no collective on the data path).
 """
