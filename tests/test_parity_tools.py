@@ -54,3 +54,30 @@ def test_mask_slack_does_not_cover_decided_flips():
         alt = _backward_with_mask(o, ref, m3, spec)
         assert np.any(np.abs(alt["dx"] - rb["dx"]) > sl["dx"] + 2e-2), i
         assert np.any(np.abs(alt["dw"] - rb["dw"]) > sl["dw"] + 2e-2), i
+
+
+def test_sampled_slack_equals_full_slack_at_the_samples():
+    """mask_slack_core evaluated only at listed pixels and taps (the full-size tests' form)
+    gives the full allowance's values there."""
+    from parity import mask_slack_core
+    spec = CONFIGS[1]
+    o, ref, rb = _case(spec, 1240)
+    full = mask_slack(spec, o, ref, rb, margin=0.2)  # a wide margin so many points are ambiguous
+    pre = ref["pre"]
+    amb = np.abs(pre) <= 0.2
+    K = pre.shape[-1]
+    a = o["gamma"] * ref["inv_std"]
+    idx = np.argwhere(amb)
+    vals = np.abs(a[idx[:, 3]] * o["dy"][amb])
+    M = pre.shape[0] * pre.shape[1] * pre.shape[2]
+    s1 = np.where(amb, np.abs(o["dy"]), 0.0).reshape(-1, K).sum(0)
+    s2 = np.where(amb, np.abs(o["dy"] * ref["xhat"]), 0.0).reshape(-1, K).sum(0)
+    u = a * (s1 + np.abs(ref["xhat"]).reshape(-1, K).max(0) * s2) / M
+    pix = np.array([(0, 0, 0), (1, 7, 7), (0, 3, 5), (1, 0, 7)])
+    taps = np.array([(0, 0, 0), (15, 2, 2), (7, 1, 0)])
+    sl = mask_slack_core(idx, vals, u, o["x"], o["w"], spec.stride, spec.pad, taps=taps, pixels=pix)
+    assert full["count"] > 0
+    np.testing.assert_allclose(sl["dx"], full["dx"][pix[:, 0], pix[:, 1], pix[:, 2]], rtol=1e-12, atol=0)
+    np.testing.assert_allclose(sl["dw"], full["dw"][taps[:, 0], taps[:, 1], taps[:, 2]], rtol=1e-12, atol=0)
+    only_taps = mask_slack_core(idx, vals, u, o["x"], o["w"], spec.stride, spec.pad, taps=taps)
+    assert only_taps["dx"] is None
