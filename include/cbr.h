@@ -58,7 +58,7 @@ typedef enum {
   CBR_OK = 0,
   CBR_ERR_INVALID_ARG = 1, /* null pointer, bad shape, bad scalar, dx aliases x, M < 2 */
   CBR_ERR_MISALIGNED = 2,  /* pointer alignment rule violated */
-  CBR_ERR_UNSUPPORTED = 3, /* valid arguments outside the shapes/dtypes this build runs */
+  CBR_ERR_UNSUPPORTED = 3, /* valid arguments outside the shapes/dtypes this library runs */
   CBR_ERR_WORKSPACE = 4,   /* ws_bytes smaller than cbr_workspace_size() requires */
   CBR_ERR_DEVICE = 5,      /* no CUDA device, or the current device is not compute 10.3 */
   CBR_ERR_CUDA = 6,        /* a CUDA runtime / driver call failed */
