@@ -154,6 +154,13 @@ FwdWs fwd_ws(const Shape& s, bool need_z) {
   L.total = need_z ? align_up(L.z + act_bytes(s.n, s.p, s.q, s.cout, s.elt), 256) : L.z;
   return L;
 }
+// Whether the fused backward kernel (dz evaluated on chip, both convolutions in one kernel)
+// takes this layer; the other layers materialise dz once in the workspace.
+bool use_fused_bwd(const Shape& s) {
+  return !is_first_layer(s) && bwd_fused_supported((int)s.n, (int)s.h, (int)s.w, (int)s.cin, (int)s.cout,
+                                                   (int)s.r, (int)s.s, (int)s.stride, (int)s.pad);
+}
+
 // Row pitch (pixels) of the materialised dz.  The halo convolutions read it in their
 // padded-linear row space (pitch w + 2*pad, the columns past q zero), so a unit's dz tile is
 // one contiguous run of rows; the first layer's wgrad reads plain [n][p][q] rows.
@@ -175,7 +182,9 @@ BwdWs bwd_ws(const Shape& s, bool need_z) {
   const size_t wpart = is_first_layer(s) ? first_wgrad_partial_floats(kMaxCtas, (int)s.cout)
                                          : wgrad_partial_floats(kMaxCtas, (int)s.cin, (int)s.cout, (int)(s.r * s.s));
   L.dz = align_up(L.wpart + wpart * sizeof(float), 256);
-  L.z = align_up(L.dz + act_bytes(s.n, s.p, dz_pitch(s), s.cout, s.elt), 256);  // materialised dz
+  // materialised dz (none when the fused kernel evaluates it on chip)
+  const size_t dz_bytes = use_fused_bwd(s) ? 0 : act_bytes(s.n, s.p, dz_pitch(s), s.cout, s.elt);
+  L.z = align_up(L.dz + dz_bytes, 256);
   L.total = need_z ? align_up(L.z + act_bytes(s.n, s.p, s.q, s.cout, s.elt), 256) : L.z;
   return L;
 }
@@ -402,7 +411,7 @@ cbr_status_t cbr_backward(const cbr_desc_t* desc, const void* dy, const void* x,
   if ((st = check_supported(s))) return (cbr_status_t)st;
   // dgrad runs as a stride-1 conv with padding R-1-pad on both axes
   if (dx && (s.r != s.s || s.pad > s.r - 1)) return CBR_ERR_UNSUPPORTED;
-  // The first layer has no dgrad (CBR page, section 6): dx must be NULL there.
+  // The first layer has no dgrad (CBR page, section 5.3): dx must be NULL there.
   if (is_first_layer(s) && dx) return CBR_ERR_UNSUPPORTED;
   const BwdWs L = bwd_ws(s, z_saved == nullptr);
   if (ws_bytes < L.total) return CBR_ERR_WORKSPACE;
@@ -450,11 +459,31 @@ cbr_status_t cbr_backward(const cbr_desc_t* desc, const void* dy, const void* x,
   if (st) return (cbr_status_t)st;
   prof.mark();
 
-  // dz = a*(dy*mask) - d*z + e is materialised once and read by TMA in both convolutions.
-  const bool dz_tma = dz_materialisable(s);
-  const bool wgrad_tma = dz_tma && (is_first_layer(s) || wgrad_dz_tma_fits(make_geom(s), (int)s.cout));
+  if (use_fused_bwd(s)) {
+    // dz = a*(dy*mask) - d*z + e evaluated once per tile on chip, feeding both convolutions
+    BwdFusedArgs fa{};
+    fa.g = make_geom(s);
+    fa.dy = dy;
+    fa.z = z;
+    fa.y = yv;
+    fa.mask = mask;
+    fa.coef = coef;
+    fa.dx = dx;
+    fa.part = reinterpret_cast<float*>(wsb + L.wpart);
+    fa.dw = dw;
+    fa.err = dev->err;
+    st = launch_bwd_fused(fa, (int)s.cin, (int)s.cout, s.bf16, x, w, dev->num_sms, cs,
+                          [](void* p) { static_cast<Prof*>(p)->mark(); }, &prof);
+    if (st) return (cbr_status_t)st;
+    prof.mark();
+    return CBR_OK;
+  }
+
+  // Other layers: dz = a*(dy*mask) - d*z + e is materialised once and read by TMA in both
+  // convolutions.
+  if (!dz_materialisable(s)) return CBR_ERR_UNSUPPORTED;
   void* dz_buf = wsb + L.dz;
-  if (dz_tma) {
+  {
     DzArgs za{};
     za.dy = dy;
     za.z = z;
@@ -472,7 +501,7 @@ cbr_status_t cbr_backward(const cbr_desc_t* desc, const void* dy, const void* x,
   }
 
   if (is_first_layer(s)) {
-    // first layer: the im2col wgrad over the materialised dz; no dgrad (CBR page, section 6)
+    // first layer: the im2col wgrad over the materialised dz; no dgrad (CBR page, section 5.3)
     st = launch_first_wgrad(make_geom(s), (int)s.stride, (int)s.cout, s.bf16, x, dz_buf,
                             reinterpret_cast<float*>(wsb + L.wpart), dw, dev->err, dev->num_sms, cs,
                             [](void* p) { static_cast<Prof*>(p)->mark(); }, &prof);
@@ -483,14 +512,10 @@ cbr_status_t cbr_backward(const cbr_desc_t* desc, const void* dy, const void* x,
 
   // WGrad first, then DGrad (CBR page, section 5.2 orders DGrad after WGrad because its dX
   // overwrote X there; here dx may not alias x, so the order is only kept for familiarity).
+  if (!wgrad_dz_tma_fits(make_geom(s), (int)s.cout)) return CBR_ERR_UNSUPPORTED;
   WgradArgs wa{};
-  wa.dz_full = wgrad_tma ? dz_buf : nullptr;
+  wa.dz_full = dz_buf;
   wa.g = make_geom(s);
-  wa.dy = dy;
-  wa.z = z;
-  wa.y = yv;
-  wa.mask = mask;
-  wa.coef = coef;
   wa.part = reinterpret_cast<float*>(wsb + L.wpart);
   wa.dw = dw;
   wa.err = dev->err;
@@ -508,13 +533,8 @@ cbr_status_t cbr_backward(const cbr_desc_t* desc, const void* dy, const void* x,
     da.g.r = (int)s.r;
     da.g.s = (int)s.s;
     da.g.pad = (int)(s.r - 1 - s.pad);
-    da.dy = dy;
-    da.z = z;
-    da.y = yv;
-    da.mask = mask;
-    da.coef = coef;
     da.dx = dx;
-    da.dz_full = dz_tma ? dz_buf : nullptr;
+    da.dz_full = dz_buf;
     da.dz_pitch = (int)dz_pitch(s);
     da.err = dev->err;
     st = launch_dgrad(da, (int)s.cin, (int)s.cout, s.bf16, w, dev->num_sms, cs);

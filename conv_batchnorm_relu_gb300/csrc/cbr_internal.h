@@ -121,13 +121,8 @@ size_t bwd_reduce_partial_floats(int num_sms, int c);
 
 struct DgradArgs {
   HaloGeom g;               // geometry of the dgrad conv: input = dz (P x Q), output = dx
-  const void* dy;
-  const void* z;
-  const void* y;
-  const uint8_t* mask;
-  const float* coef;
   void* dx;
-  const void* dz_full;      // materialised dz [n][p][dz_pitch][cout], or null to compute it in-kernel
+  const void* dz_full;      // materialised dz [n][p][dz_pitch][cout]
   int dz_pitch;             // row pitch of dz_full in pixels (>= q, zero beyond q)
   uint32_t* err;
 };
@@ -138,18 +133,46 @@ int launch_dgrad(const DgradArgs& a, int c_in, int c_out, bool bf16, const void*
 
 struct WgradArgs {
   HaloGeom g;               // geometry of the forward conv
-  const void* dy;
-  const void* z;
-  const void* y;
-  const uint8_t* mask;
-  const float* coef;
   float* part;              // [grid][taps*cin][cout] per-CTA partial dW
   float* dw;                // [cout][r][s][cin]
   // materialised dz [n][p][wp][cout] in the padded-linear row layout of the forward geometry
-  // (row pitch wp = w + 2*pad, columns q..wp-1 zero), or null to compute it in-kernel
+  // (row pitch wp = w + 2*pad, columns q..wp-1 zero)
   const void* dz_full;
   uint32_t* err;
 };
+
+// How the filter taps of a weight gradient are paired into M = 128 MMAs (two 64-channel atoms)
+// and how the pairs and 64-channel input chunks are split across CTAs (conv_bwd.cu).
+constexpr int kWgMaxGroups = 64;
+constexpr int kWgMaxSplits = 8;
+struct WgPlan {
+  int nsplit, gmax, ngroups;
+  int split_chunk[kWgMaxSplits], split_g0[kWgMaxSplits], split_ng[kWgMaxSplits];
+  int ta[kWgMaxGroups], tb[kWgMaxGroups];
+};
+bool make_wg_plan(WgPlan& P, int taps, int c_in, int nout);
+// Fixed-order sum of the per-CTA wgrad partials ([cta][group][c16][v][row][4]) into dW.
+int launch_wgrad_reduce(const float* part, float* dw, const WgPlan& plan, int grid, int c_in, int taps,
+                        int nout, cudaStream_t st);
+
+// Fused backward convolutions (conv_bwd_fused.cu): one kernel evaluates dz = a*g - d*z + e once
+// per tile in shared memory and feeds it to both the data gradient and the weight gradient.
+struct BwdFusedArgs {
+  HaloGeom g;               // geometry of the forward conv (stride 1, padding (R-1)/2)
+  const void* dy;
+  const void* z;
+  const void* y;            // mask source when mask == null (y > 0)
+  const uint8_t* mask;      // bit-packed ReLU mask or null
+  const float* coef;        // [3][cout]: a, d, e
+  void* dx;                 // [n][h][w][cin] or null (weight gradient only)
+  float* part;              // per-CTA partial dW (wgrad_partial_floats)
+  float* dw;
+  uint32_t* err;
+};
+// Whether the fused kernel takes this layer (and so the backward needs no materialised dz).
+bool bwd_fused_supported(int n, int h, int w, int c_in, int c_out, int r, int s, int stride, int pad);
+int launch_bwd_fused(const BwdFusedArgs& a, int c_in, int c_out, bool bf16, const void* x, const void* w,
+                     int num_sms, cudaStream_t st, void (*between)(void*) = nullptr, void* ctx = nullptr);
 // Whether the TMA-fed wgrad (dz read from HBM) fits shared memory for this geometry.
 bool wgrad_dz_tma_fits(const HaloGeom& g, int c_out);
 

@@ -1,8 +1,8 @@
 // B3: weight gradient (WGrad) of the convolution (Tech-Renaissance CBR page, section 5.2) over
 // dz = gamma*inv_std*(g - dbeta/M - xhat*dgamma/M), g = dy*mask (section 5.1; BatchNorm CUDA
-// page, section 3.1).  dz is normally materialised once by the dz pass (bn_kernels.cu) in the
-// padded-linear row layout and loaded here by TMA; for shapes too large for that pass, producer
-// warps evaluate it from (dy, z, mask) while building the operand tile instead.
+// page, section 3.1), for the layers the fused backward kernel (conv_bwd_fused.cu) does not
+// take: dz is materialised once by the dz pass (bn_kernels.cu) in the padded-linear row layout
+// and loaded here by TMA.
 //
 // DGrad (B2, conv_dgrad.cu) is the stride-1 convolution of dz with the tap-flipped filter and
 // padding R-1-pad on the shared halo-conv template, with the filter read MN-major.
@@ -22,32 +22,25 @@
 namespace cbr {
 namespace {
 
-constexpr int kWgThreads = 192;  // warp 0: x TMA; warp 1: MMA; warps 2-5: dz producers + epilogue
-constexpr int kMaxGroups = 64;
-constexpr int kMaxSplits = 8;
-
-struct WgPlan {
-  int nsplit, gmax, ngroups;
-  int split_chunk[kMaxSplits], split_g0[kMaxSplits], split_ng[kMaxSplits];
-  int ta[kMaxGroups], tb[kMaxGroups];
-};
+constexpr int kWgThreads = 192;  // warp 0: x and dz TMA; warp 1: MMA; warps 2-5: epilogue
 
 struct WgKArgs {
   HaloGeom g;
-  DzSrc dz;
   WgPlan plan;
   float* part;
   uint32_t* err;
 };
 
+}  // namespace
+
 // Tap pairs (0,1), (2,3), ...; an odd last tap is paired with itself (its second half is
 // discarded).  Groups are split into contiguous subsets so that one CTA's accumulators
 // (groups x NOUT fp32 columns) fit the 512 TMEM columns; every 64-channel input chunk is a
 // separate split as well.
-bool make_plan(WgPlan& P, int taps, int c_in, int nout) {
+bool make_wg_plan(WgPlan& P, int taps, int c_in, int nout) {
   P = WgPlan{};
   const int ngroups = (taps + 1) / 2;
-  if (ngroups > kMaxGroups) return false;
+  if (ngroups > kWgMaxGroups) return false;
   for (int gi = 0; gi < ngroups; ++gi) {
     P.ta[gi] = 2 * gi;
     P.tb[gi] = std::min(2 * gi + 1, taps - 1);
@@ -55,7 +48,7 @@ bool make_plan(WgPlan& P, int taps, int c_in, int nout) {
   const int gcap = std::min(512 / nout, 16);  // TMEM columns; at most 16 groups per CTA
   const int nsub = (ngroups + gcap - 1) / gcap;
   const int nchunk = (c_in + 63) / 64;
-  if (nsub * nchunk > kMaxSplits) return false;
+  if (nsub * nchunk > kWgMaxSplits) return false;
   P.ngroups = ngroups;
   P.nsplit = nsub * nchunk;
   P.gmax = 0;
@@ -71,13 +64,15 @@ bool make_plan(WgPlan& P, int taps, int c_in, int nout) {
   return true;
 }
 
+namespace {
+
 struct WgLayout {
   uint32_t halo_stride, dz_sub, dz_stride, off_dz, off_bar, total;
 };
 
-// The dz tile of a unit is its um padded-linear rows, 64 channels per sub-tile: built by the
-// producer warps, or loaded by TMA from a dz materialised in the same padded-linear row layout
-// (the rows past the last image row read as zero).
+// The dz tile of a unit is its um padded-linear rows, 64 channels per sub-tile, loaded by TMA
+// from a dz materialised in the same padded-linear row layout (the rows past the last image
+// row read as zero).
 __host__ __device__ inline WgLayout wg_layout(const HaloGeom& g, int nout) {
   WgLayout L;
   L.halo_stride = (((uint32_t)g.hr * g.wp * 128) + 1023u) & ~1023u;
@@ -90,9 +85,9 @@ __host__ __device__ inline WgLayout wg_layout(const HaloGeom& g, int nout) {
   return L;
 }
 
-// DZTMA: dz is read from HBM by TMA (materialised earlier), so warp 0 loads both operands and
-// no producer threads are needed; otherwise warps 2-5 compute dz from dy, z and the mask.
-template <int NOUT, bool BF16, bool DZTMA>
+// Warp 0 loads both operands (the x halo and the dz tile) by TMA; warp 1 issues the MMAs;
+// warps 2-5 write the per-CTA partial at the end.
+template <int NOUT, bool BF16>
 __global__ void __launch_bounds__(kWgThreads, 1)
     wgrad_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUtensorMap map_dz,
                  const WgKArgs a) {
@@ -107,7 +102,6 @@ __global__ void __launch_bounds__(kWgThreads, 1)
   const uint32_t x_addr = sbase, dz_addr = sbase + L.off_dz;
   const uint32_t bar0 = sbase + L.off_bar;
   const uint32_t bar_x_full = bar0, bar_x_empty = bar0 + 16;
-  const uint32_t bar_dz_full = bar0 + 32, bar_dz_empty = bar0 + 48;
   const uint32_t bar_acc_full = bar0 + 64, bar_drain = bar0 + 72;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L.off_bar + 12 * 8);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
@@ -124,8 +118,6 @@ __global__ void __launch_bounds__(kWgThreads, 1)
     for (int i = 0; i < 2; ++i) {
       mbar_init(bar_x_full + 8 * i, 1);
       mbar_init(bar_x_empty + 8 * i, 1);
-      mbar_init(bar_dz_full + 8 * i, 128);
-      mbar_init(bar_dz_empty + 8 * i, 1);
     }
     mbar_init(bar_acc_full, 1);
     mbar_init(bar_drain, 1);
@@ -144,8 +136,8 @@ __global__ void __launch_bounds__(kWgThreads, 1)
   if (warp == 0) {
     if (lane == 0) {
       prefetch_tensormap(&map_x);
-      if (DZTMA) prefetch_tensormap(&map_dz);
-      const uint32_t tx = (uint32_t)g.hr * g.wp * 128 + (DZTMA ? (uint32_t)kNkc * L.dz_sub : 0u);
+      prefetch_tensormap(&map_dz);
+      const uint32_t tx = (uint32_t)g.hr * g.wp * 128 + (uint32_t)kNkc * L.dz_sub;
       uint32_t it = 0;
       for (int u = ustart; u < g.total_units && !hc::is_aborted(abort_flag); u += ustride, ++it) {
         const int n = u / g.upi;
@@ -160,8 +152,7 @@ __global__ void __launch_bounds__(kWgThreads, 1)
         for (int r0 = 0; r0 < g.hr; r0 += g.box_rows)
           tma_load_4d(x_addr + s * L.halo_stride + (uint32_t)r0 * g.wp * 128, &map_x, chunk * 64, -g.pad,
                       m0 / g.wp - g.pad + r0, n, bar_x_full + 8 * s);
-        if (DZTMA)
-          for (int kc = 0; kc < kNkc; ++kc)
+        for (int kc = 0; kc < kNkc; ++kc)
             tma_load_3d(dz_addr + s * L.dz_stride + kc * L.dz_sub, &map_dz, kc * 64, m0, n,
                         bar_x_full + 8 * s);
       }
@@ -195,7 +186,7 @@ __global__ void __launch_bounds__(kWgThreads, 1)
         const int m0 = (u - n * g.upi) * g.um;
         const int off = m0 - (m0 / g.wp) * g.wp;
         const uint32_t s = it & 1, ph = (it >> 1) & 1;
-        if (!__all_sync(0xffffffffu, mbar_wait(bar_x_full + 8 * s, ph) && (DZTMA || mbar_wait(bar_dz_full + 8 * s, ph)))) {
+        if (!__all_sync(0xffffffffu, mbar_wait(bar_x_full + 8 * s, ph))) {
           hc::set_abort(abort_flag, a.err, kErrWaitOperand);
           break;
         }
@@ -232,7 +223,6 @@ __global__ void __launch_bounds__(kWgThreads, 1)
           default: break;
         }
         mma_commit_warp(bar_x_empty + 8 * s);
-        if (!DZTMA) mma_commit_warp(bar_dz_empty + 8 * s);
         first = false;
       }
       mma_commit_warp(bar_acc_full);
@@ -240,24 +230,7 @@ __global__ void __launch_bounds__(kWgThreads, 1)
       mbar_wait(bar_drain, 0);
     }
   } else {
-    // warps 2..5: dz producers, then the epilogue
-    const int tid = threadIdx.x - 64;  // 0..127
-    uint32_t it = 0;
-    for (int u = ustart; !DZTMA && u < g.total_units && !hc::is_aborted(abort_flag); u += ustride, ++it) {
-      const int n = u / g.upi;
-      const int m0 = (u - n * g.upi) * g.um;
-      const uint32_t s = it & 1, ph = (it >> 1) & 1;
-      if (!mbar_wait_backoff(bar_dz_empty + 8 * s, ph ^ 1, 128)) {
-        hc::set_abort(abort_flag, a.err, kErrWaitOperand);
-        break;
-      }
-#pragma unroll
-      for (int kc = 0; kc < kNkc; ++kc)
-        fill_dz_rows<BF16>(dz_addr + s * L.dz_stride + kc * g.um * 128, g.um, m0, g.wp, 0, 0, n, a.dz,
-                           kc, tid, 128);
-      fence_proxy_async_smem();
-      mbar_arrive(bar_dz_full + 8 * s);
-    }
+    // warps 2..5: the epilogue
     const bool ok = mbar_wait_backoff(bar_acc_full, 0, 1024);
     if (!ok) hc::set_abort(abort_flag, a.err, kErrWaitMma);
     tc_fence_after();
@@ -362,7 +335,7 @@ __global__ void __launch_bounds__(kRedThreads)
 size_t wgrad_partial_floats(int num_sms, int c_in, int c_out, int taps) {
   WgPlan P;
   const int nout = nout_for(c_out);
-  if (!make_plan(P, taps, c_in, nout)) return 0;
+  if (!make_wg_plan(P, taps, c_in, nout)) return 0;
   return (size_t)num_sms * P.gmax * 128 * nout;
 }
 
@@ -373,27 +346,37 @@ bool wgrad_dz_tma_fits(const HaloGeom& g_in, int c_out) {
   return wg_layout(g, nout).total + 1024 <= 227 * 1024;
 }
 
+int launch_wgrad_reduce(const float* part, float* dw, const WgPlan& plan, int grid, int c_in, int taps,
+                        int nout, cudaStream_t st) {
+  const size_t per_cta = (size_t)plan.gmax * (nout / 16) * 512;
+  const int rgrid = (int)((per_cta + kRedSpan - 1) / kRedSpan) * plan.nsplit;
+  switch (nout) {
+    case 16: wgrad_reduce_kernel<16><<<rgrid, kRedThreads, 0, st>>>(part, dw, plan, grid, c_in, taps); break;
+    case 32: wgrad_reduce_kernel<32><<<rgrid, kRedThreads, 0, st>>>(part, dw, plan, grid, c_in, taps); break;
+    case 64: wgrad_reduce_kernel<64><<<rgrid, kRedThreads, 0, st>>>(part, dw, plan, grid, c_in, taps); break;
+    case 128: wgrad_reduce_kernel<128><<<rgrid, kRedThreads, 0, st>>>(part, dw, plan, grid, c_in, taps); break;
+    default: return 3;
+  }
+  return cudaGetLastError() == cudaSuccess ? 0 : 6;
+}
+
 int launch_wgrad(const WgradArgs& w, int c_in, int c_out, bool bf16, const void* x, int num_sms,
                  cudaStream_t st, void (*between)(void*), void* ctx) {
   WgKArgs a{};
   a.g = w.g;
-  a.dz = DzSrc{w.dy, w.z, w.y, w.mask, w.coef, 0, 0, c_out};
   a.part = w.part;
   a.err = w.err;
   const int nout = nout_for(c_out);
-  if (c_in > 128 || nout != c_out) return 3;
+  if (c_in > 128 || nout != c_out || w.dz_full == nullptr) return 3;
   const int U = nout <= 64 ? 2 : 1;
   if (!hc::finish_geom(a.g, U)) return 3;
-  a.dz.p = a.g.p;
-  a.dz.q = a.g.q;
   const int taps = a.g.r * a.g.s;
-  if (!make_plan(a.plan, taps, c_in, nout)) return 3;
-  const bool dztma = w.dz_full != nullptr;
+  if (!make_wg_plan(a.plan, taps, c_in, nout)) return 3;
   const WgLayout L = wg_layout(a.g, nout);
   const uint32_t smem = L.total + 1024;
   if (smem > 227 * 1024) return 3;
   const CUtensorMapDataType dt = bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
-  CUtensorMap mx;
+  CUtensorMap mx, mdz;
   const HaloGeom& g = a.g;
   {
     const uint64_t dims[4] = {(uint64_t)c_in, (uint64_t)g.w, (uint64_t)g.h, (uint64_t)g.n_img};
@@ -401,8 +384,7 @@ int launch_wgrad(const WgradArgs& w, int c_in, int c_out, bool bf16, const void*
     const uint32_t box[4] = {64, (uint32_t)g.wp, (uint32_t)g.box_rows, 1};
     if (!encode_tiled(&mx, dt, 4, x, dims, strides, box)) return 6;
   }
-  CUtensorMap mdz{};
-  if (dztma) {
+  {
     // [n][p*wp][cout]: the unit's um padded-linear rows are one box
     const uint64_t rows = (uint64_t)g.p * g.wp;
     const uint64_t dims[3] = {(uint64_t)c_out, rows, (uint64_t)g.n_img};
@@ -419,12 +401,10 @@ int launch_wgrad(const WgradArgs& w, int c_in, int c_out, bool bf16, const void*
     return cudaGetLastError() == cudaSuccess ? 0 : 6;
   };
   int rc;
-  switch (nout * 4 + (bf16 ? 2 : 0) + (dztma ? 1 : 0)) {
-#define CBR_WG_CASE(N_)                                                   \
-    case N_ * 4 + 0: rc = launch(wgrad_kernel<N_, false, false>); break; \
-    case N_ * 4 + 1: rc = launch(wgrad_kernel<N_, false, true>); break;  \
-    case N_ * 4 + 2: rc = launch(wgrad_kernel<N_, true, false>); break;  \
-    case N_ * 4 + 3: rc = launch(wgrad_kernel<N_, true, true>); break;
+  switch (nout * 2 + (bf16 ? 1 : 0)) {
+#define CBR_WG_CASE(N_)                                            \
+    case N_ * 2 + 0: rc = launch(wgrad_kernel<N_, false>); break; \
+    case N_ * 2 + 1: rc = launch(wgrad_kernel<N_, true>); break;
     CBR_WG_CASE(16)
     CBR_WG_CASE(32)
     CBR_WG_CASE(64)
@@ -434,15 +414,7 @@ int launch_wgrad(const WgradArgs& w, int c_in, int c_out, bool bf16, const void*
   }
   if (rc) return rc;
   if (between) between(ctx);
-  const size_t per_cta = (size_t)a.plan.gmax * (nout / 16) * 512;
-  const int rgrid = (int)((per_cta + kRedSpan - 1) / kRedSpan) * a.plan.nsplit;
-  switch (nout) {
-    case 16: wgrad_reduce_kernel<16><<<rgrid, kRedThreads, 0, st>>>(a.part, w.dw, a.plan, grid, c_in, taps); break;
-    case 32: wgrad_reduce_kernel<32><<<rgrid, kRedThreads, 0, st>>>(a.part, w.dw, a.plan, grid, c_in, taps); break;
-    case 64: wgrad_reduce_kernel<64><<<rgrid, kRedThreads, 0, st>>>(a.part, w.dw, a.plan, grid, c_in, taps); break;
-    default: wgrad_reduce_kernel<128><<<rgrid, kRedThreads, 0, st>>>(a.part, w.dw, a.plan, grid, c_in, taps); break;
-  }
-  return cudaGetLastError() == cudaSuccess ? 0 : 6;
+  return launch_wgrad_reduce(a.part, w.dw, a.plan, grid, c_in, taps, nout, st);
 }
 
 }  // namespace cbr

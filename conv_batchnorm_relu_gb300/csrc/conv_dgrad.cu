@@ -1,8 +1,8 @@
 // DGrad: dx = stride-1 convolution of dz (P x Q, Cout channels) with the filter rotated by 180
-// degrees and its channel roles swapped (CBR page, section 5.2; padding R-1-pad).  The A
-// operand is the zero-padded dz halo: loaded by TMA from the materialised dz (its stored zero
-// columns past q and the out-of-bounds fill supply the padding), or, for shapes too large for
-// the dz pass, built in shared memory from (dy, z, mask) by four producer warps.
+// degrees and its channel roles swapped (CBR page, section 5.2; padding R-1-pad), for the
+// layers the fused backward kernel (conv_bwd_fused.cu) does not take.  The A operand is the
+// zero-padded dz halo, loaded by TMA from the materialised dz (its stored zero columns past q
+// and the out-of-bounds fill supply the padding).
 #include <algorithm>
 
 #include "halo_conv.cuh"
@@ -18,7 +18,7 @@ int launch_dgrad(const DgradArgs& d, int c_in, int c_out, bool bf16, const void*
   if (c_in % 8 != 0) return 3;  // dx rows are stored in 16-byte groups of 8 channels
   a.mode = kFpropPlain;
   a.err = d.err;
-  a.dz = DzSrc{d.dy, d.z, d.y, d.mask, d.coef, d.g.h, d.g.w, c_out};
+  if (d.dz_full == nullptr) return 3;
   const int nch = (c_out + 63) / 64;
   const int nout = nout_for(c_in);
   if (nch > 2 || c_in > 128) return 3;
@@ -26,15 +26,15 @@ int launch_dgrad(const DgradArgs& d, int c_in, int c_out, bool bf16, const void*
   int U = 2;
   HaloGeom& g = a.g;
   if (!hc::finish_geom(g, U)) return 3;
-  if (nout > 64 && hc::layout(g, kKindDgrad, nch, nout, false).total + 1024 > 227 * 1024) {
+  if (nout > 64 && hc::layout(g, kKindDgradTma, nch, nout, false).total + 1024 > 227 * 1024) {
     U = 1;
     g = d.g;
     if (!hc::finish_geom(g, U)) return 3;
   }
-  bool wres = hc::layout(g, kKindDgrad, nch, nout, true).total + 1024 <= 227 * 1024;
+  bool wres = hc::layout(g, kKindDgradTma, nch, nout, true).total + 1024 <= 227 * 1024;
   const CUtensorMapDataType dt = bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
-  CUtensorMap mx{}, mw;  // mx: the materialised dz, when there is one
-  if (d.dz_full) {
+  CUtensorMap mx, mw;  // mx: the materialised dz
+  {
     // dz rows have a pitch of dz_pitch >= q pixels, zero past q: the halo's right padding reads
     // those zeros (or the out-of-bounds fill past the pitch), its left padding the fill
     const uint64_t pitch = (uint64_t)d.dz_pitch;
@@ -56,8 +56,7 @@ int launch_dgrad(const DgradArgs& d, int c_in, int c_out, bool bf16, const void*
         : hc::launch_halo_conv<K_, NCH_, NOUT_, U_, WRES_, false>(a, mx, mw, grid, st))
 #define CBR_DGRAD_CASE(NCH_, NOUT_, U_, WRES_)                                                   \
   if (nch == NCH_ && nout == NOUT_ && U == U_ && (WRES_ == wres)) {                             \
-    return d.dz_full ? CBR_DGRAD_KIND(kKindDgradTma, NCH_, NOUT_, U_, WRES_)                    \
-                     : CBR_DGRAD_KIND(kKindDgrad, NCH_, NOUT_, U_, WRES_);                      \
+    return CBR_DGRAD_KIND(kKindDgradTma, NCH_, NOUT_, U_, WRES_);                               \
   }
   // a resident filter where an instantiation has one, else the streamed filter
   for (int pass = 0; pass < 2; ++pass, wres = false) {

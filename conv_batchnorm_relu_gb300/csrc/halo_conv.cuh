@@ -1,16 +1,16 @@
 // Generic stride-1 implicit-GEMM convolution over a halo tile, on tcgen05 tensor cores.
 //
 // Used for the forward convolution (A = input activations, loaded by TMA) and for the data
-// gradient (A = dz: loaded by TMA from the materialised dz, or, for shapes too large for the
-// dz pass, computed from dy, z and the ReLU mask by producer warps; the filter is the forward
-// filter read MN-major with flipped taps).  See HaloGeom for the padded-linear row space in
-// which every filter tap is a row-shifted view of one halo tile.
+// gradient of the layers the fused backward kernel does not take (A = dz, loaded by TMA from
+// the materialised dz; the filter is the forward filter read MN-major with flipped taps).  See
+// HaloGeom for the padded-linear row space in which every filter tap is a row-shifted view of
+// one halo tile.
 //
-// Warp roles (A = number of A-producer warps: 1 for TMA, 4 for the dz producer):
-//   warps [0, A)       A producers (one halo stage per (unit, 64-channel chunk))
-//   warp  A            TMEM owner and single-thread tcgen05.mma issuer
-//   warp  A+1          TMA producer for the filter slabs (resident when they fit in smem)
-//   warps A+2 .. A+9   epilogue, two warps per TMEM lane quadrant (each takes half of the
+// Warp roles:
+//   warp 0             TMA producer of the A halo (one halo stage per (unit, 64-channel chunk))
+//   warp 1             TMEM owner and tcgen05.mma issuer
+//   warp 2             TMA producer for the filter slabs (resident when they fit in smem)
+//   warps 3 .. 10      epilogue, two warps per TMEM lane quadrant (each takes half of the
 //                      columns): TMEM -> registers -> stats / store
 // Pipelines: 2 halo stages, 2 TMEM accumulator stages (U*NOUT fp32 columns each), and a
 // 3-deep filter ring when the filter is streamed.  All waits are bounded (ptx.cuh).
@@ -18,13 +18,12 @@
 #include <type_traits>
 #include "cbr_internal.h"
 #include "common.cuh"
-#include "dz_producer.cuh"
 
 namespace cbr {
 
-// Fprop: A = input halo by TMA.  Dgrad: A = dz halo built in-kernel from (dy, z, mask) by four
-// producer warps.  DgradTma: A = a materialised dz halo by TMA; filter and epilogue as Dgrad.
-enum ConvKind : int { kKindFprop = 0, kKindDgrad = 1, kKindDgradTma = 2 };
+// Fprop: A = input halo by TMA.  DgradTma: A = a materialised dz halo by TMA, the filter read
+// MN-major with flipped taps, plain epilogue.
+enum ConvKind : int { kKindFprop = 0, kKindDgradTma = 2 };
 
 struct ConvArgs {
   HaloGeom g;
@@ -47,8 +46,6 @@ struct ConvArgs {
   long long m_count;
   double inv_m;             // 1 / m_count
   float unbias;             // m_count / (m_count - 1)
-  // dgrad A operand
-  DzSrc dz;
   uint32_t* err;
 };
 
@@ -66,7 +63,7 @@ constexpr int pow2_at_least(int v) {
 
 template <int KIND>
 struct Roles {
-  static constexpr int kAWarps = KIND == kKindDgrad ? 4 : 1;
+  static constexpr int kAWarps = 1;
   static constexpr int kMmaWarp = kAWarps;
   static constexpr int kWWarp = kAWarps + 1;
   static constexpr int kEpiWarp0 = kAWarps + 2;
@@ -254,7 +251,7 @@ __global__ void __launch_bounds__(Roles<KIND>::kThreads, 1)
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < 2; ++i) {
-      mbar_init(bar_halo_full + 8 * i, KIND == kKindDgrad ? 32 * R::kAWarps : 1);
+      mbar_init(bar_halo_full + 8 * i, 1);
       mbar_init(bar_halo_empty + 8 * i, 1);
       mbar_init(bar_acc_full + 8 * i, 1);
       mbar_init(bar_acc_empty + 8 * i, kEpiWarps);  // one arrival per epilogue warp
@@ -277,56 +274,31 @@ __global__ void __launch_bounds__(Roles<KIND>::kThreads, 1)
   const uint32_t tmem_base = *tmem_slot;
 
   if (warp < R::kAWarps) {
-    // ------------------------------------------------------------ A producers
-    if constexpr (KIND != kKindDgrad) {
-      if (lane == 0) {
-        prefetch_tensormap(&map_x);
-        const uint32_t tx = (uint32_t)g.hr * g.wp * 128;
-        uint32_t it = 0;
-        for (int u = blockIdx.x; u < g.total_units && !is_aborted(abort_flag); u += gridDim.x) {
-          const int n = u / g.upi;
-          const int m0 = (u - n * g.upi) * g.um;
-          const int h_lo = m0 / g.wp - g.pad;
-          for (int ch = 0; ch < NCH; ++ch, ++it) {
-            const uint32_t s = it & 1, ph = (it >> 1) & 1;
-            if (!mbar_wait_backoff(bar_halo_empty + 8 * s, ph ^ 1, 128)) {
-              set_abort(abort_flag, a.err, kErrWaitHalo);
-              break;
-            }
-            mbar_arrive_expect_tx(bar_halo_full + 8 * s, tx);
-            // several smaller boxes in flight instead of one large one (lower latency)
-            for (int r0 = 0; r0 < g.hr; r0 += g.box_rows)
-              tma_load_4d(halo_addr + s * L.halo_stride + (uint32_t)r0 * g.wp * 128, &map_x, ch * 64,
-                          -g.pad, h_lo + r0, n, bar_halo_full + 8 * s);
-          }
-        }
-        // never leave the CTA with a copy in flight
-        for (uint32_t k = (it > 2 ? it - 2 : 0); k < it; ++k)
-          mbar_wait(bar_halo_full + 8 * (k & 1), (k >> 1) & 1);
-      }
-    } else {
-      // dz producer: 4 warps build the zero-padded dz halo of each unit in smem
-      const int tid = threadIdx.x;  // 0..127
+    // ------------------------------------------------------------ A producer
+    if (lane == 0) {
+      prefetch_tensormap(&map_x);
+      const uint32_t tx = (uint32_t)g.hr * g.wp * 128;
       uint32_t it = 0;
       for (int u = blockIdx.x; u < g.total_units && !is_aborted(abort_flag); u += gridDim.x) {
         const int n = u / g.upi;
         const int m0 = (u - n * g.upi) * g.um;
         const int h_lo = m0 / g.wp - g.pad;
-        bool bad = false;
         for (int ch = 0; ch < NCH; ++ch, ++it) {
           const uint32_t s = it & 1, ph = (it >> 1) & 1;
           if (!mbar_wait_backoff(bar_halo_empty + 8 * s, ph ^ 1, 128)) {
-            set_abort(abort_flag, a.err, kErrWaitOperand);
-            bad = true;
+            set_abort(abort_flag, a.err, kErrWaitHalo);
             break;
           }
-          fill_dz_rows<BF16>(halo_addr + s * L.halo_stride, g.hr * g.wp, 0, g.wp, h_lo, g.pad, n,
-                             a.dz, ch, tid, 32 * R::kAWarps);
-          fence_proxy_async_smem();
-          mbar_arrive(bar_halo_full + 8 * s);
+          mbar_arrive_expect_tx(bar_halo_full + 8 * s, tx);
+          // several smaller boxes in flight instead of one large one (lower latency)
+          for (int r0 = 0; r0 < g.hr; r0 += g.box_rows)
+            tma_load_4d(halo_addr + s * L.halo_stride + (uint32_t)r0 * g.wp * 128, &map_x, ch * 64,
+                        -g.pad, h_lo + r0, n, bar_halo_full + 8 * s);
         }
-        if (bad) break;
       }
+      // never leave the CTA with a copy in flight
+      for (uint32_t k = (it > 2 ? it - 2 : 0); k < it; ++k)
+        mbar_wait(bar_halo_full + 8 * (k & 1), (k >> 1) & 1);
     }
   } else if (warp == R::kWWarp) {
     // ------------------------------------------------------------ filter producer

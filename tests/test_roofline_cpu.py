@@ -56,4 +56,23 @@ def test_inference_pass_is_tensor_bound_at_128_channels():
     assert p.flops == 2 * (64 * 112 * 112) * (3 * 3 * 128) * 128
     peaks = {"hbm_gbs": 6795.1, "bf16_tflops": 1900.2, "bf16_tflops_sustained": 1719.8}
     us, bound = p.roof_us(peaks)
-    assert bound == "tensor" and us == pytest.approx(236.76e9 / 1719.8e12 * 1e6, rel=1e-4)
+    assert bound == "tensor" and us == pytest.approx(236.76e9 / 1900.2e12 * 1e6, rel=1e-4)
+    us_s, _ = p.roof_us(peaks, sustained=True)
+    assert us_s == pytest.approx(236.76e9 / 1719.8e12 * 1e6, rel=1e-4)
+
+
+def test_kernel_passes_of_the_fused_backward():
+    """The fused dgrad + wgrad kernel reads dy, z, the mask, x and W once and writes dx and dW:
+    3 activations of the N=256 56x56 64-channel layer plus dx, two convolutions' FLOPs."""
+    ks = {p.name: p for p in roofline.kernel_passes(CONFIGS[3], need_dx=True, fused=True)}
+    assert set(ks) == {"conv_fprop_genstats", "bn_apply_relu", "bn_bwd_reduce", "conv_bwd_fused"}
+    assert ks["conv_bwd_fused"].bytes == 4 * S3 + MASK3 + W3 + DW3
+    assert ks["conv_bwd_fused"].flops == 2 * 59_190_018_048
+    # without dx (weight gradient only): no dx write, no filter read, one convolution
+    ks = {p.name: p for p in roofline.kernel_passes(CONFIGS[3], need_dx=False, fused=True)}
+    assert ks["conv_bwd_fused"].bytes == 3 * S3 + MASK3 + DW3
+    assert ks["conv_bwd_fused"].flops == 59_190_018_048
+    # materialised dz: the dz pass writes one activation more than it reads beyond the reduction
+    ks = {p.name: p for p in roofline.kernel_passes(CONFIGS[3], need_dx=True, fused=False)}
+    assert ks["bn_dz"].bytes == 3 * S3 + MASK3
+    assert ks["conv_wgrad"].bytes == 2 * S3 + DW3 and ks["conv_dgrad"].bytes == 2 * S3 + W3
