@@ -6,6 +6,7 @@ hot path: conv+genstats+finalize, apply+ReLU+mask, masked BN reduction, wgrad, d
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl cbr|reference] [--config ID]
                     [--e2e-steps E] [--copy-chunks C] [--recompute-z] [--no-cpu-baseline]
+                    [--batch N]
 
 Prints ONE JSON line on rank 0.  Timing: one step (L2 flush, then forward + backward through
 the library's public calls) is captured once as a CUDA graph and replayed per timed step,
@@ -16,6 +17,7 @@ calls the public API directly (no graph), with host copies inside the timed regi
 128-channel workload (--config 5) the folded inference call is timed as well.
 `--recompute-z` runs the step without a kept z (the backward recomputes it).
 `--impl reference` times the CPU oracle on the host cores instead (the reference arm).
+`--batch N` shrinks or grows the workload's batch, for profiling at a smaller size.
 Multi-GPU runs are independent replicas (weak scaling; no collective on the data path).
 """
 from __future__ import annotations
@@ -52,6 +54,9 @@ def parse():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="cbr", choices=["cbr", "reference"])
     ap.add_argument("--config", type=int, default=3)
+    ap.add_argument("--batch", type=int, default=0,
+                    help="diagnostics only: override the workload's batch size (the line then names the "
+                         "reduced workload)")
     ap.add_argument("--e2e-steps", type=int, default=20)
     # 1: host-to-device copies on GB300 run at about 210 GB/s with 2 to 32 streams alike
     ap.add_argument("--copy-chunks", type=int, default=1,
@@ -292,6 +297,8 @@ def run_cbr(args, world, rank, local):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     spec = CONFIGS[args.config]
+    if args.batch:
+        spec = spec.with_(n=args.batch, name=f"{spec.name} (batch {args.batch})")
     need_dx = not spec.first_layer
     layer = cbr.Layer.from_spec(spec)
     inp = make_inputs(spec, seed_for(args.config) + rank)

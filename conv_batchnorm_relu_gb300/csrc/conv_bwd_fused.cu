@@ -53,6 +53,7 @@ constexpr int kPUY = 5;               // the same when the mask is re-derived fr
 
 struct FusedKArgs {
   HaloGeom g;               // forward geometry, finished for U = 2 (um = 256)
+  const void* x;            // the forward input (for L2 prefetches; the halo itself is read by TMA)
   const void* dy;
   const void* z;
   const void* y;
@@ -113,16 +114,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int T = g.total_units;
   const int rows_img = g.p * g.wp;
   const bool has_dx = a.has_dx != 0;
-  // units of this CTA: blockIdx.x, + gridDim.x, ...; walked from the end of the batch, where the
-  // backward reduction that ran just before left dy and z in L2
-  auto unit_of = [&](int jj) { return T - 1 - (int)(blockIdx.x + (uint32_t)jj * gridDim.x); };
-  const int nunits = (T - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x;
+  // units of this CTA: a contiguous run of the T units (balanced to within one), walked from
+  // its last unit to its first, so that consecutive units of one image share 2*D dz tile rows
+  const int per = T / (int)gridDim.x, rem = T % (int)gridDim.x;
+  const int first = (int)blockIdx.x * per + min((int)blockIdx.x, rem);
+  const int nunits = per + ((int)blockIdx.x < rem ? 1 : 0);
+  auto unit_of = [&](int jj) { return first + nunits - 1 - jj; };
 
   if (threadIdx.x == 0) {
     mbar_init(bar(kBarXFull), 1);
     mbar_init(bar(kBarXEmpty), 1);
     for (int i = 0; i < 2; ++i) {
-      mbar_init(bar(kBarDzFull + i), kProdThreads);
+      mbar_init(bar(kBarDzFull + i), kProdWarps);
       mbar_init(bar(kBarDzEmpty + i), 1);
     }
     mbar_init(bar(kBarAccFull), 1);
@@ -152,11 +155,49 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int t = 0; t < rs; ++t) tma_load_3d(w_addr + (uint32_t)t * kWslab, &map_w, 0, rs - 1 - t, 0, bar(kBarWFull));
       }
       const uint32_t tx = (uint32_t)g.hr * g.wp * 128;
+      // L2 prefetch of what a unit's producers and halo load will read: the dy, z and mask (or
+      // y) pixels of its dz tile rows, and its input halo rows.  Issued two units ahead for the
+      // producers and one ahead for the halo, so their loads hit L2 instead of waiting on HBM.
+      const size_t img_px = (size_t)g.p * g.q;
+      auto prefetch_dz_inputs = [&](int u) {
+        const int n = u / g.upi;
+        const int m0 = (u - n * g.upi) * g.um;
+        const int l0 = max(m0 - a.D, 0), l1 = min(m0 + g.um + a.D, rows_img) - 1;
+        if (l1 < l0) return;
+        const int p0 = l0 / g.wp, p1 = l1 / g.wp;
+        const size_t px0 = (size_t)n * img_px + (size_t)p0 * g.q + min(l0 - p0 * g.wp, g.q);
+        const size_t px1 = (size_t)n * img_px + (size_t)p1 * g.q + min(l1 - p1 * g.wp, g.q - 1) + 1;
+        if (px1 <= px0) return;
+        const size_t row_b = (size_t)a.cout * 2;
+        const uint32_t bytes = (uint32_t)((px1 - px0) * row_b);
+        bulk_prefetch_l2(static_cast<const uint8_t*>(a.dy) + px0 * row_b, bytes);
+        bulk_prefetch_l2(static_cast<const uint8_t*>(a.z) + px0 * row_b, bytes);
+        if (a.mask) {
+          // whole 16-byte blocks inside the mask (one bit per element, n*P*Q*cout/8 bytes)
+          const size_t mask_end = ((size_t)g.n_img * img_px * a.cout / 8) & ~(size_t)15;
+          const size_t b0 = (px0 * a.cout / 8) & ~(size_t)15;
+          const size_t b1 = min((px1 * a.cout / 8 + 15) & ~(size_t)15, mask_end);
+          if (b1 > b0) bulk_prefetch_l2(a.mask + b0, (uint32_t)(b1 - b0));
+        } else {
+          bulk_prefetch_l2(static_cast<const uint8_t*>(a.y) + px0 * row_b, bytes);
+        }
+      };
+      const size_t xrow_b = (size_t)g.w * a.cin * 2;
+      auto prefetch_halo = [&](int u) {
+        const int n = u / g.upi;
+        const int m0 = (u - n * g.upi) * g.um;
+        const int h0 = max(m0 / g.wp - g.pad, 0), h1 = min(m0 / g.wp - g.pad + g.hr, g.h);
+        if (h1 > h0)
+          bulk_prefetch_l2(static_cast<const uint8_t*>(a.x) + ((size_t)n * g.h + h0) * xrow_b,
+                           (uint32_t)((size_t)(h1 - h0) * xrow_b));
+      };
       int issued = 0;
       for (int jj = 0; jj < nunits && !hc::is_aborted(abort_flag); ++jj) {
         const int u = unit_of(jj);
         const int n = u / g.upi;
         const int m0 = (u - n * g.upi) * g.um;
+        if (jj + 2 < nunits) prefetch_dz_inputs(unit_of(jj + 2));
+        if (jj + 1 < nunits) prefetch_halo(unit_of(jj + 1));
         if (!mbar_wait_backoff(bar(kBarXEmpty), (uint32_t)(jj & 1) ^ 1u, 64)) {
           hc::set_abort(abort_flag, a.err, kErrWaitHalo);
           break;
@@ -362,29 +403,31 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint8_t* dyb = static_cast<const uint8_t*>(a.dy);
     const uint8_t* zb = static_cast<const uint8_t*>(a.z);
     const uint8_t* yb = static_cast<const uint8_t*>(a.y);
-    const int nit = (a.nb - rsub + kRowStep - 1) / kRowStep;  // tile rows of this thread
     const int P = g.p, Q = g.q, wp = g.wp;
-    // one tile: rows L = m0 - D + rsub + 24k of image n; MASKBITS: the mask is the bit-packed
-    // forward mask, else it is re-derived as y > 0
-    auto fill = [&](auto maskbits_c, uint32_t dst, int n, int m0) {
+    const int ov = 2 * a.D;  // tile rows shared by consecutive units of one image
+    // Evaluate tile rows [0, nrows) of one unit: rows L = m0 - D + rsub + 24k of image n, in
+    // batches of NP items whose loads are all issued before the first is used.  MB: the mask is
+    // the bit-packed forward mask, else it is re-derived as y > 0.
+    auto fill = [&](auto maskbits_c, uint32_t dst, int n, int m0, int nrows) {
       constexpr bool MB = decltype(maskbits_c)::value;
+      constexpr int NP = MB ? kPU : kPUY;
+      const int nit = (nrows - rsub + kRowStep - 1) / kRowStep;  // tile rows of this thread
       const int L0 = m0 - a.D + rsub;
       int p = floor_div(L0, wp);
       int q = L0 - p * wp;
-      constexpr int NP = MB ? kPU : kPUY;
       for (int k0 = 0; k0 < nit; k0 += NP) {
         uint4 dv[NP], zv[NP], yv[MB ? 1 : NP];
         uint32_t mb[MB ? NP : 1];
-        uint32_t okm = 0;  // bit kb: item kb is inside the image (loaded)
+        uint32_t okm = 0;  // bit j: item j is inside the image (loaded)
 #pragma unroll
-        for (int kb = 0; kb < NP; ++kb) {
-          if (k0 + kb < nit && ch_ok && p >= 0 && p < P && q < Q) {
-            okm |= 1u << kb;
+        for (int j = 0; j < NP; ++j) {
+          if (k0 + j < nit && ch_ok && p >= 0 && p < P && q < Q) {
+            okm |= 1u << j;
             const size_t v = (((size_t)n * P + p) * Q + q) * cout + ch0;  // element index
-            dv[kb] = ld_global_nc_v4(dyb + v * 2);
-            zv[kb] = ld_global_nc_v4(zb + v * 2);
-            if constexpr (MB) mb[kb] = a.mask[v >> 3];
-            else yv[kb] = ld_global_nc_v4(yb + v * 2);
+            dv[j] = ld_global_nc_v4(dyb + v * 2);
+            zv[j] = ld_global_nc_v4(zb + v * 2);
+            if constexpr (MB) mb[j] = a.mask[v >> 3];
+            else yv[j] = ld_global_nc_v4(yb + v * 2);
           }
           q += kRowStep;
           while (q >= wp) {
@@ -393,57 +436,73 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
 #pragma unroll
-        for (int kb = 0; kb < NP; ++kb) {
-          if (k0 + kb >= nit) break;
+        for (int j = 0; j < NP; ++j) {
+          if (k0 + j >= nit) break;
           uint4 o = make_uint4(0u, 0u, 0u, 0u);
-          if (okm & (1u << kb)) {
+          if (okm & (1u << j)) {
             uint32_t bits;
             if constexpr (MB) {
-              bits = mb[kb];
+              bits = mb[j];
             } else {
-              const uint32_t yw[4] = {yv[kb].x, yv[kb].y, yv[kb].z, yv[kb].w};
+              const uint32_t yw[4] = {yv[j].x, yv[j].y, yv[j].z, yv[j].w};
               bits = 0;
 #pragma unroll
-              for (int j = 0; j < 4; ++j) {
-                const float2 yy = unpack2<BF16>(yw[j]);
-                bits |= (yy.x > 0.f ? 1u : 0u) << (2 * j);
-                bits |= (yy.y > 0.f ? 1u : 0u) << (2 * j + 1);
+              for (int e = 0; e < 4; ++e) {
+                const float2 yy = unpack2<BF16>(yw[e]);
+                bits |= (yy.x > 0.f ? 1u : 0u) << (2 * e);
+                bits |= (yy.y > 0.f ? 1u : 0u) << (2 * e + 1);
               }
             }
-            const uint32_t dw[4] = {dv[kb].x, dv[kb].y, dv[kb].z, dv[kb].w};
-            const uint32_t zw[4] = {zv[kb].x, zv[kb].y, zv[kb].z, zv[kb].w};
+            const uint32_t dw[4] = {dv[j].x, dv[j].y, dv[j].z, dv[j].w};
+            const uint32_t zw[4] = {zv[j].x, zv[j].y, zv[j].z, zv[j].w};
             uint32_t ow[4];
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              const float2 d = unpack2<BF16>(dw[j]);
-              const float2 zz = unpack2<BF16>(zw[j]);
-              const float g0 = (bits >> (2 * j)) & 1u ? d.x : 0.f;
-              const float g1 = (bits >> (2 * j + 1)) & 1u ? d.y : 0.f;
-              const float r0 = fmaf(ca[2 * j], g0, fmaf(-cd[2 * j], zz.x, ce[2 * j]));
-              const float r1 = fmaf(ca[2 * j + 1], g1, fmaf(-cd[2 * j + 1], zz.y, ce[2 * j + 1]));
-              ow[j] = pack2<BF16>(r0, r1);
+            for (int e = 0; e < 4; ++e) {
+              const float2 d = unpack2<BF16>(dw[e]);
+              const float2 zz = unpack2<BF16>(zw[e]);
+              const float g0 = (bits >> (2 * e)) & 1u ? d.x : 0.f;
+              const float g1 = (bits >> (2 * e + 1)) & 1u ? d.y : 0.f;
+              const float r0 = fmaf(ca[2 * e], g0, fmaf(-cd[2 * e], zz.x, ce[2 * e]));
+              const float r1 = fmaf(ca[2 * e + 1], g1, fmaf(-cd[2 * e + 1], zz.y, ce[2 * e + 1]));
+              ow[e] = pack2<BF16>(r0, r1);
             }
             o = make_uint4(ow[0], ow[1], ow[2], ow[3]);
           }
-          st_shared_v4(dst + swz_off((uint32_t)(rsub + kRowStep * (k0 + kb)), (uint32_t)c8, 128), o);
+          st_shared_v4(dst + swz_off((uint32_t)(rsub + kRowStep * (k0 + j)), (uint32_t)c8, 128), o);
         }
       }
     };
-    for (int jj = 0; jj < nunits && !hc::is_aborted(abort_flag); ++jj) {
+    int prev_u = -1;
+    for (int jj = 0; jj < nunits; ++jj) {
       const int u = unit_of(jj);
       const int n = u / g.upi;
       const int m0 = (u - n * g.upi) * g.um;
       const uint32_t s = jj & 1, ph = (jj >> 1) & 1;
-      if (!mbar_wait_backoff(bar(kBarDzEmpty + s), ph ^ 1u, 64)) {
-        hc::set_abort(abort_flag, a.err, kErrWaitOperand);
-        break;
-      }
+      const bool live = !hc::is_aborted(abort_flag);
+      const bool waited = live && mbar_wait_backoff(bar(kBarDzEmpty + s), ph ^ 1u, 64);
+      if (live && !waited) hc::set_abort(abort_flag, a.err, kErrWaitOperand);
+      // Every producer thread votes here once per unit, so they all leave the loop together (a
+      // named barrier has no time limit).  Passing it also means every producer has finished
+      // writing the previous unit's tile, whose rows are copied below.
+      if (!named_bar_and(1, kProdThreads, waited)) break;
       const uint32_t dst = dz_addr + s * L.dz_stride;
-      if (a.mask) fill(std::true_type{}, dst, n, m0);
-      else fill(std::false_type{}, dst, n, m0);
-      // generic-proxy writes -> visible to the tensor cores, then one arrival per thread
+      // The previous unit (u + 1, same image) begins um rows later: its tile rows [0, 2D) are
+      // this tile's rows [um, um + 2D).  um is a multiple of 8, so both have the same swizzle
+      // phase and the 128-byte rows are copied verbatim.
+      const bool reuse = prev_u == u + 1 && prev_u / g.upi == n && ov > 0;
+      if (reuse) {
+        const uint32_t src = dz_addr + (s ^ 1u) * L.dz_stride;
+        for (int i = tid; i < ov * 8; i += kProdThreads)
+          st_shared_v4(dst + (uint32_t)g.um * 128u + (uint32_t)i * 16u, ld_shared_v4(src + (uint32_t)i * 16u));
+      }
+      const int nrows = reuse ? g.um : a.nb;
+      if (a.mask) fill(std::true_type{}, dst, n, m0, nrows);
+      else fill(std::false_type{}, dst, n, m0, nrows);
+      // generic-proxy writes -> visible to the tensor cores; one arrival per warp
       fence_proxy_async_smem();
-      mbar_arrive(bar(kBarDzFull + s));
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(kBarDzFull + s));
+      prev_u = u;
     }
   }
 
@@ -521,6 +580,7 @@ int launch_bwd_fused(const BwdFusedArgs& f, int c_in, int c_out, bool bf16, cons
     a.ta[i] = plan.ta[i];
     a.tb[i] = plan.tb[i];
   }
+  a.x = x;
   a.dy = f.dy;
   a.z = f.z;
   a.y = f.y;
