@@ -18,8 +18,7 @@ __device__ uint32_t g_error_word;
 
 namespace {
 
-constexpr size_t kHdrBytes = 256;    // arrival counters live here
-constexpr int kMaxCtas = 256;        // partial-statistics buffers are sized for this many CTAs
+constexpr size_t kHdrBytes = kWsHeaderBytes;  // arrival counters live here
 constexpr int kMaxDevices = 64;
 
 size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
@@ -267,12 +266,32 @@ bool encode_tiled_mode(CUtensorMap* map, CUtensorMapDataType dt, int rank, const
 }
 }  // namespace
 
-int forward_workspace_bytes(const void* desc, bool need_z, size_t* bytes) {
+int check_forward_train(const void* desc, const void* x, const void* w, const float* gamma,
+                        const float* beta, const float* running_mean, const float* running_var,
+                        float momentum, float eps, const void* y, const uint32_t* relu_mask,
+                        const void* z_saved, const float* saved_mean, const float* saved_inv_var,
+                        size_t* ws_need) {
   Shape s;
-  const int st = check_desc(static_cast<const cbr_desc_t*>(desc), &s);
+  int st = check_desc(static_cast<const cbr_desc_t*>(desc), &s);
   if (st) return st;
-  *bytes = fwd_ws(s, need_z).total;
+  if (!x || !w || !gamma || !beta || !running_mean || !running_var || !y || !saved_mean ||
+      !saved_inv_var)
+    return CBR_ERR_INVALID_ARG;
+  if (!(momentum >= 0.f && momentum <= 1.f) || !(eps > 0.f) || !std::isfinite(eps))
+    return CBR_ERR_INVALID_ARG;
+  if (!aligned(x, 16) || !aligned(w, 16) || !aligned(y, 16) || (z_saved && !aligned(z_saved, 16)) ||
+      (relu_mask && !aligned(relu_mask, 4)) || !aligned(gamma, 4) || !aligned(beta, 4) ||
+      !aligned(running_mean, 4) || !aligned(running_var, 4) || !aligned(saved_mean, 4) ||
+      !aligned(saved_inv_var, 4))
+    return CBR_ERR_MISALIGNED;
+  if ((st = check_supported(s))) return st;
+  *ws_need = fwd_ws(s, z_saved == nullptr).total;
   return CBR_OK;
+}
+
+int check_device() {
+  DeviceInfo* dev = nullptr;
+  return current_device(&dev);
 }
 
 bool ensure_smem_attr(const void* func, int bytes) {
@@ -329,22 +348,16 @@ cbr_status_t cbr_forward_train(const cbr_desc_t* desc, const void* x, const void
                                uint32_t* relu_mask, void* z_saved, float* saved_mean,
                                float* saved_inv_var, void* ws, size_t ws_bytes,
                                cbr_stream_t stream) {
-  Shape s;
-  int st = check_desc(desc, &s);
+  size_t need = 0;
+  int st = check_forward_train(desc, x, w, gamma, beta, running_mean, running_var, momentum, eps, y,
+                               relu_mask, z_saved, saved_mean, saved_inv_var, &need);
   if (st) return (cbr_status_t)st;
-  if (!x || !w || !gamma || !beta || !running_mean || !running_var || !y || !saved_mean ||
-      !saved_inv_var || !ws)
-    return CBR_ERR_INVALID_ARG;
-  if (!(momentum >= 0.f && momentum <= 1.f) || !(eps > 0.f) || !std::isfinite(eps))
-    return CBR_ERR_INVALID_ARG;
-  if (!aligned(x, 16) || !aligned(w, 16) || !aligned(y, 16) || !aligned(ws, 16) ||
-      (z_saved && !aligned(z_saved, 16)) || (relu_mask && !aligned(relu_mask, 4)) ||
-      !aligned(gamma, 4) || !aligned(beta, 4) || !aligned(running_mean, 4) ||
-      !aligned(running_var, 4) || !aligned(saved_mean, 4) || !aligned(saved_inv_var, 4))
-    return CBR_ERR_MISALIGNED;
-  if ((st = check_supported(s))) return (cbr_status_t)st;
+  if (!ws) return CBR_ERR_INVALID_ARG;
+  if (!aligned(ws, 16)) return CBR_ERR_MISALIGNED;
+  if (ws_bytes < need) return CBR_ERR_WORKSPACE;
+  Shape s;
+  check_desc(desc, &s);
   const FwdWs L = fwd_ws(s, z_saved == nullptr);
-  if (ws_bytes < L.total) return CBR_ERR_WORKSPACE;
   DeviceInfo* dev = nullptr;
   if ((st = current_device(&dev))) return (cbr_status_t)st;
 

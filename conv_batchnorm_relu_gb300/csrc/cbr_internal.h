@@ -8,6 +8,18 @@
 
 namespace cbr {
 
+// Workspace sizing constants (cbr_api.cu): the first kWsHeaderBytes of every workspace hold
+// arrival counters, and per-CTA partial buffers are sized for at most kMaxCtas CTAs (the grids
+// never exceed the SM count, clamped to this).
+constexpr size_t kWsHeaderBytes = 256;
+constexpr int kMaxCtas = 256;
+constexpr size_t align256(size_t v) { return (v + 255) / 256 * 256; }
+// Training-forward workspace with the conv output kept by the caller: the counters, 2*Cout
+// floats of apply coefficients and 2*Cout floats of partial statistics per CTA.
+constexpr size_t forward_scratch_bytes(int c_out) {
+  return align256(align256(kWsHeaderBytes + 2 * (size_t)c_out * 4) + (size_t)kMaxCtas * 2 * c_out * 4);
+}
+
 // Geometry of a stride-1 convolution computed over "padded-linear" rows.
 //
 // Output pixel (p, q) of image n is row m = p*wp + q of a per-image row space whose width is
@@ -58,9 +70,16 @@ enum FpropMode : int {
 // device and kernel; thread-safe).  Returns false if the runtime refuses.
 bool ensure_smem_attr(const void* func, int bytes);
 
-// Forward workspace bytes for a descriptor (z kept by the caller when !need_z); returns a
-// CBR status (cbr_api.cu).
-int forward_workspace_bytes(const void* desc, bool need_z, size_t* bytes);
+// The argument checks cbr_forward_train makes before it enqueues anything (descriptor,
+// pointers, scalars, alignment, supported shape), but not the workspace or the device; on
+// success *ws_need is the workspace the call needs (cbr_api.cu).  Returns a CBR status.
+int check_forward_train(const void* desc, const void* x, const void* w, const float* gamma,
+                        const float* beta, const float* running_mean, const float* running_var,
+                        float momentum, float eps, const void* y, const uint32_t* relu_mask,
+                        const void* z_saved, const float* saved_mean, const float* saved_inv_var,
+                        size_t* ws_need);
+// CBR_OK if the current device is one this library runs on (compute 10.3), else CBR_ERR_DEVICE.
+int check_device();
 
 // Tensor-map helpers (cbr_api.cu).
 bool encode_tiled(CUtensorMap* map, CUtensorMapDataType dt, int rank, const void* base,

@@ -1,15 +1,19 @@
-// First-layer convolution (Tech-Renaissance CBR page, section 6: the network's first CBR takes
-// the 3-channel image, 7x7 filter, stride 2, padding 3, and has no dgrad).  A 3-channel pixel
-// is 6 bytes, so the input cannot be the innermost dimension of a TMA tile; instead whole
-// input rows (W*3 contiguous elements) are staged in shared memory by TMA and four builder
-// warps assemble the im2col tile from them:
-//   - one unit = one output row (n, p): Q <= 128 pixels = the M rows of one tile;
-//   - K slot of (r, s, c) = r*24 + s*3 + c: each filter row is a 24-slot segment (S*3 <= 24
-//     values and zeros), so a row of the tile is three 128-byte K atoms (K <= 192);
-//   - the filter is laid out in the same slot order once per CTA.
-// Forward: z = im2col(x) * W^T on the tensor cores (K = 16 per MMA, ceil(R*24/16) MMAs per unit),
-// then the same epilogue as the other convolutions (statistics in registers, direct stores).
-// WGrad: dW^T = im2col(x)^T * dz, with the same tile read as an MN-major operand.
+// First-layer convolution: the CBR block that takes the 3-channel image (Tech-Renaissance CBR
+// page, section 5.3: the first layer's backward skips DGrad, because its input is the training
+// data).  The 7x7 stride-2 padding-3 shape is the standard image stem these kernels are tuned
+// for.  A 3-channel pixel is 6 bytes, so the input cannot be the innermost dimension of a TMA
+// tile or an MMA operand row; two designs handle it:
+//   - implicit im2col (the main path, stride 1 or 2; first_fprop_imp_kernel and
+//     first_wgrad_imp_kernel): every input row is padded to 16-byte groups of 8/stride channel
+//     slots per pixel, and each filter row's im2col tile is read straight out of the padded
+//     row through an unswizzled descriptor whose core matrices overlap (no tile is assembled);
+//   - builder warps (other strides, and the weight gradient at Cout other than 64;
+//     first_fprop_kernel and first_wgrad_kernel): whole input rows are staged in shared memory
+//     and four warps assemble an im2col tile with K slot r*24 + s*3 + c (each filter row a
+//     24-slot segment, three 128-byte K atoms, K <= 192).
+// Forward: z = im2col(x) * W^T on the tensor cores, with the epilogue of the other convolutions
+// (statistics in registers, direct stores).  WGrad: dW^T = im2col(x)^T * dz, with the same
+// operand read MN-major.
 #include <algorithm>
 #include <type_traits>
 
@@ -391,7 +395,7 @@ __global__ void __launch_bounds__(kFlThreads, 1)
 
 
 // ------------------------------------------------------------------------------ forward, implicit im2col
-// Stride 1 or 2 (Tech-Renaissance CBR page, section 6, the 7x7 stride-2 first layer): pad each
+// Stride 1 or 2 (the 7x7 stride-2 image stem among them): pad each
 // pixel to 8/stride channel slots, so `stride` adjacent pixels fill one 16-byte group and the
 // run of filter row rr for output pixel q starts at group q + const of the padded input row.
 // The im2col tile of a filter row is then the padded row itself read through a descriptor

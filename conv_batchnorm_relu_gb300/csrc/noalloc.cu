@@ -11,9 +11,11 @@ namespace {
 
 // Upper bound on the scratch this entry point can use.  With the conv output kept by the
 // caller (z_saved), the forward needs 256 bytes of arrival counters, 2*Cout floats of apply
-// coefficients and 2*Cout floats of partial statistics per CTA (at most 256 CTAs): about
+// coefficients and 2*Cout floats of partial statistics per CTA (at most kMaxCtas CTAs): about
 // 257 KiB for Cout = 128.  Every GPU that loads the library holds this array until exit.
 constexpr size_t kNoAllocScratchBytes = 320 * 1024;
+static_assert(kNoAllocScratchBytes >= forward_scratch_bytes(128),
+              "the fixed scratch must hold the largest supported forward (Cout = 128, kMaxCtas CTAs)");
 static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
 
 constexpr int kMaxDevices = 64;
@@ -50,18 +52,20 @@ extern "C" cbr_status_t cbr_forward_train_noalloc(
     float* running_mean, float* running_var, float momentum, float eps, void* y,
     uint32_t* relu_mask, void* z_saved, float* saved_mean, float* saved_inv_var,
     cbr_stream_t stream) {
+  // Every argument and the device are checked before the scratch is touched, so a rejected call
+  // enqueues nothing (in particular not the counter reset below, which could otherwise clear the
+  // counters of an earlier call still running on the shared array).
   size_t need = 0;
-  int st = cbr::forward_workspace_bytes(desc, false, &need);
+  int st = cbr::check_forward_train(desc, x, w, gamma, beta, running_mean, running_var, momentum, eps,
+                                    y, relu_mask, z_saved, saved_mean, saved_inv_var, &need);
   if (st) return (cbr_status_t)st;
   if (!z_saved) return CBR_ERR_INVALID_ARG;  // the conv output cannot live in the fixed scratch
   if (need > cbr::kNoAllocScratchBytes) return CBR_ERR_WORKSPACE;
-  if (!x || !w || !gamma || !beta || !running_mean || !running_var || !y || !saved_mean ||
-      !saved_inv_var)
-    return CBR_ERR_INVALID_ARG;
+  if ((st = cbr::check_device())) return (cbr_status_t)st;
   void* scratch = nullptr;
   if ((st = cbr::scratch_address(&scratch))) return (cbr_status_t)st;
   // The arrival counters must start at zero; the array keeps whatever the last call left.
-  if (cudaMemsetAsync(scratch, 0, 256, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) {
+  if (cudaMemsetAsync(scratch, 0, cbr::kWsHeaderBytes, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) {
     cudaGetLastError();
     return CBR_ERR_CUDA;
   }

@@ -112,17 +112,18 @@ def mask_slack(spec, o: dict, ref: dict, rb: dict, margin: float = MASK_MARGIN) 
     return dict(dx=sl["dx"], dw=sl["dw"], dbeta=s1, dgamma=s2, count=int(amb.sum()))
 
 
-def mask_slack_core(idx, vals, u, x, w, stride: int, pad: int, taps=None, pixels=None) -> dict:
+def mask_slack_core(idx, vals, u, x, w, stride: int, pad: int, taps=None, pixels=None,
+                    need_dx: bool | None = None) -> dict:
     """Propagate per-point dz changes through both backward convolutions.
 
     idx: (n, p, q, k) rows of the ambiguous output points; vals: the bound on |delta dz| at
     each; u[k]: the bound on |delta dz| at every point of channel k (through dbeta/dgamma).
     Returns the dx bound (all input pixels, or the listed (n, h, w) pixels; None when neither
-    pixels nor a full dx is wanted, i.e. taps given without pixels) and the dW bound (all taps,
-    or the listed (k, r, s) taps)."""
+    pixels nor a full dx is wanted, i.e. taps given without pixels, or need_dx is False) and the
+    dW bound (all taps, or the listed (k, r, s) taps)."""
     _, H, W, C = x.shape
     K, R, S = w.shape[0], w.shape[1], w.shape[2]
-    want_dx = pixels is not None or taps is None
+    want_dx = (pixels is not None or taps is None) if need_dx is None else need_dx
     dx_sl = np.zeros_like(x) if want_dx else None
     dw_sl = np.zeros_like(w)
     aw, ax = np.abs(w), np.abs(x)
@@ -150,7 +151,7 @@ def mask_slack_core(idx, vals, u, x, w, stride: int, pad: int, taps=None, pixels
 
 
 def max_err_ok_slack(got, ref, slack, name: str) -> float:
-    """max_err_ok with an element-wise allowance added to the bound."""
+    """max_err_ok with an element-wise allowance added to the bound; returns max|err|."""
     got, ref = np.asarray(got, dtype=np.float64), np.asarray(ref, dtype=np.float64)
     assert got.shape == ref.shape, (name, got.shape, ref.shape)
     assert np.all(np.isfinite(got)), f"{name}: non-finite values"
@@ -161,6 +162,8 @@ def max_err_ok_slack(got, ref, slack, name: str) -> float:
 
 
 def stat_close_slack(got, ref, scale, slack, name: str, extra=None) -> float:
+    """Per-channel |err| <= 1e-3*max(|ref|, scale) + slack (+ extra); returns the worst ratio of
+    error to that widened tolerance."""
     got, ref, scale = (np.asarray(a, dtype=np.float64) for a in (got, ref, scale))
     tol = STAT_RTOL * np.maximum(np.abs(ref), scale) + slack
     if extra is not None:
@@ -168,6 +171,13 @@ def stat_close_slack(got, ref, scale, slack, name: str, extra=None) -> float:
     worst = float((np.abs(got - ref) / tol).max())
     assert worst <= 1.0, f"{name}: worst error / tolerance {worst:.3g} > 1"
     return worst
+
+
+def scaled_error(got, ref, scale) -> float:
+    """The unwidened per-channel error |err| / max(|ref|, scale), worst over channels (the bare
+    1e-3 criterion, before any allowance is added)."""
+    got, ref, scale = (np.asarray(a, dtype=np.float64) for a in (got, ref, scale))
+    return float((np.abs(got - ref) / np.maximum(np.abs(ref), scale)).max())
 
 
 def dgamma_storage_rounding(spec, o: dict, ref: dict) -> np.ndarray:

@@ -115,6 +115,11 @@ FIRST_CASES = {
                             x_dist="uniform2.5", first_layer=True), 2013),
     "first_c128": (CBRSpec("first c128", n=1, h=16, w=16, c_in=3, c_out=128, r=7, s=7, stride=2, pad=3,
                            x_dist="uniform2.5", first_layer=True), 2014),
+    # strides 3 and 4: the builder-warp im2col kernels, forward and weight gradient
+    "first_s3_5x5": (CBRSpec("first s3 5x5", n=2, h=31, w=35, c_in=3, c_out=32, r=5, s=5, stride=3, pad=2,
+                             x_dist="uniform2.5", first_layer=True), 2015),
+    "first_s4_7x7": (CBRSpec("first s4 7x7", n=2, h=40, w=48, c_in=3, c_out=64, r=7, s=7, stride=4, pad=3,
+                             x_dist="uniform2.5", first_layer=True), 2016),
 }
 
 

@@ -38,6 +38,11 @@ CASES = {
                             x_dist="uniform2.5", first_layer=True), 2013),
     "first_c128": (CBRSpec("first c128", n=1, h=16, w=16, c_in=3, c_out=128, r=7, s=7, stride=2, pad=3,
                            x_dist="uniform2.5", first_layer=True), 2014),
+    # strides other than 1 and 2: the builder-warp im2col forward (first_fprop_kernel)
+    "first_s3_5x5": (CBRSpec("first s3 5x5", n=2, h=31, w=35, c_in=3, c_out=32, r=5, s=5, stride=3, pad=2,
+                             x_dist="uniform2.5", first_layer=True), 2015),
+    "first_s4_7x7": (CBRSpec("first s4 7x7", n=2, h=40, w=48, c_in=3, c_out=64, r=7, s=7, stride=4, pad=3,
+                             x_dist="uniform2.5", first_layer=True), 2016),
 }
 
 
@@ -86,21 +91,27 @@ def test_forward_deterministic():
         assert torch.equal(a[k], b[k]), k
 
 
-@pytest.mark.parametrize("case", ["ragged_13x29", "c128_bf16", "first_32x32"])
-def test_fold_and_infer_parity(case):
+@pytest.mark.parametrize("case,with_bias", [("ragged_13x29", False), ("c128_bf16", False),
+                                            ("first_32x32", False), ("ragged_13x29", True),
+                                            ("first_s3_5x5", True)])
+def test_fold_and_infer_parity(case, with_bias):
+    """cbr_fold_bn (with and without a conv bias) and the folded inference forward."""
     spec, seed = CASES[case]
     inp = make_inputs(spec, seed, with_dy=False)
     gen = torch.Generator().manual_seed(seed + 7)
     rm = torch.randn(spec.c_out, generator=gen) * 0.2
     rv = torch.rand(spec.c_out, generator=gen) + 0.5
+    bias = torch.randn(spec.c_out, generator=gen) * 0.3 if with_bias else None
     layer = cbr.Layer.from_spec(spec)
     g = {k: v.cuda() for k, v in inp.items()}
-    w_fold, b_fold = cbr.fold_bn(layer, g["w"], g["gamma"], g["beta"], rm.cuda(), rv.cuda(), spec.eps)
+    w_fold, b_fold = cbr.fold_bn(layer, g["w"], g["gamma"], g["beta"], rm.cuda(), rv.cuda(), spec.eps,
+                                 conv_bias=None if bias is None else bias.cuda())
     y = cbr.forward_infer(layer, g["x"], w_fold, b_fold)
     cbr.stream_status()
     o = oracle_inputs(inp)
     ref = oracle.forward_infer(o["x"], o["w"], o["gamma"], o["beta"], rm.double().numpy(),
-                               rv.double().numpy(), spec.eps, spec.stride, spec.pad)
+                               rv.double().numpy(), spec.eps, spec.stride, spec.pad,
+                               conv_bias=None if bias is None else bias.double().numpy())
     max_err_ok(to_np(b_fold), ref["b_fold"], "b_fold")
     max_err_ok(to_np(w_fold), ref["w_fold"], "w_fold")
     max_err_ok(to_np(y), ref["y"], "y_infer")

@@ -7,10 +7,11 @@ The oracle computes the forward in full: the 7-loop convolution over every outpu
 two-pass batch statistics, and the normalise/affine/ReLU step.  z, y and the mask are compared
 element by element (in chunks of images, to bound host memory), the statistics and the running
 statistics channel by channel, and dgamma/dbeta from the oracle's full BN backward.  The two
-backward convolutions are compared on sampled outputs that the oracle evaluates one by one:
-dx at sampled input pixels (every image corner and edge among them) and dW at sampled filter
-taps.  The 128->128 layer also checks the folded inference path (fold in full, y at sampled
-output pixels).  Tolerances and the mask-ambiguity allowance are those of tests/parity.py.
+backward convolutions are compared in full: every element of dx and of dW against the
+oracle's 7-loop data and weight gradients of its own dz.  dgamma's error is also printed
+before the allowances are added.  The 128->128 layer also checks the folded inference path
+(fold in full, y at sampled output pixels).  Tolerances and the mask-ambiguity allowance are
+those of tests/parity.py.
 """
 from __future__ import annotations
 
@@ -22,7 +23,7 @@ import oracle
 from conv_batchnorm_relu_gb300 import cbr
 from conv_batchnorm_relu_gb300.inputs import CONFIGS, make_inputs, seed_for
 from parity import (ATOL, MASK_MARGIN, RTOL_MAX, UNIT_ROUNDOFF, mask_slack_core, max_err_ok,
-                    max_err_ok_slack, rel_close, stat_close, stat_close_slack)
+                    max_err_ok_slack, rel_close, scaled_error, stat_close, stat_close_slack)
 
 pytestmark = pytest.mark.gpu
 
@@ -55,10 +56,11 @@ def host_bytes_available() -> int:
 
 
 def host_bytes_needed(spec) -> int:
-    """Peak fp64 host memory of this check: x, z, xhat, dy, dz (and dx's allowance), bytes."""
+    """Peak fp64 host memory of this check: x, z, xhat, dy, dz and the full dx comparison, bytes."""
     out = spec.m * spec.c_out
     inp = spec.n * spec.h * spec.w * spec.c_in
-    return 8 * (4 * out + 3 * inp) + 2 * out + 8 * CHUNK_ELEMS * 8
+    dx_bufs = 0 if spec.first_layer else 3 * inp  # dx: oracle, allowance, GPU result
+    return 8 * (4 * out + 3 * inp + dx_bufs) + 2 * out + 8 * CHUNK_ELEMS * 8
 
 
 def sample_pixels(rng, n, h, w, count):
@@ -71,12 +73,6 @@ def sample_pixels(rng, n, h, w, count):
             fixed.append((img, hh, ww))
     rnd = np.stack([rng.integers(0, n, count), rng.integers(0, h, count),
                     rng.integers(0, w, count)], axis=1)
-    return np.unique(np.concatenate([np.array(fixed), rnd]), axis=0).astype(np.int32)
-
-
-def sample_taps(rng, k, r, s, count):
-    fixed = [(0, 0, 0), (k - 1, r - 1, s - 1), (0, r - 1, 0), (k - 1, 0, s - 1), (k // 2, r // 2, s // 2)]
-    rnd = np.stack([rng.integers(0, k, count), rng.integers(0, r, count), rng.integers(0, s, count)], axis=1)
     return np.unique(np.concatenate([np.array(fixed), rnd]), axis=0).astype(np.int32)
 
 
@@ -96,10 +92,10 @@ class MaxErr:
         assert self.err <= bound, f"{self.name}: max|err| {self.err:.4g} > {bound:.4g}"
 
 
-def check_full_size(spec, inp, gpu, rng):
+def check_full_size(spec, inp, gpu):
     """Compare one full-size GPU training step against the oracle.  ``gpu`` maps names to
     fp64 numpy results: per-channel vectors and dW whole; z, y (and the unpacked mask) through
-    ``gpu["chunk"](name, n0, n1)``; dx through ``gpu["dx_at"](pixels)``."""
+    ``gpu["chunk"](name, n0, n1)``; dx through ``gpu["dx"]()``."""
     K, st, pad = spec.c_out, spec.stride, spec.pad
     x = inp["x"].double().numpy()
     w = inp["w"].double().numpy()
@@ -173,23 +169,27 @@ def check_full_size(spec, inp, gpu, rng):
     vals = np.abs(a[idx[:, 3]] * np.concatenate(amb_dy))
     u = a * (s1 + xh_max * s2) / M
     u_rounding = UNIT_ROUNDOFF[spec.dtype]
-    stat_close_slack(gpu["dbeta"], dbeta, np.sqrt(rss_b2), s1, "dbeta")
-    stat_close_slack(gpu["dgamma"], dgamma, np.sqrt(rss_g2), s2, "dgamma",
-                     extra=4.0 * (u_rounding / np.sqrt(3.0)) * inv * np.sqrt(gz2))
+    db_ratio = stat_close_slack(gpu["dbeta"], dbeta, np.sqrt(rss_b2), s1, "dbeta")
+    dg_ratio = stat_close_slack(gpu["dgamma"], dgamma, np.sqrt(rss_g2), s2, "dgamma",
+                                extra=4.0 * (u_rounding / np.sqrt(3.0)) * inv * np.sqrt(gz2))
+    # the bare 1e-3 criterion, before the mask and storage-rounding allowances, reported beside
+    db_bare = scaled_error(gpu["dbeta"], dbeta, np.sqrt(rss_b2))
+    dg_bare = scaled_error(gpu["dgamma"], dgamma, np.sqrt(rss_g2))
+    print(f"\n{spec.name}: dgamma unwidened error {dg_bare:.3g} (of the 1e-3 bound: {dg_bare / 1e-3:.2f}x), "
+          f"error / widened tolerance {dg_ratio:.3g}; dbeta unwidened {db_bare:.3g}, ratio {db_ratio:.3g}")
 
-    # ---- dW at sampled taps, dx at sampled input pixels
-    taps = sample_taps(rng, K, spec.r, spec.s, 48)
+    # ---- dW and dx in full (oracle 7-loop convolutions over every output)
     need_dx = not spec.first_layer
-    pix = sample_pixels(rng, spec.n, spec.h, spec.w, 384) if need_dx else None
-    sl = mask_slack_core(idx, vals, u, x, w, st, pad, taps=taps, pixels=pix)
-    dw_ref = oracle.conv2d_wgrad_at(dz, x, (spec.r, spec.s), st, pad, taps)
-    dw_got = gpu["dw"][taps[:, 0], taps[:, 1], taps[:, 2]]
-    max_err_ok_slack(dw_got, dw_ref, sl["dw"], "dw (sampled taps)")
+    sl = mask_slack_core(idx, vals, u, x, w, st, pad, need_dx=need_dx)
+    dw_ref = oracle.conv2d_wgrad(dz, x, (spec.r, spec.s), st, pad)
+    err_dw = max_err_ok_slack(gpu["dw"], dw_ref, sl["dw"], "dw")
+    err_dx = None
     if need_dx:
-        dx_ref = oracle.conv2d_dgrad_at(dz, w, (spec.h, spec.w), st, pad, pix)
-        max_err_ok_slack(gpu["dx_at"](pix), dx_ref, sl["dx"], "dx (sampled pixels)")
-    return dict(ambiguous=int(idx.shape[0]), taps=int(taps.shape[0]),
-                pixels=0 if pix is None else int(pix.shape[0]))
+        dx_ref = oracle.conv2d_dgrad(dz, w, (spec.h, spec.w), st, pad)
+        err_dx = max_err_ok_slack(gpu["dx"](), dx_ref, sl["dx"], "dx")
+    return dict(ambiguous=int(idx.shape[0]), err_dw=err_dw, err_dx=err_dx,
+                dgamma_unwidened=dg_bare, dbeta_unwidened=db_bare,
+                dgamma_ratio=dg_ratio, dbeta_ratio=db_ratio)
 
 
 def _unpack_chunk(words: torch.Tensor, e0: int, e1: int) -> np.ndarray:
@@ -221,14 +221,13 @@ def run_full_step(spec):
             return _unpack_chunk(out["mask"], n0 * per_img, n1 * per_img)
         return out[name][n0:n1].double().cpu().numpy()
 
-    def dx_at(pix):
-        t = torch.as_tensor(pix, dtype=torch.long)
-        return bwd["dx"][t[:, 0].cuda(), t[:, 1].cuda(), t[:, 2].cuda()].double().cpu().numpy()
+    def dx_all():
+        return bwd["dx"].double().cpu().numpy()
 
     res = dict(saved_mean=vec(out["saved_mean"]), saved_inv_var=vec(out["saved_inv_var"]),
                running_mean=vec(g["running_mean"]), running_var=vec(g["running_var"]),
                dgamma=vec(bwd["dgamma"]), dbeta=vec(bwd["dbeta"]), dw=vec(bwd["dw"]),
-               chunk=chunk, dx_at=dx_at)
+               chunk=chunk, dx=dx_all)
     return inp, g, res
 
 
@@ -247,8 +246,8 @@ def test_full_size_training_step(cfg):
     if have < 2 * need:
         pytest.skip(f"host memory: {have / 2**30:.1f} GiB available, {2 * need / 2**30:.1f} GiB wanted")
     inp, g, res = run_full_step(spec)
-    info = check_full_size(spec, inp, res, np.random.default_rng(seed_for(cfg)))
-    assert info["taps"] > 0
+    info = check_full_size(spec, inp, res)
+    assert info["err_dw"] is not None and (spec.first_layer or info["err_dx"] is not None)
 
 
 def test_full_size_folded_inference():

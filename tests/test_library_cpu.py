@@ -54,7 +54,8 @@ def test_workspace_sizes(lib):
         f, b = ctypes.c_size_t(), ctypes.c_size_t()
         assert lib.cbr_workspace_size(ctypes.byref(d), ctypes.byref(f), ctypes.byref(b)) == 0
         act = spec.n * spec.p * spec.q * spec.c_out * 2
-        # fwd: z when the caller does not save it; bwd: the materialised dz (and z if recomputed)
+        # fwd: z when the caller does not save it; bwd: z if recomputed (and the materialised dz
+        # for layers the fused backward kernel does not take)
         assert f.value >= act and b.value >= act
         assert f.value < act + (64 << 20) and b.value < 2 * act + (256 << 20)
 
@@ -125,6 +126,24 @@ def test_noalloc_forward_requires_z_saved(lib):
     assert f(ctypes.byref(d), P, P, P, P, P, P, 0.1, 1e-5, P, P, None, P, P, None) == 1
     bad = _desc(c_out=12)
     assert f(ctypes.byref(bad), P, P, P, P, P, P, 0.1, 1e-5, P, P, P, P, P, None) == 1
+
+
+def test_noalloc_forward_rejects_before_touching_scratch(lib):
+    """Argument, alignment and shape errors come back with the same codes as cbr_forward_train,
+    before the device check and before anything is enqueued on the shared scratch."""
+    f = lib.cbr_forward_train_noalloc
+    vp, fp = ctypes.c_void_p, ctypes.c_float
+    f.argtypes = [ctypes.POINTER(cbr.Desc), vp, vp, vp, vp, vp, vp, fp, fp, vp, vp, vp, vp, vp, vp]
+    f.restype = ctypes.c_int32
+    d = _desc()
+    assert f(ctypes.byref(d), P, P, P, P, P, P, 1.5, 1e-5, P, P, P, P, P, None) == 1   # momentum
+    assert f(ctypes.byref(d), P, P, P, P, P, P, 0.1, 0.0, P, P, P, P, P, None) == 1    # eps
+    assert f(ctypes.byref(d), P + 2, P, P, P, P, P, 0.1, 1e-5, P, P, P, P, P, None) == 2  # x misaligned
+    assert f(ctypes.byref(d), P, P, P, P, P, P, 0.1, 1e-5, P, P, P + 8, P, P, None) == 2  # z misaligned
+    assert f(ctypes.byref(_desc(c_out=24)), P, P, P, P, P, P, 0.1, 1e-5, P, P, P, P, P, None) == 3
+    if not torch.cuda.is_available():
+        # valid arguments reach the device check, which reports the missing GPU
+        assert f(ctypes.byref(d), P, P, P, P, P, P, 0.1, 1e-5, P, P, P, P, P, None) == 5
 
 
 def test_selftest_limit_checked_before_device(lib):

@@ -6,16 +6,20 @@ cannot pay for cudaMalloc's cost and implicit synchronisation.  This entry point
 from scratch compiled into the library.  The test calls it through the C ABI twice in a row,
 so the second call runs on scratch left behind by the first, and compares each call's
 outputs with those of the workspace-based entry point on the same inputs, using the parity
-tolerances of the other GPU tests.  It runs last so that a failure here cannot hide others.
+tolerances of the other GPU tests; the first call is also checked against the CPU oracle
+directly, so the test does not rest on the other entry point alone.  It runs last so that a
+failure here cannot hide others.
 """
 import ctypes
 
+import numpy as np
 import pytest
 import torch
 
+import oracle
 from conv_batchnorm_relu_gb300 import build, cbr
 from conv_batchnorm_relu_gb300.inputs import CONFIGS, CBRSpec, make_inputs
-from parity import max_err_ok, rel_close, stat_close, to_np
+from parity import mask_ok, max_err_ok, oracle_inputs, rel_close, stat_close, to_np, unpack_mask
 
 pytestmark = pytest.mark.gpu
 
@@ -49,7 +53,8 @@ def test_noalloc_forward_matches_workspace_forward_twice(case):
     lib = _lib()
     dev = torch.device("cuda", 0)
     layer = cbr.Layer.from_spec(spec)
-    g = {k: v.to(dev) for k, v in make_inputs(spec, seed, with_dy=False).items()}
+    inp = make_inputs(spec, seed, with_dy=False)
+    g = {k: v.to(dev) for k, v in inp.items()}
     fwd_bytes, _ = cbr.workspace_size(layer)
     ws = cbr.new_workspace(fwd_bytes, dev)
     d = layer.desc()
@@ -76,3 +81,14 @@ def test_noalloc_forward_matches_workspace_forward_twice(case):
         rel_close(to_np(o["saved_inv_var"]), to_np(ref["saved_inv_var"]), f"saved_inv_var (call {call})")
         stat_close(to_np(rm), to_np(rm_ref), spec.momentum * sd, f"running_mean (call {call})")
         rel_close(to_np(rv), to_np(rv_ref), f"running_var (call {call})")
+        if call == 0:
+            o_np = oracle_inputs(inp)
+            want = oracle.forward_train(o_np["x"], o_np["w"], o_np["gamma"], o_np["beta"],
+                                        o_np["running_mean"], o_np["running_var"], spec.momentum,
+                                        spec.eps, spec.stride, spec.pad)
+            max_err_ok(to_np(o["y"]), want["y"], "y vs oracle")
+            max_err_ok(to_np(o["z"]), want["z"], "z vs oracle")
+            mask_ok(unpack_mask(o["mask"], want["pre"].size), want["pre"], "mask vs oracle")
+            sd = np.sqrt(want["var"])
+            stat_close(to_np(o["saved_mean"]), want["mean"], sd, "saved_mean vs oracle")
+            rel_close(to_np(o["saved_inv_var"]), want["inv_std"], "saved_inv_var vs oracle")
