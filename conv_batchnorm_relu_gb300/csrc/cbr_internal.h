@@ -15,9 +15,10 @@ constexpr size_t kWsHeaderBytes = 256;
 constexpr int kMaxCtas = 256;
 constexpr size_t align256(size_t v) { return (v + 255) / 256 * 256; }
 // Training-forward workspace with the conv output kept by the caller: the counters, 2*Cout
-// floats of apply coefficients and 2*Cout floats of partial statistics per CTA.
+// floats of apply coefficients and, per CTA, the partial statistics (2*Cout moments and a row
+// count, padded to 2*Cout + 4 floats).
 constexpr size_t forward_scratch_bytes(int c_out) {
-  return align256(align256(kWsHeaderBytes + 2 * (size_t)c_out * 4) + (size_t)kMaxCtas * 2 * c_out * 4);
+  return align256(align256(kWsHeaderBytes + 2 * (size_t)c_out * 4) + (size_t)kMaxCtas * (2 * c_out + 4) * 4);
 }
 
 // Geometry of a stride-1 convolution computed over "padded-linear" rows.

@@ -9,7 +9,8 @@
 
 namespace cbr {
 
-size_t fprop_partial_floats(int num_sms, int c_out) { return (size_t)num_sms * 2 * c_out; }
+// per CTA: the means and M2s of its rows, then its row count (stats.cuh)
+size_t fprop_partial_floats(int num_sms, int c_out) { return (size_t)num_sms * st::partial_floats(c_out); }
 
 int launch_fprop(const FpropArgs& f, int c_in, int c_out, bool bf16, const void* x, const void* w,
                  int num_sms, cudaStream_t st) {

@@ -276,9 +276,12 @@ __global__ void __launch_bounds__(kFlThreads, 1)
 #pragma unroll
     for (int b = 0; b < kNB; ++b) s1[b] = s2[b] = 0.f;
     constexpr bool kRegStats = kCPH <= 32;
+    // r1, r2: running mean and M2 of this thread's rows (Welford), rn: their count
     float r1[kRegStats ? kCPH : 1], r2[kRegStats ? kCPH : 1];
+    float rn = 0.f;
 #pragma unroll
     for (int i = 0; i < (kRegStats ? kCPH : 1); ++i) r1[i] = r2[i] = 0.f;
+    float sn = 0.f;  // rows merged into s1 / s2 (the mean and M2 of channel lane >> kSh)
     const bool stats = a.mode == kFpropStats;
     const bool bias_relu = a.mode == kFpropBiasRelu;
     const int out_c = a.out_c;
@@ -334,19 +337,21 @@ __global__ void __launch_bounds__(kFlThreads, 1)
           }
           if (stats) {
             if constexpr (kRegStats) {
-#pragma unroll
-              for (int i = 0; i < kSB; ++i) {
-                r1[b * kSB + i] += v[i];
-                r2[b * kSB + i] = fmaf(v[i], v[i], r2[b * kSB + i]);
+              // kNB == 1: one Welford update per valid row
+              if (valid) {
+                rn += 1.f;
+                st::welford_row<kSB>(r1 + b * kSB, r2 + b * kSB, v, __fdividef(1.f, rn));
               }
             } else {
-              float sq[kSB];
+              // the tile's rows (each: count 1, mean v, M2 0) merged across the warp, then into
+              // the lane's running moments of its channel
+              float q0[kSB];
 #pragma unroll
-              for (int i = 0; i < kSB; ++i) sq[i] = v[i] * v[i];
-              hc::reduce_scatter<kSB>(v, lane);
-              hc::reduce_scatter<kSB>(sq, lane);
-              s1[b] += v[0];
-              s2[b] += sq[0];
+              for (int i = 0; i < kSB; ++i) q0[i] = 0.f;
+              const float tn = st::chan_scatter<kSB>(v, q0, valid ? 1.f : 0.f, lane);
+              float nn = sn;
+              st::chan_merge(nn, s1[b], s2[b], tn, v[0], q0[0]);
+              if (b == kNB - 1) sn = nn;
             }
           }
         }
@@ -365,8 +370,7 @@ __global__ void __launch_bounds__(kFlThreads, 1)
             v1[i] = r1[b * kSB + i];
             v2[i] = r2[b * kSB + i];
           }
-          hc::reduce_scatter<kSB>(v1, lane);
-          hc::reduce_scatter<kSB>(v2, lane);
+          sn = st::chan_scatter<kSB>(v1, v2, rn, lane);
           s1[b] = v1[0];
           s2[b] = v2[0];
         }
@@ -380,6 +384,7 @@ __global__ void __launch_bounds__(kFlThreads, 1)
         red[(quad * 2 + 0) * NOUT + c] = s1[b];
         red[(quad * 2 + 1) * NOUT + c] = s2[b];
       }
+      if (half == 0 && lane == 0) red[8 * NOUT + quad] = sn;  // the quadrant's row count
     }
   }
   tc_fence_before();
@@ -803,9 +808,12 @@ __global__ void __launch_bounds__(kImpThreads, 1)
 #pragma unroll
     for (int b = 0; b < kNB; ++b) s1[b] = s2[b] = 0.f;
     constexpr bool kRegStats = kCPH <= 32;
+    // r1, r2: running mean and M2 of this thread's rows (Welford), rn: their count
     float r1[kRegStats ? kCPH : 1], r2[kRegStats ? kCPH : 1];
+    float rn = 0.f;
 #pragma unroll
     for (int i = 0; i < (kRegStats ? kCPH : 1); ++i) r1[i] = r2[i] = 0.f;
+    float sn = 0.f;  // rows merged into s1 / s2 (the mean and M2 of channel lane >> kSh)
     const bool stats = a.mode == kFpropStats;
     const bool bias_relu = a.mode == kFpropBiasRelu;
     const bool valid = e < g.q;
@@ -869,19 +877,21 @@ __global__ void __launch_bounds__(kImpThreads, 1)
           }
           if (stats) {
             if constexpr (kRegStats) {
-#pragma unroll
-              for (int i = 0; i < kSB; ++i) {
-                r1[b * kSB + i] += v[i];
-                r2[b * kSB + i] = fmaf(v[i], v[i], r2[b * kSB + i]);
+              // kNB == 1: one Welford update per valid row
+              if (valid) {
+                rn += 1.f;
+                st::welford_row<kSB>(r1 + b * kSB, r2 + b * kSB, v, __fdividef(1.f, rn));
               }
             } else {
-              float sq[kSB];
+              // the tile's rows (each: count 1, mean v, M2 0) merged across the warp, then into
+              // the lane's running moments of its channel
+              float q0[kSB];
 #pragma unroll
-              for (int i = 0; i < kSB; ++i) sq[i] = v[i] * v[i];
-              hc::reduce_scatter<kSB>(v, lane);
-              hc::reduce_scatter<kSB>(sq, lane);
-              s1[b] += v[0];
-              s2[b] += sq[0];
+              for (int i = 0; i < kSB; ++i) q0[i] = 0.f;
+              const float tn = st::chan_scatter<kSB>(v, q0, valid ? 1.f : 0.f, lane);
+              float nn = sn;
+              st::chan_merge(nn, s1[b], s2[b], tn, v[0], q0[0]);
+              if (b == kNB - 1) sn = nn;
             }
           }
         }
@@ -908,8 +918,7 @@ __global__ void __launch_bounds__(kImpThreads, 1)
             v1[i] = r1[b * kSB + i];
             v2[i] = r2[b * kSB + i];
           }
-          hc::reduce_scatter<kSB>(v1, lane);
-          hc::reduce_scatter<kSB>(v2, lane);
+          sn = st::chan_scatter<kSB>(v1, v2, rn, lane);
           s1[b] = v1[0];
           s2[b] = v2[0];
         }
@@ -924,6 +933,7 @@ __global__ void __launch_bounds__(kImpThreads, 1)
         red[(quad * 2 + 0) * NOUT + c] = s1[b];
         red[(quad * 2 + 1) * NOUT + c] = s2[b];
       }
+      if (half == 0 && lane == 0) red[8 * NOUT + quad] = sn;  // the quadrant's row count
     }
   }
   tc_fence_before();

@@ -18,6 +18,7 @@
 #include <type_traits>
 #include "cbr_internal.h"
 #include "common.cuh"
+#include "stats.cuh"
 
 namespace cbr {
 
@@ -106,37 +107,19 @@ __device__ __forceinline__ void set_abort(volatile int* flag, uint32_t* err, uin
   report_error(err, bits);
 }
 
-// Warp reduce-scatter: on entry each lane holds L values (L = 16 or 32 channels of its own
-// row); on exit v[0] of every lane holds the sum over the 32 lanes of channel (lane >> s),
-// s = log2(32 / L).  log2(L) butterfly steps each halve the channel set a lane keeps.
-template <int L>
-__device__ __forceinline__ void reduce_scatter(float (&v)[L], int lane) {
-  int o = 16;
-#pragma unroll
-  for (int len = L; len > 1; len >>= 1, o >>= 1) {
-    const bool hi = (lane & o) != 0;
-#pragma unroll
-    for (int j = 0; j < len / 2; ++j) {
-      const float send = hi ? v[j] : v[j + len / 2];
-      const float keep = hi ? v[j + len / 2] : v[j];
-      v[j] = keep + __shfl_xor_sync(0xffffffffu, send, o);
-    }
-  }
-#pragma unroll
-  for (; o >= 1; o >>= 1) v[0] += __shfl_xor_sync(0xffffffffu, v[0], o);
-}
-
-// Forward statistics, after the main loop: `red` holds the per-TMEM-lane-quarter sums
-// [4][2][COUT] of this CTA (written by the epilogue, visible after a __syncthreads).  Every
-// thread calls this: the CTA's partial is written, a wrap-around ticket elects the last CTA,
-// and that CTA runs bn_finalize.  `scratch` (SCRATCH bytes, may alias `red`) holds the
-// finalize's working set.
+// Forward statistics, after the main loop: `red` holds the moments of each TMEM lane quadrant
+// of this CTA, [4][2][COUT] (mean, M2) followed by the 4 row counts (written by the epilogue,
+// visible after a __syncthreads).  Every thread calls this: the quadrants are merged in fixed
+// order into the CTA's partial, a wrap-around ticket elects the last CTA, and that CTA merges
+// the grid's partials in a fixed order and runs bn_finalize.  `scratch` (SCRATCH bytes, may
+// alias `red`) holds the finalize's working set.
 template <int COUT, int kThreads, int SCRATCH>
 __device__ void stats_partial_finalize(const ConvArgs& a, const float* red, uint8_t* scratch,
                                        volatile uint32_t* ticket_slot, volatile int* abort_flag) {
   static_assert(kThreads >= COUT, "one thread per channel in the finalize");
+  constexpr int kPF = st::partial_floats(COUT);
   // the per-channel inputs of the finalize, loaded before the ticket by every CTA (cheap) so
-  // the last one does not wait for them after its sums
+  // the last one does not wait for them after its merges
   float gm = 0.f, bt = 0.f, rm = 0.f, rv = 0.f;
   if (threadIdx.x < COUT) {
     gm = a.gamma[threadIdx.x];
@@ -144,13 +127,16 @@ __device__ void stats_partial_finalize(const ConvArgs& a, const float* red, uint
     rm = a.running_mean[threadIdx.x];
     rv = a.running_var[threadIdx.x];
   }
-  for (int i = threadIdx.x; i < 2 * COUT; i += kThreads) {
-    const int st = i / COUT, c = i - st * COUT;
-    float v = red[(0 * 2 + st) * COUT + c];
-    v += red[(1 * 2 + st) * COUT + c];
-    v += red[(2 * 2 + st) * COUT + c];
-    v += red[(3 * 2 + st) * COUT + c];
-    a.part[(size_t)blockIdx.x * 2 * COUT + i] = v;
+  float* mypart = a.part + (size_t)blockIdx.x * kPF;
+  if (threadIdx.x < COUT) {
+    const int c = threadIdx.x;
+    const float* cnt = red + 8 * COUT;
+    float n = cnt[0], m = red[0 * COUT + c], q = red[1 * COUT + c];
+#pragma unroll
+    for (int k = 1; k < 4; ++k) st::chan_merge(n, m, q, cnt[k], red[(2 * k) * COUT + c], red[(2 * k + 1) * COUT + c]);
+    mypart[c] = m;
+    mypart[COUT + c] = q;
+    if (c == 0) mypart[2 * COUT] = n;
   }
   __threadfence();
   __syncthreads();
@@ -159,53 +145,69 @@ __device__ void stats_partial_finalize(const ConvArgs& a, const float* red, uint
   if (*ticket_slot == gridDim.x - 1 && !is_aborted(abort_flag)) {
     // ---------------------------------------------------- bn_finalize (last CTA)
     __threadfence();
-    // This runs on one SM after all the others, so it is kept short: every CTA partial is
-    // loaded in one batch (thread t sums float4 column t % kV4 of CTAs t / kV4, + kRG, ...,
-    // in fp32 and a fixed order), the row groups are combined in fixed order in fp64, and
-    // the per-channel math avoids fp64 division and square root (slow at this part's FP64
-    // rate): mean and variance by fp64 multiplies with the host's 1/M, 1/sqrt in fp32.
-    constexpr int kV4 = (2 * COUT) / 4;        // float4 columns of one partial
-    // row groups, bounded by the scratch region (which also holds fin)
-    constexpr int kRGfit = (SCRATCH - 2 * COUT * 8) / (2 * COUT * 4);
-    constexpr int kRG1 = kThreads / kV4 < kRGfit ? kThreads / kV4 : kRGfit;
-    constexpr int kRG = kRG1 < 32 ? kRG1 : 32;  // at most the fp64 tree's width
+    // This runs on one SM after all the others, so it is kept short: thread t merges, for 4
+    // channels (column t % kV), the partials of CTAs t / kV, + kRG, ... in order, with the
+    // loads of kLd CTAs in flight; the kRG group results are then merged by a fixed pairwise
+    // tree, and the per-channel math multiplies by the host's 1/M (no division by M).
+    constexpr int kV = COUT / 4;               // float4 columns of the means (and of the M2s)
+    constexpr int kGF = 2 * COUT + 4;          // floats per group result: means, M2s, count
+    constexpr int kRGfit = SCRATCH / (kGF * 4);
+    constexpr int kRG1 = kThreads / kV < kRGfit ? kThreads / kV : kRGfit;
+    constexpr int kRG = kRG1 < 32 ? kRG1 : 32;
     static_assert(kRG >= 1, "finalize scratch");
-    constexpr int kLd = 16;                    // loads in flight per thread
-    float* fred = reinterpret_cast<float*>(scratch);  // [kRG][2*COUT]
-    double* fin = reinterpret_cast<double*>(fred + kRG * 2 * COUT);
-    const int c4 = threadIdx.x % kV4, rg = threadIdx.x / kV4;
+    constexpr int kLd = 8;                     // CTAs whose loads are in flight per thread
+    float* fg = reinterpret_cast<float*>(scratch);  // [kRG][kGF]
+    const int c4 = threadIdx.x % kV, rg = threadIdx.x / kV;
     if (rg < kRG) {
-      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+      float n = 0.f;
+      float m[4] = {0.f, 0.f, 0.f, 0.f}, q[4] = {0.f, 0.f, 0.f, 0.f};
       for (int b0 = rg; b0 < (int)gridDim.x; b0 += kLd * kRG) {
-        float4 v[kLd];
+        float4 vm[kLd], vq[kLd];
+        float vn[kLd];
 #pragma unroll
         for (int k = 0; k < kLd; ++k) {
           const int b = b0 + k * kRG;
-          v[k] = b < (int)gridDim.x ? __ldcg(reinterpret_cast<const float4*>(a.part + (size_t)b * 2 * COUT) + c4)
-                                    : make_float4(0.f, 0.f, 0.f, 0.f);
+          const float* pb = a.part + (size_t)b * kPF;
+          const bool ok = b < (int)gridDim.x;
+          vm[k] = ok ? __ldcg(reinterpret_cast<const float4*>(pb) + c4) : make_float4(0.f, 0.f, 0.f, 0.f);
+          vq[k] = ok ? __ldcg(reinterpret_cast<const float4*>(pb + COUT) + c4) : make_float4(0.f, 0.f, 0.f, 0.f);
+          vn[k] = ok ? __ldcg(pb + 2 * COUT) : 0.f;
         }
 #pragma unroll
         for (int k = 0; k < kLd; ++k) {
-          acc.x += v[k].x;
-          acc.y += v[k].y;
-          acc.z += v[k].z;
-          acc.w += v[k].w;
+          const float bm[4] = {vm[k].x, vm[k].y, vm[k].z, vm[k].w};
+          const float bq[4] = {vq[k].x, vq[k].y, vq[k].z, vq[k].w};
+          const st::ChanW w = st::chan_weights(n, vn[k]);  // one division for the 4 channels
+#pragma unroll
+          for (int j = 0; j < 4; ++j) st::chan_merge_w(m[j], q[j], bm[j], bq[j], w);
+          n += vn[k];
         }
       }
-      reinterpret_cast<float4*>(fred + rg * 2 * COUT)[c4] = acc;
+      float* gr = fg + rg * kGF;
+      reinterpret_cast<float4*>(gr)[c4] = make_float4(m[0], m[1], m[2], m[3]);
+      reinterpret_cast<float4*>(gr + COUT)[c4] = make_float4(q[0], q[1], q[2], q[3]);
+      if (c4 == 0) gr[2 * COUT] = n;
     }
-    __syncthreads();
-    // row groups combined in fp64 by a fixed pairwise tree (a dependent chain of fp64 adds is
-    // slow at this part's FP64 latency)
-    for (int i = threadIdx.x; i < 2 * COUT; i += kThreads) fin[i] = tree_sum<kRG>(fred + i, 2 * COUT);
     __syncthreads();
     if (threadIdx.x < COUT) {
       const int c = threadIdx.x;
-      const double mean = fin[c] * a.inv_m;
-      const double var_d = fin[COUT + c] * a.inv_m - mean * mean;
-      const float var = var_d > 0.0 ? (float)var_d : 0.f;
+      // groups merged by a fixed pairwise tree (log2(kRG) dependent steps)
+      constexpr int P = kRG <= 1 ? 1 : kRG <= 2 ? 2 : kRG <= 4 ? 4 : kRG <= 8 ? 8 : kRG <= 16 ? 16 : 32;
+      float tn[P], tm[P], tq[P];
+#pragma unroll
+      for (int r = 0; r < P; ++r) {
+        const bool ok = r < kRG;
+        tn[r] = ok ? fg[r * kGF + 2 * COUT] : 0.f;
+        tm[r] = ok ? fg[r * kGF + c] : 0.f;
+        tq[r] = ok ? fg[r * kGF + COUT + c] : 0.f;
+      }
+#pragma unroll
+      for (int w = P / 2; w >= 1; w /= 2)
+#pragma unroll
+        for (int k = 0; k < w; ++k) st::chan_merge(tn[k], tm[k], tq[k], tn[k + w], tm[k + w], tq[k + w]);
+      const float meanf = tm[0];
+      const float var = fmaxf(tq[0] * (float)a.inv_m, 0.f);  // biased: M2 / M
       const float inv = rsqrtf(var + a.eps);
-      const float meanf = (float)mean;
       a.saved_mean[c] = meanf;
       a.saved_inv_var[c] = inv;
       a.eq[c] = gm * inv;
@@ -464,14 +466,17 @@ __global__ void __launch_bounds__(Roles<KIND>::kThreads, 1)
     float s1[kNB], s2[kNB];
 #pragma unroll
     for (int b = 0; b < kNB; ++b) s1[b] = s2[b] = 0.f;
-    // Statistics: with at most 32 channels per thread, each thread keeps per-channel sums of
-    // its own rows in registers for the whole kernel and the warp reduction runs once at the
-    // end (shuffles share the shared-memory pipe with the tensor cores' operand reads);
-    // otherwise every tile is reduced across the warp as it is produced.
+    // Statistics (moments, stats.cuh): with at most 32 channels per thread, each thread keeps
+    // the running mean and M2 of its own rows in registers for the whole kernel and the warp
+    // merge runs once at the end (shuffles share the shared-memory pipe with the tensor cores'
+    // operand reads); otherwise every tile is merged across the warp as it is produced.
     constexpr bool kRegStats = kCPH <= 32;
+    // r1, r2: running mean and M2 of this thread's rows (Welford), rn: their count
     float r1[kRegStats ? kCPH : 1], r2[kRegStats ? kCPH : 1];
+    float rn = 0.f;
 #pragma unroll
     for (int i = 0; i < (kRegStats ? kCPH : 1); ++i) r1[i] = r2[i] = 0.f;
+    float sn = 0.f;  // rows merged into s1 / s2 (the mean and M2 of channel lane >> kSh)
     const bool stats = KIND == kKindFprop && a.mode == kFpropStats;
     const bool bias_relu = KIND == kKindFprop && a.mode == kFpropBiasRelu;
     const int out_c = a.out_c;
@@ -540,19 +545,21 @@ __global__ void __launch_bounds__(Roles<KIND>::kThreads, 1)
             }
             if (stats) {
               if constexpr (kRegStats) {
-#pragma unroll
-                for (int i = 0; i < kSB; ++i) {
-                  r1[b * kSB + i] += v[i];
-                  r2[b * kSB + i] = fmaf(v[i], v[i], r2[b * kSB + i]);
+                // kNB == 1: one Welford update per valid row
+                if (valid) {
+                  rn += 1.f;
+                  st::welford_row<kSB>(r1 + b * kSB, r2 + b * kSB, v, __fdividef(1.f, rn));
                 }
               } else {
-                float sq[kSB];
+                // the tile's rows (each: count 1, mean v, M2 0) merged across the warp, then into
+                // the lane's running moments of its channel
+                float q0[kSB];
 #pragma unroll
-                for (int i = 0; i < kSB; ++i) sq[i] = v[i] * v[i];
-                reduce_scatter<kSB>(v, lane);
-                reduce_scatter<kSB>(sq, lane);
-                s1[b] += v[0];
-                s2[b] += sq[0];
+                for (int i = 0; i < kSB; ++i) q0[i] = 0.f;
+                const float tn = st::chan_scatter<kSB>(v, q0, valid ? 1.f : 0.f, lane);
+                float nn = sn;
+                st::chan_merge(nn, s1[b], s2[b], tn, v[0], q0[0]);
+                if (b == kNB - 1) sn = nn;
               }
             }
           }
@@ -574,8 +581,7 @@ __global__ void __launch_bounds__(Roles<KIND>::kThreads, 1)
             v1[i] = r1[b * kSB + i];
             v2[i] = r2[b * kSB + i];
           }
-          reduce_scatter<kSB>(v1, lane);
-          reduce_scatter<kSB>(v2, lane);
+          sn = st::chan_scatter<kSB>(v1, v2, rn, lane);
           s1[b] = v1[0];
           s2[b] = v2[0];
         }
@@ -590,6 +596,7 @@ __global__ void __launch_bounds__(Roles<KIND>::kThreads, 1)
         red[(quad * 2 + 0) * NOUT + c] = s1[b];
         red[(quad * 2 + 1) * NOUT + c] = s2[b];
       }
+      if (half == 0 && lane == 0) red[8 * NOUT + quad] = sn;  // the quadrant's row count
     }
   }
 

@@ -11,8 +11,8 @@ namespace {
 
 // Upper bound on the scratch this entry point can use.  With the conv output kept by the
 // caller (z_saved), the forward needs 256 bytes of arrival counters, 2*Cout floats of apply
-// coefficients and 2*Cout floats of partial statistics per CTA (at most kMaxCtas CTAs): about
-// 257 KiB for Cout = 128.  Every GPU that loads the library holds this array until exit.
+// coefficients and 2*Cout + 4 floats of partial statistics per CTA (at most kMaxCtas CTAs):
+// about 261 KiB for Cout = 128.  Every GPU that loads the library holds this array until exit.
 constexpr size_t kNoAllocScratchBytes = 320 * 1024;
 static_assert(kNoAllocScratchBytes >= forward_scratch_bytes(128),
               "the fixed scratch must hold the largest supported forward (Cout = 128, kMaxCtas CTAs)");

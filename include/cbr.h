@@ -173,7 +173,7 @@ cbr_status_t cbr_forward_infer(const cbr_desc_t* desc, const void* x, const void
  *   Scratch: a 320 KiB array compiled into the library, held by every GPU that loads it
  *   until the process exits.  A problem whose scratch need exceeds it returns
  *   CBR_ERR_WORKSPACE before anything is enqueued (with Cout <= 128 the need is about
- *   257 KiB, so supported shapes fit).
+ *   261 KiB, so supported shapes fit).
  *   The first call on each device looks up the array's device address (one
  *   cudaGetSymbolAddress with that device current); make that first call before any stream
  *   capture.  Each call clears the array's arrival counters with an asynchronous memset on

@@ -69,9 +69,10 @@ def unpack_mask(words: torch.Tensor, total: int) -> np.ndarray:
     return np.unpackbits(b, bitorder="little")[:total].astype(bool)
 
 
-def mask_ok(got_bits: np.ndarray, pre_ref: np.ndarray, name: str = "mask") -> int:
+def mask_ok(got_bits: np.ndarray, pre_ref: np.ndarray, name: str = "mask", margin=MASK_MARGIN) -> int:
+    """The mask agrees exactly wherever |pre| > margin (a scalar, or one value per element)."""
     pre = pre_ref.reshape(-1)
-    decided = np.abs(pre) > MASK_MARGIN
+    decided = np.abs(pre) > np.broadcast_to(margin, pre_ref.shape).reshape(-1)
     bad = int(np.count_nonzero(got_bits[decided] != (pre[decided] > 0)))
     assert bad == 0, f"{name}: {bad} decided positions differ"
     return bad
@@ -93,9 +94,10 @@ def grad_sum_scales(dy: np.ndarray, mask: np.ndarray, xhat: np.ndarray) -> tuple
 UNIT_ROUNDOFF = {"f16": 2.0 ** -11, "bf16": 2.0 ** -8}
 
 
-def mask_slack(spec, o: dict, ref: dict, rb: dict, margin: float = MASK_MARGIN) -> dict:
+def mask_slack(spec, o: dict, ref: dict, rb: dict, margin=MASK_MARGIN) -> dict:
     """Element-wise bounds on how much the backward outputs may move when the ReLU mask is
-    decided either way at the ambiguous positions |pre| <= margin (oracle data only)."""
+    decided either way at the ambiguous positions |pre| <= margin (a scalar or one value per
+    element; oracle data only)."""
     pre = ref["pre"]
     amb = np.abs(pre) <= margin
     N, P, Q, K = pre.shape
@@ -178,6 +180,15 @@ def scaled_error(got, ref, scale) -> float:
     1e-3 criterion, before any allowance is added)."""
     got, ref, scale = (np.asarray(a, dtype=np.float64) for a in (got, ref, scale))
     return float((np.abs(got - ref) / np.maximum(np.abs(ref), scale)).max())
+
+
+def storage_rounding_margin(spec, ref: dict, o: dict) -> np.ndarray:
+    """Per-element bound on how far the GPU's pre-activation, computed from z rounded to the
+    storage dtype, may lie from the oracle's: gamma*inv_std*|z|*u (at least the 1e-3 margin).
+    Negligible when z is centred near 0, it dominates when |mean/std| of z is large."""
+    u = UNIT_ROUNDOFF[spec.dtype]
+    a = np.asarray(o["gamma"]) * ref["inv_std"]
+    return np.maximum(MASK_MARGIN, a * np.abs(ref["z"]) * u)
 
 
 def dgamma_storage_rounding(spec, o: dict, ref: dict) -> np.ndarray:
