@@ -25,7 +25,7 @@ STATUS_NAMES = {0: "CBR_OK", 1: "CBR_ERR_INVALID_ARG", 2: "CBR_ERR_MISALIGNED",
                 3: "CBR_ERR_UNSUPPORTED", 4: "CBR_ERR_WORKSPACE", 5: "CBR_ERR_DEVICE",
                 6: "CBR_ERR_CUDA", 7: "CBR_ERR_TIMEOUT"}
 CBR_F16, CBR_BF16 = 0, 1
-CBR_MASK_BITS, CBR_MASK_FROM_Y = 0, 1
+CBR_MASK_BITS, CBR_MASK_FROM_Y, CBR_MASK_BYTES = 0, 1, 2
 
 
 class CBRError(RuntimeError):
@@ -65,12 +65,22 @@ def load(path: str | None = None) -> ctypes.CDLL:
             lib.cbr_fold_bn.argtypes = [D, vp, vp, vp, vp, vp, vp, fp, vp, vp, vp]
             lib.cbr_forward_infer.argtypes = [D, vp, vp, vp, vp, vp]
             lib.cbr_stream_status.argtypes = [vp]
+            lib.cbr_forward_train_stats.argtypes = [D, vp, vp, vp, vp, vp, sz, vp]
+            lib.cbr_forward_train_finish.argtypes = [D, vp, i32, vp, vp, vp, vp, fp, fp, vp, vp, vp, vp, vp,
+                                                     vp, sz, vp]
+            lib.cbr_backward_sums.argtypes = [D, vp, vp, i32, vp, vp, vp, vp, sz, vp]
+            lib.cbr_backward_finish.argtypes = [D, vp, ctypes.c_int64, vp, vp, vp, vp, i32, vp, vp, vp, vp, vp,
+                                                vp, vp, vp, vp, sz, vp]
+            lib.cbr_mask_bits_to_bytes.argtypes = [vp, vp, ctypes.c_int64, vp]
+            lib.cbr_mask_bytes_to_bits.argtypes = [vp, vp, ctypes.c_int64, vp]
             lib.cbr_selftest_bounded_wait.argtypes = [i32, vp]
             lib.cbr_profile_next_call.argtypes = [ctypes.POINTER(vp), i32]
             lib.cbr_profile_last_count.restype = i32
             for f in ("cbr_workspace_size", "cbr_forward_train", "cbr_backward", "cbr_fold_bn",
                       "cbr_forward_infer", "cbr_stream_status", "cbr_profile_next_call",
-                      "cbr_selftest_bounded_wait"):
+                      "cbr_selftest_bounded_wait", "cbr_mask_bits_to_bytes", "cbr_mask_bytes_to_bits",
+                      "cbr_forward_train_stats", "cbr_forward_train_finish", "cbr_backward_sums",
+                      "cbr_backward_finish"):
                 getattr(lib, f).restype = i32
             _lib = lib
     return _lib
@@ -193,6 +203,123 @@ def backward(layer: Layer, dy, x, w, y_or_mask, mask_kind, z_saved, gamma, saved
     return o
 
 
+# ----------------------------------------------------------------------------- synchronised BN
+# The split calls bracket one collective each; the collectives run through torch.distributed
+# (NCCL on GPUs), the arithmetic on both sides of them in the library's kernels.
+
+def moments_floats(layer: Layer) -> int:
+    """Floats of one rank's moments: mean [c_out], M2 [c_out], row count."""
+    return 2 * layer.c_out + 1
+
+
+def forward_train_stats(layer: Layer, x, w, *, ws, z=None):
+    """cbr_forward_train_stats -> (z, moments [2*c_out + 1])."""
+    if z is None:
+        z = torch.empty((layer.n, layer.p, layer.q, layer.c_out), dtype=layer.dtype, device=x.device)
+    mom = torch.empty(moments_floats(layer), dtype=torch.float32, device=x.device)
+    d = layer.desc()
+    _check(load().cbr_forward_train_stats(ctypes.byref(d), _ptr(x), _ptr(w), _ptr(z), _ptr(mom), _ptr(ws),
+                                          ws.numel(), _stream()), "cbr_forward_train_stats")
+    return z, mom
+
+
+def forward_train_finish(layer: Layer, moments_all, gamma, beta, running_mean, running_var, momentum, eps, z, *,
+                         ws, want_mask=True, out=None) -> dict:
+    """cbr_forward_train_finish: moments_all [world][2*c_out + 1] in rank order."""
+    dev = z.device
+    o = dict(out or {})
+    if "y" not in o:
+        o["y"] = torch.empty_like(z)
+    if want_mask and "mask" not in o:
+        o["mask"] = torch.empty(mask_words(layer), dtype=torch.int32, device=dev)
+    for k in ("saved_mean", "saved_inv_var"):
+        if k not in o:
+            o[k] = torch.empty(layer.c_out, dtype=torch.float32, device=dev)
+    world = moments_all.shape[0]
+    d = layer.desc()
+    _check(load().cbr_forward_train_finish(
+        ctypes.byref(d), _ptr(moments_all), int(world), _ptr(gamma), _ptr(beta), _ptr(running_mean),
+        _ptr(running_var), float(momentum), float(eps), _ptr(z), _ptr(o["y"]), _ptr(o.get("mask")),
+        _ptr(o["saved_mean"]), _ptr(o["saved_inv_var"]), _ptr(ws), ws.numel(), _stream()),
+        "cbr_forward_train_finish")
+    o["z"] = z
+    o["m_total"] = int(round(float(moments_all[:, -1].double().sum())))
+    return o
+
+
+def backward_sums(layer: Layer, dy, y_or_mask, mask_kind, z, saved_mean, *, ws) -> torch.Tensor:
+    """cbr_backward_sums -> [sum g (c_out)][sum g*(z - mean) (c_out)] of this rank."""
+    sums = torch.empty(2 * layer.c_out, dtype=torch.float32, device=dy.device)
+    d = layer.desc()
+    _check(load().cbr_backward_sums(ctypes.byref(d), _ptr(dy), _ptr(y_or_mask), int(mask_kind), _ptr(z),
+                                    _ptr(saved_mean), _ptr(sums), _ptr(ws), ws.numel(), _stream()),
+           "cbr_backward_sums")
+    return sums
+
+
+def backward_finish(layer: Layer, sums_all, m_total: int, dy, x, w, y_or_mask, mask_kind, z, gamma,
+                    saved_mean, saved_inv_var, *, ws, need_dx=True, out=None) -> dict:
+    """cbr_backward_finish -> dict(dx (or None), dw, dgamma, dbeta)."""
+    dev = dy.device
+    o = dict(out or {})
+    if need_dx and "dx" not in o:
+        o["dx"] = torch.empty((layer.n, layer.h, layer.w, layer.c_in), dtype=layer.dtype, device=dev)
+    if "dw" not in o:
+        o["dw"] = torch.empty((layer.c_out, layer.r, layer.s, layer.c_in), dtype=torch.float32, device=dev)
+    for k in ("dgamma", "dbeta"):
+        if k not in o:
+            o[k] = torch.empty(layer.c_out, dtype=torch.float32, device=dev)
+    d = layer.desc()
+    _check(load().cbr_backward_finish(
+        ctypes.byref(d), _ptr(sums_all), int(m_total), _ptr(dy), _ptr(x), _ptr(w), _ptr(y_or_mask),
+        int(mask_kind), _ptr(z), _ptr(gamma), _ptr(saved_mean), _ptr(saved_inv_var),
+        _ptr(o.get("dx")) if need_dx else None, _ptr(o["dw"]), _ptr(o["dgamma"]), _ptr(o["dbeta"]), _ptr(ws),
+        ws.numel(), _stream()), "cbr_backward_finish")
+    if not need_dx:
+        o["dx"] = None
+    return o
+
+
+def gather_moments(moments: torch.Tensor, group=None) -> torch.Tensor:
+    """Every rank's moments in rank order, [world][2*c_out + 1] (an all-gather: moments are merged,
+    not summed).  Without an initialised process group this rank is the whole batch."""
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()):
+        return moments.unsqueeze(0)
+    world = dist.get_world_size(group)
+    out = [torch.empty_like(moments) for _ in range(world)]
+    dist.all_gather(out, moments.contiguous(), group=group)
+    return torch.stack(out)
+
+
+def reduce_sums(sums: torch.Tensor, group=None) -> torch.Tensor:
+    """The backward's per-channel sums added over all ranks (an all-reduce)."""
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()):
+        return sums
+    out = sums.clone()
+    dist.all_reduce(out, op=dist.ReduceOp.SUM, group=group)
+    return out
+
+
+def syncbn_forward_train(layer: Layer, x, w, gamma, beta, running_mean, running_var, momentum=0.1,
+                         eps=1e-5, *, ws, group=None, want_mask=True, out=None) -> dict:
+    """Synchronised training forward: statistics over every rank's share of the batch."""
+    z, mom = forward_train_stats(layer, x, w, ws=ws, z=(out or {}).get("z"))
+    gathered = gather_moments(mom, group)
+    return forward_train_finish(layer, gathered, gamma, beta, running_mean, running_var, momentum, eps, z,
+                                ws=ws, want_mask=want_mask, out=out)
+
+
+def syncbn_backward(layer: Layer, dy, x, w, y_or_mask, mask_kind, z, gamma, saved_mean, saved_inv_var,
+                    m_total: int, *, ws, group=None, need_dx=True, out=None) -> dict:
+    """Synchronised training backward: dgamma, dbeta and the BN data gradient over the global
+    batch of m_total rows (from syncbn_forward_train's "m_total")."""
+    sums = reduce_sums(backward_sums(layer, dy, y_or_mask, mask_kind, z, saved_mean, ws=ws), group)
+    return backward_finish(layer, sums, m_total, dy, x, w, y_or_mask, mask_kind, z, gamma, saved_mean,
+                           saved_inv_var, ws=ws, need_dx=need_dx, out=out)
+
+
 def fold_bn(layer: Layer, w, gamma, beta, running_mean, running_var, eps=1e-5, conv_bias=None):
     w_fold = torch.empty_like(w)
     b_fold = torch.empty(layer.c_out, dtype=torch.float32, device=w.device)
@@ -211,6 +338,20 @@ def forward_infer(layer: Layer, x, w_fold, b_fold, out=None):
     _check(load().cbr_forward_infer(ctypes.byref(d), _ptr(x), _ptr(w_fold), _ptr(b_fold),
                                     _ptr(y), _stream()), "cbr_forward_infer")
     return y
+
+
+def mask_bits_to_bytes(bits: torch.Tensor, count: int, out: torch.Tensor | None = None) -> torch.Tensor:
+    """cbr_mask_bits_to_bytes: the bit-packed mask (int32 words) as one uint8 (0/1) per element."""
+    out = out if out is not None else torch.empty(count, dtype=torch.uint8, device=bits.device)
+    _check(load().cbr_mask_bits_to_bytes(_ptr(bits), _ptr(out), int(count), _stream()), "cbr_mask_bits_to_bytes")
+    return out
+
+
+def mask_bytes_to_bits(mask_bytes: torch.Tensor, count: int, out: torch.Tensor | None = None) -> torch.Tensor:
+    """cbr_mask_bytes_to_bits: a byte-per-element mask (non-zero = set) as bit-packed int32 words."""
+    out = out if out is not None else torch.empty((count + 31) // 32, dtype=torch.int32, device=mask_bytes.device)
+    _check(load().cbr_mask_bytes_to_bits(_ptr(mask_bytes), _ptr(out), int(count), _stream()), "cbr_mask_bytes_to_bits")
+    return out
 
 
 def stream_status(stream: int | None = None) -> None:

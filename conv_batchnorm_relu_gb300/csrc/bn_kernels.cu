@@ -75,6 +75,9 @@ __global__ void __launch_bounds__(kApplyThreads)
   }
 }
 
+__device__ __forceinline__ void bwd_coef(double g, double gx, float gamma, float mean, float inv_std, double inv_m,
+                                         int c, int ch, float* dgamma, float* dbeta, float* coef);
+
 template <bool BF16, bool MASKBITS>
 __global__ void __launch_bounds__(kRedThreads)
     bn_bwd_reduce_kernel(const BwdReduceArgs a) {
@@ -93,7 +96,7 @@ __global__ void __launch_bounds__(kRedThreads)
   for (int e = 0; e < 8; ++e) mean[e] = a.mean[c0 + e];
   // the per-channel inputs of the finalize, loaded up front (see below)
   float f_inv = 0.f, f_gamma = 0.f, f_mean = 0.f;
-  if (threadIdx.x < c) {
+  if (threadIdx.x < c && !a.sums_out) {
     f_inv = a.inv_std[threadIdx.x];
     f_gamma = a.gamma[threadIdx.x];
     f_mean = a.mean[threadIdx.x];
@@ -207,19 +210,75 @@ __global__ void __launch_bounds__(kRedThreads)
   __syncthreads();
   if (threadIdx.x < c) {
     const int ch = threadIdx.x;
-    const double g = fin[ch], gx = fin[c + ch];
-    const double inv = f_inv;
-    const double dgamma = gx * inv;  // sum g * xhat
-    const double dbeta = g;
-    const double ac = (double)f_gamma * inv;
-    const double dc = ac * dgamma * inv * a.inv_m;
-    const double ec = -ac * dbeta * a.inv_m + dc * (double)f_mean;
-    a.dgamma[ch] = (float)dgamma;
-    a.dbeta[ch] = (float)dbeta;
-    a.coef[ch] = (float)ac;
-    a.coef[c + ch] = (float)dc;
-    a.coef[2 * c + ch] = (float)ec;
+    if (a.sums_out) {
+      // split backward: the raw sums go to the caller, who adds other ranks' before the
+      // coefficients are formed
+      a.sums_out[ch] = (float)fin[ch];
+      a.sums_out[c + ch] = (float)fin[c + ch];
+    } else {
+      bwd_coef(fin[ch], fin[c + ch], f_gamma, f_mean, f_inv, a.inv_m, c, ch, a.dgamma, a.dbeta, a.coef);
+    }
   }
+}
+
+// dgamma, dbeta and the coefficients of dz = a*g - d*z + e for channel ch of c, from the sums
+// g = sum of dy*mask and gx = sum of dy*mask*(z - mean) over the M rows (inv_m = 1/M):
+// dgamma = gx*inv_std, dbeta = g, a = gamma*inv_std, d = a*dgamma*inv_std/M,
+// e = -a*dbeta/M + d*mean (BatchNorm CUDA page, section 3.1).
+__device__ __forceinline__ void bwd_coef(double g, double gx, float gamma, float mean, float inv_std, double inv_m,
+                                         int c, int ch, float* dgamma, float* dbeta, float* coef) {
+  const double inv = inv_std;
+  const double dg = gx * inv;  // sum g * xhat
+  const double db = g;
+  const double ac = (double)gamma * inv;
+  const double dc = ac * dg * inv * inv_m;
+  const double ec = -ac * db * inv_m + dc * (double)mean;
+  dgamma[ch] = (float)dg;
+  dbeta[ch] = (float)db;
+  coef[ch] = (float)ac;
+  coef[c + ch] = (float)dc;
+  coef[2 * c + ch] = (float)ec;
+}
+
+// Split backward, second half: one thread per channel, from the sums reduced over all ranks.
+__global__ void bn_bwd_coef_kernel(const float* __restrict__ sums, int c, double inv_m, const float* gamma,
+                                   const float* mean, const float* inv_std, float* dgamma, float* dbeta,
+                                   float* coef) {
+  const int ch = blockIdx.x * blockDim.x + threadIdx.x;
+  if (ch < c) bwd_coef(sums[ch], sums[c + ch], gamma[ch], mean[ch], inv_std[ch], inv_m, c, ch, dgamma, dbeta, coef);
+}
+
+// Split forward, second half: merges `world` moment sets [mean c][M2 c][count] in order
+// (Chan, in fp64: a few hundred values) and finalizes as the forward's last CTA does.
+__global__ void bn_merge_finalize_kernel(const float* __restrict__ moments, int world, int c, const float* gamma,
+                                         const float* beta, float* running_mean, float* running_var, float momentum,
+                                         float eps, float* saved_mean, float* saved_inv_var, float* eq) {
+  const int ch = blockIdx.x * blockDim.x + threadIdx.x;
+  if (ch >= c) return;
+  const int stride = 2 * c + 1;
+  double n = 0.0, m = 0.0, q = 0.0;
+  for (int r = 0; r < world; ++r) {
+    const double nb = moments[(size_t)r * stride + 2 * c];
+    const double mb = moments[(size_t)r * stride + ch], qb = moments[(size_t)r * stride + c + ch];
+    const double nn = n + nb;
+    if (nb > 0.0) {
+      const double d = mb - m, fb = nb / nn;
+      m += d * fb;
+      q += qb + d * d * n * fb;
+    }
+    n = nn;
+  }
+  const float meanf = (float)m;
+  const float var = n > 0.0 ? (float)(q / n) : 0.f;  // biased, for normalising
+  const float inv = rsqrtf(var + eps);
+  const float gm = gamma[ch];
+  saved_mean[ch] = meanf;
+  saved_inv_var[ch] = inv;
+  eq[ch] = gm * inv;
+  eq[c + ch] = beta[ch] - gm * meanf * inv;
+  const float unbias = n > 1.0 ? (float)(n / (n - 1.0)) : 1.f;
+  running_mean[ch] = (1.f - momentum) * running_mean[ch] + momentum * meanf;
+  running_var[ch] = (1.f - momentum) * running_var[ch] + momentum * var * unbias;
 }
 
 __device__ __forceinline__ uint32_t fastdiv(uint32_t n, const FastDiv& f) {
@@ -389,6 +448,21 @@ int launch_apply(const ApplyArgs& a, bool bf16, int num_sms, cudaStream_t st) {
 }
 
 size_t bwd_reduce_partial_floats(int num_sms, int c) { return (size_t)num_sms * 2 * 2 * c; }
+
+int launch_merge_finalize(const float* moments, int world, int c, const float* gamma, const float* beta,
+                          float* running_mean, float* running_var, float momentum, float eps,
+                          float* saved_mean, float* saved_inv_var, float* eq, cudaStream_t st) {
+  bn_merge_finalize_kernel<<<(c + 127) / 128, 128, 0, st>>>(moments, world, c, gamma, beta, running_mean, running_var,
+                                                            momentum, eps, saved_mean, saved_inv_var, eq);
+  return cudaGetLastError() == cudaSuccess ? 0 : 6;
+}
+
+int launch_bwd_coef(const float* sums, int c, long long m_count, const float* gamma, const float* mean,
+                    const float* inv_std, float* dgamma, float* dbeta, float* coef, cudaStream_t st) {
+  bn_bwd_coef_kernel<<<(c + 127) / 128, 128, 0, st>>>(sums, c, 1.0 / (double)m_count, gamma, mean, inv_std, dgamma,
+                                                      dbeta, coef);
+  return cudaGetLastError() == cudaSuccess ? 0 : 6;
+}
 
 int launch_bwd_reduce(const BwdReduceArgs& a, bool bf16, int num_sms, cudaStream_t st) {
   if (a.c % 8 != 0 || a.c > 256 || (kRedThreads % (a.c / 8)) != 0) return 3;

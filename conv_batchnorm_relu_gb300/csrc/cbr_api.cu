@@ -171,12 +171,14 @@ bool dz_materialisable(const Shape& s) {
 }
 
 struct BwdWs {
-  size_t coef, part, wpart, dz, z, total;
+  size_t coef, mbits, part, wpart, dz, z, total;
 };
 BwdWs bwd_ws(const Shape& s, bool need_z) {
   BwdWs L;
   L.coef = kHdrBytes;
-  L.part = align_up(L.coef + 3 * s.cout * sizeof(float), 256);
+  // the bit-packed form of a byte-per-element mask (CBR_MASK_BYTES), one bit per element
+  L.mbits = align_up(L.coef + 3 * s.cout * sizeof(float), 256);
+  L.part = align_up(L.mbits + (size_t)((s.m * s.cout + 31) / 32) * 4, 256);
   L.wpart = align_up(L.part + bwd_reduce_partial_floats(kMaxCtas, (int)s.cout) * sizeof(float), 256);
   const size_t wpart = is_first_layer(s) ? first_wgrad_partial_floats(kMaxCtas, (int)s.cout)
                                          : wgrad_partial_floats(kMaxCtas, (int)s.cin, (int)s.cout, (int)(s.r * s.s));
@@ -400,24 +402,119 @@ cbr_status_t cbr_forward_train(const cbr_desc_t* desc, const void* x, const void
   return CBR_OK;
 }
 
-cbr_status_t cbr_backward(const cbr_desc_t* desc, const void* dy, const void* x, const void* w,
-                          const void* y_or_relu_mask, int32_t mask_kind, const void* z_saved,
-                          const float* gamma, const float* saved_mean,
-                          const float* saved_inv_var, void* dx, float* dw, float* dgamma,
-                          float* dbeta, void* ws, size_t ws_bytes, cbr_stream_t stream) {
+cbr_status_t cbr_forward_train_stats(const cbr_desc_t* desc, const void* x, const void* w, void* z,
+                                     float* moments, void* ws, size_t ws_bytes, cbr_stream_t stream) {
   Shape s;
   int st = check_desc(desc, &s);
   if (st) return (cbr_status_t)st;
-  if (!dy || !x || !w || !y_or_relu_mask || !gamma || !saved_mean || !saved_inv_var || !dw ||
-      !dgamma || !dbeta || !ws)
+  if (!x || !w || !z || !moments || !ws) return CBR_ERR_INVALID_ARG;
+  if (!aligned(x, 16) || !aligned(w, 16) || !aligned(z, 16) || !aligned(ws, 16) || !aligned(moments, 4))
+    return CBR_ERR_MISALIGNED;
+  if ((st = check_supported(s))) return (cbr_status_t)st;
+  const FwdWs L = fwd_ws(s, false);
+  if (ws_bytes < L.total) return CBR_ERR_WORKSPACE;
+  DeviceInfo* dev = nullptr;
+  if ((st = current_device(&dev))) return (cbr_status_t)st;
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  uint8_t* wsb = static_cast<uint8_t*>(ws);
+  Prof prof(cs);
+  FpropArgs a{};
+  a.g = make_geom(s);
+  a.z = z;
+  a.part = reinterpret_cast<float*>(wsb + L.part);
+  a.ticket = reinterpret_cast<uint32_t*>(wsb);
+  a.moments = moments;
+  a.m_count = s.m;
+  a.err = dev->err;
+  a.mode = kFpropStats;
+  st = run_fprop(a, s, x, w, dev->num_sms, cs);
+  if (st) return (cbr_status_t)st;
+  prof.mark();
+  return CBR_OK;
+}
+
+cbr_status_t cbr_forward_train_finish(const cbr_desc_t* desc, const float* moments_all, int32_t world,
+                                      const float* gamma, const float* beta, float* running_mean,
+                                      float* running_var, float momentum, float eps, const void* z,
+                                      void* y, uint32_t* relu_mask, float* saved_mean,
+                                      float* saved_inv_var, void* ws, size_t ws_bytes,
+                                      cbr_stream_t stream) {
+  Shape s;
+  int st = check_desc(desc, &s);
+  if (st) return (cbr_status_t)st;
+  if (!moments_all || world < 1 || world > 65536 || !gamma || !beta || !running_mean || !running_var || !z ||
+      !y || !saved_mean || !saved_inv_var || !ws)
     return CBR_ERR_INVALID_ARG;
-  if (mask_kind != CBR_MASK_BITS && mask_kind != CBR_MASK_FROM_Y) return CBR_ERR_INVALID_ARG;
+  if (!(momentum >= 0.f && momentum <= 1.f) || !(eps > 0.f) || !std::isfinite(eps)) return CBR_ERR_INVALID_ARG;
+  if (!aligned(z, 16) || !aligned(y, 16) || !aligned(ws, 16) || (relu_mask && !aligned(relu_mask, 4)) ||
+      !aligned(moments_all, 4) || !aligned(gamma, 4) || !aligned(beta, 4) || !aligned(running_mean, 4) ||
+      !aligned(running_var, 4) || !aligned(saved_mean, 4) || !aligned(saved_inv_var, 4))
+    return CBR_ERR_MISALIGNED;
+  if ((st = check_supported(s))) return (cbr_status_t)st;
+  const FwdWs L = fwd_ws(s, false);
+  if (ws_bytes < L.total) return CBR_ERR_WORKSPACE;
+  DeviceInfo* dev = nullptr;
+  if ((st = current_device(&dev))) return (cbr_status_t)st;
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  uint8_t* wsb = static_cast<uint8_t*>(ws);
+  Prof prof(cs);
+  float* eq = reinterpret_cast<float*>(wsb + L.eq);
+  st = launch_merge_finalize(moments_all, world, (int)s.cout, gamma, beta, running_mean, running_var, momentum, eps,
+                             saved_mean, saved_inv_var, eq, cs);
+  if (st) return (cbr_status_t)st;
+  prof.mark();
+  ApplyArgs ap{};
+  ap.z = z;
+  ap.y = y;
+  ap.mask = reinterpret_cast<uint8_t*>(relu_mask);
+  ap.eq = eq;
+  ap.total = s.m * s.cout;
+  ap.c = (int)s.cout;
+  st = launch_apply(ap, s.bf16, dev->num_sms, cs);
+  if (st) return (cbr_status_t)st;
+  prof.mark();
+  return CBR_OK;
+}
+
+}  // extern "C"
+
+namespace cbr {
+namespace {
+
+// The three uses of the backward path: the whole backward; the split backward's first half
+// (the masked reduction's raw sums, then stop); its second half (coefficients from sums
+// reduced over all ranks, then the convolutions).
+enum BwdMode { kBwdFull, kBwdSums, kBwdFinish };
+
+int backward_run(BwdMode mode, const cbr_desc_t* desc, const void* dy, const void* x, const void* w,
+                 const void* y_or_relu_mask, int32_t mask_kind, const void* z_saved, const float* gamma,
+                 const float* saved_mean, const float* saved_inv_var, void* dx, float* dw, float* dgamma,
+                 float* dbeta, void* ws, size_t ws_bytes, cbr_stream_t stream, float* sums_out,
+                 const float* sums_all, long long m_total) {
+  Shape s;
+  int st = check_desc(desc, &s);
+  if (st) return (cbr_status_t)st;
+  if (mode == kBwdSums) {
+    // only the reduction runs: it reads dy, the mask and z against the mean
+    if (!dy || !y_or_relu_mask || !z_saved || !saved_mean || !sums_out || !ws) return CBR_ERR_INVALID_ARG;
+    // x, W, gamma, inv_std and the gradient outputs are not touched; aliases keep the shared
+    // checks below simple (the sums need only 4-byte alignment)
+    x = w = dy;
+    gamma = saved_inv_var = dgamma = dbeta = dw = sums_out;
+    dx = nullptr;
+  } else if (!dy || !x || !w || !y_or_relu_mask || !gamma || !saved_mean || !saved_inv_var || !dw ||
+             !dgamma || !dbeta || !ws) {
+    return CBR_ERR_INVALID_ARG;
+  }
+  if (mode == kBwdFinish && (!sums_all || m_total < 2)) return CBR_ERR_INVALID_ARG;
+  if (mask_kind != CBR_MASK_BITS && mask_kind != CBR_MASK_FROM_Y && mask_kind != CBR_MASK_BYTES)
+    return CBR_ERR_INVALID_ARG;
   if (dx && overlaps(dx, act_bytes(s.n, s.h, s.w, s.cin, s.elt), x,
                      act_bytes(s.n, s.h, s.w, s.cin, s.elt)))
     return CBR_ERR_INVALID_ARG;
   if (!aligned(dy, 16) || !aligned(x, 16) || !aligned(w, 16) || !aligned(ws, 16) ||
       (dx && !aligned(dx, 16)) || (z_saved && !aligned(z_saved, 16)) ||
-      !aligned(y_or_relu_mask, mask_kind == CBR_MASK_FROM_Y ? 16 : 4) || !aligned(dw, 16) ||
+      !aligned(y_or_relu_mask, mask_kind == CBR_MASK_BITS ? 4 : 16) || (mode != kBwdSums && !aligned(dw, 16)) ||
       !aligned(gamma, 4) || !aligned(saved_mean, 4) || !aligned(saved_inv_var, 4) ||
       !aligned(dgamma, 4) || !aligned(dbeta, 4))
     return CBR_ERR_MISALIGNED;
@@ -450,27 +547,44 @@ cbr_status_t cbr_backward(const cbr_desc_t* desc, const void* dy, const void* x,
   }
   const uint8_t* mask = mask_kind == CBR_MASK_BITS ? static_cast<const uint8_t*>(y_or_relu_mask) : nullptr;
   const void* yv = mask_kind == CBR_MASK_FROM_Y ? y_or_relu_mask : nullptr;
+  if (mask_kind == CBR_MASK_BYTES) {
+    // a byte-per-element mask is packed into the workspace once; the kernels read bits
+    uint32_t* mb = reinterpret_cast<uint32_t*>(wsb + L.mbits);
+    st = launch_mask_bytes_to_bits(static_cast<const uint8_t*>(y_or_relu_mask), mb, s.m * s.cout, dev->num_sms, cs);
+    if (st) return (cbr_status_t)st;
+    prof.mark();
+    mask = reinterpret_cast<const uint8_t*>(mb);
+  }
   float* coef = reinterpret_cast<float*>(wsb + L.coef);
 
-  BwdReduceArgs b{};
-  b.dy = dy;
-  b.z = z;
-  b.y = yv;
-  b.mask = mask;
-  b.gamma = gamma;
-  b.mean = saved_mean;
-  b.inv_std = saved_inv_var;
-  b.dgamma = dgamma;
-  b.dbeta = dbeta;
-  b.coef = coef;
-  b.part = reinterpret_cast<float*>(wsb + L.part);
-  b.ticket = reinterpret_cast<uint32_t*>(wsb) + 1;
-  b.m_count = s.m;
-  b.c = (int)s.cout;
-  b.err = dev->err;
-  st = launch_bwd_reduce(b, s.bf16, dev->num_sms, cs);
-  if (st) return (cbr_status_t)st;
-  prof.mark();
+  if (mode == kBwdFinish) {
+    // sums reduced over all ranks: dgamma, dbeta and the coefficients over the global batch
+    st = launch_bwd_coef(sums_all, (int)s.cout, m_total, gamma, saved_mean, saved_inv_var, dgamma, dbeta, coef, cs);
+    if (st) return (cbr_status_t)st;
+    prof.mark();
+  } else {
+    BwdReduceArgs b{};
+    b.dy = dy;
+    b.z = z;
+    b.y = yv;
+    b.mask = mask;
+    b.gamma = gamma;
+    b.mean = saved_mean;
+    b.inv_std = saved_inv_var;
+    b.dgamma = dgamma;
+    b.dbeta = dbeta;
+    b.coef = coef;
+    b.sums_out = mode == kBwdSums ? sums_out : nullptr;
+    b.part = reinterpret_cast<float*>(wsb + L.part);
+    b.ticket = reinterpret_cast<uint32_t*>(wsb) + 1;
+    b.m_count = s.m;
+    b.c = (int)s.cout;
+    b.err = dev->err;
+    st = launch_bwd_reduce(b, s.bf16, dev->num_sms, cs);
+    if (st) return (cbr_status_t)st;
+    prof.mark();
+    if (mode == kBwdSums) return CBR_OK;
+  }
 
   if (use_fused_bwd(s)) {
     // dz = a*(dy*mask) - d*z + e evaluated once per tile on chip, feeding both convolutions
@@ -557,6 +671,40 @@ cbr_status_t cbr_backward(const cbr_desc_t* desc, const void* dy, const void* x,
   return CBR_OK;
 }
 
+}  // namespace
+}  // namespace cbr
+
+extern "C" {
+
+cbr_status_t cbr_backward(const cbr_desc_t* desc, const void* dy, const void* x, const void* w,
+                          const void* y_or_relu_mask, int32_t mask_kind, const void* z_saved,
+                          const float* gamma, const float* saved_mean,
+                          const float* saved_inv_var, void* dx, float* dw, float* dgamma,
+                          float* dbeta, void* ws, size_t ws_bytes, cbr_stream_t stream) {
+  return (cbr_status_t)backward_run(kBwdFull, desc, dy, x, w, y_or_relu_mask, mask_kind, z_saved, gamma,
+                                    saved_mean, saved_inv_var, dx, dw, dgamma, dbeta, ws, ws_bytes, stream,
+                                    nullptr, nullptr, 0);
+}
+
+cbr_status_t cbr_backward_sums(const cbr_desc_t* desc, const void* dy, const void* y_or_relu_mask,
+                               int32_t mask_kind, const void* z_saved, const float* saved_mean,
+                               float* sums, void* ws, size_t ws_bytes, cbr_stream_t stream) {
+  return (cbr_status_t)backward_run(kBwdSums, desc, dy, nullptr, nullptr, y_or_relu_mask, mask_kind, z_saved,
+                                    nullptr, saved_mean, nullptr, nullptr, nullptr, nullptr, nullptr, ws,
+                                    ws_bytes, stream, sums, nullptr, 0);
+}
+
+cbr_status_t cbr_backward_finish(const cbr_desc_t* desc, const float* sums_all, int64_t m_total,
+                                 const void* dy, const void* x, const void* w,
+                                 const void* y_or_relu_mask, int32_t mask_kind, const void* z_saved,
+                                 const float* gamma, const float* saved_mean,
+                                 const float* saved_inv_var, void* dx, float* dw, float* dgamma,
+                                 float* dbeta, void* ws, size_t ws_bytes, cbr_stream_t stream) {
+  return (cbr_status_t)backward_run(kBwdFinish, desc, dy, x, w, y_or_relu_mask, mask_kind, z_saved, gamma,
+                                    saved_mean, saved_inv_var, dx, dw, dgamma, dbeta, ws, ws_bytes, stream,
+                                    nullptr, sums_all, m_total);
+}
+
 cbr_status_t cbr_fold_bn(const cbr_desc_t* desc, const void* w, const float* conv_bias,
                          const float* gamma, const float* beta, const float* running_mean,
                          const float* running_var, float eps, void* w_fold, float* b_fold,
@@ -602,6 +750,30 @@ cbr_status_t cbr_forward_infer(const cbr_desc_t* desc, const void* x, const void
   if (st) return (cbr_status_t)st;
   prof.mark();
   return CBR_OK;
+}
+
+cbr_status_t cbr_mask_bits_to_bytes(const uint32_t* bits, uint8_t* bytes, int64_t count,
+                                    cbr_stream_t stream) {
+  if (count < 0 || (count > 0 && (!bits || !bytes))) return CBR_ERR_INVALID_ARG;
+  if (count == 0) return CBR_OK;
+  if (!aligned(bits, 4) || !aligned(bytes, 16)) return CBR_ERR_MISALIGNED;
+  DeviceInfo* dev = nullptr;
+  int st = current_device(&dev);
+  if (st) return (cbr_status_t)st;
+  return (cbr_status_t)launch_mask_bits_to_bytes(bits, bytes, count, dev->num_sms,
+                                                 reinterpret_cast<cudaStream_t>(stream));
+}
+
+cbr_status_t cbr_mask_bytes_to_bits(const uint8_t* bytes, uint32_t* bits, int64_t count,
+                                    cbr_stream_t stream) {
+  if (count < 0 || (count > 0 && (!bits || !bytes))) return CBR_ERR_INVALID_ARG;
+  if (count == 0) return CBR_OK;
+  if (!aligned(bits, 4) || !aligned(bytes, 16)) return CBR_ERR_MISALIGNED;
+  DeviceInfo* dev = nullptr;
+  int st = current_device(&dev);
+  if (st) return (cbr_status_t)st;
+  return (cbr_status_t)launch_mask_bytes_to_bits(bytes, bits, count, dev->num_sms,
+                                                 reinterpret_cast<cudaStream_t>(stream));
 }
 
 cbr_status_t cbr_stream_status(cbr_stream_t stream) {

@@ -53,6 +53,9 @@ struct FpropArgs {
   float* saved_mean;
   float* saved_inv_var;
   float* eq;                // [2][cout] eq_scale, eq_bias for the apply pass
+  // split (synchronised) forward: when set, the last CTA writes the merged moments of this
+  // call's rows here, [mean cout][M2 cout][row count], instead of finalizing
+  float* moments;
   const float* bias;        // inference: per-channel bias added before ReLU
   float momentum;
   float eps;
@@ -129,6 +132,9 @@ struct BwdReduceArgs {
   float* dgamma;
   float* dbeta;
   float* coef;              // [3][c]: a, d, e with dz = a*g - d*z + e
+  // split (synchronised) backward: when set, the last block writes the raw per-channel sums
+  // [sum g c][sum g*(z - mean) c] here instead of dgamma, dbeta and the coefficients
+  float* sums_out;
   float* part;              // [grid][2][c]
   uint32_t* ticket;
   long long m_count;
@@ -137,6 +143,14 @@ struct BwdReduceArgs {
   uint32_t* err;
 };
 int launch_bwd_reduce(const BwdReduceArgs& a, bool bf16, int num_sms, cudaStream_t st);
+// Split forward, second half: merge `world` moment sets ([mean c][M2 c][count] each, in order)
+// and finalize the statistics as the forward does (bn_kernels.cu).
+int launch_merge_finalize(const float* moments, int world, int c, const float* gamma, const float* beta,
+                          float* running_mean, float* running_var, float momentum, float eps,
+                          float* saved_mean, float* saved_inv_var, float* eq, cudaStream_t st);
+// Split backward, second half: dgamma, dbeta and the dz coefficients from reduced sums.
+int launch_bwd_coef(const float* sums, int c, long long m_count, const float* gamma, const float* mean,
+                    const float* inv_std, float* dgamma, float* dbeta, float* coef, cudaStream_t st);
 size_t bwd_reduce_partial_floats(int num_sms, int c);
 
 struct DgradArgs {
@@ -223,6 +237,10 @@ struct DzArgs {
   int pitch;                // dz row pitch in pixels (>= q); columns q..pitch-1 are written as zero
   FastDiv fd_cvec, fd_q;    // division by c/8 and by q (set by the launcher)
 };
+// ReLU-mask transcoding, bit-packed <-> one byte per element (mask.cu).  count = elements.
+int launch_mask_bytes_to_bits(const uint8_t* bytes, uint32_t* bits, long long count, int num_sms, cudaStream_t st);
+int launch_mask_bits_to_bytes(const uint32_t* bits, uint8_t* bytes, long long count, int num_sms, cudaStream_t st);
+
 // One warp that gives up on a never-completed barrier after limit_ns (selftest.cu).
 int launch_selftest_wait(uint32_t* err, uint64_t limit_ns, cudaStream_t st);
 // dz = a*(dy*mask) - d*z + e, elementwise (bn_kernels.cu).

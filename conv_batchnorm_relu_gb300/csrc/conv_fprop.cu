@@ -28,6 +28,7 @@ int launch_fprop(const FpropArgs& f, int c_in, int c_out, bool bf16, const void*
   a.saved_mean = f.saved_mean;
   a.saved_inv_var = f.saved_inv_var;
   a.eq = f.eq;
+  a.moments = f.moments;
   a.bias = f.bias;
   a.momentum = f.momentum;
   a.eps = f.eps;

@@ -1602,6 +1602,7 @@ int launch_first_fprop(const FpropArgs& f, int stride, int c_out, bool bf16, con
   a.saved_mean = f.saved_mean;
   a.saved_inv_var = f.saved_inv_var;
   a.eq = f.eq;
+  a.moments = f.moments;
   a.bias = f.bias;
   a.momentum = f.momentum;
   a.eps = f.eps;

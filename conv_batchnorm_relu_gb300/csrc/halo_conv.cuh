@@ -41,6 +41,7 @@ struct ConvArgs {
   float* saved_mean;
   float* saved_inv_var;
   float* eq;
+  float* moments;           // split forward: merged moments out instead of the finalize
   const float* bias;
   float momentum;
   float eps;
@@ -121,7 +122,7 @@ __device__ void stats_partial_finalize(const ConvArgs& a, const float* red, uint
   // the per-channel inputs of the finalize, loaded before the ticket by every CTA (cheap) so
   // the last one does not wait for them after its merges
   float gm = 0.f, bt = 0.f, rm = 0.f, rv = 0.f;
-  if (threadIdx.x < COUT) {
+  if (threadIdx.x < COUT && !a.moments) {
     gm = a.gamma[threadIdx.x];
     bt = a.beta[threadIdx.x];
     rm = a.running_mean[threadIdx.x];
@@ -205,6 +206,14 @@ __device__ void stats_partial_finalize(const ConvArgs& a, const float* red, uint
       for (int w = P / 2; w >= 1; w /= 2)
 #pragma unroll
         for (int k = 0; k < w; ++k) st::chan_merge(tn[k], tm[k], tq[k], tn[k + w], tm[k + w], tq[k + w]);
+      if (a.moments) {
+        // split forward: this call's moments go to the caller, who merges them with other
+        // ranks' and finalizes later
+        a.moments[c] = tm[0];
+        a.moments[COUT + c] = tq[0];
+        if (c == 0) a.moments[2 * COUT] = tn[0];
+        return;
+      }
       const float meanf = tm[0];
       const float var = fmaxf(tq[0] * (float)a.inv_m, 0.f);  // biased: M2 / M
       const float inv = rsqrtf(var + a.eps);

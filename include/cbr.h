@@ -69,8 +69,10 @@ typedef enum { CBR_F16 = 0, CBR_BF16 = 1 } cbr_dtype_t;
 
 /* Source of the ReLU mask for cbr_backward. */
 typedef enum {
-  CBR_MASK_BITS = 0,  /* bit-packed mask written by cbr_forward_train */
-  CBR_MASK_FROM_Y = 1 /* recompute the mask as y > 0 from the forward output y */
+  CBR_MASK_BITS = 0,   /* bit-packed mask written by cbr_forward_train */
+  CBR_MASK_FROM_Y = 1, /* recompute the mask as y > 0 from the forward output y */
+  CBR_MASK_BYTES = 2   /* one byte per NHWC element, non-zero = active (a standalone ReLU's
+                          INT8 mask); packed into the workspace before use */
 } cbr_mask_kind_t;
 
 /* One CBR layer.  dtype is a cbr_dtype_t. */
@@ -121,8 +123,9 @@ cbr_status_t cbr_forward_train(const cbr_desc_t* desc, const void* x, const void
  * Training backward (CBR page, sections 5.1-5.3; BatchNorm page, section 3.1).
  *   dy [n][p][q][c_out]            upstream gradient, storage dtype
  *   x, w                           the forward's inputs
- *   y_or_relu_mask, mask_kind      the forward's relu_mask words (CBR_MASK_BITS) or its y
- *                                  (CBR_MASK_FROM_Y)
+ *   y_or_relu_mask, mask_kind      the forward's relu_mask words (CBR_MASK_BITS, 4-byte
+ *                                  aligned), its y (CBR_MASK_FROM_Y) or a byte-per-element
+ *                                  mask (CBR_MASK_BYTES, n*p*q*c_out bytes, 16-byte aligned)
  *   z_saved                        the forward's z_saved, or NULL to recompute conv(x, W)
  *   gamma, saved_mean, saved_inv_var   fp32 [c_out] (saved_* from cbr_forward_train)
  *   dx [n][h][w][c_in] or NULL     NULL = first layer: the data gradient is skipped
@@ -141,6 +144,57 @@ cbr_status_t cbr_backward(const cbr_desc_t* desc, const void* dy, const void* x,
                           const float* gamma, const float* saved_mean,
                           const float* saved_inv_var, void* dx, float* dw, float* dgamma,
                           float* dbeta, void* ws, size_t ws_bytes, cbr_stream_t stream);
+
+/*
+ * Synchronised BatchNorm across data-parallel ranks ("BatchNorm CUDA implementation",
+ * section 7.1: the per-channel statistics of every rank's share of the batch are combined
+ * before normalising, and so are the backward's per-channel sums).  Each call pair brackets
+ * one collective that the caller runs (e.g. with NCCL); the library itself stays on one GPU.
+ *
+ * Forward, first half: conv and this rank's statistics, no finalize and no apply.
+ *   z [n][p][q][c_out]     the conv output (required: the second half normalises it)
+ *   moments [2*c_out + 1]  fp32 out: per-channel mean [c_out], M2 (sum of squared deviations
+ *                          from the mean) [c_out], then this rank's row count n*p*q
+ *   ws, ws_bytes           the forward workspace (cbr_workspace_size's fwd_bytes suffices)
+ * The caller gathers every rank's moments, in rank order, into moments_all
+ * [world][2*c_out + 1] (an all-gather, not a sum: moments merge exactly, sums of squares
+ * would cancel), then calls
+ * Forward, second half: merges the `world` moment sets in that order (Chan's parallel
+ * formula), writes saved_mean / saved_inv_var, updates the running statistics with the
+ * global unbiased variance (M = the sum of the counts), and applies BN + ReLU to this rank's z,
+ * as cbr_forward_train does.  Every rank computes identical statistics.
+ * Errors: INVALID_ARG (NULL, world < 1, momentum / eps out of range), MISALIGNED,
+ * UNSUPPORTED, WORKSPACE, DEVICE, CUDA.
+ */
+cbr_status_t cbr_forward_train_stats(const cbr_desc_t* desc, const void* x, const void* w, void* z,
+                                     float* moments, void* ws, size_t ws_bytes, cbr_stream_t stream);
+cbr_status_t cbr_forward_train_finish(const cbr_desc_t* desc, const float* moments_all, int32_t world,
+                                      const float* gamma, const float* beta, float* running_mean,
+                                      float* running_var, float momentum, float eps, const void* z,
+                                      void* y, uint32_t* relu_mask, float* saved_mean,
+                                      float* saved_inv_var, void* ws, size_t ws_bytes,
+                                      cbr_stream_t stream);
+
+/*
+ * Backward, first half: this rank's masked per-channel sums, written to sums [2*c_out] as
+ * [sum of dy*mask][sum of dy*mask*(z - saved_mean)] (saved_mean: the merged mean from
+ * cbr_forward_train_finish; z and the mask as for cbr_backward; ws: the backward workspace).
+ * The caller sums them over the ranks (an all-reduce) into sums_all and calls
+ * Backward, second half: dgamma, dbeta and the BN data gradient from the global sums over
+ * m_total = the global n*p*q, then wgrad and dgrad of this rank's share, as cbr_backward does.
+ * dgamma and dbeta are the global ones (identical on every rank); dW is this rank's share (the
+ * caller's data-parallel gradient all-reduce sums it).
+ * Errors as for cbr_backward, and INVALID_ARG for a NULL sums / sums_all or m_total < 2.
+ */
+cbr_status_t cbr_backward_sums(const cbr_desc_t* desc, const void* dy, const void* y_or_relu_mask,
+                               int32_t mask_kind, const void* z_saved, const float* saved_mean,
+                               float* sums, void* ws, size_t ws_bytes, cbr_stream_t stream);
+cbr_status_t cbr_backward_finish(const cbr_desc_t* desc, const float* sums_all, int64_t m_total,
+                                 const void* dy, const void* x, const void* w,
+                                 const void* y_or_relu_mask, int32_t mask_kind, const void* z_saved,
+                                 const float* gamma, const float* saved_mean,
+                                 const float* saved_inv_var, void* dx, float* dw, float* dgamma,
+                                 float* dbeta, void* ws, size_t ws_bytes, cbr_stream_t stream);
 
 /*
  * BN folding for inference (CBR page, section 2; BatchNorm page, section 4.4):
@@ -186,6 +240,24 @@ cbr_status_t cbr_forward_train_noalloc(const cbr_desc_t* desc, const void* x, co
                                        float* running_var, float momentum, float eps, void* y,
                                        uint32_t* relu_mask, void* z_saved, float* saved_mean,
                                        float* saved_inv_var, cbr_stream_t stream);
+
+/*
+ * ReLU-mask transcoding between this library's bit-packed mask (bit i of 32-bit word j is NHWC
+ * element 32*j + i) and one byte per element (0 or 1), the form a standalone ReLU keeps
+ * (CBR page, sections 8 and 9: the fused operator's BOOLEAN mask against the standalone
+ * ReLU's INT8 mask, transcoded by its equivalence tests).
+ *   count       elements (>= 0; 0 is a no-op)
+ *   bits        ceil(count/32) uint32 words, 4-byte aligned
+ *   bytes       count bytes, 16-byte aligned
+ * cbr_mask_bits_to_bytes writes 0 or 1 per element.  cbr_mask_bytes_to_bits sets a bit for
+ * every non-zero byte and writes the bits past `count` in the last word as 0.  Asynchronous on
+ * `stream`.  Errors: INVALID_ARG (count < 0, or a NULL buffer with count > 0), MISALIGNED,
+ * DEVICE, CUDA.
+ */
+cbr_status_t cbr_mask_bits_to_bytes(const uint32_t* bits, uint8_t* bytes, int64_t count,
+                                    cbr_stream_t stream);
+cbr_status_t cbr_mask_bytes_to_bits(const uint8_t* bytes, uint32_t* bits, int64_t count,
+                                    cbr_stream_t stream);
 
 /*
  * Synchronise `stream`, then read and clear the device error word of the current device.

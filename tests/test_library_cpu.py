@@ -151,3 +151,28 @@ def test_selftest_limit_checked_before_device(lib):
         assert lib.cbr_selftest_bounded_wait(bad, None) == 1
     # a valid limit gets as far as the device check (no GPU here)
     assert lib.cbr_selftest_bounded_wait(1000, None) == 5
+
+
+def test_mask_transcoding_validation(lib):
+    """Argument checks of cbr_mask_bits_to_bytes / cbr_mask_bytes_to_bits, before any launch."""
+    for f in (lib.cbr_mask_bits_to_bytes, lib.cbr_mask_bytes_to_bits):
+        assert f(P, P, -1, None) == 1            # negative count
+        assert f(None, P, 64, None) == 1         # NULL buffer
+        assert f(P, None, 64, None) == 1
+        assert f(None, None, 0, None) == 0       # empty: nothing to do
+    assert lib.cbr_mask_bits_to_bytes(P + 2, P, 64, None) == 2   # words must be 4-byte aligned
+    assert lib.cbr_mask_bits_to_bytes(P, P + 4, 64, None) == 2   # bytes must be 16-byte aligned
+    assert lib.cbr_mask_bytes_to_bits(P + 8, P, 64, None) == 2
+    if not torch.cuda.is_available():
+        assert lib.cbr_mask_bits_to_bytes(P, P, 64, None) == 5
+
+
+def test_backward_accepts_byte_mask_kind(lib):
+    d = _desc()
+    # CBR_MASK_BYTES (2) wants a 16-byte aligned mask; kinds past it are rejected
+    st = lib.cbr_backward(ctypes.byref(d), P, P, P, P + 4, 2, P, P, P, P, P + (1 << 20), P, P, P, P,
+                          1 << 40, None)
+    assert st == 2
+    st = lib.cbr_backward(ctypes.byref(d), P, P, P, P, 3, P, P, P, P, P + (1 << 20), P, P, P, P,
+                          1 << 40, None)
+    assert st == 1
