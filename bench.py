@@ -251,44 +251,55 @@ def traffic_for(kernel: str, config_index: int):
 
 
 def time_inference(spec, layer, g, flush, stream, K, peaks) -> dict:
-    """The folded inference path: cbr_fold_bn once (untimed), then cbr_forward_infer timed as a
-    replayed CUDA graph [L2 flush, event, infer, event], like the training step."""
+    """The two inference forms, each timed as a replayed CUDA graph [L2 flush, event, call,
+    event], like the training step: the folded form (cbr_fold_bn once, untimed, then
+    cbr_forward_infer) and the epilogue-only form (cbr_forward_infer_bn, BatchNorm on the
+    accumulator of the unfolded filter)."""
     from conv_batchnorm_relu_gb300 import cbr
     w_fold, b_fold = cbr.fold_bn(layer, g["w"], g["gamma"], g["beta"], g["running_mean"],
                                  g["running_var"], spec.eps)
     y = torch.empty((spec.n, spec.p, spec.q, spec.c_out), dtype=spec.torch_dtype, device=g["x"].device)
-    for _ in range(3):
-        cbr.forward_infer(layer, g["x"], w_fold, b_fold, out=y)
-    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    t0.record(stream)
-    t1.record(stream)
-    torch.cuda.synchronize()
-    graph = torch.cuda.CUDAGraph()
-    cap = torch.cuda.Stream()
-    cap.wait_stream(stream)
-    with torch.cuda.graph(graph, stream=cap, capture_error_mode="thread_local"):
-        flush.zero_()
-        record_external(t0, torch.cuda.current_stream())
-        cbr.forward_infer(layer, g["x"], w_fold, b_fold, out=y)
-        record_external(t1, torch.cuda.current_stream())
-    torch.cuda.synchronize()
-    for _ in range(3):
-        graph.replay()
-    torch.cuda.synchronize()
-    ms = 0.0
-    for _ in range(K):
-        graph.replay()
-        torch.cuda.synchronize()
-        ms += t0.elapsed_time(t1)
-    cbr.stream_status()
-    ms /= K
+    calls = {
+        "folded": lambda: cbr.forward_infer(layer, g["x"], w_fold, b_fold, out=y),
+        "bn_epilogue": lambda: cbr.forward_infer_bn(layer, g["x"], g["w"], g["gamma"], g["beta"],
+                                                    g["running_mean"], g["running_var"], spec.eps, out=y),
+    }
     p = roofline.infer_pass(spec)
     roof_us, bound = p.roof_us(peaks)
-    t_s = ms * 1e-3
-    return {"us": round(ms * 1e3, 2), "images_per_s": spec.n / t_s, "tflops": p.flops / t_s / 1e12,
-            "gbs": p.bytes / t_s / 1e9, "roof_us": round(roof_us, 2), "bound": bound,
-            "frac": round(roof_us / (ms * 1e3), 4), "launches_per_call": 1,
-            "note": "cbr_forward_infer alone (fold done once before timing), L2 flushed before each call"}
+    res = {}
+    for name, call in calls.items():
+        for _ in range(3):
+            call()
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0.record(stream)
+        t1.record(stream)
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        cap = torch.cuda.Stream()
+        cap.wait_stream(stream)
+        with torch.cuda.graph(graph, stream=cap, capture_error_mode="thread_local"):
+            flush.zero_()
+            record_external(t0, torch.cuda.current_stream())
+            call()
+            record_external(t1, torch.cuda.current_stream())
+        torch.cuda.synchronize()
+        for _ in range(3):
+            graph.replay()
+        torch.cuda.synchronize()
+        ms = 0.0
+        for _ in range(K):
+            graph.replay()
+            torch.cuda.synchronize()
+            ms += t0.elapsed_time(t1)
+        cbr.stream_status()
+        ms /= K
+        t_s = ms * 1e-3
+        res[name] = {"us": round(ms * 1e3, 2), "images_per_s": spec.n / t_s, "tflops": p.flops / t_s / 1e12,
+                     "gbs": p.bytes / t_s / 1e9, "roof_us": round(roof_us, 2), "bound": bound,
+                     "frac": round(roof_us / (ms * 1e3), 4), "launches_per_call": 1}
+    res["note"] = ("folded: cbr_forward_infer after one untimed cbr_fold_bn; bn_epilogue: cbr_forward_infer_bn; "
+                   "L2 flushed before each call")
+    return res
 
 
 def run_cbr(args, world, rank, local):

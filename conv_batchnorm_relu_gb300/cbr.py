@@ -64,6 +64,7 @@ def load(path: str | None = None) -> ctypes.CDLL:
                                          vp, sz, vp]
             lib.cbr_fold_bn.argtypes = [D, vp, vp, vp, vp, vp, vp, fp, vp, vp, vp]
             lib.cbr_forward_infer.argtypes = [D, vp, vp, vp, vp, vp]
+            lib.cbr_forward_infer_bn.argtypes = [D, vp, vp, vp, vp, vp, vp, vp, fp, vp, vp]
             lib.cbr_stream_status.argtypes = [vp]
             lib.cbr_forward_train_stats.argtypes = [D, vp, vp, vp, vp, vp, sz, vp]
             lib.cbr_forward_train_finish.argtypes = [D, vp, i32, vp, vp, vp, vp, fp, fp, vp, vp, vp, vp, vp,
@@ -77,7 +78,7 @@ def load(path: str | None = None) -> ctypes.CDLL:
             lib.cbr_profile_next_call.argtypes = [ctypes.POINTER(vp), i32]
             lib.cbr_profile_last_count.restype = i32
             for f in ("cbr_workspace_size", "cbr_forward_train", "cbr_backward", "cbr_fold_bn",
-                      "cbr_forward_infer", "cbr_stream_status", "cbr_profile_next_call",
+                      "cbr_forward_infer", "cbr_forward_infer_bn", "cbr_stream_status", "cbr_profile_next_call",
                       "cbr_selftest_bounded_wait", "cbr_mask_bits_to_bytes", "cbr_mask_bytes_to_bits",
                       "cbr_forward_train_stats", "cbr_forward_train_finish", "cbr_backward_sums",
                       "cbr_backward_finish"):
@@ -352,6 +353,18 @@ def mask_bytes_to_bits(mask_bytes: torch.Tensor, count: int, out: torch.Tensor |
     out = out if out is not None else torch.empty((count + 31) // 32, dtype=torch.int32, device=mask_bytes.device)
     _check(load().cbr_mask_bytes_to_bits(_ptr(mask_bytes), _ptr(out), int(count), _stream()), "cbr_mask_bytes_to_bits")
     return out
+
+
+def forward_infer_bn(layer: Layer, x, w, gamma, beta, running_mean, running_var, eps=1e-5, conv_bias=None,
+                     out=None):
+    """cbr_forward_infer_bn: relu(conv(x, w)*scale + shift) with BatchNorm on the accumulator."""
+    y = out if out is not None else torch.empty((layer.n, layer.p, layer.q, layer.c_out),
+                                                dtype=layer.dtype, device=x.device)
+    d = layer.desc()
+    _check(load().cbr_forward_infer_bn(ctypes.byref(d), _ptr(x), _ptr(w), _ptr(conv_bias), _ptr(gamma),
+                                       _ptr(beta), _ptr(running_mean), _ptr(running_var), float(eps), _ptr(y),
+                                       _stream()), "cbr_forward_infer_bn")
+    return y
 
 
 def stream_status(stream: int | None = None) -> None:

@@ -776,6 +776,42 @@ cbr_status_t cbr_mask_bytes_to_bits(const uint8_t* bytes, uint32_t* bits, int64_
                                                  reinterpret_cast<cudaStream_t>(stream));
 }
 
+cbr_status_t cbr_forward_infer_bn(const cbr_desc_t* desc, const void* x, const void* w,
+                                  const float* conv_bias, const float* gamma, const float* beta,
+                                  const float* running_mean, const float* running_var, float eps,
+                                  void* y, cbr_stream_t stream) {
+  Shape s;
+  int st = check_desc(desc, &s);
+  if (st) return (cbr_status_t)st;
+  if (!x || !w || !gamma || !beta || !running_mean || !running_var || !y) return CBR_ERR_INVALID_ARG;
+  if (!(eps > 0.f) || !std::isfinite(eps)) return CBR_ERR_INVALID_ARG;
+  if (!aligned(x, 16) || !aligned(w, 16) || !aligned(y, 16) || !aligned(gamma, 4) || !aligned(beta, 4) ||
+      !aligned(running_mean, 4) || !aligned(running_var, 4) || (conv_bias && !aligned(conv_bias, 4)))
+    return CBR_ERR_MISALIGNED;
+  if ((st = check_supported(s))) return (cbr_status_t)st;
+  // the 3-channel first layer has its own kernels, which take the folded form only
+  if (is_first_layer(s)) return CBR_ERR_UNSUPPORTED;
+  DeviceInfo* dev = nullptr;
+  if ((st = current_device(&dev))) return (cbr_status_t)st;
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  Prof prof(cs);
+  FpropArgs a{};
+  a.g = make_geom(s);
+  a.z = y;
+  a.eps = eps;
+  a.bn_gamma = gamma;
+  a.bn_beta = beta;
+  a.bn_mean = running_mean;
+  a.bn_var = running_var;
+  a.conv_bias = conv_bias;
+  a.m_count = s.m;
+  a.err = dev->err;
+  st = launch_fprop_bn(a, (int)s.cin, (int)s.cout, s.bf16, x, w, dev->num_sms, cs);
+  if (st) return (cbr_status_t)st;
+  prof.mark();
+  return CBR_OK;
+}
+
 cbr_status_t cbr_stream_status(cbr_stream_t stream) {
   DeviceInfo* dev = nullptr;
   int st = current_device(&dev);

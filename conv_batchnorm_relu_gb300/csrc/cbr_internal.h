@@ -57,6 +57,12 @@ struct FpropArgs {
   // call's rows here, [mean cout][M2 cout][row count], instead of finalizing
   float* moments;
   const float* bias;        // inference: per-channel bias added before ReLU
+  // epilogue-only inference (launch_fprop_bn): BatchNorm parameters, conv bias (may be null)
+  const float* bn_gamma;
+  const float* bn_beta;
+  const float* bn_mean;
+  const float* bn_var;
+  const float* conv_bias;
   float momentum;
   float eps;
   long long m_count;        // n*p*q
@@ -110,6 +116,10 @@ size_t first_wgrad_partial_floats(int num_sms, int c_out);
 int launch_fprop(const FpropArgs& a, int c_in, int c_out, bool bf16, const void* x,
                  const void* w, int num_sms, cudaStream_t st);
 size_t fprop_partial_floats(int num_sms, int c_out);
+// Inference forward with BatchNorm applied to the fp32 accumulator: relu(conv(x, W)*scale +
+// shift), stride-1 layers (conv_infer_bn.cu).
+int launch_fprop_bn(const FpropArgs& a, int c_in, int c_out, bool bf16, const void* x, const void* w,
+                    int num_sms, cudaStream_t st);
 
 struct ApplyArgs {
   const void* z;

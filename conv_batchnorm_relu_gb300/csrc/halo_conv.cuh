@@ -23,8 +23,12 @@
 namespace cbr {
 
 // Fprop: A = input halo by TMA.  DgradTma: A = a materialised dz halo by TMA, the filter read
-// MN-major with flipped taps, plain epilogue.
-enum ConvKind : int { kKindFprop = 0, kKindDgradTma = 2 };
+// MN-major with flipped taps, plain epilogue.  FpropBn: the forward convolution whose epilogue
+// applies inference BatchNorm and ReLU to the fp32 accumulator, relu(acc*scale + shift), with
+// the per-channel scale and shift computed by each CTA into shared memory at its start.
+enum ConvKind : int { kKindFprop = 0, kKindDgradTma = 2, kKindFpropBn = 3 };
+
+__host__ __device__ constexpr bool is_forward_kind(int kind) { return kind == kKindFprop || kind == kKindFpropBn; }
 
 struct ConvArgs {
   HaloGeom g;
@@ -43,6 +47,13 @@ struct ConvArgs {
   float* eq;
   float* moments;           // split forward: merged moments out instead of the finalize
   const float* bias;
+  // epilogue-only inference (kKindFpropBn): scale = gamma/sqrt(rv + eps),
+  // shift = beta + (conv_bias - rm)*scale (conv_bias may be null)
+  const float* bn_gamma;
+  const float* bn_beta;
+  const float* bn_mean;
+  const float* bn_var;
+  const float* conv_bias;
   float momentum;
   float eps;
   long long m_count;
@@ -74,11 +85,11 @@ struct Roles {
 
 // Bytes of one filter slab (one 64-channel K chunk x one tap).
 __host__ __device__ constexpr int wslab_bytes(int kind, int nout) {
-  return kind == kKindFprop ? nout * 128 : (nout > 64 ? nout : 64) * 128;
+  return is_forward_kind(kind) ? nout * 128 : (nout > 64 ? nout : 64) * 128;
 }
 
 struct Layout {
-  uint32_t halo_stride, off_w, off_stage, off_bar, total, wslab;
+  uint32_t halo_stride, off_w, off_stage, off_bar, total, wslab, off_bn;
   int nsw;
 };
 
@@ -98,6 +109,11 @@ __host__ __device__ inline Layout layout(const HaloGeom& g, int kind, int nch, i
   L.off_bar = ((alias ? L.off_w + (uint32_t)L.nsw * L.wslab : L.off_stage + stage) + 15u) & ~15u;
   const uint32_t nbar = 8 + 2 * L.nsw + 1;
   L.total = L.off_bar + nbar * 8 + 16;
+  if (kind == kKindFpropBn) {
+    // the per-channel inference scale and shift
+    L.off_bn = (L.total + 15u) & ~15u;
+    L.total = L.off_bn + 2u * (uint32_t)nout * 4u;
+  }
   return L;
 }
 
@@ -275,6 +291,17 @@ __global__ void __launch_bounds__(Roles<KIND>::kThreads, 1)
     *abort_flag = 0;
     fence_mbarrier_init();
   }
+  if constexpr (KIND == kKindFpropBn) {
+    // inference BatchNorm folded into the epilogue: one thread per output channel
+    float* st = reinterpret_cast<float*>(smem + L.off_bn);
+    for (int c = threadIdx.x; c < NOUT; c += kThreads) {
+      const bool ok = c < a.out_c;
+      const float sc = ok ? a.bn_gamma[c] * rsqrtf(a.bn_var[c] + a.eps) : 0.f;
+      const float b = ok && a.conv_bias ? a.conv_bias[c] : 0.f;
+      st[c] = sc;
+      st[NOUT + c] = ok ? fmaf(b - a.bn_mean[c], sc, a.bn_beta[c]) : 0.f;
+    }
+  }
   if (warp == R::kMmaWarp) {
     tmem_alloc(smem_u32(tmem_slot), kTmemCols);
     tmem_relinquish();
@@ -317,7 +344,7 @@ __global__ void __launch_bounds__(Roles<KIND>::kThreads, 1)
       prefetch_tensormap(&map_w);
       auto load_slab = [&](uint32_t dst, int ch, int tap, uint32_t bar) {
         mbar_arrive_expect_tx(bar, L.wslab);
-        if constexpr (KIND == kKindFprop) {
+        if constexpr (is_forward_kind(KIND)) {
           tma_load_3d(dst, &map_w, ch * 64, tap, 0, bar);
         } else {
           const int ftap = rs - 1 - tap;  // (R-1-r, S-1-s)
@@ -358,7 +385,7 @@ __global__ void __launch_bounds__(Roles<KIND>::kThreads, 1)
     // sequence is also kept free of runtime conditions: a guard beside each MMA halves the
     // rate.
     {
-      constexpr bool kBMn = KIND != kKindFprop;
+      constexpr bool kBMn = !is_forward_kind(KIND);
       const uint32_t idesc = make_idesc_f16(128, NOUT, BF16, false, kBMn);
       const uint64_t b_base = kBMn ? make_sw128_desc(w_addr, 8192, 1024, 0) : make_sw128_desc(w_addr, 16, 1024, 0);
       const uint64_t a_row_skip = (uint64_t)((g.wp - g.s) * 128 / 16);  // end of a filter row
@@ -488,6 +515,7 @@ __global__ void __launch_bounds__(Roles<KIND>::kThreads, 1)
     float sn = 0.f;  // rows merged into s1 / s2 (the mean and M2 of channel lane >> kSh)
     const bool stats = KIND == kKindFprop && a.mode == kFpropStats;
     const bool bias_relu = KIND == kKindFprop && a.mode == kFpropBiasRelu;
+    const float* bn_st = reinterpret_cast<const float*>(smem + L.off_bn);  // kKindFpropBn: [scale][shift]
     const int out_c = a.out_c;
     const size_t opitch = (size_t)out_c * 2;
     // 32-byte stores when every 16-channel group of a row is whole and aligned
@@ -534,6 +562,7 @@ __global__ void __launch_bounds__(Roles<KIND>::kThreads, 1)
             for (int i = 0; i < kSB; ++i) {
               float x = __uint_as_float(r[i]);
               if (bias_relu) x = fmaxf(x + __ldg(a.bias + c0 + i), 0.f);
+              if constexpr (KIND == kKindFpropBn) x = fmaxf(fmaf(x, bn_st[c0 + i], bn_st[NOUT + c0 + i]), 0.f);
               v[i] = valid ? x : 0.f;
             }
             if (valid) {

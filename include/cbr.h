@@ -216,6 +216,21 @@ cbr_status_t cbr_forward_infer(const cbr_desc_t* desc, const void* x, const void
                                const float* b_fold, void* y, cbr_stream_t stream);
 
 /*
+ * Inference with BatchNorm applied to the convolution's fp32 accumulator, the CBR page's
+ * single-graph form (section 6: conv, MUL by eq_scale, ADD eq_bias, ReLU):
+ *   y = relu(conv(x, w)*scale + shift),  scale = gamma/sqrt(running_var + eps),
+ *   shift = beta + (conv_bias - running_mean)*scale          (conv_bias may be NULL: 0)
+ * Unlike cbr_fold_bn + cbr_forward_infer, the filter is used as trained, so nothing is rounded
+ * to the storage dtype before the convolution.  Stride-1 layers only: the 3-channel first layer
+ * returns UNSUPPORTED (fold it instead).  Errors: INVALID_ARG (NULL, eps <= 0), MISALIGNED,
+ * UNSUPPORTED, DEVICE, CUDA.
+ */
+cbr_status_t cbr_forward_infer_bn(const cbr_desc_t* desc, const void* x, const void* w,
+                                  const float* conv_bias, const float* gamma, const float* beta,
+                                  const float* running_mean, const float* running_var, float eps,
+                                  void* y, cbr_stream_t stream);
+
+/*
  * Training forward that allocates nothing and takes no workspace.  The pages have no
  * counterpart; this exists for callers that must not allocate device memory on their
  * execution path, such as plug-ins that run inside another framework's execution loop with

@@ -154,3 +154,28 @@ def test_statistics_at_extreme_mean_to_std_ratio(case):
     rel_close(to_np(out["saved_inv_var"]), inv, "saved_inv_var")
     stat_close(to_np(g["running_mean"]), rm, spec.momentum * sd, "running_mean")
     rel_close(to_np(g["running_var"]), rv, "running_var")
+
+
+@pytest.mark.parametrize("case,with_bias", [("cfg1", False), ("ragged_13x29", True), ("k1x1", False),
+                                            ("c128_bf16", True), ("c128_f16_odd", False), ("cin16_cout32_bf16", True)])
+def test_infer_bn_epilogue_parity(case, with_bias):
+    """cbr_forward_infer_bn: BatchNorm with running statistics applied to the fp32 accumulator of
+    conv(x, W) with the unfolded filter, against the oracle's conv -> BN(running) -> ReLU."""
+    spec, seed = CASES[case]
+    inp = make_inputs(spec, seed, with_dy=False)
+    gen = torch.Generator().manual_seed(seed + 11)
+    rm = torch.randn(spec.c_out, generator=gen) * 0.2
+    rv = torch.rand(spec.c_out, generator=gen) + 0.5
+    bias = torch.randn(spec.c_out, generator=gen) * 0.3 if with_bias else None
+    layer = cbr.Layer.from_spec(spec)
+    g = {k: v.cuda() for k, v in inp.items()}
+    y = cbr.forward_infer_bn(layer, g["x"], g["w"], g["gamma"], g["beta"], rm.cuda(), rv.cuda(), spec.eps,
+                             conv_bias=None if bias is None else bias.cuda())
+    cbr.stream_status()
+    o = oracle_inputs(inp)
+    z = oracle.conv2d_fwd(o["x"], o["w"], spec.stride, spec.pad)
+    if bias is not None:
+        z = z + bias.double().numpy()
+    pre = oracle.bn_infer(z.reshape(-1, spec.c_out), rm.double().numpy(), rv.double().numpy(),
+                          o["gamma"], o["beta"], spec.eps)
+    max_err_ok(to_np(y), np.maximum(pre, 0.0).reshape(z.shape), "y_infer_bn")

@@ -16,7 +16,11 @@ from conv_batchnorm_relu_gb300.inputs import CONFIGS
 @pytest.fixture(scope="module")
 def lib():
     build.build()
-    return cbr.load()
+    lib = cbr.load()
+    lib.cbr_forward_infer_bn.argtypes = [ctypes.POINTER(cbr.Desc)] + [ctypes.c_void_p] * 7 + [ctypes.c_float] + \
+        [ctypes.c_void_p] * 2
+    lib.cbr_forward_infer_bn.restype = ctypes.c_int32
+    return lib
 
 
 def _desc(**kw):
@@ -176,3 +180,13 @@ def test_backward_accepts_byte_mask_kind(lib):
     st = lib.cbr_backward(ctypes.byref(d), P, P, P, P, 3, P, P, P, P, P + (1 << 20), P, P, P, P,
                           1 << 40, None)
     assert st == 1
+
+
+def test_infer_bn_validation(lib):
+    d = _desc()
+    f = lib.cbr_forward_infer_bn
+    assert f(ctypes.byref(d), P, P, None, P, P, P, P, 1e-5, None, None) == 1     # no y
+    assert f(ctypes.byref(d), P, P, None, P, P, P, P, 0.0, P, None) == 1         # eps
+    assert f(ctypes.byref(d), P + 2, P, None, P, P, P, P, 1e-5, P, None) == 2    # x misaligned
+    first = _desc(c_in=3, c_out=64, r=7, s=7, stride=2, pad=3, h=32, w=32)
+    assert f(ctypes.byref(first), P, P, None, P, P, P, P, 1e-5, P, None) == 3     # first layer: fold it
