@@ -262,14 +262,18 @@ __global__ void __launch_bounds__(kWgThreads, 1)
   }
 }
 
-// dW = sum over the CTAs of each split of their partials, in a fixed order.  A block owns 64
-// consecutive float4 of the per-CTA partial (the same span in every CTA, so every load is
-// coalesced) and four slices of the split's CTA list: slice sl sums CTAs sl, sl+4, ... in fp32
-// with eight loads in flight, and the four slices are combined in slice order in fp64.  Each
-// partial element is then written to its dW[k][tap][c] position.
-constexpr int kRedThreads = 256;
-constexpr int kRedSpan = 64;                  // float4 per block
-constexpr int kRedSlices = kRedThreads / kRedSpan;
+// dW = sum over the CTAs of each split of their partials, in a fixed order.  A block owns 16
+// consecutive float4 of the per-CTA partial (the same span in every CTA, so the loads are
+// coalesced) and 32 slices of the split's CTA list: slice sl sums CTAs sl, sl+32, ... in fp32
+// with all of its (at most 8) loads in flight, and the slices are combined by a fixed pairwise
+// tree in shared memory.  Each summed element is then written to its dW[k][tap][c] position.
+// (Few CTAs per slice keep the whole 25 MB of partials in flight at once: the partials sit in
+// L2 and the pass is bound by its latency, not by bandwidth.)
+constexpr int kRedSpan = 16;                         // float4 columns per block
+constexpr int kRedSlices = 32;                       // CTA slices per column
+constexpr int kRedThreads = kRedSpan * kRedSlices;   // 512
+constexpr int kRedLd = 8;                            // CTAs per slice in flight (grids up to 256)
+static_assert(kRedSlices * kRedLd >= kMaxCtas, "one round of loads covers every CTA's partial");
 
 template <int NOUT>
 __global__ void __launch_bounds__(kRedThreads)
@@ -280,21 +284,22 @@ __global__ void __launch_bounds__(kRedThreads)
   const size_t per_cta = (size_t)P.gmax * kC16 * 512;  // float4 per CTA partial
   const int blocks_per_split = (int)((per_cta + kRedSpan - 1) / kRedSpan);
   const int split = blockIdx.x / blocks_per_split;
-  const size_t f4 = (size_t)(blockIdx.x % blocks_per_split) * kRedSpan + threadIdx.x % kRedSpan;
+  const int col = threadIdx.x % kRedSpan;
+  const size_t f4 = (size_t)(blockIdx.x % blocks_per_split) * kRedSpan + col;
   const int sl = threadIdx.x / kRedSpan;
   const int nb = (grid - split + P.nsplit - 1) / P.nsplit;  // CTAs of this split
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
   if (f4 < per_cta) {
     const float4* base = reinterpret_cast<const float4*>(part) + f4;
-    for (int t0 = sl; t0 < nb; t0 += 8 * kRedSlices) {
-      float4 v[8];
+    for (int t0 = sl; t0 < nb; t0 += kRedLd * kRedSlices) {
+      float4 v[kRedLd];
 #pragma unroll
-      for (int u = 0; u < 8; ++u) {
+      for (int u = 0; u < kRedLd; ++u) {
         const int t = t0 + u * kRedSlices;
         v[u] = t < nb ? __ldg(base + (size_t)(split + t * P.nsplit) * per_cta) : make_float4(0.f, 0.f, 0.f, 0.f);
       }
 #pragma unroll
-      for (int u = 0; u < 8; ++u) {
+      for (int u = 0; u < kRedLd; ++u) {
         acc.x += v[u].x;
         acc.y += v[u].y;
         acc.z += v[u].z;
@@ -302,17 +307,22 @@ __global__ void __launch_bounds__(kRedThreads)
       }
     }
   }
-  red[sl][threadIdx.x % kRedSpan] = acc;
-  __syncthreads();
-  if (sl != 0 || f4 >= per_cta) return;
-  double t4[4] = {0.0, 0.0, 0.0, 0.0};
-  for (int q = 0; q < kRedSlices; ++q) {
-    const float4 v = red[q][threadIdx.x];
-    t4[0] += v.x;
-    t4[1] += v.y;
-    t4[2] += v.z;
-    t4[3] += v.w;
+  red[sl][col] = acc;
+#pragma unroll
+  for (int w = kRedSlices / 2; w >= 1; w >>= 1) {
+    __syncthreads();
+    if (sl < w) {
+      const float4 b = red[sl + w][col];
+      float4& a = red[sl][col];
+      a.x += b.x;
+      a.y += b.y;
+      a.z += b.z;
+      a.w += b.w;
+    }
   }
+  if (sl != 0 || f4 >= per_cta) return;
+  const float4 v = red[0][col];
+  const float t4[4] = {v.x, v.y, v.z, v.w};
   // f4 -> (group, c16, v, row): see the partial layout in wgrad_kernel
   const int row = (int)(f4 % 128);
   const int vq = (int)((f4 / 128) % 4);
@@ -326,7 +336,7 @@ __global__ void __launch_bounds__(kRedThreads)
   if (c >= cin) return;
   for (int j = 0; j < 4; ++j) {
     const int k = c16 * 16 + vq * 4 + j;
-    dw[((size_t)k * taps + tap) * cin + c] = (float)t4[j];
+    dw[((size_t)k * taps + tap) * cin + c] = t4[j];
   }
 }
 
