@@ -176,13 +176,14 @@ __global__ void __launch_bounds__(kRedThreads)
   __threadfence();
   // One SM runs this after all the others, so it is kept short: every block partial is loaded
   // in one batch (thread t sums float4 column t % nv4 of blocks t / nv4, + rgs, ..., in fp32
-  // and a fixed order), row groups are combined in fixed order in fp64, and the coefficient
-  // math multiplies by the host's 1/M instead of dividing (fp64 division is slow here).
+  // and a fixed order), the row groups are combined by a fixed pairwise tree in fp32 whose steps
+  // run all their (pair, column) additions in parallel over the block (FP64 is slow on this
+  // part), and the coefficient math multiplies by the host's 1/M instead of dividing.
   constexpr int kLd = 16;
   const int nv4 = (2 * c) / 4;                    // float4 columns of one partial (<= 128)
-  const int rgs = min(kRedThreads / nv4, 32);     // row groups (at most the fp64 tree's width)
+  const int rgs = min(kRedThreads / nv4, 32);     // row groups
   float* fred = red;                              // [rgs][2c]
-  double* fin = reinterpret_cast<double*>(red + rgs * 2 * c);  // [2c]
+  float4* fred4 = reinterpret_cast<float4*>(red);
   if (threadIdx.x < rgs * nv4) {
     const int c4 = threadIdx.x % nv4, rg = threadIdx.x / nv4;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -202,19 +203,35 @@ __global__ void __launch_bounds__(kRedThreads)
         acc.w += v[k].w;
       }
     }
-    reinterpret_cast<float4*>(fred + rg * 2 * c)[c4] = acc;
+    fred4[rg * nv4 + c4] = acc;
   }
   __syncthreads();
-  // row groups combined in fp64 by a fixed pairwise tree
-  for (int i = threadIdx.x; i < 2 * c; i += kRedThreads) fin[i] = tree_sum<32>(fred + i, 2 * c, rgs);
-  __syncthreads();
+  // step w = 1, 2, 4, ...: row group r (r % 2w == 0, r + w < rgs) adds in row group r + w
+#pragma unroll 1
+  for (int w = 1; w < rgs; w *= 2) {
+    const int npairs = (rgs - w + 2 * w - 1) / (2 * w);
+#pragma unroll 1
+    for (int i = threadIdx.x; i < npairs * nv4; i += kRedThreads) {
+      const int pi = i / nv4, c4 = i - pi * nv4;
+      float4* pa = fred4 + (pi * 2 * w) * nv4 + c4;
+      const float4 b = pa[w * nv4];
+      float4 v = *pa;
+      v.x += b.x;
+      v.y += b.y;
+      v.z += b.z;
+      v.w += b.w;
+      *pa = v;
+    }
+    __syncthreads();
+  }
+  const float* fin = fred;  // row group 0: [2c]
   if (threadIdx.x < c) {
     const int ch = threadIdx.x;
     if (a.sums_out) {
       // split backward: the raw sums go to the caller, who adds other ranks' before the
       // coefficients are formed
-      a.sums_out[ch] = (float)fin[ch];
-      a.sums_out[c + ch] = (float)fin[c + ch];
+      a.sums_out[ch] = fin[ch];
+      a.sums_out[c + ch] = fin[c + ch];
     } else {
       bwd_coef(fin[ch], fin[c + ch], f_gamma, f_mean, f_inv, a.inv_m, c, ch, a.dgamma, a.dbeta, a.coef);
     }

@@ -20,22 +20,6 @@ enum : uint32_t {
   kErrBadLaunch = 1u << 8,
 };
 
-// Fixed-order fp64 sum of n fp32 values v[0], v[stride], ... (n <= N): all loads first, then a
-// pairwise tree, so the fp64 additions form log2(N) dependent steps instead of n.
-template <int N>
-__device__ __forceinline__ double tree_sum(const float* v, int stride, int n = N) {
-  constexpr int P = N <= 1 ? 1 : N <= 2 ? 2 : N <= 4 ? 4 : N <= 8 ? 8 : N <= 16 ? 16 : 32;
-  static_assert(N <= 32, "tree_sum width");
-  double t[P];
-#pragma unroll
-  for (int r = 0; r < P; ++r) t[r] = r < n && r < N ? (double)v[r * stride] : 0.0;
-#pragma unroll
-  for (int w = P / 2; w >= 1; w /= 2)
-#pragma unroll
-    for (int k = 0; k < w; ++k) t[k] += t[k + w];
-  return t[0];
-}
-
 __device__ __forceinline__ void report_error(uint32_t* err, uint32_t bits) {
   if (err) atomicOr(err, bits);
 }

@@ -165,15 +165,18 @@ __device__ void stats_partial_finalize(const ConvArgs& a, const float* red, uint
     // This runs on one SM after all the others, so it is kept short: thread t merges, for 4
     // channels (column t % kV), the partials of CTAs t / kV, + kRG, ... in order, with the
     // loads of kLd CTAs in flight; the kRG group results are then merged by a fixed pairwise
-    // tree, and the per-channel math multiplies by the host's 1/M (no division by M).
+    // tree whose steps run all their (pair, channel) merges in parallel over the CTA, and the
+    // per-channel math multiplies by the host's 1/M (no division by M).
     constexpr int kV = COUT / 4;               // float4 columns of the means (and of the M2s)
     constexpr int kGF = 2 * COUT + 4;          // floats per group result: means, M2s, count
-    constexpr int kRGfit = SCRATCH / (kGF * 4);
+    constexpr int kCntF = 6 * 32;              // group counts, one row per tree step
+    constexpr int kRGfit = (SCRATCH - kCntF * 4) / (kGF * 4);
     constexpr int kRG1 = kThreads / kV < kRGfit ? kThreads / kV : kRGfit;
     constexpr int kRG = kRG1 < 32 ? kRG1 : 32;
     static_assert(kRG >= 1, "finalize scratch");
     constexpr int kLd = 8;                     // CTAs whose loads are in flight per thread
     float* fg = reinterpret_cast<float*>(scratch);  // [kRG][kGF]
+    float* cnt = fg + kRG * kGF;                    // [step][kRG]
     const int c4 = threadIdx.x % kV, rg = threadIdx.x / kV;
     if (rg < kRG) {
       float n = 0.f;
@@ -203,35 +206,48 @@ __device__ void stats_partial_finalize(const ConvArgs& a, const float* red, uint
       float* gr = fg + rg * kGF;
       reinterpret_cast<float4*>(gr)[c4] = make_float4(m[0], m[1], m[2], m[3]);
       reinterpret_cast<float4*>(gr + COUT)[c4] = make_float4(q[0], q[1], q[2], q[3]);
-      if (c4 == 0) gr[2 * COUT] = n;
+      if (c4 == 0) cnt[rg] = n;
     }
     __syncthreads();
+    // step s (w = 2^s): group r (r % 2w == 0, r + w < kRG) takes in group r + w (r first).
+    // The right member is not written during its step, and each (pair, channel) item is read
+    // and written by one thread; the merged counts go to the next step's row.
+    int step = 0;
+#pragma unroll 1
+    for (int w = 1; w < kRG; w *= 2, ++step) {
+      const float* cs = cnt + step * kRG;
+      const int npairs = (kRG - w + 2 * w - 1) / (2 * w);
+#pragma unroll 1
+      for (int i = threadIdx.x; i < npairs * COUT; i += kThreads) {
+        const int pi = i / COUT, ch = i - pi * COUT;
+        const int r = pi * 2 * w;
+        float* ga = fg + r * kGF;
+        const float* gb = ga + w * kGF;
+        float ma = ga[ch], qa = ga[COUT + ch];
+        st::chan_merge_w(ma, qa, gb[ch], gb[COUT + ch], st::chan_weights(cs[r], cs[r + w]));
+        ga[ch] = ma;
+        ga[COUT + ch] = qa;
+      }
+      if (threadIdx.x < kRG) {
+        const int r = threadIdx.x;
+        cnt[(step + 1) * kRG + r] = (r % (2 * w) == 0 && r + w < kRG) ? cs[r] + cs[r + w] : cs[r];
+      }
+      __syncthreads();
+    }
     if (threadIdx.x < COUT) {
       const int c = threadIdx.x;
-      // groups merged by a fixed pairwise tree (log2(kRG) dependent steps)
-      constexpr int P = kRG <= 1 ? 1 : kRG <= 2 ? 2 : kRG <= 4 ? 4 : kRG <= 8 ? 8 : kRG <= 16 ? 16 : 32;
-      float tn[P], tm[P], tq[P];
-#pragma unroll
-      for (int r = 0; r < P; ++r) {
-        const bool ok = r < kRG;
-        tn[r] = ok ? fg[r * kGF + 2 * COUT] : 0.f;
-        tm[r] = ok ? fg[r * kGF + c] : 0.f;
-        tq[r] = ok ? fg[r * kGF + COUT + c] : 0.f;
-      }
-#pragma unroll
-      for (int w = P / 2; w >= 1; w /= 2)
-#pragma unroll
-        for (int k = 0; k < w; ++k) st::chan_merge(tn[k], tm[k], tq[k], tn[k + w], tm[k + w], tq[k + w]);
+      const float tot_n = cnt[step * kRG];
+      const float tot_m = fg[c], tot_q = fg[COUT + c];
       if (a.moments) {
         // split forward: this call's moments go to the caller, who merges them with other
         // ranks' and finalizes later
-        a.moments[c] = tm[0];
-        a.moments[COUT + c] = tq[0];
-        if (c == 0) a.moments[2 * COUT] = tn[0];
+        a.moments[c] = tot_m;
+        a.moments[COUT + c] = tot_q;
+        if (c == 0) a.moments[2 * COUT] = tot_n;
         return;
       }
-      const float meanf = tm[0];
-      const float var = fmaxf(tq[0] * (float)a.inv_m, 0.f);  // biased: M2 / M
+      const float meanf = tot_m;
+      const float var = fmaxf(tot_q * (float)a.inv_m, 0.f);  // biased: M2 / M
       const float inv = rsqrtf(var + a.eps);
       a.saved_mean[c] = meanf;
       a.saved_inv_var[c] = inv;
