@@ -451,7 +451,10 @@ __global__ void __launch_bounds__(Roles<KIND>::kThreads, 1)
             constexpr int NT = decltype(nt_c)::value, RS = decltype(rs_c)::value;
             uint64_t a_tap = make_sw128_desc(hbase + (uint32_t)off * 128u, 16, 1024, 0);
             int sx = 0;
-#pragma unroll
+            // With several input-channel chunks the fully unrolled issue code no longer stays in
+            // the instruction cache; the forward then issues one tap per loop iteration (7-8%
+            // faster there, and slightly slower for a single chunk or the data gradient).
+#pragma unroll(is_forward_kind(KIND) && NCH > 1 ? 1 : 9)
             for (int tap = 0; tap < (RS ? RS : rs); ++tap) {
               uint32_t wslab_off, ws = 0;
               if (WRES) {
