@@ -62,6 +62,9 @@ def parse():
     ap.add_argument("--copy-chunks", type=int, default=1,
                     help="e2e: host-to-device copies per input tensor and step, each on its own stream")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--persistent-forward", action="store_true",
+                    help="time cbr_forward_train_persistent (one cooperative launch for the forward) "
+                         "instead of cbr_forward_train")
     ap.add_argument("--recompute-z", action="store_true",
                     help="do not keep z: the forward passes z_saved = NULL and the backward recomputes it")
     return ap.parse_args()
@@ -333,7 +336,7 @@ def run_cbr(args, world, rank, local):
             cbr.profile_next_call(fev)
         cbr.forward_train(layer, x, g["w"], g["gamma"], g["beta"], g["running_mean"],
                           g["running_var"], spec.momentum, spec.eps, ws=ws_f, out=fo,
-                          save_z=not args.recompute_z)
+                          save_z=not args.recompute_z, persistent=args.persistent_forward)
         if bev:
             cbr.profile_next_call(bev)
         cbr.backward(layer, dy, x, g["w"], fo["mask"], cbr.CBR_MASK_BITS, fo.get("z"), g["gamma"],
@@ -348,7 +351,19 @@ def run_cbr(args, world, rank, local):
         flush.zero_()
         step(g["x"], g["dy"])
     cbr.stream_status()
-    # which backward kernels run (the library records one event per launched kernel)
+    # which kernels run (the library records one event per launched kernel): the forward is
+    # one persistent kernel (--persistent-forward), else conv + apply
+    probe_f = [mk() for _ in range(nf)]
+    for e in probe_f:
+        e.record(stream)
+    cbr.profile_next_call(probe_f)
+    cbr.forward_train(layer, g["x"], g["w"], g["gamma"], g["beta"], g["running_mean"], g["running_var"],
+                      spec.momentum, spec.eps, ws=ws_f, out=fo, save_z=not args.recompute_z,
+                      persistent=args.persistent_forward)
+    used_f = cbr.profile_last_count() - 1
+    fwd_names = ["conv_fprop_apply"] if used_f == 1 else FWD_KERNELS
+    if len(fwd_names) != used_f:
+        raise RuntimeError(f"forward launched {used_f} kernels, expected {fwd_names}")
     probe = [mk() for _ in range(nb)]
     for e in probe:
         e.record(stream)
@@ -370,9 +385,9 @@ def run_cbr(args, world, rank, local):
     # graph of the same step with the library's profiling events at every kernel boundary,
     # replayed separately. Each replay is synchronised before the next so its events are read
     # before they are recorded again.
-    kern_names = FWD_KERNELS + bwd_names
+    kern_names = fwd_names + bwd_names
     t_start, t_end = mk(), mk()
-    fev_g = [mk() for _ in range(nf)]
+    fev_g = [mk() for _ in range(used_f + 1)]
     bev_g = [mk() for _ in range(used_b + 1)]
     for e in [t_start, t_end] + fev_g + bev_g:
         e.record(stream)  # materialise the CUDA event handles
@@ -442,10 +457,10 @@ def run_cbr(args, world, rank, local):
         graph_p.replay()
         torch.cuda.synchronize()
         prof_ms += fev_g[0].elapsed_time(bev_g[-1])
-        for j in range(len(FWD_KERNELS)):
+        for j in range(len(fwd_names)):
             kern_sum[j] += fev_g[j].elapsed_time(fev_g[j + 1])
         for j in range(len(bwd_names)):
-            kern_sum[len(FWD_KERNELS) + j] += bev_g[j].elapsed_time(bev_g[j + 1])
+            kern_sum[len(fwd_names) + j] += bev_g[j].elapsed_time(bev_g[j + 1])
     torch.cuda.synchronize()
     cbr.stream_status()
     barrier(world)
@@ -523,7 +538,7 @@ def run_cbr(args, world, rank, local):
     peaks, peak_src = roofline.load_peaks()
     # per-kernel roofs of the implemented step, against the burst peaks (a step lasts well under a
     # millisecond); the sustained-GEMM fraction is given beside for tensor-bound kernels
-    kpass = {p.name: p for p in roofline.kernel_passes(spec, need_dx, fused)}
+    kpass = {p.name: p for p in roofline.kernel_passes(spec, need_dx, fused, persist=len(fwd_names) == 1)}
     passes = {}
     for nm, p in kpass.items():
         roof_us, bound = p.roof_us(peaks)
@@ -559,6 +574,8 @@ def run_cbr(args, world, rank, local):
                               "timed by two event nodes around the step; per-kernel times ('passes') from "
                               "separate replays with an event node at every kernel boundary",
                        profiled_step_ms=round(prof_ms, 4),
+                       forward=("persistent conv + statistics + finalize + apply (one cooperative launch)"
+                                if len(fwd_names) == 1 else "conv + statistics, then apply"),
                        backward="fused dgrad+wgrad (dz on chip)" if fused else "materialised dz",
                        **({"ms_per_step_unflushed": round(unflushed_ms, 4)} if unflushed_ms is not None else {})),
         "tflops": conv_flops * world / (ms * 1e-3) / 1e12,

@@ -60,6 +60,7 @@ def load(path: str | None = None) -> ctypes.CDLL:
             lib.cbr_workspace_size.argtypes = [D, ctypes.POINTER(sz), ctypes.POINTER(sz)]
             lib.cbr_forward_train.argtypes = [D, vp, vp, vp, vp, vp, vp, fp, fp, vp, vp, vp, vp,
                                               vp, vp, sz, vp]
+            lib.cbr_forward_train_persistent.argtypes = lib.cbr_forward_train.argtypes
             lib.cbr_backward.argtypes = [D, vp, vp, vp, vp, i32, vp, vp, vp, vp, vp, vp, vp, vp,
                                          vp, sz, vp]
             lib.cbr_fold_bn.argtypes = [D, vp, vp, vp, vp, vp, vp, fp, vp, vp, vp]
@@ -77,7 +78,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
             lib.cbr_selftest_bounded_wait.argtypes = [i32, vp]
             lib.cbr_profile_next_call.argtypes = [ctypes.POINTER(vp), i32]
             lib.cbr_profile_last_count.restype = i32
-            for f in ("cbr_workspace_size", "cbr_forward_train", "cbr_backward", "cbr_fold_bn",
+            for f in ("cbr_workspace_size", "cbr_forward_train", "cbr_forward_train_persistent", "cbr_backward",
+                      "cbr_fold_bn",
                       "cbr_forward_infer", "cbr_forward_infer_bn", "cbr_stream_status", "cbr_profile_next_call",
                       "cbr_selftest_bounded_wait", "cbr_mask_bits_to_bytes", "cbr_mask_bytes_to_bits",
                       "cbr_forward_train_stats", "cbr_forward_train_finish", "cbr_backward_sums",
@@ -157,8 +159,9 @@ def mask_words(layer: Layer) -> int:
 
 
 def forward_train(layer: Layer, x, w, gamma, beta, running_mean, running_var, momentum=0.1,
-                  eps=1e-5, *, ws, want_mask=True, save_z=True, out=None) -> dict:
-    """cbr_forward_train.  running_mean / running_var are updated in place."""
+                  eps=1e-5, *, ws, want_mask=True, save_z=True, out=None, persistent=False) -> dict:
+    """cbr_forward_train (persistent: cbr_forward_train_persistent, the one-launch form).
+    running_mean / running_var are updated in place."""
     dev = x.device
     o = dict(out or {})
     if "y" not in o:
@@ -171,12 +174,13 @@ def forward_train(layer: Layer, x, w, gamma, beta, running_mean, running_var, mo
         if k not in o:
             o[k] = torch.empty(layer.c_out, dtype=torch.float32, device=dev)
     d = layer.desc()
-    st = load().cbr_forward_train(
+    name = "cbr_forward_train_persistent" if persistent else "cbr_forward_train"
+    st = getattr(load(), name)(
         ctypes.byref(d), _ptr(x), _ptr(w), _ptr(gamma), _ptr(beta), _ptr(running_mean),
         _ptr(running_var), float(momentum), float(eps), _ptr(o["y"]), _ptr(o.get("mask")),
         _ptr(o.get("z")), _ptr(o["saved_mean"]), _ptr(o["saved_inv_var"]), _ptr(ws),
         ws.numel(), _stream())
-    _check(st, "cbr_forward_train")
+    _check(st, name)
     return o
 
 

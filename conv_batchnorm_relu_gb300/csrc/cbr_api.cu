@@ -19,6 +19,9 @@ __device__ uint32_t g_error_word;
 namespace {
 
 constexpr size_t kHdrBytes = kWsHeaderBytes;  // arrival counters live here
+// header words: 0 the forward's finalize ticket, 1 the backward's, kReadyWord the persistent
+// forward's ready word
+constexpr int kReadyWord = 8;
 constexpr int kMaxDevices = 64;
 
 size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
@@ -344,12 +347,18 @@ cbr_status_t cbr_workspace_size(const cbr_desc_t* desc, size_t* fwd_bytes, size_
   return CBR_OK;
 }
 
-cbr_status_t cbr_forward_train(const cbr_desc_t* desc, const void* x, const void* w,
-                               const float* gamma, const float* beta, float* running_mean,
-                               float* running_var, float momentum, float eps, void* y,
-                               uint32_t* relu_mask, void* z_saved, float* saved_mean,
-                               float* saved_inv_var, void* ws, size_t ws_bytes,
-                               cbr_stream_t stream) {
+}  // extern "C"
+
+namespace {
+
+// The training forward; persistent: the one-launch form (conv, statistics, finalize and apply in
+// one cooperative kernel), or CBR_ERR_UNSUPPORTED where the batch's accumulators do not all fit
+// in TMEM at once.
+cbr_status_t forward_train_impl(bool persistent, const cbr_desc_t* desc, const void* x, const void* w,
+                                const float* gamma, const float* beta, float* running_mean, float* running_var,
+                                float momentum, float eps, void* y, uint32_t* relu_mask, void* z_saved,
+                                float* saved_mean, float* saved_inv_var, void* ws, size_t ws_bytes,
+                                cbr_stream_t stream) {
   size_t need = 0;
   int st = check_forward_train(desc, x, w, gamma, beta, running_mean, running_var, momentum, eps, y,
                                relu_mask, z_saved, saved_mean, saved_inv_var, &need);
@@ -385,6 +394,16 @@ cbr_status_t cbr_forward_train(const cbr_desc_t* desc, const void* x, const void
   a.m_count = s.m;
   a.err = dev->err;
   a.mode = kFpropStats;
+  if (persistent) {
+    if (is_first_layer(s) || s.stride != 1 || !aligned(y, 32) ||
+        !fprop_apply_supported(a.g, (int)s.cin, (int)s.cout, dev->num_sms))
+      return CBR_ERR_UNSUPPORTED;
+    st = launch_fprop_apply(a, y, relu_mask, reinterpret_cast<uint32_t*>(wsb) + kReadyWord, (int)s.cin,
+                            (int)s.cout, s.bf16, x, w, dev->num_sms, cs);
+    if (st) return (cbr_status_t)st;
+    prof.mark();
+    return CBR_OK;
+  }
   st = run_fprop(a, s, x, w, dev->num_sms, cs);
   if (st) return (cbr_status_t)st;
   prof.mark();
@@ -400,6 +419,30 @@ cbr_status_t cbr_forward_train(const cbr_desc_t* desc, const void* x, const void
   if (st) return (cbr_status_t)st;
   prof.mark();
   return CBR_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+cbr_status_t cbr_forward_train(const cbr_desc_t* desc, const void* x, const void* w,
+                               const float* gamma, const float* beta, float* running_mean,
+                               float* running_var, float momentum, float eps, void* y,
+                               uint32_t* relu_mask, void* z_saved, float* saved_mean,
+                               float* saved_inv_var, void* ws, size_t ws_bytes,
+                               cbr_stream_t stream) {
+  return forward_train_impl(false, desc, x, w, gamma, beta, running_mean, running_var, momentum, eps, y, relu_mask,
+                            z_saved, saved_mean, saved_inv_var, ws, ws_bytes, stream);
+}
+
+cbr_status_t cbr_forward_train_persistent(const cbr_desc_t* desc, const void* x, const void* w,
+                                          const float* gamma, const float* beta, float* running_mean,
+                                          float* running_var, float momentum, float eps, void* y,
+                                          uint32_t* relu_mask, void* z_saved, float* saved_mean,
+                                          float* saved_inv_var, void* ws, size_t ws_bytes,
+                                          cbr_stream_t stream) {
+  return forward_train_impl(true, desc, x, w, gamma, beta, running_mean, running_var, momentum, eps, y, relu_mask,
+                            z_saved, saved_mean, saved_inv_var, ws, ws_bytes, stream);
 }
 
 cbr_status_t cbr_forward_train_stats(const cbr_desc_t* desc, const void* x, const void* w, void* z,

@@ -115,6 +115,11 @@ int launch_first_wgrad(const HaloGeom& hg, int stride, int c_out, bool bf16, con
 size_t first_wgrad_partial_floats(int num_sms, int c_out);
 int launch_fprop(const FpropArgs& a, int c_in, int c_out, bool bf16, const void* x,
                  const void* w, int num_sms, cudaStream_t st);
+// The persistent training forward (conv_fprop.cu): z, statistics, finalize, y and the mask in
+// one cooperative launch; `ready` is a workspace word the kernel increments once per call.
+bool fprop_apply_supported(const HaloGeom& g, int c_in, int c_out, int num_sms);
+int launch_fprop_apply(const FpropArgs& f, void* y, uint32_t* mask, uint32_t* ready, int c_in, int c_out, bool bf16,
+                       const void* x, const void* w, int num_sms, cudaStream_t st);
 size_t fprop_partial_floats(int num_sms, int c_out);
 // Inference forward with BatchNorm applied to the fp32 accumulator: relu(conv(x, W)*scale +
 // shift), stride-1 layers (conv_infer_bn.cu).

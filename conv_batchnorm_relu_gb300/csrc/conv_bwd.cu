@@ -264,15 +264,15 @@ __global__ void __launch_bounds__(kWgThreads, 1)
 
 // dW = sum over the CTAs of each split of their partials, in a fixed order.  A block owns 16
 // consecutive float4 of the per-CTA partial (the same span in every CTA, so the loads are
-// coalesced) and 32 slices of the split's CTA list: slice sl sums CTAs sl, sl+32, ... in fp32
-// with all of its (at most 8) loads in flight, and the slices are combined by a fixed pairwise
+// coalesced) and 16 slices of the split's CTA list: slice sl sums CTAs sl, sl+16, ... in fp32
+// with all of its (at most 16) loads in flight, and the slices are combined by a fixed pairwise
 // tree in shared memory.  Each summed element is then written to its dW[k][tap][c] position.
-// (Few CTAs per slice keep the whole 25 MB of partials in flight at once: the partials sit in
-// L2 and the pass is bound by its latency, not by bandwidth.)
+// 256-thread blocks keep the grid within one wave of resident blocks at 128 channels (a
+// 512-thread shape ran a tail wave: 20.5 against 16.4 us there, the same at 64 channels).
 constexpr int kRedSpan = 16;                         // float4 columns per block
-constexpr int kRedSlices = 32;                       // CTA slices per column
-constexpr int kRedThreads = kRedSpan * kRedSlices;   // 512
-constexpr int kRedLd = 8;                            // CTAs per slice in flight (grids up to 256)
+constexpr int kRedSlices = 16;                       // CTA slices per column
+constexpr int kRedThreads = kRedSpan * kRedSlices;   // 256
+constexpr int kRedLd = 16;                           // CTAs per slice in flight (grids up to 256)
 static_assert(kRedSlices * kRedLd >= kMaxCtas, "one round of loads covers every CTA's partial");
 
 template <int NOUT>

@@ -26,9 +26,16 @@ namespace cbr {
 // MN-major with flipped taps, plain epilogue.  FpropBn: the forward convolution whose epilogue
 // applies inference BatchNorm and ReLU to the fp32 accumulator, relu(acc*scale + shift), with
 // the per-channel scale and shift computed by each CTA into shared memory at its start.
-enum ConvKind : int { kKindFprop = 0, kKindDgradTma = 2, kKindFpropBn = 3 };
+// FpropApply: the whole training forward in one persistent, cooperative launch for batches
+// whose accumulators all fit in TMEM at once (at most 4 units per CTA): convolution, z and
+// statistics, the finalize by the last CTA, a grid-wide wait for its scale and bias, then
+// y = relu(acc*scale + bias) and the bit mask from the accumulators still in TMEM.
+enum ConvKind : int { kKindFprop = 0, kKindDgradTma = 2, kKindFpropBn = 3, kKindFpropApply = 4 };
 
-__host__ __device__ constexpr bool is_forward_kind(int kind) { return kind == kKindFprop || kind == kKindFpropBn; }
+__host__ __device__ constexpr bool is_forward_kind(int kind) {
+  return kind == kKindFprop || kind == kKindFpropBn || kind == kKindFpropApply;
+}
+constexpr int kPersistMaxUnits = 4;  // FpropApply: units per CTA (U*NOUT TMEM columns each, 512 in all)
 
 struct ConvArgs {
   HaloGeom g;
@@ -46,6 +53,11 @@ struct ConvArgs {
   float* saved_inv_var;
   float* eq;
   float* moments;           // split forward: merged moments out instead of the finalize
+  // FpropApply: y, the bit mask (may be null) and the grid-wide word the last CTA bumps once
+  // eq is written (each CTA reads it at its start, then waits for a different value)
+  void* y;
+  uint32_t* mask;
+  uint32_t* ready;
   const float* bias;
   // epilogue-only inference (kKindFpropBn): scale = gamma/sqrt(rv + eps),
   // shift = beta + (conv_bias - rm)*scale (conv_bias may be null)
@@ -266,7 +278,9 @@ __global__ void __launch_bounds__(Roles<KIND>::kThreads, 1)
                      const __grid_constant__ CUtensorMap map_w, const ConvArgs a) {
   using R = Roles<KIND>;
   constexpr int kThreads = R::kThreads;
-  constexpr int kTmemCols = pow2_at_least(2 * U * NOUT);
+  constexpr bool kPersist = KIND == kKindFpropApply;
+  static_assert(!kPersist || kPersistMaxUnits * U * NOUT <= 512, "persistent accumulators");
+  constexpr int kTmemCols = kPersist ? 512 : pow2_at_least(2 * U * NOUT);
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -291,13 +305,17 @@ __global__ void __launch_bounds__(Roles<KIND>::kThreads, 1)
   const int lane = threadIdx.x & 31;
   const int rs = g.r * g.s;
   const int rows_img = g.p * g.wp;
+  // FpropApply: the ready word as this launch found it (the last CTA changes it only after
+  // every CTA has taken its finalize ticket, so after every CTA has read it here)
+  const uint32_t gen0 = kPersist && threadIdx.x == 0 ? ld_acquire_gpu(a.ready) : 0u;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < 2; ++i) {
       mbar_init(bar_halo_full + 8 * i, 1);
       mbar_init(bar_halo_empty + 8 * i, 1);
       mbar_init(bar_acc_full + 8 * i, 1);
-      mbar_init(bar_acc_empty + 8 * i, kEpiWarps);  // one arrival per epilogue warp
+      // (FpropApply: acc_full and acc_empty are four one-shot unit barriers, bar_acc_full + 8k)
+      mbar_init(bar_acc_empty + 8 * i, kPersist ? 1 : kEpiWarps);  // one arrival per epilogue warp
     }
     for (int i = 0; i < L.nsw; ++i) {
       mbar_init(bar_w_full + 8 * i, 1);
@@ -427,14 +445,15 @@ __global__ void __launch_bounds__(Roles<KIND>::kThreads, 1)
         const uint32_t as = ait & 1, aph = (ait >> 1) & 1;
         // the accumulator stage and the first halo are tested back to back (their latencies
         // overlap); only when one is not complete yet are they waited for one by one
-        const bool ready = __all_sync(0xffffffffu, mbar_test(bar_acc_empty + 8 * as, aph ^ 1) &
+        // (FpropApply: every unit has its own accumulator columns, nothing to wait for)
+        const bool ready = __all_sync(0xffffffffu, (kPersist || mbar_test(bar_acc_empty + 8 * as, aph ^ 1)) &
                                                        mbar_test(bar_halo_full + 8 * (hit & 1), (hit >> 1) & 1));
-        if (!ready && !__all_sync(0xffffffffu, mbar_wait(bar_acc_empty + 8 * as, aph ^ 1))) {
+        if (!kPersist && !ready && !__all_sync(0xffffffffu, mbar_wait(bar_acc_empty + 8 * as, aph ^ 1))) {
           set_abort(abort_flag, a.err, kErrWaitAccum);
           break;
         }
         tc_fence_after();
-        const uint32_t d0 = tmem_base + as * (U * NOUT);
+        const uint32_t d0 = tmem_base + (kPersist ? ait : as) * (U * NOUT);
         for (int ch = 0; ch < NCH && !bad; ++ch, ++hit) {
           const uint32_t hs = hit & 1, hph = (hit >> 1) & 1;
           if (!(ch == 0 && ready) && !__all_sync(0xffffffffu, mbar_wait(bar_halo_full + 8 * hs, hph))) {
@@ -501,7 +520,7 @@ __global__ void __launch_bounds__(Roles<KIND>::kThreads, 1)
           mma_commit_warp(bar_halo_empty + 8 * hs);
         }
         if (bad) break;
-        mma_commit_warp(bar_acc_full + 8 * as);
+        mma_commit_warp(kPersist ? bar_acc_full + 8 * ait : bar_acc_full + 8 * as);
         ++ait;
       }
       mma_commit_warp(bar_drain);
@@ -532,7 +551,7 @@ __global__ void __launch_bounds__(Roles<KIND>::kThreads, 1)
 #pragma unroll
     for (int i = 0; i < (kRegStats ? kCPH : 1); ++i) r1[i] = r2[i] = 0.f;
     float sn = 0.f;  // rows merged into s1 / s2 (the mean and M2 of channel lane >> kSh)
-    const bool stats = KIND == kKindFprop && a.mode == kFpropStats;
+    const bool stats = kPersist || (KIND == kKindFprop && a.mode == kFpropStats);
     const bool bias_relu = KIND == kKindFprop && a.mode == kFpropBiasRelu;
     const float* bn_st = reinterpret_cast<const float*>(smem + L.off_bn);  // kKindFpropBn: [scale][shift]
     const int out_c = a.out_c;
@@ -546,11 +565,12 @@ __global__ void __launch_bounds__(Roles<KIND>::kThreads, 1)
       const int m0 = (u - n * g.upi) * g.um;
       const int ntiles = min(U, (rows_img - m0 + 127) / 128);
       const uint32_t as = ait & 1, aph = (ait >> 1) & 1;
-      if (!mbar_wait_backoff(bar_acc_full + 8 * as, aph, 256)) {
+      if (!mbar_wait_backoff(kPersist ? bar_acc_full + 8 * ait : bar_acc_full + 8 * as, kPersist ? 0u : aph, 256)) {
         set_abort(abort_flag, a.err, kErrWaitMma);
         break;
       }
       tc_fence_after();
+      const uint32_t acol = (kPersist ? ait : as) * (U * NOUT);  // the unit's accumulator columns
       // Each thread owns one accumulator row (an output pixel) and kCPH channels of it: the
       // values go from TMEM to registers to HBM without a shared-memory round trip (shared
       // memory bandwidth is what the tensor cores' operand reads need).
@@ -566,10 +586,10 @@ __global__ void __launch_bounds__(Roles<KIND>::kThreads, 1)
             uint32_t r[kSB];
 #pragma unroll
             for (int q16 = 0; q16 < kSB / 16; ++q16)
-              tmem_ld16(tmem_base + ((uint32_t)(quad * 32) << 16) + as * (U * NOUT) + t * NOUT + c0 + q16 * 16,
+              tmem_ld16(tmem_base + ((uint32_t)(quad * 32) << 16) + acol + t * NOUT + c0 + q16 * 16,
                         *reinterpret_cast<uint32_t(*)[16]>(r + q16 * 16));
             tmem_ld_wait();
-            if (t == ntiles - 1 && b == kNB - 1) {
+            if (!kPersist && t == ntiles - 1 && b == kNB - 1) {
               // the warp's last read of the accumulator stage (a warp-uniform branch): every
               // lane orders its TMEM reads before the warp sync, then one lane arrives
               tc_fence_before();
@@ -620,7 +640,7 @@ __global__ void __launch_bounds__(Roles<KIND>::kThreads, 1)
               }
             }
           }
-        } else if (t == ntiles - 1) {
+        } else if (!kPersist && t == ntiles - 1) {
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(bar_acc_empty + 8 * as);
@@ -660,9 +680,97 @@ __global__ void __launch_bounds__(Roles<KIND>::kThreads, 1)
   tc_fence_before();
   __syncthreads();
 
-  if (KIND == kKindFprop && a.mode == kFpropStats)
+  if (kPersist || (KIND == kKindFprop && a.mode == kFpropStats))
     stats_partial_finalize<NOUT, kThreads, 128 * NOUT * 2>(a, reinterpret_cast<const float*>(smem + L.off_stage),
                                                            smem + L.off_stage, ticket_slot, abort_flag);
+
+  if constexpr (kPersist) {
+    // The last CTA has written eq (scale, bias); once all its threads are past the finalize it
+    // releases the ready word.  Every other CTA waits for the word to change (bounded), then
+    // applies BatchNorm and ReLU to its accumulators, which are still in TMEM.
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      if (*ticket_slot == gridDim.x - 1) {
+        __threadfence();
+        atomicAdd(a.ready, 1u);
+      } else {
+        const uint64_t t0 = globaltimer_ns();
+        while (ld_acquire_gpu(a.ready) == gen0) {
+          if (globaltimer_ns() - t0 > kWaitLimitNs) {
+            set_abort(abort_flag, a.err, kErrWaitMma);
+            break;
+          }
+          __nanosleep(128);
+        }
+      }
+    }
+    __syncthreads();
+    constexpr int kHalves = NOUT >= 64 ? 2 : 1;
+    constexpr int kCPH = NOUT / kHalves;  // 32: one 32-bit mask word per row and half
+    static_assert(kCPH == 32, "persistent apply: 32 channels per epilogue thread");
+    if (warp >= R::kEpiWarp0 && !is_aborted(abort_flag)) {
+      const int ew = warp - R::kEpiWarp0;
+      const int quad = warp & 3;
+      const int half = ew >> 2;
+      const int e = quad * 32 + lane;
+      if (half < kHalves) {
+        const int c0 = half * kCPH;
+        float sc[kCPH], bi[kCPH];
+#pragma unroll
+        for (int i = 0; i < kCPH; ++i) {
+          sc[i] = __ldcg(a.eq + c0 + i);
+          bi[i] = __ldcg(a.eq + NOUT + c0 + i);
+        }
+        const size_t opitch = (size_t)NOUT * 2;
+        uint8_t* ybase = static_cast<uint8_t*>(a.y);
+        uint32_t k = 0;
+        for (int u = blockIdx.x; u < g.total_units; u += gridDim.x, ++k) {
+          const int n = u / g.upi;
+          const int m0 = (u - n * g.upi) * g.um;
+          const int ntiles = min(U, (rows_img - m0 + 127) / 128);
+          for (int t = 0; t < ntiles; ++t) {
+            const int m = m0 + t * 128 + e;
+            const int p = m / g.wp, q = m - p * g.wp;
+            const bool valid = (p < g.p) && (q < g.q);
+            uint32_t r[kCPH];
+            tmem_ld16(tmem_base + ((uint32_t)(quad * 32) << 16) + k * (U * NOUT) + t * NOUT + c0,
+                      *reinterpret_cast<uint32_t(*)[16]>(r));
+            tmem_ld16(tmem_base + ((uint32_t)(quad * 32) << 16) + k * (U * NOUT) + t * NOUT + c0 + 16,
+                      *reinterpret_cast<uint32_t(*)[16]>(r + 16));
+            tmem_ld_wait();
+            if (!valid) continue;
+            // the accumulator rounded to the storage dtype, as the stored z the apply pass of
+            // the two-kernel forward reads: both forms give the same y and mask
+            float yv[kCPH];
+            uint32_t bits = 0;
+#pragma unroll
+            for (int i = 0; i < kCPH; i += 2) {
+              const float2 zz = unpack2<BF16>(pack2<BF16>(__uint_as_float(r[i]), __uint_as_float(r[i + 1])));
+              const float p0 = fmaf(zz.x, sc[i], bi[i]);
+              const float p1 = fmaf(zz.y, sc[i + 1], bi[i + 1]);
+              bits |= (p0 > 0.f ? 1u : 0u) << i;  // CMP_GT: 0 at pre == 0
+              bits |= (p1 > 0.f ? 1u : 0u) << (i + 1);
+              yv[i] = fmaxf(p0, 0.f);
+              yv[i + 1] = fmaxf(p1, 0.f);
+            }
+            const long long pix = ((long long)n * g.p + p) * g.q + q;
+            uint8_t* yrow = ybase + (size_t)pix * opitch;
+#pragma unroll
+            for (int cc = 0; cc < kCPH / 16; ++cc) {
+              const uint4 lo = make_uint4(pack2<BF16>(yv[16 * cc + 0], yv[16 * cc + 1]), pack2<BF16>(yv[16 * cc + 2], yv[16 * cc + 3]),
+                                          pack2<BF16>(yv[16 * cc + 4], yv[16 * cc + 5]), pack2<BF16>(yv[16 * cc + 6], yv[16 * cc + 7]));
+              const uint4 hi = make_uint4(pack2<BF16>(yv[16 * cc + 8], yv[16 * cc + 9]), pack2<BF16>(yv[16 * cc + 10], yv[16 * cc + 11]),
+                                          pack2<BF16>(yv[16 * cc + 12], yv[16 * cc + 13]), pack2<BF16>(yv[16 * cc + 14], yv[16 * cc + 15]));
+              st_global_v8(yrow + (c0 + 16 * cc) * 2, lo, hi);
+            }
+            if (a.mask) a.mask[(pix * NOUT + c0) >> 5] = bits;
+          }
+        }
+      }
+    }
+    tc_fence_before();
+    __syncthreads();
+  }
 
   if (warp == R::kMmaWarp) {
     tc_fence_after();
@@ -697,6 +805,21 @@ int launch_halo_conv(const ConvArgs& a, const CUtensorMap& mx, const CUtensorMap
   const uint32_t smem = L.total + 1024;
   if (smem > 227 * 1024) return 3;
   if (!ensure_smem_attr(reinterpret_cast<const void*>(kern), 227 * 1024)) return 6;
+  if constexpr (KIND == kKindFpropApply) {
+    // every CTA waits for the last one: a cooperative launch, which the runtime refuses unless
+    // the whole grid is resident at once
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(Roles<KIND>::kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, mx, mw, a) == cudaSuccess ? 0 : 6;
+  }
   kern<<<grid, Roles<KIND>::kThreads, smem, st>>>(mx, mw, a);
   return cudaGetLastError() == cudaSuccess ? 0 : 6;
 }

@@ -69,9 +69,10 @@ def ledger(spec, need_dx: bool = True) -> list[Pass]:
     return passes
 
 
-def kernel_passes(spec, need_dx: bool = True, fused: bool = True) -> list[Pass]:
+def kernel_passes(spec, need_dx: bool = True, fused: bool = True, persist: bool = False) -> list[Pass]:
     """Minimum bytes and algorithmic FLOPs of each kernel of the implemented step (names as the
-    benchmark reports them)."""
+    benchmark reports them). persist: the forward is one persistent kernel (conv, statistics,
+    finalize, apply) that writes z, y and the mask."""
     e = 2
     x = spec.n * spec.h * spec.w * spec.c_in * e
     s = spec.n * spec.p * spec.q * spec.c_out * e
@@ -79,11 +80,11 @@ def kernel_passes(spec, need_dx: bool = True, fused: bool = True) -> list[Pass]:
     w = spec.c_out * spec.r * spec.s * spec.c_in * e
     dw = spec.c_out * spec.r * spec.s * spec.c_in * 4
     cv = spec.conv_flops()
-    passes = [
-        Pass("conv_fprop_genstats", x + w + s, cv),
-        Pass("bn_apply_relu", s + s + mask, 0),
-        Pass("bn_bwd_reduce", s + s + mask, 0),
-    ]
+    if persist:
+        passes = [Pass("conv_fprop_apply", x + w + s + s + mask, cv)]
+    else:
+        passes = [Pass("conv_fprop_genstats", x + w + s, cv), Pass("bn_apply_relu", s + s + mask, 0)]
+    passes.append(Pass("bn_bwd_reduce", s + s + mask, 0))
     if fused:
         # dy, z, mask and x read once; dx and the fp32 dW written once
         passes.append(Pass("conv_bwd_fused", s + s + mask + x + dw + ((w + x) if need_dx else 0),

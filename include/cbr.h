@@ -120,6 +120,28 @@ cbr_status_t cbr_forward_train(const cbr_desc_t* desc, const void* x, const void
                                cbr_stream_t stream);
 
 /*
+ * The same training forward in one persistent, cooperative kernel launch: the convolution, the
+ * statistics, the finalize by the last CTA, then (every CTA waiting, with a time limit, for the
+ * finalize) BatchNorm and ReLU applied to the accumulators still held in tensor memory.  z is
+ * never re-read (the single-read fusion of the BatchNorm CUDA page, section 4.1).  Arguments,
+ * outputs and errors as cbr_forward_train, whose results it reproduces bit for bit (y is
+ * computed from the accumulator rounded to the storage dtype, as z is stored).  It takes stride-1
+ * convolutions of at most 64 input channels, 32 or 64 output channels, a filter that fits in
+ * shared memory, y 32-byte aligned, and batches of at most 4 units of 256 output rows per SM
+ * (for example 46 images of 56x56); otherwise it returns CBR_ERR_UNSUPPORTED and does nothing.
+ * It is not faster than cbr_forward_train on the measured shapes (the finalize and the apply
+ * phase then run one after the other inside one launch); it is there for callers who want one
+ * launch per forward.  The runtime refuses the launch (CBR_ERR_CUDA) if the whole grid cannot be
+ * resident at once.
+ */
+cbr_status_t cbr_forward_train_persistent(const cbr_desc_t* desc, const void* x, const void* w,
+                                          const float* gamma, const float* beta, float* running_mean,
+                                          float* running_var, float momentum, float eps, void* y,
+                                          uint32_t* relu_mask, void* z_saved, float* saved_mean,
+                                          float* saved_inv_var, void* ws, size_t ws_bytes,
+                                          cbr_stream_t stream);
+
+/*
  * Training backward (CBR page, sections 5.1-5.3; BatchNorm page, section 3.1).
  *   dy [n][p][q][c_out]            upstream gradient, storage dtype
  *   x, w                           the forward's inputs

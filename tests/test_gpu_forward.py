@@ -21,6 +21,9 @@ CASES = {
     "k1x1": (CBRSpec("1x1", n=2, h=20, w=20, c_in=64, c_out=64, r=1, s=1, pad=0), 2006),
     "k5x5": (CBRSpec("5x5", n=2, h=16, w=16, c_in=32, c_out=64, r=5, s=5, pad=2), 2007),
     "cfg2": (CONFIGS[2], 1236),
+    # 48 images of 56x56 are 624 units of 256 rows, more than 4 per CTA: the conv + apply path
+    # (the smaller 32- and 64-channel cases take the persistent forward)
+    "n48_56_64": (CONFIGS[3].with_(n=48), 2008),
     # first layer (3 channels, im2col kernel): the config-4 shape on small and ragged inputs
     "first_32x32": (CBRSpec("first small", n=2, h=32, w=32, c_in=3, c_out=64, r=7, s=7, stride=2, pad=3,
                             x_dist="uniform2.5", first_layer=True), 2008),
@@ -81,6 +84,42 @@ def test_forward_without_z_saved_matches():
     _, _, b = run_forward(spec, seed, save_z=False)
     assert torch.equal(a["y"], b["y"])
     assert torch.equal(a["saved_mean"], b["saved_mean"])
+
+
+PERSISTENT_CASES = ["n3_56_64", "ragged_13x29", "cin16_cout32_bf16", "k1x1", "cfg2"]
+
+
+@pytest.mark.parametrize("case", PERSISTENT_CASES)
+def test_persistent_forward_equals_forward(case):
+    """cbr_forward_train_persistent (one cooperative launch) gives cbr_forward_train's z, y, mask,
+    statistics and running statistics bit for bit; parity of those with the oracle is
+    test_forward_train_parity."""
+    spec, seed = CASES[case]
+    inp = make_inputs(spec, seed, with_dy=False)
+    g = {k: v.cuda() for k, v in inp.items()}
+    layer = cbr.Layer.from_spec(spec)
+    outs = []
+    for persistent in (False, True):
+        ws = cbr.new_workspace(cbr.workspace_size(layer)[0])
+        rm, rv = g["running_mean"].clone(), g["running_var"].clone()
+        o = cbr.forward_train(layer, g["x"], g["w"], g["gamma"], g["beta"], rm, rv, spec.momentum, spec.eps, ws=ws,
+                              persistent=persistent)
+        o["running_mean"], o["running_var"] = rm, rv
+        outs.append(o)
+    cbr.stream_status()
+    for k in ("z", "y", "mask", "saved_mean", "saved_inv_var", "running_mean", "running_var"):
+        assert torch.equal(outs[0][k], outs[1][k]), k
+
+
+def test_persistent_forward_declines_large_batches():
+    """48 images of 56x56 are 624 units of 256 rows, more than 4 per SM: unsupported, nothing run."""
+    spec, seed = CASES["n48_56_64"]
+    layer = cbr.Layer.from_spec(spec)
+    g = {k: v.cuda() for k, v in make_inputs(spec, seed, with_dy=False).items()}
+    ws = cbr.new_workspace(cbr.workspace_size(layer)[0])
+    with pytest.raises(RuntimeError, match="UNSUPPORTED"):
+        cbr.forward_train(layer, g["x"], g["w"], g["gamma"], g["beta"], g["running_mean"], g["running_var"],
+                          spec.momentum, spec.eps, ws=ws, persistent=True)
 
 
 def test_forward_deterministic():

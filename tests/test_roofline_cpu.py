@@ -76,3 +76,13 @@ def test_kernel_passes_of_the_fused_backward():
     ks = {p.name: p for p in roofline.kernel_passes(CONFIGS[3], need_dx=True, fused=False)}
     assert ks["bn_dz"].bytes == 3 * S3 + MASK3
     assert ks["conv_wgrad"].bytes == 2 * S3 + DW3 and ks["conv_dgrad"].bytes == 2 * S3 + W3
+
+
+def test_kernel_passes_of_the_persistent_forward():
+    """The persistent forward reads x and W once and writes z, y and the mask in one kernel."""
+    ks = {p.name: p for p in roofline.kernel_passes(CONFIGS[2], need_dx=True, fused=True, persist=True)}
+    assert set(ks) == {"conv_fprop_apply", "bn_bwd_reduce", "conv_bwd_fused"}
+    s2 = 32 * 56 * 56 * 64 * 2
+    x2 = 32 * 56 * 56 * 64 * 2
+    assert ks["conv_fprop_apply"].bytes == x2 + W3 + 2 * s2 + s2 // 16
+    assert ks["conv_fprop_apply"].flops == 59_190_018_048 // 8
