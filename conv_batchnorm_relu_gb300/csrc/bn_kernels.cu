@@ -11,10 +11,12 @@
 #include <algorithm>
 #include <map>
 #include <mutex>
+#include <type_traits>
 #include <utility>
 
 #include "cbr_internal.h"
 #include "common.cuh"
+#include "stats.cuh"
 
 namespace cbr {
 namespace {
@@ -51,6 +53,130 @@ __global__ void __launch_bounds__(kApplyThreads)
     for (int k = 0; k < kApplyUnroll; ++k) {
       const long long v = nvec - 1 - (v0 + k * stride);
       if (v >= 0) in[k] = ld_global_nc_v4(zb + v * 16);
+    }
+#pragma unroll
+    for (int k = 0; k < kApplyUnroll; ++k) {
+      const long long v = nvec - 1 - (v0 + k * stride);
+      if (v >= 0) {
+        const uint32_t w[4] = {in[k].x, in[k].y, in[k].z, in[k].w};
+        uint32_t o[4];
+        uint32_t bits = 0;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const float2 zz = unpack2<BF16>(w[j]);
+          const float p0 = fmaf(zz.x, sc[2 * j], bi[2 * j]);
+          const float p1 = fmaf(zz.y, sc[2 * j + 1], bi[2 * j + 1]);
+          bits |= (p0 > 0.f ? 1u : 0u) << (2 * j);
+          bits |= (p1 > 0.f ? 1u : 0u) << (2 * j + 1);
+          o[j] = pack2<BF16>(fmaxf(p0, 0.f), fmaxf(p1, 0.f));
+        }
+        st_global_v4(yb + v * 16, make_uint4(o[0], o[1], o[2], o[3]));
+        if (MASK) a.mask[v] = (uint8_t)bits;
+      }
+    }
+  }
+}
+
+// K2 + K3 for a training forward whose convolution left only its per-CTA partial moments
+// (FpropArgs::defer): the finalize runs in this pass's prologue instead of on the last CTA of
+// the convolution, where it was a serial tail of the forward.  Every block stages all partials
+// in shared memory with one bulk copy, issues its first z loads, merges the partials with the
+// same st::merge_partials the convolution's last CTA runs (so the statistics and y are the
+// same bits either way) and keeps eq_scale / eq_bias in shared memory; block 0 also writes the
+// saved and the running statistics.  The sweep is bn_apply_relu_kernel's, with one block of
+// kMergeThreads per SM.
+constexpr int kMergeThreads = 1024;
+
+template <int C>
+__host__ __device__ constexpr uint32_t merge_smem_bytes(int nparts) {
+  return (uint32_t)nparts * st::partial_floats(C) * 4u + st::merge_scratch_floats<C>() * 4u + 2u * C * 4u + 16u;
+}
+
+template <bool BF16, bool MASK, int C>
+__global__ void __launch_bounds__(kMergeThreads, 1)
+    bn_apply_merge_kernel(const ApplyArgs a) {
+  constexpr int kPF = st::partial_floats(C);
+  constexpr int kCvec = C / 8;
+  static_assert(kMergeThreads % kCvec == 0, "the grid stride must keep each thread's channel group");
+  extern __shared__ __align__(16) uint8_t smem_apply[];
+  float* parts = reinterpret_cast<float*>(smem_apply);   // [nparts][kPF]
+  float* scratch = parts + (size_t)a.nparts * kPF;       // the merge's working set
+  float* eqs = scratch + st::merge_scratch_floats<C>();  // eq_scale [C], eq_bias [C]
+  const uint32_t bar = smem_u32(eqs + 2 * C);
+  const uint32_t bytes = (uint32_t)a.nparts * kPF * 4u;
+  if (threadIdx.x == 0) {
+    mbar_init(bar, 1);
+    fence_mbarrier_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    mbar_arrive_expect_tx(bar, bytes);
+    bulk_load_1d(smem_u32(parts), a.part, bytes, bar);
+  }
+  // the first z vectors of this thread, in flight while the partials are merged
+  const long long nvec = a.total / 8;
+  const long long stride = (long long)gridDim.x * kMergeThreads;
+  const long long vfirst = (long long)blockIdx.x * kMergeThreads + threadIdx.x;
+  const uint8_t* zb = static_cast<const uint8_t*>(a.z);
+  uint8_t* yb = static_cast<uint8_t*>(a.y);
+  uint4 in[kApplyUnroll];
+#pragma unroll
+  for (int k = 0; k < kApplyUnroll; ++k) {
+    const long long v = nvec - 1 - (vfirst + k * stride);
+    if (v >= 0) in[k] = ld_global_nc_v4(zb + v * 16);
+  }
+  float gm = 0.f, bt = 0.f, rm = 0.f, rv = 0.f;
+  if (threadIdx.x < C) {
+    gm = __ldg(a.gamma + threadIdx.x);
+    bt = __ldg(a.beta + threadIdx.x);
+    if (blockIdx.x == 0) {
+      rm = a.running_mean[threadIdx.x];
+      rv = a.running_var[threadIdx.x];
+    }
+  }
+  bool staged = true;
+  if (threadIdx.x < st::merge_threads<C>()) {
+    staged = mbar_wait(bar, 0);
+    if (!staged) report_error(a.err, kErrWaitOperand);
+  }
+  st::merge_partials<C, kMergeThreads, 2>(a.nparts, scratch, [&](int b, int c4, float4& m, float4& q, float& n) {
+    const float* pb = parts + b * kPF;
+    m = reinterpret_cast<const float4*>(pb)[c4];
+    q = reinterpret_cast<const float4*>(pb + C)[c4];
+    n = pb[2 * C];
+  });
+  if (threadIdx.x < C) {
+    const int c = threadIdx.x;
+    const float mean = scratch[c];
+    const st::BnFinal f = st::bn_finalize(mean, scratch[C + c], gm, bt, rm, rv, a.inv_m, a.eps, a.momentum, a.unbias);
+    eqs[c] = f.scale;
+    eqs[C + c] = f.bias;
+    if (blockIdx.x == 0) {
+      a.saved_mean[c] = mean;
+      a.saved_inv_var[c] = f.inv;
+      a.running_mean[c] = f.run_mean;
+      a.running_var[c] = f.run_var;
+    }
+  }
+  __syncthreads();
+  // a copy that never completed (reported above) is given one more bounded wait before the
+  // block's shared memory is released
+  if (!staged && threadIdx.x == 0) mbar_wait(bar, 0);
+  if (vfirst >= nvec) return;
+  const int c0 = (int)((nvec - 1 - vfirst) % kCvec) * 8;
+  float sc[8], bi[8];
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    sc[e] = eqs[c0 + e];
+    bi[e] = eqs[C + c0 + e];
+  }
+  for (long long v0 = vfirst; v0 < nvec; v0 += stride * kApplyUnroll) {
+    if (v0 != vfirst) {
+#pragma unroll
+      for (int k = 0; k < kApplyUnroll; ++k) {
+        const long long v = nvec - 1 - (v0 + k * stride);
+        if (v >= 0) in[k] = ld_global_nc_v4(zb + v * 16);
+      }
     }
 #pragma unroll
     for (int k = 0; k < kApplyUnroll; ++k) {
@@ -446,11 +572,48 @@ int launch_dz(const DzArgs& a_in, bool bf16, int num_sms, cudaStream_t st) {
   return cudaGetLastError() == cudaSuccess ? 0 : 6;
 }
 
+bool apply_merge_supported(int c, int max_parts) {
+  uint32_t bytes = 0;
+  switch (c) {
+    case 16: bytes = merge_smem_bytes<16>(max_parts); break;
+    case 32: bytes = merge_smem_bytes<32>(max_parts); break;
+    case 64: bytes = merge_smem_bytes<64>(max_parts); break;
+    case 128: bytes = merge_smem_bytes<128>(max_parts); break;
+    default: return false;
+  }
+  return max_parts >= 1 && bytes <= 200u * 1024u;
+}
+
 int launch_apply(const ApplyArgs& a, bool bf16, int num_sms, cudaStream_t st) {
   // kApplyThreads (and so the grid stride) must be a multiple of the c/8 vectors of a pixel
   if (a.c % 8 != 0 || a.c > 256 || kApplyThreads % (a.c / 8) != 0) return 3;
   const long long nvec = a.total / 8;
   const bool mask = a.mask != nullptr;
+  if (a.part) {
+    // the statistics merge in the prologue: one block of kMergeThreads per SM
+    if (!apply_merge_supported(a.c, a.nparts) || (reinterpret_cast<uintptr_t>(a.part) & 15) != 0) return 3;
+    const long long want = (nvec + (long long)kApplyUnroll * kMergeThreads - 1) / ((long long)kApplyUnroll * kMergeThreads);
+    const int grid = (int)std::max<long long>(1, std::min<long long>(want, num_sms));
+    auto go = [&](auto kern, uint32_t smem) {
+      // the attribute is set once per kernel: to the largest size any launch may ask for
+      if (!ensure_smem_attr(reinterpret_cast<const void*>(kern), 227 * 1024)) return 6;
+      kern<<<grid, kMergeThreads, smem, st>>>(a);
+      return cudaGetLastError() == cudaSuccess ? 0 : 6;
+    };
+    auto by_c = [&](auto bf16_c, auto mask_c) {
+      constexpr bool B = decltype(bf16_c)::value, M = decltype(mask_c)::value;
+      switch (a.c) {
+        case 16: return go(bn_apply_merge_kernel<B, M, 16>, merge_smem_bytes<16>(a.nparts));
+        case 32: return go(bn_apply_merge_kernel<B, M, 32>, merge_smem_bytes<32>(a.nparts));
+        case 64: return go(bn_apply_merge_kernel<B, M, 64>, merge_smem_bytes<64>(a.nparts));
+        default: return go(bn_apply_merge_kernel<B, M, 128>, merge_smem_bytes<128>(a.nparts));
+      }
+    };
+    using T = std::true_type;
+    using F = std::false_type;
+    if (bf16) return mask ? by_c(T{}, T{}) : by_c(T{}, F{});
+    return mask ? by_c(F{}, T{}) : by_c(F{}, F{});
+  }
   auto go = [&](auto kern) {
     kern<<<stream_grid(kern, kApplyThreads, nvec / kApplyUnroll, num_sms), kApplyThreads, 0, st>>>(a);
   };

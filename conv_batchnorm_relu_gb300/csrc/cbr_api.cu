@@ -404,6 +404,12 @@ cbr_status_t forward_train_impl(bool persistent, const cbr_desc_t* desc, const v
     prof.mark();
     return CBR_OK;
   }
+  // The convolution writes its per-CTA partial moments and the apply pass merges and
+  // finalizes them in its prologue (where the partials fit its shared memory); otherwise the
+  // convolution's last CTA finalizes.
+  int nparts = 0;
+  a.defer = apply_merge_supported((int)s.cout, dev->num_sms) ? 1 : 0;
+  a.parts_out = &nparts;
   st = run_fprop(a, s, x, w, dev->num_sms, cs);
   if (st) return (cbr_status_t)st;
   prof.mark();
@@ -415,6 +421,21 @@ cbr_status_t forward_train_impl(bool persistent, const cbr_desc_t* desc, const v
   ap.eq = a.eq;
   ap.total = s.m * s.cout;
   ap.c = (int)s.cout;
+  if (a.defer) {
+    ap.part = a.part;
+    ap.nparts = nparts;
+    ap.gamma = gamma;
+    ap.beta = beta;
+    ap.running_mean = running_mean;
+    ap.running_var = running_var;
+    ap.saved_mean = saved_mean;
+    ap.saved_inv_var = saved_inv_var;
+    ap.momentum = momentum;
+    ap.eps = eps;
+    ap.inv_m = (float)(1.0 / (double)s.m);
+    ap.unbias = s.m > 1 ? (float)((double)s.m / (double)(s.m - 1)) : 1.f;
+    ap.err = dev->err;
+  }
   st = launch_apply(ap, s.bf16, dev->num_sms, cs);
   if (st) return (cbr_status_t)st;
   prof.mark();

@@ -56,6 +56,10 @@ struct FpropArgs {
   // split (synchronised) forward: when set, the last CTA writes the merged moments of this
   // call's rows here, [mean cout][M2 cout][row count], instead of finalizing
   float* moments;
+  // training forward whose apply pass merges the statistics: the CTAs write their partials
+  // and no CTA finalizes (eq, the saved and the running statistics are left to the apply)
+  int defer;
+  int* parts_out;           // host: set to the number of partials (the grid) before the launch
   const float* bias;        // inference: per-channel bias added before ReLU
   // epilogue-only inference (launch_fprop_bn): BatchNorm parameters, conv bias (may be null)
   const float* bn_gamma;
@@ -130,10 +134,28 @@ struct ApplyArgs {
   const void* z;
   void* y;
   uint8_t* mask;            // bit-packed, bit i of byte j <-> element 8j+i; may be null
-  const float* eq;          // [2][c]
+  const float* eq;          // [2][c] (unused when part is set)
   long long total;          // elements
   int c;
+  // When set, the forward convolution left `nparts` partial moments here (FpropArgs::defer):
+  // every block merges them into eq in its prologue and block 0 writes the finalize's outputs.
+  const float* part;
+  int nparts;
+  const float* gamma;
+  const float* beta;
+  float* running_mean;
+  float* running_var;
+  float* saved_mean;
+  float* saved_inv_var;
+  float momentum;
+  float eps;
+  float inv_m;              // 1 / rows
+  float unbias;             // rows / (rows - 1)
+  uint32_t* err;
 };
+// Whether the apply pass can merge the statistics of a forward with c channels and at most
+// max_parts partials (the staged partials must fit in shared memory).
+bool apply_merge_supported(int c, int max_parts);
 int launch_apply(const ApplyArgs& a, bool bf16, int num_sms, cudaStream_t st);
 
 struct BwdReduceArgs {

@@ -29,6 +29,7 @@ int launch_fprop(const FpropArgs& f, int c_in, int c_out, bool bf16, const void*
   a.saved_inv_var = f.saved_inv_var;
   a.eq = f.eq;
   a.moments = f.moments;
+  a.defer = f.defer;
   a.bias = f.bias;
   a.momentum = f.momentum;
   a.eps = f.eps;
@@ -66,6 +67,7 @@ int launch_fprop(const FpropArgs& f, int c_in, int c_out, bool bf16, const void*
     if (!encode_tiled(&mw, dt, 3, w, dims, strides, box)) return 6;
   }
   const int grid = std::min(g.total_units, num_sms);
+  if (f.parts_out) *f.parts_out = grid;
 
 #define CBR_FPROP_CASE(NCH_, COUT_, U_, WRES_)                                                        \
   if (nch == NCH_ && c_out == COUT_ && U == U_ && (WRES_ == wres)) {                                 \

@@ -1603,6 +1603,7 @@ int launch_first_fprop(const FpropArgs& f, int stride, int c_out, bool bf16, con
   a.saved_inv_var = f.saved_inv_var;
   a.eq = f.eq;
   a.moments = f.moments;
+  a.defer = f.defer;
   a.bias = f.bias;
   a.momentum = f.momentum;
   a.eps = f.eps;
@@ -1638,6 +1639,7 @@ int launch_first_fprop(const FpropArgs& f, int stride, int c_out, bool bf16, con
         encode_tiled_span(&mz, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, f.z,
                           dims, strides, box, cph * 2)) {
       const int igrid = std::min(g.units, num_sms);
+      if (f.parts_out) *f.parts_out = igrid;
       auto go = [&](auto kern) {
         if (!ensure_smem_attr(reinterpret_cast<const void*>(kern), 227 * 1024)) return 6;
         kern<<<igrid, kImpThreads, ismem, st>>>(mz, a, g, w, x);
@@ -1659,6 +1661,7 @@ int launch_first_fprop(const FpropArgs& f, int stride, int c_out, bool bf16, con
   const uint32_t smem = kFlXStages * fl_xstage_bytes(g) + 2 * kFlTile + kFlAtoms * nout * 128 + 256 + 1024;
   if (smem > 227 * 1024) return 3;
   const int grid = std::min(g.units, num_sms);
+  if (f.parts_out) *f.parts_out = grid;
   auto go = [&](auto kern) {
     if (!ensure_smem_attr(reinterpret_cast<const void*>(kern), 227 * 1024)) return 6;
     kern<<<grid, kFlThreads, smem, st>>>(mx, a, g, w, x);

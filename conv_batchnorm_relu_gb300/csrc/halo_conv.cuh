@@ -53,6 +53,7 @@ struct ConvArgs {
   float* saved_inv_var;
   float* eq;
   float* moments;           // split forward: merged moments out instead of the finalize
+  int defer;                // write the CTA partials only: the apply pass merges and finalizes
   // FpropApply: y, the bit mask (may be null) and the grid-wide word the last CTA bumps once
   // eq is written (each CTA reads it at its start, then waits for a different value)
   void* y;
@@ -139,18 +140,20 @@ __device__ __forceinline__ void set_abort(volatile int* flag, uint32_t* err, uin
 // Forward statistics, after the main loop: `red` holds the moments of each TMEM lane quadrant
 // of this CTA, [4][2][COUT] (mean, M2) followed by the 4 row counts (written by the epilogue,
 // visible after a __syncthreads).  Every thread calls this: the quadrants are merged in fixed
-// order into the CTA's partial, a wrap-around ticket elects the last CTA, and that CTA merges
-// the grid's partials in a fixed order and runs bn_finalize.  `scratch` (SCRATCH bytes, may
-// alias `red`) holds the finalize's working set.
+// order into the CTA's partial.  With a.defer set that is all (the apply pass merges the grid's
+// partials in its prologue); otherwise a wrap-around ticket elects the last CTA, which merges
+// the grid's partials (st::merge_partials) and runs bn_finalize.  `scratch` (SCRATCH bytes, may
+// alias `red`) holds the merge's working set.
 template <int COUT, int kThreads, int SCRATCH>
 __device__ void stats_partial_finalize(const ConvArgs& a, const float* red, uint8_t* scratch,
                                        volatile uint32_t* ticket_slot, volatile int* abort_flag) {
   static_assert(kThreads >= COUT, "one thread per channel in the finalize");
+  static_assert(st::merge_scratch_floats<COUT>() * 4 <= SCRATCH, "finalize scratch");
   constexpr int kPF = st::partial_floats(COUT);
   // the per-channel inputs of the finalize, loaded before the ticket by every CTA (cheap) so
   // the last one does not wait for them after its merges
   float gm = 0.f, bt = 0.f, rm = 0.f, rv = 0.f;
-  if (threadIdx.x < COUT && !a.moments) {
+  if (threadIdx.x < COUT && !a.moments && !a.defer) {
     gm = a.gamma[threadIdx.x];
     bt = a.beta[threadIdx.x];
     rm = a.running_mean[threadIdx.x];
@@ -167,6 +170,7 @@ __device__ void stats_partial_finalize(const ConvArgs& a, const float* red, uint
     mypart[COUT + c] = q;
     if (c == 0) mypart[2 * COUT] = n;
   }
+  if (a.defer) return;
   __threadfence();
   __syncthreads();
   if (threadIdx.x == 0) *ticket_slot = atomicInc(a.ticket, gridDim.x - 1);
@@ -174,81 +178,17 @@ __device__ void stats_partial_finalize(const ConvArgs& a, const float* red, uint
   if (*ticket_slot == gridDim.x - 1 && !is_aborted(abort_flag)) {
     // ---------------------------------------------------- bn_finalize (last CTA)
     __threadfence();
-    // This runs on one SM after all the others, so it is kept short: thread t merges, for 4
-    // channels (column t % kV), the partials of CTAs t / kV, + kRG, ... in order, with the
-    // loads of kLd CTAs in flight; the kRG group results are then merged by a fixed pairwise
-    // tree whose steps run all their (pair, channel) merges in parallel over the CTA, and the
-    // per-channel math multiplies by the host's 1/M (no division by M).
-    constexpr int kV = COUT / 4;               // float4 columns of the means (and of the M2s)
-    constexpr int kGF = 2 * COUT + 4;          // floats per group result: means, M2s, count
-    constexpr int kCntF = 6 * 32;              // group counts, one row per tree step
-    constexpr int kRGfit = (SCRATCH - kCntF * 4) / (kGF * 4);
-    constexpr int kRG1 = kThreads / kV < kRGfit ? kThreads / kV : kRGfit;
-    constexpr int kRG = kRG1 < 32 ? kRG1 : 32;
-    static_assert(kRG >= 1, "finalize scratch");
-    constexpr int kLd = 8;                     // CTAs whose loads are in flight per thread
-    float* fg = reinterpret_cast<float*>(scratch);  // [kRG][kGF]
-    float* cnt = fg + kRG * kGF;                    // [step][kRG]
-    const int c4 = threadIdx.x % kV, rg = threadIdx.x / kV;
-    if (rg < kRG) {
-      float n = 0.f;
-      float m[4] = {0.f, 0.f, 0.f, 0.f}, q[4] = {0.f, 0.f, 0.f, 0.f};
-      for (int b0 = rg; b0 < (int)gridDim.x; b0 += kLd * kRG) {
-        float4 vm[kLd], vq[kLd];
-        float vn[kLd];
-#pragma unroll
-        for (int k = 0; k < kLd; ++k) {
-          const int b = b0 + k * kRG;
+    float* fg = reinterpret_cast<float*>(scratch);
+    // the other CTAs' partials were written during this launch: read them from L2
+    const float tot_n = st::merge_partials<COUT, kThreads, 10>(
+        (int)gridDim.x, fg, [&](int b, int c4, float4& m, float4& q, float& n) {
           const float* pb = a.part + (size_t)b * kPF;
-          const bool ok = b < (int)gridDim.x;
-          vm[k] = ok ? __ldcg(reinterpret_cast<const float4*>(pb) + c4) : make_float4(0.f, 0.f, 0.f, 0.f);
-          vq[k] = ok ? __ldcg(reinterpret_cast<const float4*>(pb + COUT) + c4) : make_float4(0.f, 0.f, 0.f, 0.f);
-          vn[k] = ok ? __ldcg(pb + 2 * COUT) : 0.f;
-        }
-#pragma unroll
-        for (int k = 0; k < kLd; ++k) {
-          const float bm[4] = {vm[k].x, vm[k].y, vm[k].z, vm[k].w};
-          const float bq[4] = {vq[k].x, vq[k].y, vq[k].z, vq[k].w};
-          const st::ChanW w = st::chan_weights(n, vn[k]);  // one division for the 4 channels
-#pragma unroll
-          for (int j = 0; j < 4; ++j) st::chan_merge_w(m[j], q[j], bm[j], bq[j], w);
-          n += vn[k];
-        }
-      }
-      float* gr = fg + rg * kGF;
-      reinterpret_cast<float4*>(gr)[c4] = make_float4(m[0], m[1], m[2], m[3]);
-      reinterpret_cast<float4*>(gr + COUT)[c4] = make_float4(q[0], q[1], q[2], q[3]);
-      if (c4 == 0) cnt[rg] = n;
-    }
-    __syncthreads();
-    // step s (w = 2^s): group r (r % 2w == 0, r + w < kRG) takes in group r + w (r first).
-    // The right member is not written during its step, and each (pair, channel) item is read
-    // and written by one thread; the merged counts go to the next step's row.
-    int step = 0;
-#pragma unroll 1
-    for (int w = 1; w < kRG; w *= 2, ++step) {
-      const float* cs = cnt + step * kRG;
-      const int npairs = (kRG - w + 2 * w - 1) / (2 * w);
-#pragma unroll 1
-      for (int i = threadIdx.x; i < npairs * COUT; i += kThreads) {
-        const int pi = i / COUT, ch = i - pi * COUT;
-        const int r = pi * 2 * w;
-        float* ga = fg + r * kGF;
-        const float* gb = ga + w * kGF;
-        float ma = ga[ch], qa = ga[COUT + ch];
-        st::chan_merge_w(ma, qa, gb[ch], gb[COUT + ch], st::chan_weights(cs[r], cs[r + w]));
-        ga[ch] = ma;
-        ga[COUT + ch] = qa;
-      }
-      if (threadIdx.x < kRG) {
-        const int r = threadIdx.x;
-        cnt[(step + 1) * kRG + r] = (r % (2 * w) == 0 && r + w < kRG) ? cs[r] + cs[r + w] : cs[r];
-      }
-      __syncthreads();
-    }
+          m = __ldcg(reinterpret_cast<const float4*>(pb) + c4);
+          q = __ldcg(reinterpret_cast<const float4*>(pb + COUT) + c4);
+          n = __ldcg(pb + 2 * COUT);
+        });
     if (threadIdx.x < COUT) {
       const int c = threadIdx.x;
-      const float tot_n = cnt[step * kRG];
       const float tot_m = fg[c], tot_q = fg[COUT + c];
       if (a.moments) {
         // split forward: this call's moments go to the caller, who merges them with other
@@ -258,16 +198,13 @@ __device__ void stats_partial_finalize(const ConvArgs& a, const float* red, uint
         if (c == 0) a.moments[2 * COUT] = tot_n;
         return;
       }
-      const float meanf = tot_m;
-      const float var = fmaxf(tot_q * (float)a.inv_m, 0.f);  // biased: M2 / M
-      const float inv = rsqrtf(var + a.eps);
-      a.saved_mean[c] = meanf;
-      a.saved_inv_var[c] = inv;
-      a.eq[c] = gm * inv;
-      a.eq[COUT + c] = bt - gm * meanf * inv;
-      const float mom = a.momentum;
-      a.running_mean[c] = (1.f - mom) * rm + mom * meanf;
-      a.running_var[c] = (1.f - mom) * rv + mom * var * a.unbias;
+      const st::BnFinal f = st::bn_finalize(tot_m, tot_q, gm, bt, rm, rv, (float)a.inv_m, a.eps, a.momentum, a.unbias);
+      a.saved_mean[c] = tot_m;
+      a.saved_inv_var[c] = f.inv;
+      a.eq[c] = f.scale;
+      a.eq[COUT + c] = f.bias;
+      a.running_mean[c] = f.run_mean;
+      a.running_var[c] = f.run_var;
     }
   }
 }

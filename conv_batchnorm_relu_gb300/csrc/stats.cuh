@@ -131,5 +131,122 @@ __device__ __forceinline__ float chan_scatter(float (&mean)[L], float (&m2)[L], 
 // Floats of one CTA's partial statistics: means [C], M2 [C], then the row count and padding.
 __host__ __device__ constexpr int partial_floats(int c) { return 2 * c + 4; }
 
+// ------------------------------------------------------------------ grid merge and finalize
+// Every kernel that merges the grid's partial moments (the convolution's last CTA, the
+// persistent forward, the apply pass) runs the same merge, so the statistics and y come out
+// bit-identical whichever kernel merged them.  The row-group count depends on the channel count
+// alone: kRG groups of C/4 threads (one per float4 column of channels, 256 threads for C >= 64);
+// group r merges partials r, r + kRG, r + 2 kRG, ... in order, and a fixed pairwise tree merges
+// the group results.
+template <int C>
+__host__ __device__ constexpr int merge_groups() {
+  return 1024 / C < 16 ? 1024 / C : 16;
+}
+template <int C>
+__host__ __device__ constexpr int merge_threads() {
+  return merge_groups<C>() * (C / 4);
+}
+constexpr int kMergeCntF = 8 * 16;  // group counts, one row of kRG per tree step
+// Working set of the merge: [kRG][2C + 4] group results, then the count rows.
+template <int C>
+__host__ __device__ constexpr int merge_scratch_floats() {
+  return merge_groups<C>() * partial_floats(C) + kMergeCntF;
+}
+
+// Merge `nparts` partial moments into scratch[0 .. 2C): means, then M2s; returns the total row
+// count.  Every thread of the block calls it (it synchronises the block); `load(b, c4, m, q, n)`
+// fetches float4 column c4 of partial b's means and M2s and its row count.  kLd partials of a
+// thread are loaded before the first is merged (the order of the merges does not depend on it).
+template <int C, int kThreads, int kLd, class Load>
+__device__ float merge_partials(int nparts, float* scratch, Load load) {
+  constexpr int kV = C / 4;
+  constexpr int kRG = merge_groups<C>();
+  constexpr int kGF = partial_floats(C);
+  static_assert(kThreads >= merge_threads<C>() && kThreads >= C, "merge threads");
+  static_assert((1 << 7) >= kRG, "count rows");
+  float* fg = scratch;            // [kRG][kGF]
+  float* cnt = fg + kRG * kGF;    // [step][kRG]
+  const int c4 = threadIdx.x % kV, rg = threadIdx.x / kV;
+  if (rg < kRG) {
+    float n = 0.f;
+    float m[4] = {0.f, 0.f, 0.f, 0.f}, q[4] = {0.f, 0.f, 0.f, 0.f};
+    for (int b0 = rg; b0 < nparts; b0 += kLd * kRG) {
+      float4 vm[kLd], vq[kLd];
+      float vn[kLd];
+#pragma unroll
+      for (int k = 0; k < kLd; ++k) {
+        const int b = b0 + k * kRG;
+        if (b < nparts) {
+          load(b, c4, vm[k], vq[k], vn[k]);
+        } else {
+          vm[k] = vq[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+          vn[k] = 0.f;
+        }
+      }
+#pragma unroll
+      for (int k = 0; k < kLd; ++k) {
+        const float bm[4] = {vm[k].x, vm[k].y, vm[k].z, vm[k].w};
+        const float bq[4] = {vq[k].x, vq[k].y, vq[k].z, vq[k].w};
+        const ChanW w = chan_weights(n, vn[k]);  // one division for the 4 channels
+#pragma unroll
+        for (int j = 0; j < 4; ++j) chan_merge_w(m[j], q[j], bm[j], bq[j], w);
+        n += vn[k];
+      }
+    }
+    float* gr = fg + rg * kGF;
+    reinterpret_cast<float4*>(gr)[c4] = make_float4(m[0], m[1], m[2], m[3]);
+    reinterpret_cast<float4*>(gr + C)[c4] = make_float4(q[0], q[1], q[2], q[3]);
+    if (c4 == 0) cnt[rg] = n;
+  }
+  __syncthreads();
+  // step s (w = 2^s): group r (r % 2w == 0, r + w < kRG) takes in group r + w (r first).  The
+  // right member is not written during its step and each (pair, channel) item has one thread;
+  // the merged counts go to the next step's row.
+  int step = 0;
+#pragma unroll 1
+  for (int w = 1; w < kRG; w *= 2, ++step) {
+    const float* cs = cnt + step * kRG;
+    const int npairs = (kRG - w + 2 * w - 1) / (2 * w);
+#pragma unroll 1
+    for (int i = threadIdx.x; i < npairs * C; i += kThreads) {
+      const int pi = i / C, ch = i - pi * C;
+      const int r = pi * 2 * w;
+      float* ga = fg + r * kGF;
+      const float* gb = ga + w * kGF;
+      float ma = ga[ch], qa = ga[C + ch];
+      chan_merge_w(ma, qa, gb[ch], gb[C + ch], chan_weights(cs[r], cs[r + w]));
+      ga[ch] = ma;
+      ga[C + ch] = qa;
+    }
+    if (threadIdx.x < kRG) {
+      const int r = threadIdx.x;
+      cnt[(step + 1) * kRG + r] = (r % (2 * w) == 0 && r + w < kRG) ? cs[r] + cs[r + w] : cs[r];
+    }
+    __syncthreads();
+  }
+  return cnt[step * kRG];
+}
+
+// BatchNorm finalize of one channel from its batch mean and M2 over M rows (inv_m = 1/M):
+// var = M2/M (biased), inv = 1/sqrt(var + eps), eq_scale = gamma*inv, eq_bias = beta -
+// eq_scale*mean; the running statistics move by `momentum` towards the batch mean and the
+// unbiased variance (BatchNorm CUDA page, sections 2 and 3).  Explicit roundings, so that every
+// kernel computes the same bits.
+struct BnFinal {
+  float inv, scale, bias, run_mean, run_var;
+};
+__device__ __forceinline__ BnFinal bn_finalize(float mean, float m2, float gamma, float beta, float run_mean,
+                                               float run_var, float inv_m, float eps, float momentum, float unbias) {
+  BnFinal f;
+  const float var = fmaxf(__fmul_rn(m2, inv_m), 0.f);
+  f.inv = rsqrtf(__fadd_rn(var, eps));
+  f.scale = __fmul_rn(gamma, f.inv);
+  f.bias = __fmaf_rn(-f.scale, mean, beta);
+  const float keep = __fsub_rn(1.f, momentum);
+  f.run_mean = __fmaf_rn(keep, run_mean, __fmul_rn(momentum, mean));
+  f.run_var = __fmaf_rn(keep, run_var, __fmul_rn(__fmul_rn(momentum, var), unbias));
+  return f;
+}
+
 }  // namespace st
 }  // namespace cbr
