@@ -209,7 +209,7 @@ __global__ void __launch_bounds__(kRedThreads)
     bn_bwd_reduce_kernel(const BwdReduceArgs a) {
   // vectors in flight per thread (the y-derived mask needs a third operand)
   constexpr int kU = MASKBITS ? kRedUnroll : kRedUnroll / 2;
-  __shared__ __align__(16) float red[kRedThreads * 16];  // reused as fp64 [8][2*c] at the end
+  __shared__ __align__(16) float red[kRedThreads * 16];  // the warps' sums; the grid sums at the end
   __shared__ uint32_t ticket;
   const int c = a.c;
   const int cvec = c / 8;
@@ -279,18 +279,32 @@ __global__ void __launch_bounds__(kRedThreads)
       }
     }
   }
+  // block partial, in a fixed order: the lanes of a warp that share a channel group (lane mod
+  // cvec) are combined by a butterfly, then the warps' sums by one thread per value
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll 1
+  for (int o = cvec; o < 32; o <<= 1) {
 #pragma unroll
-  for (int e = 0; e < 8; ++e) {
-    red[threadIdx.x * 16 + e] = sg[e];
-    red[threadIdx.x * 16 + 8 + e] = sgx[e];
+    for (int e = 0; e < 8; ++e) {
+      sg[e] += __shfl_xor_sync(0xffffffffu, sg[e], o);
+      sgx[e] += __shfl_xor_sync(0xffffffffu, sgx[e], o);
+    }
+  }
+  // (cvec <= 32, checked by the launcher: lane l < cvec of every warp holds channel group l)
+  constexpr int kWarps = kRedThreads / 32;
+  if (lane < cvec) {
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      red[(warp * cvec + lane) * 16 + e] = sg[e];
+      red[(warp * cvec + lane) * 16 + 8 + e] = sgx[e];
+    }
   }
   __syncthreads();
-  // block partial: threads t = grp + k*cvec share channel group grp (fixed summation order)
   for (int i = threadIdx.x; i < 2 * c; i += kRedThreads) {
     const int st = i / c, ch = i - st * c;
     const int grp = ch >> 3, e = ch & 7;
     float acc = 0.f;
-    for (int t = grp; t < kRedThreads; t += cvec) acc += red[t * 16 + st * 8 + e];
+    for (int w = 0; w < kWarps; ++w) acc += red[(w * cvec + grp) * 16 + st * 8 + e];
     a.part[(size_t)blockIdx.x * 2 * c + i] = acc;
   }
   __threadfence();
@@ -301,17 +315,16 @@ __global__ void __launch_bounds__(kRedThreads)
   // ------------------------------------------------------------ last block: finalize
   __threadfence();
   // One SM runs this after all the others, so it is kept short: every block partial is loaded
-  // in one batch (thread t sums float4 column t % nv4 of blocks t / nv4, + rgs, ..., in fp32
-  // and a fixed order), the row groups are combined by a fixed pairwise tree in fp32 whose steps
-  // run all their (pair, column) additions in parallel over the block (FP64 is slow on this
-  // part), and the coefficient math multiplies by the host's 1/M instead of dividing.
+  // in one batch (thread t sums float4 column t / rgs of blocks t % rgs, + rgs, ..., in fp32 and
+  // a fixed order), the row groups, rgs consecutive lanes of one warp, are combined by a fixed
+  // pairwise butterfly (FP64 is slow on this part), and the coefficient math multiplies by the
+  // host's 1/M instead of dividing.
   constexpr int kLd = 16;
   const int nv4 = (2 * c) / 4;                    // float4 columns of one partial (<= 128)
-  const int rgs = min(kRedThreads / nv4, 32);     // row groups
-  float* fred = red;                              // [rgs][2c]
-  float4* fred4 = reinterpret_cast<float4*>(red);
+  const int rgs = min(kRedThreads / nv4, 32);     // row groups (a power of two)
+  float* fred = red;                              // [2c]
   if (threadIdx.x < rgs * nv4) {
-    const int c4 = threadIdx.x % nv4, rg = threadIdx.x / nv4;
+    const int rg = threadIdx.x % rgs, c4 = threadIdx.x / rgs;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     for (int b0 = rg; b0 < (int)gridDim.x; b0 += kLd * rgs) {
       float4 v[kLd];
@@ -329,28 +342,23 @@ __global__ void __launch_bounds__(kRedThreads)
         acc.w += v[k].w;
       }
     }
-    fred4[rg * nv4 + c4] = acc;
+    // step w: lane r (r % 2w == 0) adds in lane r + w
+    for (int w = 1; w < rgs; w *= 2) {
+      const float bx = __shfl_down_sync(0xffffffffu, acc.x, w, rgs);
+      const float by = __shfl_down_sync(0xffffffffu, acc.y, w, rgs);
+      const float bz = __shfl_down_sync(0xffffffffu, acc.z, w, rgs);
+      const float bw = __shfl_down_sync(0xffffffffu, acc.w, w, rgs);
+      if ((rg & (2 * w - 1)) == 0) {
+        acc.x += bx;
+        acc.y += by;
+        acc.z += bz;
+        acc.w += bw;
+      }
+    }
+    if (rg == 0) reinterpret_cast<float4*>(fred)[c4] = acc;
   }
   __syncthreads();
-  // step w = 1, 2, 4, ...: row group r (r % 2w == 0, r + w < rgs) adds in row group r + w
-#pragma unroll 1
-  for (int w = 1; w < rgs; w *= 2) {
-    const int npairs = (rgs - w + 2 * w - 1) / (2 * w);
-#pragma unroll 1
-    for (int i = threadIdx.x; i < npairs * nv4; i += kRedThreads) {
-      const int pi = i / nv4, c4 = i - pi * nv4;
-      float4* pa = fred4 + (pi * 2 * w) * nv4 + c4;
-      const float4 b = pa[w * nv4];
-      float4 v = *pa;
-      v.x += b.x;
-      v.y += b.y;
-      v.z += b.z;
-      v.w += b.w;
-      *pa = v;
-    }
-    __syncthreads();
-  }
-  const float* fin = fred;  // row group 0: [2c]
+  const float* fin = fred;
   if (threadIdx.x < c) {
     const int ch = threadIdx.x;
     if (a.sums_out) {
@@ -645,6 +653,7 @@ int launch_bwd_coef(const float* sums, int c, long long m_count, const float* ga
 }
 
 int launch_bwd_reduce(const BwdReduceArgs& a, bool bf16, int num_sms, cudaStream_t st) {
+  // c <= 256: at most 32 channel groups, one per lane of a warp (the block partial relies on it)
   if (a.c % 8 != 0 || a.c > 256 || (kRedThreads % (a.c / 8)) != 0) return 3;
   const long long nvec = a.m_count * (a.c / 8);
   const bool bits = a.mask != nullptr;

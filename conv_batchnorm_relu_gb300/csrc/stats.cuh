@@ -134,10 +134,11 @@ __host__ __device__ constexpr int partial_floats(int c) { return 2 * c + 4; }
 // ------------------------------------------------------------------ grid merge and finalize
 // Every kernel that merges the grid's partial moments (the convolution's last CTA, the
 // persistent forward, the apply pass) runs the same merge, so the statistics and y come out
-// bit-identical whichever kernel merged them.  The row-group count depends on the channel count
-// alone: kRG groups of C/4 threads (one per float4 column of channels, 256 threads for C >= 64);
-// group r merges partials r, r + kRG, r + 2 kRG, ... in order, and a fixed pairwise tree merges
-// the group results.
+// bit-identical whichever kernel merged them.  The row-group count kRG depends on the channel
+// count alone (a power of two that divides 32): thread t < kRG * C/4 takes row group t % kRG of
+// float4 column t / kRG, so the kRG groups of a column are kRG consecutive lanes of one warp.
+// Group r merges partials r, r + kRG, r + 2 kRG, ... in order; a fixed pairwise tree then merges
+// the groups across those lanes (step w: lane r, r % 2w == 0, takes in lane r + w, r first).
 template <int C>
 __host__ __device__ constexpr int merge_groups() {
   return 1024 / C < 16 ? 1024 / C : 16;
@@ -146,28 +147,24 @@ template <int C>
 __host__ __device__ constexpr int merge_threads() {
   return merge_groups<C>() * (C / 4);
 }
-constexpr int kMergeCntF = 8 * 16;  // group counts, one row of kRG per tree step
-// Working set of the merge: [kRG][2C + 4] group results, then the count rows.
+// Working set of the merge: the merged means [C], M2s [C] and the row count.
 template <int C>
 __host__ __device__ constexpr int merge_scratch_floats() {
-  return merge_groups<C>() * partial_floats(C) + kMergeCntF;
+  return partial_floats(C);
 }
 
 // Merge `nparts` partial moments into scratch[0 .. 2C): means, then M2s; returns the total row
-// count.  Every thread of the block calls it (it synchronises the block); `load(b, c4, m, q, n)`
-// fetches float4 column c4 of partial b's means and M2s and its row count.  kLd partials of a
-// thread are loaded before the first is merged (the order of the merges does not depend on it).
+// count.  Every thread of the block calls it (it synchronises the block once); `load(b, c4, m,
+// q, n)` fetches float4 column c4 of partial b's means and M2s and its row count.  kLd partials
+// of a thread are loaded before the first is merged (the merge order does not depend on it).
 template <int C, int kThreads, int kLd, class Load>
 __device__ float merge_partials(int nparts, float* scratch, Load load) {
   constexpr int kV = C / 4;
   constexpr int kRG = merge_groups<C>();
-  constexpr int kGF = partial_floats(C);
   static_assert(kThreads >= merge_threads<C>() && kThreads >= C, "merge threads");
-  static_assert((1 << 7) >= kRG, "count rows");
-  float* fg = scratch;            // [kRG][kGF]
-  float* cnt = fg + kRG * kGF;    // [step][kRG]
-  const int c4 = threadIdx.x % kV, rg = threadIdx.x / kV;
-  if (rg < kRG) {
+  static_assert(32 % kRG == 0 && merge_threads<C>() % 32 == 0, "row groups within whole warps");
+  if (threadIdx.x < merge_threads<C>()) {
+    const int rg = threadIdx.x % kRG, c4 = threadIdx.x / kRG;
     float n = 0.f;
     float m[4] = {0.f, 0.f, 0.f, 0.f}, q[4] = {0.f, 0.f, 0.f, 0.f};
     for (int b0 = rg; b0 < nparts; b0 += kLd * kRG) {
@@ -193,38 +190,30 @@ __device__ float merge_partials(int nparts, float* scratch, Load load) {
         n += vn[k];
       }
     }
-    float* gr = fg + rg * kGF;
-    reinterpret_cast<float4*>(gr)[c4] = make_float4(m[0], m[1], m[2], m[3]);
-    reinterpret_cast<float4*>(gr + C)[c4] = make_float4(q[0], q[1], q[2], q[3]);
-    if (c4 == 0) cnt[rg] = n;
+#pragma unroll
+    for (int w = 1; w < kRG; w *= 2) {
+      const float pn = __shfl_down_sync(0xffffffffu, n, w, kRG);
+      float pm[4], pq[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        pm[j] = __shfl_down_sync(0xffffffffu, m[j], w, kRG);
+        pq[j] = __shfl_down_sync(0xffffffffu, q[j], w, kRG);
+      }
+      if ((rg & (2 * w - 1)) == 0) {
+        const ChanW cw = chan_weights(n, pn);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) chan_merge_w(m[j], q[j], pm[j], pq[j], cw);
+        n += pn;
+      }
+    }
+    if (rg == 0) {
+      reinterpret_cast<float4*>(scratch)[c4] = make_float4(m[0], m[1], m[2], m[3]);
+      reinterpret_cast<float4*>(scratch + C)[c4] = make_float4(q[0], q[1], q[2], q[3]);
+      if (c4 == 0) scratch[2 * C] = n;
+    }
   }
   __syncthreads();
-  // step s (w = 2^s): group r (r % 2w == 0, r + w < kRG) takes in group r + w (r first).  The
-  // right member is not written during its step and each (pair, channel) item has one thread;
-  // the merged counts go to the next step's row.
-  int step = 0;
-#pragma unroll 1
-  for (int w = 1; w < kRG; w *= 2, ++step) {
-    const float* cs = cnt + step * kRG;
-    const int npairs = (kRG - w + 2 * w - 1) / (2 * w);
-#pragma unroll 1
-    for (int i = threadIdx.x; i < npairs * C; i += kThreads) {
-      const int pi = i / C, ch = i - pi * C;
-      const int r = pi * 2 * w;
-      float* ga = fg + r * kGF;
-      const float* gb = ga + w * kGF;
-      float ma = ga[ch], qa = ga[C + ch];
-      chan_merge_w(ma, qa, gb[ch], gb[C + ch], chan_weights(cs[r], cs[r + w]));
-      ga[ch] = ma;
-      ga[C + ch] = qa;
-    }
-    if (threadIdx.x < kRG) {
-      const int r = threadIdx.x;
-      cnt[(step + 1) * kRG + r] = (r % (2 * w) == 0 && r + w < kRG) ? cs[r] + cs[r + w] : cs[r];
-    }
-    __syncthreads();
-  }
-  return cnt[step * kRG];
+  return scratch[2 * C];
 }
 
 // BatchNorm finalize of one channel from its batch mean and M2 over M rows (inv_m = 1/M):
