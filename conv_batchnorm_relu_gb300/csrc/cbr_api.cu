@@ -2,6 +2,7 @@
 // ordering of the kernel launches for each public call (declared in include/cbr.h).
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <cmath>
 #include <cstring>
 #include <mutex>
@@ -306,8 +307,20 @@ bool ensure_smem_attr(const void* func, int bytes) {
   if (cudaGetDevice(&dev) != cudaSuccess) return false;
   std::lock_guard<std::mutex> lk(mu);
   if (done.count({dev, func})) return true;
-  if (cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess)
+  // the opt-in limit covers static and dynamic shared memory together: clamp to what is left
+  // beside the kernel's static shared memory
+  int optin = 0;
+  cudaFuncAttributes fa{};
+  if (cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess ||
+      cudaFuncGetAttributes(&fa, func) != cudaSuccess) {
+    cudaGetLastError();
     return false;
+  }
+  bytes = std::min(bytes, optin - (int)fa.sharedSizeBytes);
+  if (cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess) {
+    cudaGetLastError();  // do not leave the failure for the next launch check to find
+    return false;
+  }
   done.insert({dev, func});
   return true;
 }
