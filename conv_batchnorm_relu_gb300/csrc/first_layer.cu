@@ -415,9 +415,20 @@ constexpr int kImpRaw = 8;                            // raw input rows in fligh
 constexpr int kImpProdWarp = 0;                       // warp 0: bulk copies of raw input rows
 constexpr int kImpConv0 = 1, kImpConvWarps = 4;       // warps 1-4 convert input rows
 constexpr int kImpMmaWarp = 5;
-constexpr int kImpEpiWarp0 = 6;                       // warps 6-13: epilogue
-constexpr int kImpThreads = (kImpEpiWarp0 + 8) * 32;  // 448
-constexpr uint32_t kImpStageBytes = 32 * 128;         // one epilogue warp's staging buffer
+constexpr int kImpEpiWarp0 = 6;                       // warps 6+: epilogue
+// The epilogue: kHalves warps per TMEM lane quadrant, each taking kCPH of the channels of its
+// 32 rows.  16 channels a warp up to 64 channels: the epilogue sets the pace of this kernel
+// (a unit is only 14 MMAs), and with 32 channels a warp its per-unit chain of TMEM load, pack,
+// staging, Welford update and store ran at about 0.9 us a unit; at 128 channels two warps per
+// quadrant keep the registers of 64 channels a thread within the budget.
+template <int NOUT>
+struct ImpEpi {
+  static constexpr int kHalves = NOUT == 128 ? 2 : NOUT / 16;
+  static constexpr int kWarps = 4 * kHalves;
+  static constexpr int kThreads = (kImpEpiWarp0 + kWarps) * 32;
+  static constexpr int kCPH = NOUT / kHalves;                 // channels of one warp's block
+  static constexpr uint32_t kStageBytes = 32u * kCPH * 2u;    // one warp's staged 32-row block
+};
 constexpr int kImpGroupsPerLane = 5;                  // ceil(max groups per row / 32)
 constexpr int kImpAcc = 4;                            // accumulator stages in TMEM
 
@@ -433,7 +444,7 @@ __host__ __device__ inline ImpLayout imp_layout(const FirstGeom& g) {
   L.off_raw = imp_align((uint32_t)kImpRing * g.rowb);
   L.off_b = imp_align(L.off_raw + (g.rawtma ? (uint32_t)kImpRaw * g.rawb : 0u));
   L.off_stage = L.off_b + imp_align((uint32_t)(g.r * g.nmr) * NOUT * 32);
-  L.off_bar = L.off_stage + 8 * 2 * kImpStageBytes;
+  L.off_bar = L.off_stage + (uint32_t)ImpEpi<NOUT>::kWarps * 2u * ImpEpi<NOUT>::kStageBytes;
   L.total = L.off_bar + 512;
   return L;
 }
@@ -554,7 +565,7 @@ __device__ __forceinline__ void imp_convert_row_smem(uint32_t raw, const FirstGe
 }
 
 template <int NOUT, bool BF16>
-__global__ void __launch_bounds__(kImpThreads, 1)
+__global__ void __launch_bounds__(ImpEpi<NOUT>::kThreads, 1)
     first_fprop_imp_kernel(const __grid_constant__ CUtensorMap map_z, const ConvArgs a, const FirstGeom g,
                            const void* wts, const void* xin) {
   constexpr int kTmemCols = hc::pow2_at_least(kImpAcc * NOUT);
@@ -581,7 +592,7 @@ __global__ void __launch_bounds__(kImpThreads, 1)
   // of filter row rr; 16 bytes of (group kc, output channel o) at t*NOUT*32 + kc*NOUT*16 + o*16
   {
     const uint16_t* wsrc = static_cast<const uint16_t*>(wts);
-    for (int i = threadIdx.x; i < nk * 2 * NOUT; i += kImpThreads) {
+    for (int i = threadIdx.x; i < nk * 2 * NOUT; i += ImpEpi<NOUT>::kThreads) {
       const int t = i / (2 * NOUT), rem = i - t * 2 * NOUT;
       const int kc = rem / NOUT, o = rem - kc * NOUT;
       const int rr = t / g.nmr, jj = 2 * (t - rr * g.nmr) + kc;
@@ -609,7 +620,7 @@ __global__ void __launch_bounds__(kImpThreads, 1)
     }
     for (int i = 0; i < kImpAcc; ++i) {
       mbar_init(bar_acc_full + 8 * i, 1);
-      mbar_init(bar_acc_empty + 8 * i, 8);  // lane 0 of each epilogue warp
+      mbar_init(bar_acc_empty + 8 * i, ImpEpi<NOUT>::kWarps);  // lane 0 of each epilogue warp
     }
     mbar_init(bar_drain, 1);
     *abort_flag = 0;
@@ -793,11 +804,12 @@ __global__ void __launch_bounds__(kImpThreads, 1)
     mbar_wait(bar_drain, 0);
   } else {
     // ---------------------------------------------------------------- epilogue (8 warps)
-    constexpr int kHalves = NOUT >= 64 ? 2 : 1;
-    constexpr int kCPH = NOUT / kHalves;         // channels of one warp's block
+    constexpr int kHalves = ImpEpi<NOUT>::kHalves;
+    constexpr int kCPH = ImpEpi<NOUT>::kCPH;     // channels of one warp's block
     constexpr int kSB = kCPH < 32 ? kCPH : 32;
     constexpr int kNB = kCPH / kSB;
     constexpr int kSh = kSB == 32 ? 0 : 1;
+    static_assert(kSB == 16 || kSB == 32, "the merge-scatter leaves channel lane >> kSh");
     constexpr uint32_t kSpan = kCPH * 2;         // staged row bytes = the TMA swizzle span
     constexpr uint32_t kSwz = kSpan / 16 - 1;    // 16-byte chunk bits XOR-ed with bits 7+ of the offset
     const int ew = warp - kImpEpiWarp0;
@@ -817,7 +829,7 @@ __global__ void __launch_bounds__(kImpThreads, 1)
     const bool stats = a.mode == kFpropStats;
     const bool bias_relu = a.mode == kFpropBiasRelu;
     const bool valid = e < g.q;
-    const uint32_t stage0 = sbase + L.off_stage + (uint32_t)ew * 2 * kImpStageBytes;
+    const uint32_t stage0 = sbase + L.off_stage + (uint32_t)ew * 2 * ImpEpi<NOUT>::kStageBytes;
     // the unit sequence, to release ring rows: once a unit's MMAs are complete, the rows the
     // next unit does not read are free (first epilogue warp, lane 0)
     int n = u_begin / g.p, p = u_begin - n * g.p, f = 0;
@@ -846,7 +858,7 @@ __global__ void __launch_bounds__(kImpThreads, 1)
           for (int j = 0; j < g.r - f; ++j) mbar_arrive(bar_row_empty + 8 * ((iend - g.r + j) % kImpRing));
       }
       if (half < kHalves) {
-        const uint32_t sb = stage0 + (it & 1) * kImpStageBytes;
+        const uint32_t sb = stage0 + (it & 1) * ImpEpi<NOUT>::kStageBytes;
 #pragma unroll
         for (int b = 0; b < kNB; ++b) {
           const int c0 = half * kCPH + b * kSB;
@@ -939,7 +951,7 @@ __global__ void __launch_bounds__(kImpThreads, 1)
   tc_fence_before();
   __syncthreads();
   if (a.mode == kFpropStats)
-    hc::stats_partial_finalize<NOUT, kImpThreads, 32768>(a, reinterpret_cast<const float*>(smem), smem, ticket_slot,
+    hc::stats_partial_finalize<NOUT, ImpEpi<NOUT>::kThreads, 32768>(a, reinterpret_cast<const float*>(smem), smem, ticket_slot,
                                                           abort_flag);
   if (warp == kImpMmaWarp) {
     tc_fence_after();
@@ -1622,7 +1634,7 @@ int launch_first_fprop(const FpropArgs& f, int stride, int c_out, bool bf16, con
     g.xal4 = (reinterpret_cast<uintptr_t>(x) & 3) == 0;
     g.rawb = g.w * 6;
     g.rawtma = (g.rawb % 16) == 0 && (reinterpret_cast<uintptr_t>(x) & 15) == 0;
-    const int cph = nout >= 64 ? nout / 2 : nout;
+    const int cph = nout == 128 ? 64 : 16;  // ImpEpi<nout>::kCPH
     CUtensorMap mz{};
     const uint64_t dims[3] = {(uint64_t)c_out, (uint64_t)g.q, (uint64_t)g.units};
     const uint64_t strides[2] = {(uint64_t)c_out * 2, (uint64_t)g.q * c_out * 2};
@@ -1640,20 +1652,20 @@ int launch_first_fprop(const FpropArgs& f, int stride, int c_out, bool bf16, con
                           dims, strides, box, cph * 2)) {
       const int igrid = std::min(g.units, num_sms);
       if (f.parts_out) *f.parts_out = igrid;
-      auto go = [&](auto kern) {
+      auto go = [&](auto kern, int threads) {
         if (!ensure_smem_attr(reinterpret_cast<const void*>(kern), 227 * 1024)) return 6;
-        kern<<<igrid, kImpThreads, ismem, st>>>(mz, a, g, w, x);
+        kern<<<igrid, threads, ismem, st>>>(mz, a, g, w, x);
         return cudaGetLastError() == cudaSuccess ? 0 : 6;
       };
       switch (nout * 2 + (bf16 ? 1 : 0)) {
-        case 16 * 2: return go(first_fprop_imp_kernel<16, false>);
-        case 16 * 2 + 1: return go(first_fprop_imp_kernel<16, true>);
-        case 32 * 2: return go(first_fprop_imp_kernel<32, false>);
-        case 32 * 2 + 1: return go(first_fprop_imp_kernel<32, true>);
-        case 64 * 2: return go(first_fprop_imp_kernel<64, false>);
-        case 64 * 2 + 1: return go(first_fprop_imp_kernel<64, true>);
-        case 128 * 2: return go(first_fprop_imp_kernel<128, false>);
-        case 128 * 2 + 1: return go(first_fprop_imp_kernel<128, true>);
+        case 16 * 2: return go(first_fprop_imp_kernel<16, false>, ImpEpi<16>::kThreads);
+        case 16 * 2 + 1: return go(first_fprop_imp_kernel<16, true>, ImpEpi<16>::kThreads);
+        case 32 * 2: return go(first_fprop_imp_kernel<32, false>, ImpEpi<32>::kThreads);
+        case 32 * 2 + 1: return go(first_fprop_imp_kernel<32, true>, ImpEpi<32>::kThreads);
+        case 64 * 2: return go(first_fprop_imp_kernel<64, false>, ImpEpi<64>::kThreads);
+        case 64 * 2 + 1: return go(first_fprop_imp_kernel<64, true>, ImpEpi<64>::kThreads);
+        case 128 * 2: return go(first_fprop_imp_kernel<128, false>, ImpEpi<128>::kThreads);
+        case 128 * 2 + 1: return go(first_fprop_imp_kernel<128, true>, ImpEpi<128>::kThreads);
         default: return 3;
       }
     }

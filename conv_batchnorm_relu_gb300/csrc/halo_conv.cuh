@@ -179,8 +179,10 @@ __device__ void stats_partial_finalize(const ConvArgs& a, const float* red, uint
     // ---------------------------------------------------- bn_finalize (last CTA)
     __threadfence();
     float* fg = reinterpret_cast<float*>(scratch);
-    // the other CTAs' partials were written during this launch: read them from L2
-    const float tot_n = st::merge_partials<COUT, kThreads, 10>(
+    // the other CTAs' partials were written during this launch: read them from L2, ten a
+    // thread in flight (four in kernels of more than 512 threads, whose register budget is less)
+    constexpr int kLdF = kThreads > 512 ? 4 : 10;
+    const float tot_n = st::merge_partials<COUT, kThreads, kLdF>(
         (int)gridDim.x, fg, [&](int b, int c4, float4& m, float4& q, float& n) {
           const float* pb = a.part + (size_t)b * kPF;
           m = __ldcg(reinterpret_cast<const float4*>(pb) + c4);
