@@ -803,7 +803,7 @@ __global__ void __launch_bounds__(ImpEpi<NOUT>::kThreads, 1)
     mma_commit_warp(bar_drain);
     mbar_wait(bar_drain, 0);
   } else {
-    // ---------------------------------------------------------------- epilogue (8 warps)
+    // ---------------------------------------------------------------- epilogue (ImpEpi warps)
     constexpr int kHalves = ImpEpi<NOUT>::kHalves;
     constexpr int kCPH = ImpEpi<NOUT>::kCPH;     // channels of one warp's block
     constexpr int kSB = kCPH < 32 ? kCPH : 32;
