@@ -685,8 +685,8 @@ __global__ void __launch_bounds__(ImpEpi<NOUT>::kThreads, 1)
         bool ready = mbar_test(bar_row_empty + 8 * slot, (fill & 1) ^ 1);
         if (g.rawtma) ready &= mbar_test(bar_raw_full + 8 * rs, (i / kImpRaw) & 1);
         if (!__all_sync(0xffffffffu, ready)) {
-          bool got = mbar_wait_backoff(bar_row_empty + 8 * slot, (fill & 1) ^ 1, 32);
-          if (g.rawtma) got = got && mbar_wait_backoff(bar_raw_full + 8 * rs, (i / kImpRaw) & 1, 32);
+          bool got = mbar_wait_backoff(bar_row_empty + 8 * slot, (fill & 1) ^ 1, 256);
+          if (g.rawtma) got = got && mbar_wait_backoff(bar_raw_full + 8 * rs, (i / kImpRaw) & 1, 256);
           if (!__all_sync(0xffffffffu, got)) {
             hc::set_abort(abort_flag, a.err, kErrWaitHalo);
             ok = false;
@@ -878,7 +878,9 @@ __global__ void __launch_bounds__(ImpEpi<NOUT>::kThreads, 1)
           for (int i = 0; i < kSB; ++i) {
             float xv = __uint_as_float(r[i]);
             if (bias_relu) xv = fmaxf(xv + __ldg(a.bias + c0 + i), 0.f);
-            v[i] = valid ? xv : 0.f;
+            // rows >= q are not stored (the TMA store clips them) and not counted by the
+            // per-row Welford update; the warp merge of the 128-channel form weighs them by 0
+            v[i] = (kRegStats || valid) ? xv : 0.f;
           }
 #pragma unroll
           for (int cc = 0; cc < kSB / 8; ++cc) {
