@@ -130,7 +130,7 @@ int check_desc(const cbr_desc_t* d, Shape* sh) {
 
 bool is_first_layer(const Shape& s) { return s.cin == 3; }
 
-// Shapes this build runs on the device.
+// Shapes the library runs on the device.
 int check_supported(const Shape& s) {
   if (!(s.cout == 16 || s.cout == 32 || s.cout == 64 || s.cout == 128)) return CBR_ERR_UNSUPPORTED;
   // first layer (3 channels): im2col kernels, any stride, filters up to 8x8, rows up to 128
